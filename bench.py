@@ -1,0 +1,358 @@
+"""Benchmark of the Fairy2i widely-linear 2-bit layer on B300.
+
+Workload (the decode metric): batch-1 decode through the seven LLaMA-2-7B
+projections of a decoder block (q/k/v/o 4096x4096, gate/up 11008x4096, down
+4096x11008 as real matrices; T = 2), for 32 distinct blocks = the 224
+projections of the 7B stack, 1.64 GB of packed codes and scales, far above
+the 126 MB L2, so no flush is needed between steps.  One step = one token
+through all 224 projections, one grouped launch per block (7 layers each).
+
+value      = packed bytes streamed per step / device time per step (GB/s)
+e2e        = the same bytes / time per step including the host->device copy of
+             every projection's activation row and the device->host copy of
+             every output row (pinned host buffers)
+roofline   = the decode kernel's average launch: packed bytes of one block
+             (51,273,728 B) / launch time, against the measured HBM copy peak
+cpu_baseline / --impl reference = the oracle (plain C, double precision,
+             one thread) on a sample of output rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from bit_complex_valued_fairy2i_b300 import inputs  # noqa: E402
+
+METRIC = "2-bit WL-complex GEMV weight GB/s vs HBM peak; prefill GEMM TFLOP/s"
+UNIT = "GB/s"
+T_STAGES = 2
+BLOCKS = inputs.LLAMA2_7B_BLOCKS
+WORKLOAD = ("llama2-7b decode GEMV, M=1, T=2: 7 projections per block x 32 distinct blocks "
+            "(224 projections, 1.64 GB packed > L2), one grouped launch per block")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# oracle on a sample of rows (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def _oracle_sample_setup(max_rows_per_proj: int, seed_config: int = 5):
+    """Oracle-quantized rows of block 0 (rows j = 0, s, 2s, ... of each projection)."""
+    import oracle
+    samples = []
+    for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
+        n, m = out_f // 2, in_f // 2
+        step = max(1, n // max_rows_per_proj)
+        rows = np.arange(0, n, step)[:max_rows_per_proj]
+        R = inputs.weight_R(seed_config, pi, out_f, in_f)
+        Rs = torch.cat([R[rows], R[n + rows]]).numpy()
+        Uo, Wo = oracle.convert_f32(Rs)
+        qU, qW = oracle.quantize(Uo, T_STAGES), oracle.quantize(Wo, T_STAGES)
+        x = inputs.bf16_bits(inputs.activations(seed_config, pi, 1, in_f))
+        # packed bytes these rows stand for: 2T planes of 2-bit codes + 4T fp32 scales per row
+        nbytes = len(rows) * (2 * T_STAGES * m // 4 + 4 * T_STAGES * 4)
+        samples.append((qU, qW, x, nbytes))
+    return samples
+
+
+def _oracle_run(samples):
+    import oracle
+    t0 = time.perf_counter()
+    nbytes = 0
+    for qU, qW, x, nb in samples:
+        oracle.linear_mulfree(qU, qW, x)
+        nbytes += nb
+    return nbytes, time.perf_counter() - t0
+
+
+def cpu_baseline(target_s: float = 10.0):
+    rows = 8
+    samples = _oracle_sample_setup(rows)
+    nb, dt = _oracle_run(samples)
+    rows = max(1, min(2048, int(rows * target_s / max(dt, 1e-6))))
+    samples = _oracle_sample_setup(rows)
+    nb, dt = _oracle_run(samples)
+    return {"value": nb / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"oracle decode (plain C, fp64, 1 thread) of {rows} evenly spaced output rows of each of "
+                      f"the 7 projections of block 0, M=1, T=2; {nb} packed-equivalent bytes in {dt:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    steps_total = args.steps + args.warmup
+    budget_s = 120.0
+    rows = 4
+    samples = _oracle_sample_setup(rows)
+    nb, dt = _oracle_run(samples)
+    per_row = dt / rows
+    rows = max(1, min(512, int(budget_s / steps_total / max(per_row, 1e-9))))
+    samples = _oracle_sample_setup(rows)
+    for _ in range(args.warmup):
+        _oracle_run(samples)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        b, _ = _oracle_run(samples)
+        nbytes += b
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    sample = (f"each step: oracle decode (plain C, fp64, 1 thread) of {rows} evenly spaced output rows of each "
+              f"of the 7 projections of block 0, M=1, T=2")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def build_stack(f2i, blocks: int, dev):
+    """Convert + quantize the stack on the GPU; times both (events)."""
+    stack = []
+    conv_ms = quant_ms = 0.0
+    conv_bytes = quant_bytes = 0
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for b in range(blocks):
+        layers = []
+        for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
+            R = inputs.weight_R(5, 7 * b + pi, out_f, in_f, device=dev)
+            e[0].record()
+            U, W = f2i.convert(R)
+            e[1].record()
+            q = f2i.quantize(U, W, T_STAGES, check=False)
+            e[2].record()
+            e[2].synchronize()
+            conv_ms += e[0].elapsed_time(e[1])
+            quant_ms += e[1].elapsed_time(e[2])
+            conv_bytes += R.numel() * 4 * 2  # read R, write U and W
+            quant_bytes += R.numel() * 4 + q.nbytes  # read U and W, write codes + scales
+            layers.append(q)
+            del R, U, W
+        stack.append(layers)
+    f2i.sync_status()
+    return stack, {"convert_GBps": conv_bytes / conv_ms / 1e6, "quantize_GBps": quant_bytes / quant_ms / 1e6,
+                   "convert_ms_stack": conv_ms, "quantize_ms_stack": quant_ms}
+
+
+def run_ours(args, world, rank, local):
+    import bit_complex_valued_fairy2i_b300 as f2i
+    from bit_complex_valued_fairy2i_b300 import build as f2i_build
+
+    f2i_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = _peaks()
+
+    stack, offline = build_stack(f2i, BLOCKS, dev)
+    bytes_per_block = sum(q.nbytes for q in stack[0])
+    bytes_per_step = sum(q.nbytes for layers in stack for q in layers)
+
+    # activations and outputs: one contiguous device buffer each, one row per projection
+    x_sizes = [2 * q.m for layers in stack for q in layers]
+    y_sizes = [2 * q.n for layers in stack for q in layers]
+    x_all = torch.cat([inputs.activations(5, 7 * b + pi, 1, inf, device=dev).reshape(-1)
+                       for b in range(BLOCKS) for pi, (_, _, inf) in enumerate(inputs.LLAMA2_7B_BLOCK)])
+    y_all = torch.empty(sum(y_sizes), dtype=torch.float32, device=dev)
+    xv = list(torch.split(x_all, x_sizes))
+    yv = list(torch.split(y_all, y_sizes))
+    xs = [[xv[7 * b + i].view(1, -1) for i in range(7)] for b in range(BLOCKS)]
+    ys = [[yv[7 * b + i].view(1, -1) for i in range(7)] for b in range(BLOCKS)]
+
+    def step():
+        for b in range(BLOCKS):
+            f2i.linear_group(stack[b], xs[b], ys[b])
+
+    step()  # outside capture: first-use setup (shared-memory attributes)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        stop.record(stream)
+        torch.cuda.synchronize()
+    _barrier(world)
+    total_ms = _max_over_ranks(start.elapsed_time(stop), world)
+    ms_per_step = total_ms / args.steps
+    launch_ms = ms_per_step / BLOCKS  # every launch of the step is the decode kernel
+    value = bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
+
+    # end to end: the step's activations from pinned host memory, its outputs back
+    x_host = torch.empty_like(x_all, device="cpu").pin_memory()
+    x_host.copy_(x_all.cpu())
+    y_host = torch.empty_like(y_all, device="cpu").pin_memory()
+    h2d = x_all.numel() * x_all.element_size()
+    d2h = y_all.numel() * y_all.element_size()
+    e2e_steps = max(3, args.steps // 4)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        x_all.copy_(x_host, non_blocking=True)
+        graph.replay()
+        y_host.copy_(y_all, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_s = _max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+    e2e_value = bytes_per_step * world / e2e_s / 1e9
+
+    achieved = bytes_per_block / (launch_ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 mma (codes {+-2,+-0}, bf16 x split hi/lo), fp32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "T": T_STAGES, "blocks": BLOCKS, "projections": 7 * BLOCKS,
+                   "bytes_per_step": bytes_per_step, "l2": "inputs larger than L2 (1.64 GB working set)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": BLOCKS * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "linear_mma_fp8_kernel<4,1,4>", "bytes_per_launch": bytes_per_block,
+                     "launch_us": launch_ms * 1e3, "peak_source": peaks["source"],
+                     "frac_of_nominal_8TBps": achieved / 8000.0},
+        "clocks": clk.summary(),
+        "offline": offline,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,210 @@
+"""Fairy2i widely-linear 2-bit complex linear layer on B300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/fairy2i.h`` (libfairy2i.so,
+built in-tree by ``build.py``).  This module only marshals arguments: device
+memory comes from PyTorch tensors, every step of the layer runs in the
+library's CUDA kernels.  There is no CPU fallback; if the library or a GPU is
+missing, calls raise.
+
+    U, W = convert(R)                 # R: cuda float32 [2n, 2m]
+    q = quantize(U, W, T=2)           # packed 2-bit codes + per-row scales
+    y = linear(q, x)                  # x: cuda bfloat16 [M, 2m] -> y float32 [M, 2n]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfairy2i.so")
+
+OK = 0
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "SHAPE", 3: "NONFINITE", 4: "UNSUPPORTED", 5: "CUDA",
+                6: "TIMEOUT"}
+ALGO = {"auto": 0, "addsub": 1, "mma_fp8": 2, "tcgen05": 3}
+LAYOUT_VERSION = 1
+
+# every extern "C" symbol declared in include/fairy2i.h
+EXPORTED = (
+    "fairy2i_codes_bytes", "fairy2i_scales_count", "fairy2i_convert", "fairy2i_quantize",
+    "fairy2i_linear", "fairy2i_linear_ex", "fairy2i_linear_group", "fairy2i_unpack_codes",
+    "fairy2i_sync_status", "fairy2i_last_error", "fairy2i_layout_version",
+)
+
+
+class Fairy2iError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class PackedDesc(ctypes.Structure):
+    _fields_ = [("version", ctypes.c_int32), ("T", ctypes.c_int32), ("n", ctypes.c_int64),
+                ("m", ctypes.c_int64), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libfairy2i.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libfairy2i.so not found at {path}; run bit_complex_valued_fairy2i_b300/build.py")
+    lib = ctypes.CDLL(path)
+    P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    PD = ctypes.POINTER(PackedDesc)
+    sig = {
+        "fairy2i_codes_bytes": (SZ, [I64, I64, I32]),
+        "fairy2i_scales_count": (SZ, [I64, I32]),
+        "fairy2i_convert": (ctypes.c_int, [P, I64, I64, P, P, P]),
+        "fairy2i_quantize": (ctypes.c_int, [P, P, I64, I64, I32, PD, P]),
+        "fairy2i_linear": (ctypes.c_int, [PD, P, I64, P, P]),
+        "fairy2i_linear_ex": (ctypes.c_int, [PD, P, I64, P, ctypes.c_int, P]),
+        "fairy2i_linear_group": (ctypes.c_int, [PD, ctypes.POINTER(P), ctypes.POINTER(P), I32, I64,
+                                                ctypes.c_int, P]),
+        "fairy2i_unpack_codes": (ctypes.c_int, [PD, P, P]),
+        "fairy2i_sync_status": (ctypes.c_int, [P]),
+        "fairy2i_last_error": (ctypes.c_char_p, []),
+        "fairy2i_layout_version": (I32, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype, f.argtypes = res, args
+    if lib.fairy2i_layout_version() != LAYOUT_VERSION:
+        raise ImportError("libfairy2i.so layout version mismatch")
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != OK:
+        raise Fairy2iError(status, load_library().fairy2i_last_error().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def codes_bytes(n: int, m: int, T: int) -> int:
+    return int(load_library().fairy2i_codes_bytes(n, m, T))
+
+
+def scales_count(n: int, T: int) -> int:
+    return int(load_library().fairy2i_scales_count(n, T))
+
+
+@dataclass
+class Packed:
+    """Packed quantized layer: device codes (uint8) and scales [2][T][2][n]."""
+    n: int
+    m: int
+    T: int
+    codes: torch.Tensor
+    scales: torch.Tensor
+
+    def desc(self) -> PackedDesc:
+        return PackedDesc(LAYOUT_VERSION, self.T, self.n, self.m, self.codes.data_ptr(), self.scales.data_ptr())
+
+    @property
+    def nbytes(self) -> int:
+        """Packed bytes streamed per evaluation: codes + scales."""
+        return self.codes.numel() + 4 * self.scales.numel()
+
+    @staticmethod
+    def empty(n: int, m: int, T: int, device="cuda") -> "Packed":
+        nb = codes_bytes(n, m, T)
+        ns = scales_count(n, T)
+        if nb == 0 or ns == 0:
+            raise Fairy2iError(4, f"unsupported shape n={n} m={m} T={T}")
+        codes = torch.empty(nb, dtype=torch.uint8, device=device)
+        scales = torch.empty(ns, dtype=torch.float32, device=device).view(2, T, 2, n)
+        return Packed(n, m, T, codes, scales)
+
+
+def convert(R: torch.Tensor, stream=None):
+    """Real [2n, 2m] float32 weight -> complex64 (U, W), each [n, m]."""
+    _dev(R, "R")
+    if R.dtype != torch.float32 or R.dim() != 2:
+        raise ValueError("R must be a 2-D float32 tensor")
+    n, m = R.shape[0] // 2, R.shape[1] // 2
+    U = torch.empty((n, m), dtype=torch.complex64, device=R.device)
+    W = torch.empty((n, m), dtype=torch.complex64, device=R.device)
+    _check(load_library().fairy2i_convert(R.data_ptr(), R.shape[0], R.shape[1], U.data_ptr(), W.data_ptr(),
+                                          _stream(stream)))
+    return U, W
+
+
+def quantize(U: torch.Tensor, W: torch.Tensor, T: int = 2, out: Packed | None = None, stream=None,
+             check: bool = True) -> Packed:
+    """Phase-aware recursive residual quantization of U and W (complex64 [n, m]).
+    With ``check`` the stream is synchronized and a non-finite weight raises."""
+    _dev(U, "U")
+    _dev(W, "W")
+    if U.dtype != torch.complex64 or W.dtype != torch.complex64 or U.shape != W.shape or U.dim() != 2:
+        raise ValueError("U and W must be complex64 tensors of the same 2-D shape")
+    n, m = U.shape
+    q = out if out is not None else Packed.empty(n, m, T, U.device)
+    d = q.desc()
+    _check(load_library().fairy2i_quantize(U.data_ptr(), W.data_ptr(), n, m, T, ctypes.byref(d), _stream(stream)))
+    if check:
+        sync_status(stream)
+    return q
+
+
+def linear(q: Packed, x: torch.Tensor, algo: str = "auto", out: torch.Tensor | None = None,
+           stream=None) -> torch.Tensor:
+    """y = U^ x + W^ conj(x) for x bfloat16 [M, 2m] ([Re x | Im x] rows) -> y float32 [M, 2n]."""
+    _dev(x, "x")
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != 2 * q.m:
+        raise ValueError(f"x must be bfloat16 [M, {2 * q.m}]")
+    y = out if out is not None else torch.empty((x.shape[0], 2 * q.n), dtype=torch.float32, device=x.device)
+    d = q.desc()
+    _check(load_library().fairy2i_linear_ex(ctypes.byref(d), x.data_ptr(), x.shape[0], y.data_ptr(), ALGO[algo],
+                                            _stream(stream)))
+    return y
+
+
+def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None):
+    """Evaluate several layers (same T and token count) in one launch."""
+    count = len(qs)
+    M = xs[0].shape[0]
+    if ys is None:
+        ys = [torch.empty((M, 2 * q.n), dtype=torch.float32, device=x.device) for q, x in zip(qs, xs)]
+    descs = (PackedDesc * count)(*[q.desc() for q in qs])
+    xp = (ctypes.c_void_p * count)(*[x.data_ptr() for x in xs])
+    yp = (ctypes.c_void_p * count)(*[y.data_ptr() for y in ys])
+    for q, x, y in zip(qs, xs, ys):
+        _dev(x, "x")
+        _dev(y, "y")
+        if x.dtype != torch.bfloat16 or x.shape != (M, 2 * q.m) or y.shape != (M, 2 * q.n):
+            raise ValueError("group members need matching x [M, 2m] bfloat16 and y [M, 2n] float32")
+    _check(load_library().fairy2i_linear_group(descs, xp, yp, count, M, ALGO[algo], _stream(stream)))
+    return ys
+
+
+def unpack_codes(q: Packed, stream=None) -> torch.Tensor:
+    """Canonical codes uint8 [2, T, n, m] (0=+1, 1=-1, 2=+i, 3=-i) on the device."""
+    out = torch.empty((2, q.T, q.n, q.m), dtype=torch.uint8, device=q.codes.device)
+    d = q.desc()
+    _check(load_library().fairy2i_unpack_codes(ctypes.byref(d), out.data_ptr(), _stream(stream)))
+    return out
+
+
+def sync_status(stream=None):
+    """Synchronize the stream and raise if a kernel reported an error."""
+    _check(load_library().fairy2i_sync_status(_stream(stream)))

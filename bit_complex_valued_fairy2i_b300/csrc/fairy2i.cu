@@ -1,0 +1,346 @@
+// Host side of the C ABI declared in include/fairy2i.h: argument checks,
+// launch configuration and error reporting.  All arithmetic of the layer runs
+// in the kernels included below.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/fairy2i.h"
+#include "layout.cuh"
+#include "convert_quantize.cuh"
+#include "linear_decode.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+fairy2i_status fail(fairy2i_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+fairy2i_status ok() {
+  g_last_error.clear();
+  return FAIRY2I_OK;
+}
+
+fairy2i_status check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+// Opt a kernel in to more than 48 KB of dynamic shared memory, once per
+// (kernel, device): later calls, including calls made while a stream is being
+// captured into a CUDA graph, issue no attribute call.
+struct SmemAttr {
+  const void* fn;
+  int device;
+  size_t bytes;
+};
+std::mutex g_attr_mu;
+std::vector<SmemAttr> g_attr;
+
+fairy2i_status ensure_smem(const void* fn, size_t smem, const char* what) {
+  if (smem <= 48 * 1024) return FAIRY2I_OK;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  for (const SmemAttr& a : g_attr)
+    if (a.fn == fn && a.device == dev && a.bytes >= smem) return FAIRY2I_OK;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "%s shared memory attribute: %s", what, cudaGetErrorString(e));
+  g_attr.push_back({fn, dev, smem});
+  return FAIRY2I_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int sm_count() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 148;
+}
+
+fairy2i_status check_packed(const fairy2i_packed* q) {
+  if (!q) return fail(FAIRY2I_ERR_INVALID_ARG, "packed descriptor is NULL");
+  if (q->version != FAIRY2I_LAYOUT_VERSION)
+    return fail(FAIRY2I_ERR_INVALID_ARG, "packed layout version %d, library expects %d", q->version,
+                FAIRY2I_LAYOUT_VERSION);
+  if (q->n < 1 || q->m < 1) return fail(FAIRY2I_ERR_SHAPE, "n=%lld m=%lld must be >= 1", (long long)q->n, (long long)q->m);
+  if (q->T < 1 || q->T > FAIRY2I_MAX_T) return fail(FAIRY2I_ERR_UNSUPPORTED, "T=%d outside [1, %d]", q->T, FAIRY2I_MAX_T);
+  if (q->m > FAIRY2I_MAX_M) return fail(FAIRY2I_ERR_UNSUPPORTED, "m=%lld above %d", (long long)q->m, FAIRY2I_MAX_M);
+  if (!q->codes || !q->scales) return fail(FAIRY2I_ERR_INVALID_ARG, "codes or scales pointer is NULL");
+  if (!aligned(q->codes, 256)) return fail(FAIRY2I_ERR_INVALID_ARG, "codes pointer not 256-byte aligned");
+  if (!aligned(q->scales, 16)) return fail(FAIRY2I_ERR_INVALID_ARG, "scales pointer not 16-byte aligned");
+  return FAIRY2I_OK;
+}
+
+// --- decode launch helpers --------------------------------------------------
+
+constexpr int kMmaRgc = 1;  // row groups in flight per CTA in the fp8 decode kernel
+
+// Resident CTAs per SM for a kernel at a given dynamic shared memory size,
+// cached per (kernel, device, bytes).
+struct OccEntry {
+  const void* fn;
+  int device;
+  size_t smem;
+  int blocks;
+};
+std::mutex g_occ_mu;
+std::vector<OccEntry> g_occ;
+
+int resident_ctas(const void* fn, int threads, size_t smem) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_occ_mu);
+  for (const OccEntry& e : g_occ)
+    if (e.fn == fn && e.device == dev && e.smem == smem) return e.blocks;
+  int nb = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem) != cudaSuccess || nb < 1) nb = 1;
+  g_occ.push_back({fn, dev, smem, nb});
+  return nb;
+}
+
+// Persistent partition: `slots` CTAs shared among the problems in proportion
+// to their bytes; every CTA of a problem owns rg_per_cta consecutive row
+// groups (a multiple of rgc).  Returns the number of CTAs.
+int partition(f2i::LinearGroup& G, int slots, int rgc) {
+  double total = 0.0;
+  for (int i = 0; i < G.count; ++i)
+    total += (double)f2i::row_groups(G.p[i].n) * (double)f2i::col_blocks(G.p[i].m);
+  int ctas = 0;
+  for (int i = 0; i < G.count; ++i) {
+    const int64_t RG = f2i::row_groups(G.p[i].n);
+    const double share = (double)RG * (double)f2i::col_blocks(G.p[i].m) / total;
+    int64_t want = std::max<int64_t>(1, (int64_t)(slots * share));
+    int64_t rpc = (RG + want - 1) / want;
+    rpc = ((rpc + rgc - 1) / rgc) * rgc;
+    G.p[i].cta_begin = ctas;
+    G.p[i].rg_per_cta = (int32_t)rpc;
+    ctas += (int)((RG + rpc - 1) / rpc);
+  }
+  return ctas;
+}
+
+template <int NPL, int TILES>
+fairy2i_status launch_mma_t(f2i::LinearGroup& G, size_t smem, cudaStream_t s) {
+  auto k = f2i::linear_mma_fp8_kernel<NPL, TILES, kMmaRgc>;
+  const void* fn = reinterpret_cast<const void*>(k);
+  fairy2i_status st = ensure_smem(fn, smem, "mma decode");
+  if (st != FAIRY2I_OK) return st;
+  const int slots = sm_count() * resident_ctas(fn, f2i::kMmaWarps * 32, smem);
+  const int ctas = partition(G, slots, kMmaRgc);
+  k<<<ctas, f2i::kMmaWarps * 32, smem, s>>>(G);
+  return check_launch("mma decode launch");
+}
+
+template <int NPL>
+fairy2i_status launch_mma_tiles(f2i::LinearGroup& G, int tiles, size_t smem, cudaStream_t s) {
+  switch (tiles) {
+    case 1: return launch_mma_t<NPL, 1>(G, smem, s);
+    case 2: return launch_mma_t<NPL, 2>(G, smem, s);
+    default: return launch_mma_t<NPL, 4>(G, smem, s);
+  }
+}
+
+// One launch of the fp8 mma decode for up to 8 tokens of every problem in G.
+fairy2i_status run_mma(f2i::LinearGroup& G, int T, cudaStream_t s) {
+  const int tiles_needed = (G.M + 1) / 2;
+  const int tiles = tiles_needed <= 1 ? 1 : tiles_needed <= 2 ? 2 : 4;
+  int64_t m_pad_max = 0;
+  for (int i = 0; i < G.count; ++i) m_pad_max = std::max(m_pad_max, f2i::col_blocks(G.p[i].m) * 64);
+  const size_t smem = (size_t)tiles * 8 * m_pad_max + (size_t)f2i::kMmaWarps * tiles * 2 * 32 * sizeof(float);
+  if (smem > 227 * 1024)
+    return fail(FAIRY2I_ERR_UNSUPPORTED, "fp8 decode needs %zu bytes of shared memory", smem);
+  switch (T) {
+    case 1: return launch_mma_tiles<2>(G, tiles, smem, s);
+    case 2: return launch_mma_tiles<4>(G, tiles, smem, s);
+    case 3: return launch_mma_tiles<6>(G, tiles, smem, s);
+    case 4: return launch_mma_tiles<8>(G, tiles, smem, s);
+    default: return fail(FAIRY2I_ERR_UNSUPPORTED, "fp8 decode supports T <= 4 (got %d)", T);
+  }
+}
+
+fairy2i_status run_addsub(f2i::LinearGroup& G, cudaStream_t s) {
+  int ctas = 0;
+  int64_t m_pad_max = 0;
+  for (int i = 0; i < G.count; ++i) {
+    G.p[i].cta_begin = ctas;
+    ctas += (int)((f2i::row_groups(G.p[i].n) + f2i::kAddSubWarps - 1) / f2i::kAddSubWarps);
+    m_pad_max = std::max(m_pad_max, f2i::col_blocks(G.p[i].m) * 64);
+  }
+  const size_t smem = (size_t)f2i::kAddSubTok * m_pad_max * sizeof(uint32_t);
+  fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(f2i::linear_addsub_kernel), smem, "addsub decode");
+  if (st != FAIRY2I_OK) return st;
+  f2i::linear_addsub_kernel<<<ctas, f2i::kAddSubWarps * 32, smem, s>>>(G);
+  return check_launch("addsub decode launch");
+}
+
+fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int32_t count,
+                                 int64_t M, fairy2i_algo algo, cudaStream_t s) {
+  if (count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "count=%d outside [1, 256]", count);
+  if (!qs || !xs || !ys) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL array argument");
+  if (M < 0) return fail(FAIRY2I_ERR_SHAPE, "M=%lld is negative", (long long)M);
+  if ((int)algo < 0 || (int)algo > 3) return fail(FAIRY2I_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
+  const int T = qs[0].T;
+  for (int i = 0; i < count; ++i) {
+    fairy2i_status st = check_packed(&qs[i]);
+    if (st != FAIRY2I_OK) return st;
+    if (qs[i].T != T) return fail(FAIRY2I_ERR_SHAPE, "all layers of a group need the same T");
+  }
+  if (M == 0) return ok();  // no tokens: nothing is read or written
+  for (int i = 0; i < count; ++i) {
+    if (!xs[i] || !ys[i]) return fail(FAIRY2I_ERR_INVALID_ARG, "x or y of layer %d is NULL", i);
+    if (!aligned(xs[i], 16) || !aligned(ys[i], 16))
+      return fail(FAIRY2I_ERR_INVALID_ARG, "x and y must be 16-byte aligned (layer %d)", i);
+  }
+  if (M > (int64_t)1 << 30) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
+
+  fairy2i_algo a = algo;
+  if (a == FAIRY2I_ALGO_AUTO) a = (T <= 4) ? FAIRY2I_ALGO_MMA_FP8 : FAIRY2I_ALGO_ADDSUB;
+  if (a == FAIRY2I_ALGO_TCGEN05) return fail(FAIRY2I_ERR_UNSUPPORTED, "tcgen05 prefill path not built yet");
+  if (a == FAIRY2I_ALGO_MMA_FP8 && T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "fp8 decode supports T <= 4");
+
+  const int chunk = (a == FAIRY2I_ALGO_MMA_FP8) ? 8 : f2i::kAddSubTok * 1024;
+  for (int p0 = 0; p0 < count; p0 += f2i::kMaxGroup) {
+    const int cnt = std::min(f2i::kMaxGroup, count - p0);
+    for (int64_t t0 = 0; t0 < M; t0 += chunk) {
+      f2i::LinearGroup G;
+      memset(&G, 0, sizeof(G));
+      G.count = cnt;
+      G.M = (int32_t)std::min<int64_t>(chunk, M - t0);
+      for (int i = 0; i < cnt; ++i) {
+        const fairy2i_packed& q = qs[p0 + i];
+        f2i::LinearProblem& P = G.p[i];
+        P.codes = static_cast<const uint8_t*>(q.codes);
+        P.scales = q.scales;
+        P.x = static_cast<const uint16_t*>(xs[p0 + i]) + t0 * 2 * q.m;
+        P.y = ys[p0 + i] + t0 * 2 * q.n;
+        P.n = q.n;
+        P.m = q.m;
+        P.T = q.T;
+      }
+      fairy2i_status st = (a == FAIRY2I_ALGO_MMA_FP8) ? run_mma(G, T, s) : run_addsub(G, s);
+      if (st != FAIRY2I_OK) return st;
+    }
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t fairy2i_layout_version(void) { return FAIRY2I_LAYOUT_VERSION; }
+
+const char* fairy2i_last_error(void) { return g_last_error.c_str(); }
+
+size_t fairy2i_codes_bytes(int64_t n, int64_t m, int32_t T) {
+  if (n < 1 || m < 1 || T < 1 || T > FAIRY2I_MAX_T) return 0;
+  return (size_t)(2 * T) * (size_t)f2i::plane_bytes(n, m);
+}
+
+size_t fairy2i_scales_count(int64_t n, int32_t T) {
+  if (n < 1 || T < 1 || T > FAIRY2I_MAX_T) return 0;
+  return (size_t)4 * (size_t)T * (size_t)n;
+}
+
+fairy2i_status fairy2i_convert(const float* R, int64_t rows, int64_t cols, void* U, void* W, void* stream) {
+  if (!R || !U || !W) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL pointer argument");
+  if (rows < 2 || cols < 2 || (rows & 1) || (cols & 1))
+    return fail(FAIRY2I_ERR_SHAPE, "R is %lld x %lld; both dimensions must be even and >= 2", (long long)rows,
+                (long long)cols);
+  if (!aligned(R, 16) || !aligned(U, 16) || !aligned(W, 16))
+    return fail(FAIRY2I_ERR_INVALID_ARG, "R, U and W must be 16-byte aligned");
+  const int64_t n = rows / 2, m = cols / 2;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int blocks = sm_count() * 8;
+  if ((m & 3) == 0) {
+    f2i::convert_vec4_kernel<<<blocks, 256, 0, s>>>(R, n, m, static_cast<float4*>(U), static_cast<float4*>(W));
+  } else {
+    f2i::convert_scalar_kernel<<<blocks, 256, 0, s>>>(R, n, m, static_cast<float2*>(U), static_cast<float2*>(W));
+  }
+  return check_launch("convert launch");
+}
+
+fairy2i_status fairy2i_quantize(const void* U, const void* W, int64_t n, int64_t m, int32_t T,
+                                const fairy2i_packed* out, void* stream) {
+  if (!U || !W) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL weight pointer");
+  if (!aligned(U, 8) || !aligned(W, 8)) return fail(FAIRY2I_ERR_INVALID_ARG, "U and W must be 8-byte aligned");
+  fairy2i_status st = check_packed(out);
+  if (st != FAIRY2I_OK) return st;
+  if (out->n != n || out->m != m || out->T != T)
+    return fail(FAIRY2I_ERR_SHAPE, "descriptor (n=%lld, m=%lld, T=%d) does not match the call (n=%lld, m=%lld, T=%d)",
+                (long long)out->n, (long long)out->m, out->T, (long long)n, (long long)m, T);
+  if (n > INT32_MAX) return fail(FAIRY2I_ERR_UNSUPPORTED, "n too large");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((n & 7) != 0) {  // padding rows of the last row group stay zero
+    cudaError_t e = cudaMemsetAsync(out->codes, 0, fairy2i_codes_bytes(n, m, T), s);
+    if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "memset codes: %s", cudaGetErrorString(e));
+  }
+  const size_t smem = (size_t)m * (sizeof(float2) + 1);
+  st = ensure_smem(reinterpret_cast<const void*>(f2i::quantize_rows_kernel), smem, "quantize");
+  if (st != FAIRY2I_OK) return st;
+  dim3 grid((unsigned)n, 2);
+  f2i::quantize_rows_kernel<<<grid, f2i::kQuantThreads, smem, s>>>(
+      static_cast<const float2*>(U), static_cast<const float2*>(W), n, m, T, static_cast<uint8_t*>(out->codes),
+      out->scales);
+  return check_launch("quantize launch");
+}
+
+fairy2i_status fairy2i_linear_ex(const fairy2i_packed* q, const void* x, int64_t M, float* y, fairy2i_algo algo,
+                                 void* stream) {
+  if (!q) return fail(FAIRY2I_ERR_INVALID_ARG, "packed descriptor is NULL");
+  const void* xs[1] = {x};
+  float* ys[1] = {y};
+  return linear_group_impl(q, xs, ys, 1, M, algo, static_cast<cudaStream_t>(stream));
+}
+
+fairy2i_status fairy2i_linear(const fairy2i_packed* q, const void* x, int64_t M, float* y, void* stream) {
+  return fairy2i_linear_ex(q, x, M, y, FAIRY2I_ALGO_AUTO, stream);
+}
+
+fairy2i_status fairy2i_linear_group(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int32_t count,
+                                    int64_t M, fairy2i_algo algo, void* stream) {
+  return linear_group_impl(qs, xs, ys, count, M, algo, static_cast<cudaStream_t>(stream));
+}
+
+fairy2i_status fairy2i_unpack_codes(const fairy2i_packed* q, uint8_t* codes_out, void* stream) {
+  fairy2i_status st = check_packed(q);
+  if (st != FAIRY2I_OK) return st;
+  if (!codes_out) return fail(FAIRY2I_ERR_INVALID_ARG, "codes_out is NULL");
+  f2i::unpack_codes_kernel<<<sm_count() * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint8_t*>(q->codes), q->n, q->m, q->T, codes_out);
+  return check_launch("unpack launch");
+}
+
+fairy2i_status fairy2i_sync_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  unsigned word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_fairy2i_error_word, sizeof(word));
+  if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "read error word: %s", cudaGetErrorString(e));
+  if (word != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_fairy2i_error_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "clear error word: %s", cudaGetErrorString(e));
+  }
+  if (word & f2i::kErrNonFinite) return fail(FAIRY2I_ERR_NONFINITE, "non-finite weight seen by quantize");
+  if (word & f2i::kErrTimeout) return fail(FAIRY2I_ERR_TIMEOUT, "a bounded device wait gave up");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,169 @@
+/*
+ * fairy2i.h -- C ABI of the Fairy2i widely-linear 2-bit complex linear layer
+ * for NVIDIA B300 (sm_103a).
+ *
+ * The layer ("Fairy2i-W2" model card, section "Widely-linear transformation";
+ * "Fairy2i: Ultra-Low-Bit LLM Quantization Using Complex Weights {±1, ±i}",
+ * Step 1) is
+ *
+ *        y = U x + W conj(x),      U, W complex n x m,  x complex m-vector,
+ *
+ * the exact complex rewrite of a real PyTorch-style linear weight R of shape
+ * [2n, 2m] acting on the real activation row [Re x | Im x].  U and W are each
+ * stored as T recursive-residual stages (same page, Step 3) of 2-bit phase
+ * codes in {+1, -1, +i, -i} (Step 2) with one real-axis and one
+ * imaginary-axis scale per output row and stage.
+ *
+ * Conventions for every call:
+ *   - Every tensor pointer is a DEVICE pointer on the current CUDA device,
+ *     allocated and owned by the caller.  The library allocates nothing.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream: the returned status
+ *     covers argument checks and the kernel launch only.
+ *   - Errors a kernel detects (non-finite weights, a bounded wait that gave
+ *     up) set a per-device error word that fairy2i_sync_status() reads.
+ *   - On any status other than FAIRY2I_OK nothing was launched (or the launch
+ *     failed) and fairy2i_last_error() returns a message for this thread.
+ *   - Layouts are row-major (C order).
+ */
+#ifndef FAIRY2I_H
+#define FAIRY2I_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FAIRY2I_OK = 0,
+    FAIRY2I_ERR_INVALID_ARG = 1, /* null or misaligned pointer, negative size, bad enum */
+    FAIRY2I_ERR_SHAPE = 2,       /* odd real dimension, empty matrix, size mismatch */
+    FAIRY2I_ERR_NONFINITE = 3,   /* NaN or Inf among the weights given to quantize */
+    FAIRY2I_ERR_UNSUPPORTED = 4, /* T outside [1, 8], m above 16384, token count too large */
+    FAIRY2I_ERR_CUDA = 5,        /* a CUDA call failed; see fairy2i_last_error() */
+    FAIRY2I_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up */
+} fairy2i_status;
+
+#define FAIRY2I_LAYOUT_VERSION 1
+#define FAIRY2I_MAX_T 8
+#define FAIRY2I_MAX_M 16384
+
+/* Packed quantized layer (both U and W).
+ *
+ * codes: FAIRY2I_LAYOUT_VERSION 1 layout, fairy2i_codes_bytes(n, m, T)
+ *   bytes, 256-byte aligned.  2T code planes, plane (X, t) for X = 0 (U),
+ *   1 (W) at byte offset (X*T + t) * plane_bytes with plane_bytes =
+ *   ceil(n/8) * ceil(m/64) * 128.  Inside a plane, rows come in groups of 8
+ *   and columns in blocks of 64; each (row group, column block) is 32
+ *   little-endian 32-bit words, word (4g + q) holding 16 codes of row
+ *   8*group + g: byte i, bit pair p (bits 7-2p and 6-2p) is the code of
+ *   column 64*block + 16p + 4q + i as (sign, real-axis flag) -- sign 1 means
+ *   negative, flag 1 means the code is +-1, flag 0 means +-i.  Within a row
+ *   group, blocks are stored in chunks of four so that a thread's words for
+ *   four consecutive blocks are 16 contiguous bytes (a tail chunk holds the
+ *   remaining 1-3 blocks the same way).  Padding rows and columns hold zero
+ *   bits.  The layout is opaque to callers; fairy2i_unpack_codes() gives the
+ *   canonical view.
+ * scales: fairy2i_scales_count(n, T) floats, [2 (U, W)][T][2 (real axis,
+ *   imaginary axis)][n], 16-byte aligned. */
+typedef struct {
+    int32_t version; /* must be FAIRY2I_LAYOUT_VERSION */
+    int32_t T;       /* number of residual stages, 1..FAIRY2I_MAX_T */
+    int64_t n;       /* complex output rows (real rows 2n) */
+    int64_t m;       /* complex input columns (real columns 2m), 1..FAIRY2I_MAX_M */
+    void *codes;     /* device, caller-owned */
+    float *scales;   /* device, caller-owned */
+} fairy2i_packed;
+
+/* Algorithm choice for fairy2i_linear_ex / fairy2i_linear_group. */
+typedef enum {
+    FAIRY2I_ALGO_AUTO = 0,    /* pick the fastest kernel for the token count */
+    FAIRY2I_ALGO_ADDSUB = 1,  /* CUDA cores: adds/subtracts only, fp32 accumulation */
+    FAIRY2I_ALGO_MMA_FP8 = 2, /* decode: codes expanded to e4m3 {+-2, +-0} in registers, mma.sync */
+    FAIRY2I_ALGO_TCGEN05 = 3  /* prefill: codes expanded to bf16 in shared memory, tcgen05.mma */
+} fairy2i_algo;
+
+/* Bytes of the code planes of an n x m layer with T stages (0 on bad input). */
+size_t fairy2i_codes_bytes(int64_t n, int64_t m, int32_t T);
+
+/* Number of fp32 scales, 4 * T * n (0 on bad input). */
+size_t fairy2i_scales_count(int64_t n, int32_t T);
+
+/* Widely-linear conversion (Theorem 1; "Fairy2i: Ultra-Low-Bit ...", Step 1):
+ *   Re U = (R11 + R22)/2, Im U = (R21 - R12)/2,
+ *   Re W = (R11 - R22)/2, Im W = (R12 + R21)/2,
+ * R11 = R[0:n, 0:m], R12 = R[0:n, m:2m], R21 = R[n:2n, 0:m], R22 = R[n:2n, m:2m].
+ *   R      : device float32 [rows][cols] = [2n][2m], 16-byte aligned
+ *   U, W   : device complex64 (float32 re, im pairs) [n][m], 16-byte aligned
+ * Each output is the float32 sum rounded once, then halved (exact).
+ * Errors: FAIRY2I_ERR_SHAPE for odd or non-positive rows/cols; INVALID_ARG for
+ * null or misaligned pointers. */
+fairy2i_status fairy2i_convert(const float *R, int64_t rows, int64_t cols,
+                               void *U, void *W, void *stream);
+
+/* Phase-aware recursive residual quantization ("Fairy2i: Ultra-Low-Bit ...",
+ * Step 2 and Step 3; "Fairy2i-W2" card, "Phase-aware complex quantization",
+ * "Recursive residual quantization").  For each of U and W separately,
+ * r^(0) = the matrix, and for t = 0..T-1:
+ *   code   = argmax over s in {+1,-1,+i,-i} of Re(r conj(s)), first maximum
+ *            in that order (so |Re r| >= |Im r| picks the real axis);
+ *   s_re   = mean |Re r| over the row's real-coded entries, s_im = mean |Im r|
+ *            over its imaginary-coded entries (0 if none), computed exactly
+ *            (64-bit integer sum of |v| * 2^(48-e), e the exponent of the
+ *            row-axis maximum, then one double division, rounded to float);
+ *   r     <- r - (s_re b_re + i s_im b_im), float32, one rounding.
+ *   U, W   : device complex64 [n][m] (e.g. from fairy2i_convert)
+ *   out    : host descriptor; out->n, out->m, out->T, out->version must match
+ *            the call, out->codes and out->scales receive the result.
+ * Non-finite weights set FAIRY2I_ERR_NONFINITE in the device error word
+ * (read it with fairy2i_sync_status); the codes are then unspecified.
+ * Errors: SHAPE (n, m < 1 or descriptor mismatch), UNSUPPORTED (T outside
+ * [1, 8] or m > 16384), INVALID_ARG (null/misaligned pointers). */
+fairy2i_status fairy2i_quantize(const void *U, const void *W, int64_t n, int64_t m,
+                                int32_t T, const fairy2i_packed *out, void *stream);
+
+/* The layer on a batch of tokens ("Fairy2i-W2" card, y = Ux + W conj(x);
+ * "Fairy2i: Ultra-Low-Bit ...", "Industry implications: multiplication-free
+ * inference"):
+ *   y = sum over stages t of  [ s_re A_re + i s_im A_im ]_U
+ *                           + [ s_re conj(A_re) + i s_im conj(A_im) ]_W,
+ * A_re = (signed) sum of x over real-coded columns, A_im over
+ * imaginary-coded columns.
+ *   x : device bfloat16 [M][2m], each token's row is [Re x | Im x] (the real
+ *       activation row of the original layer), 16-byte aligned
+ *   y : device float32 [M][2n], each row [Re y | Im y], 16-byte aligned
+ * M = 0 is a no-op.  fairy2i_linear uses FAIRY2I_ALGO_AUTO.
+ * Errors: INVALID_ARG (null/misaligned/bad version), SHAPE, UNSUPPORTED. */
+fairy2i_status fairy2i_linear(const fairy2i_packed *q, const void *x, int64_t M,
+                              float *y, void *stream);
+fairy2i_status fairy2i_linear_ex(const fairy2i_packed *q, const void *x, int64_t M,
+                                 float *y, fairy2i_algo algo, void *stream);
+
+/* Several independent layers evaluated by one launch (same token count M,
+ * each with its own x and y), e.g. the seven projections of a decoder block.
+ * qs, xs, ys are HOST arrays of `count` entries (1..256). */
+fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const *xs,
+                                    float *const *ys, int32_t count, int64_t M,
+                                    fairy2i_algo algo, void *stream);
+
+/* Canonical view of the codes: device uint8 [2 (U, W)][T][n][m] with values
+ * 0 = +1, 1 = -1, 2 = +i, 3 = -i. */
+fairy2i_status fairy2i_unpack_codes(const fairy2i_packed *q, uint8_t *codes_out, void *stream);
+
+/* Synchronize `stream`, then read and clear this device's error word.
+ * Returns FAIRY2I_OK, FAIRY2I_ERR_NONFINITE, FAIRY2I_ERR_TIMEOUT or
+ * FAIRY2I_ERR_CUDA. */
+fairy2i_status fairy2i_sync_status(void *stream);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char *fairy2i_last_error(void);
+
+/* FAIRY2I_LAYOUT_VERSION of the library. */
+int32_t fairy2i_layout_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FAIRY2I_H */
