@@ -313,7 +313,7 @@ def run_ours(args, world, rank, local):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 mma (codes {+-2,+-0}, bf16 x split hi/lo), fp32 accumulate",
+        "vs_baseline": None, "dtype": "bf16 mma.sync (codes as bf16 {+-2,+-0}, bf16 x), fp32 accumulate",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "T": T_STAGES, "blocks": BLOCKS, "projections": 7 * BLOCKS,
                    "bytes_per_step": bytes_per_step, "l2": "inputs larger than L2 (1.64 GB working set)",
@@ -322,7 +322,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": BLOCKS * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                     "kernel": "linear_mma_fp8_kernel<4,1,4>", "bytes_per_launch": bytes_per_block,
+                     "kernel": "linear_mma_kernel<4,1> (mma.sync bf16)", "bytes_per_launch": bytes_per_block,
                      "launch_us": launch_ms * 1e3, "peak_source": peaks["source"],
                      "frac_of_nominal_8TBps": achieved / 8000.0},
         "clocks": clk.summary(),

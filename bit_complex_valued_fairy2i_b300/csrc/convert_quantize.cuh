@@ -206,19 +206,16 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(
       row[k] = v;
     }
 
-    // pack: word (kb, q) of row g holds columns 64 kb + 16 p + 4 q + i
+    // pack: word (kb, q) of row g holds the 16 columns 64 kb + code_col(c, q)
     uint8_t* plane = codes + (int64_t)(X * T + t) * pbytes;
     for (int64_t w = tid; w < KB * 4; w += kQuantThreads) {
       const int64_t kb = w >> 2;
       const int q = (int)(w & 3);
       uint32_t word = 0;
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int64_t k = kb * 64 + 16 * p + 4 * q + i;
-          if (k < m) word |= (uint32_t)cbits[k] << code_shift(i, p);
-        }
+      for (int c = 0; c < 16; ++c) {
+        const int64_t k = kb * 64 + code_col(c, q);
+        if (k < m) word |= (uint32_t)cbits[k] << code_shift(c);
       }
       *reinterpret_cast<uint32_t*>(plane + word_offset(rg, kb, 4 * g + q, KB)) = word;
     }
@@ -250,12 +247,10 @@ __global__ void __launch_bounds__(256) unpack_codes_kernel(const uint8_t* __rest
     const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + plane * pbytes + word_offset(rg, kb, lane, KB));
     uint8_t* dst = out + (plane * n + j) * m;
 #pragma unroll
-    for (int p = 0; p < 4; ++p)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int64_t k = kb * 64 + 16 * p + 4 * q + i;
-        if (k < m) dst[k] = (uint8_t)canonical_from_bits((w >> code_shift(i, p)) & 3u);
-      }
+    for (int c = 0; c < 16; ++c) {
+      const int64_t k = kb * 64 + code_col(c, q);
+      if (k < m) dst[k] = (uint8_t)canonical_from_bits((w >> code_shift(c)) & 3u);
+    }
   }
 }
 

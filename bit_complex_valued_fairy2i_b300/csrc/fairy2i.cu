@@ -53,7 +53,7 @@ std::mutex g_attr_mu;
 std::vector<SmemAttr> g_attr;
 
 fairy2i_status ensure_smem(const void* fn, size_t smem, const char* what) {
-  if (smem <= 48 * 1024) return FAIRY2I_OK;
+  if (smem <= 32 * 1024) return FAIRY2I_OK;  // well inside the default limit, static smem included
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(g_attr_mu);
@@ -89,8 +89,6 @@ fairy2i_status check_packed(const fairy2i_packed* q) {
 
 // --- decode launch helpers --------------------------------------------------
 
-constexpr int kMmaRgc = 1;  // row groups in flight per CTA in the fp8 decode kernel
-
 // Resident CTAs per SM for a kernel at a given dynamic shared memory size,
 // cached per (kernel, device, bytes).
 struct OccEntry {
@@ -114,10 +112,10 @@ int resident_ctas(const void* fn, int threads, size_t smem) {
   return nb;
 }
 
-// Persistent partition: `slots` CTAs shared among the problems in proportion
-// to their bytes; every CTA of a problem owns rg_per_cta consecutive row
-// groups (a multiple of rgc).  Returns the number of CTAs.
-int partition(f2i::LinearGroup& G, int slots, int rgc) {
+// Decode partition: `slots` resident CTAs shared among the problems in
+// proportion to their bytes; every CTA of a problem owns rg_per_cta
+// (<= rpc_max) consecutive row groups.  Returns the number of CTAs.
+int partition(f2i::LinearGroup& G, int slots, int rpc_max) {
   double total = 0.0;
   for (int i = 0; i < G.count; ++i)
     total += (double)f2i::row_groups(G.p[i].n) * (double)f2i::col_blocks(G.p[i].m);
@@ -125,9 +123,8 @@ int partition(f2i::LinearGroup& G, int slots, int rgc) {
   for (int i = 0; i < G.count; ++i) {
     const int64_t RG = f2i::row_groups(G.p[i].n);
     const double share = (double)RG * (double)f2i::col_blocks(G.p[i].m) / total;
-    int64_t want = std::max<int64_t>(1, (int64_t)(slots * share));
-    int64_t rpc = (RG + want - 1) / want;
-    rpc = ((rpc + rgc - 1) / rgc) * rgc;
+    const int64_t want = std::max<int64_t>(1, (int64_t)(slots * share));
+    const int64_t rpc = std::max<int64_t>(1, std::min<int64_t>(rpc_max, (RG + want - 1) / want));
     G.p[i].cta_begin = ctas;
     G.p[i].rg_per_cta = (int32_t)rpc;
     ctas += (int)((RG + rpc - 1) / rpc);
@@ -136,41 +133,44 @@ int partition(f2i::LinearGroup& G, int slots, int rgc) {
 }
 
 template <int NPL, int TILES>
-fairy2i_status launch_mma_t(f2i::LinearGroup& G, size_t smem, cudaStream_t s) {
-  auto k = f2i::linear_mma_fp8_kernel<NPL, TILES, kMmaRgc>;
+fairy2i_status launch_mma_t(f2i::LinearGroup& G, size_t smem, int rpc_max, cudaStream_t s) {
+  auto k = f2i::linear_mma_kernel<NPL, TILES>;
   const void* fn = reinterpret_cast<const void*>(k);
   fairy2i_status st = ensure_smem(fn, smem, "mma decode");
   if (st != FAIRY2I_OK) return st;
   const int slots = sm_count() * resident_ctas(fn, f2i::kMmaWarps * 32, smem);
-  const int ctas = partition(G, slots, kMmaRgc);
+  const int ctas = partition(G, slots, rpc_max);
   k<<<ctas, f2i::kMmaWarps * 32, smem, s>>>(G);
   return check_launch("mma decode launch");
 }
 
 template <int NPL>
-fairy2i_status launch_mma_tiles(f2i::LinearGroup& G, int tiles, size_t smem, cudaStream_t s) {
-  switch (tiles) {
-    case 1: return launch_mma_t<NPL, 1>(G, smem, s);
-    case 2: return launch_mma_t<NPL, 2>(G, smem, s);
-    default: return launch_mma_t<NPL, 4>(G, smem, s);
-  }
+fairy2i_status launch_mma_tiles(f2i::LinearGroup& G, int tiles, size_t smem, int rpc_max, cudaStream_t s) {
+  return tiles == 1 ? launch_mma_t<NPL, 1>(G, smem, rpc_max, s) : launch_mma_t<NPL, 2>(G, smem, rpc_max, s);
 }
 
-// One launch of the fp8 mma decode for up to 8 tokens of every problem in G.
+// One launch of the bf16 mma decode for up to 8 tokens of every problem in
+// G.  Shared memory: the staged activations ([M][2][x_stride] bfloat16) and
+// the per-warp partial outputs of up to rpc_max row groups.
+constexpr int kMmaTokens = 8;
+
 fairy2i_status run_mma(f2i::LinearGroup& G, int T, cudaStream_t s) {
-  const int tiles_needed = (G.M + 1) / 2;
-  const int tiles = tiles_needed <= 1 ? 1 : tiles_needed <= 2 ? 2 : 4;
-  int64_t m_pad_max = 0;
-  for (int i = 0; i < G.count; ++i) m_pad_max = std::max(m_pad_max, f2i::col_blocks(G.p[i].m) * 64);
-  const size_t smem = (size_t)tiles * 8 * m_pad_max + (size_t)f2i::kMmaWarps * tiles * 2 * 32 * sizeof(float);
-  if (smem > 227 * 1024)
-    return fail(FAIRY2I_ERR_UNSUPPORTED, "fp8 decode needs %zu bytes of shared memory", smem);
+  const int tiles = G.M <= 4 ? 1 : 2;
+  int64_t xstr_max = 0;
+  for (int i = 0; i < G.count; ++i) xstr_max = std::max(xstr_max, f2i::x_stride(G.p[i].m));
+  const size_t xbytes = (((size_t)G.M * 2 * xstr_max * sizeof(uint16_t)) + 15) & ~(size_t)15;
+  const size_t per_rg = (size_t)f2i::kMmaWarps * tiles * 32 * sizeof(float2);
+  const size_t limit = 200 * 1024;
+  if (xbytes + per_rg > limit)
+    return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode: staged activations need %zu bytes of shared memory", xbytes);
+  const int rpc_max = (int)std::min<size_t>(f2i::kMaxRowGroupsPerCta, (limit - xbytes) / per_rg);
+  const size_t smem = xbytes + (size_t)rpc_max * per_rg;
   switch (T) {
-    case 1: return launch_mma_tiles<2>(G, tiles, smem, s);
-    case 2: return launch_mma_tiles<4>(G, tiles, smem, s);
-    case 3: return launch_mma_tiles<6>(G, tiles, smem, s);
-    case 4: return launch_mma_tiles<8>(G, tiles, smem, s);
-    default: return fail(FAIRY2I_ERR_UNSUPPORTED, "fp8 decode supports T <= 4 (got %d)", T);
+    case 1: return launch_mma_tiles<2>(G, tiles, smem, rpc_max, s);
+    case 2: return launch_mma_tiles<4>(G, tiles, smem, rpc_max, s);
+    case 3: return launch_mma_tiles<6>(G, tiles, smem, rpc_max, s);
+    case 4: return launch_mma_tiles<8>(G, tiles, smem, rpc_max, s);
+    default: return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode supports T <= 4 (got %d)", T);
   }
 }
 
@@ -210,11 +210,11 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
   if (M > (int64_t)1 << 30) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
 
   fairy2i_algo a = algo;
-  if (a == FAIRY2I_ALGO_AUTO) a = (T <= 4) ? FAIRY2I_ALGO_MMA_FP8 : FAIRY2I_ALGO_ADDSUB;
+  if (a == FAIRY2I_ALGO_AUTO) a = (T <= 4) ? FAIRY2I_ALGO_MMA : FAIRY2I_ALGO_ADDSUB;
   if (a == FAIRY2I_ALGO_TCGEN05) return fail(FAIRY2I_ERR_UNSUPPORTED, "tcgen05 prefill path not built yet");
-  if (a == FAIRY2I_ALGO_MMA_FP8 && T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "fp8 decode supports T <= 4");
+  if (a == FAIRY2I_ALGO_MMA && T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode supports T <= 4");
 
-  const int chunk = (a == FAIRY2I_ALGO_MMA_FP8) ? 8 : f2i::kAddSubTok * 1024;
+  const int chunk = (a == FAIRY2I_ALGO_MMA) ? kMmaTokens : f2i::kAddSubTok * 1024;
   for (int p0 = 0; p0 < count; p0 += f2i::kMaxGroup) {
     const int cnt = std::min(f2i::kMaxGroup, count - p0);
     for (int64_t t0 = 0; t0 < M; t0 += chunk) {
@@ -233,7 +233,7 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
         P.m = q.m;
         P.T = q.T;
       }
-      fairy2i_status st = (a == FAIRY2I_ALGO_MMA_FP8) ? run_mma(G, T, s) : run_addsub(G, s);
+      fairy2i_status st = (a == FAIRY2I_ALGO_MMA) ? run_mma(G, T, s) : run_addsub(G, s);
       if (st != FAIRY2I_OK) return st;
     }
   }

@@ -3,15 +3,19 @@
 // A code plane (one matrix U or W, one stage t) of an n x m layer:
 //   rows in groups of 8 (row group rg = j / 8, g = j % 8),
 //   columns in blocks of 64 (block kb = k / 64),
-//   one 128-byte tile of 32 words per (rg, kb); word (4g + q) holds the 16
-//   codes of row j at columns 64 kb + 16 p + 4 q + i, p, i in [0, 4):
-//   byte i, bits (7 - 2p, 6 - 2p) = (sign, real-axis flag).
-// This places, for an mma.sync m16n8k32 A fragment in which row g is the
-// real-axis row of output j and row g + 8 its imaginary-axis row, the four
-// codes of one fragment register in the top two bits of the register's
-// bytes, so that `word & 0xC0C0C0C0` is the real-axis operand and
-// `(word & 0x80808080) | (~word & 0x40404040)` the imaginary-axis operand,
-// both as e4m3 values in {+2, -2, +0, -0}.
+//   one 128-byte tile of 32 words per (rg, kb); word (4g + q) holds 16 codes
+//   of row j, each as two bits (sign, real-axis flag).
+// Code c = 0..15 of a word, with s = c >> 2, h = (c >> 1) & 1, e = c & 1,
+// is column  64 kb + 16 s + 8 h + 2 q + e  and sits in bits
+// (15 + 16 e - 2 P, 14 + 16 e - 2 P) with P = 2 s + h.
+// Why: in an mma.sync m16n8k16 bf16 A fragment whose row g is the real-axis
+// row of output 8 rg + g and row g + 8 its imaginary-axis row, lane (g, q)
+// holds for step s the columns 16 s + 2 q + {0, 1} (P = 2 s) and
+// 16 s + 8 + 2 q + {0, 1} (P = 2 s + 1), two per register, low column in
+// the low half.  Shifting the word left by 2 P puts both codes of pair P in
+// bits (15, 14) and (31, 30); then `& 0xC000C000` is the real-axis register
+// and `(w & 0x80008000) | (~w & 0x40004000)` the imaginary-axis register,
+// as bfloat16 values in {+2, -2, +0, -0} (2.0 = 0x4000).
 // Within a row group the 128-byte tiles are stored in chunks of four blocks
 // so that lane (4g + q) finds its words of four consecutive blocks in 16
 // contiguous bytes; the last chunk holds the remaining r = KB % 4 blocks
@@ -42,8 +46,14 @@ __host__ __device__ __forceinline__ int64_t word_offset(int64_t rg, int64_t kb, 
   return base + full * 512 + lane * (4 * r) + (kb - (full << 2)) * 4;
 }
 
-// Shift that brings the code of (byte i, bit pair p) to bits 1..0.
-__host__ __device__ __forceinline__ int code_shift(int i, int p) { return 8 * i + 6 - 2 * p; }
+// Column offset inside the 64-column block of code c (0..15) of lane q.
+__host__ __device__ __forceinline__ int code_col(int c, int q) {
+  return 16 * (c >> 2) + 8 * ((c >> 1) & 1) + 2 * q + (c & 1);
+}
+// Shift that brings code c (0..15) of a word to bits 1..0.
+__host__ __device__ __forceinline__ int code_shift(int c) {
+  return 14 + 16 * (c & 1) - 2 * (2 * (c >> 2) + ((c >> 1) & 1));
+}
 
 // 2-bit internal code (sign << 1 | real_flag)  <->  canonical 0..3
 // (0 = +1, 1 = -1, 2 = +i, 3 = -i).

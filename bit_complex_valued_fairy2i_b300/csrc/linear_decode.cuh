@@ -14,8 +14,6 @@
 // real-coded / imaginary-coded columns.
 #pragma once
 #include <cstdint>
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include "layout.cuh"
 
 namespace f2i {
@@ -30,7 +28,7 @@ struct LinearProblem {
   int64_t n, m;
   int32_t T;
   int32_t cta_begin;   // first CTA of this problem in the launch
-  int32_t rg_per_cta;  // row groups per CTA (persistent partition)
+  int32_t rg_per_cta;  // row groups per CTA (decode partition)
   int32_t pad_;
 };
 
@@ -46,9 +44,6 @@ __device__ __forceinline__ int find_problem(const LinearGroup& G) {
     if ((int)blockIdx.x >= G.p[i].cta_begin) pi = i;
   return pi;
 }
-
-__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 // Words of lane `lane` for chunk c (column blocks 4c .. 4c+3) of row group rg
 // in one plane; nb = number of valid blocks (4 except in the tail chunk).
@@ -75,7 +70,7 @@ __device__ __forceinline__ uint32_t word_of(const uint4& w, int b) {
   return b == 0 ? w.x : b == 1 ? w.y : b == 2 ? w.z : w.w;
 }
 
-// Adds y contributions of one plane for one token: ra/rb = <re-row, a/b>,
+// Adds the y contributions of one plane for one token: ra/rb = <re-row, a/b>,
 // ia/ib = <im-row, a/b>.
 __device__ __forceinline__ void plane_epilogue(int X, float s_re, float s_im, float ra, float rb, float ia, float ib,
                                                float& y_re, float& y_im) {
@@ -91,9 +86,9 @@ __device__ __forceinline__ void plane_epilogue(int X, float s_re, float s_im, fl
 // ---------------------------------------------------------------------------
 // ALGO_ADDSUB: CUDA cores, adds and subtracts only (the pages' inference
 // arithmetic taken literally).  One warp per row group (8 rows); lane (g, q)
-// owns row 8 rg + g and the columns 64 kb + 16 p + 4 q + i of every block.
-// x is staged in shared memory as packed bfloat16 (a, b) pairs; each code
-// flips the sign bit of a and b and adds them to the real-axis or the
+// owns row 8 rg + g and the 16 columns of its word in every block.  x is
+// staged in shared memory as packed bfloat16 (a, b) pairs; each code flips
+// the sign bit of a and b and adds them to the real-axis or the
 // imaginary-axis accumulator.  A quad shuffle sums the four lanes of a row.
 // Compute-bound at about 6-8 instructions per code per token.
 // ---------------------------------------------------------------------------
@@ -144,25 +139,22 @@ __global__ void __launch_bounds__(kAddSubWarps * 32) linear_addsub_kernel(const 
         const uint4 wv = load_chunk(pl, rg, c, lane, KB, nb);
         for (int b = 0; b < nb; ++b) {
           const uint32_t w = word_of(wv, b);
-          const int64_t kbase = (4 * c + b) * 64 + 4 * q;
+          const int64_t kbase = (4 * c + b) * 64;
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
+          for (int cc = 0; cc < 16; ++cc) {
+            const uint32_t v = (w >> code_shift(cc)) & 3u;
+            const uint32_t sgn = (v >> 1) << 31;
+            const bool real = v & 1u;
+            const int64_t k = kbase + code_col(cc, q);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t v = (w >> code_shift(i, p)) & 3u;
-              const uint32_t sgn = (v >> 1) << 31;
-              const bool real = v & 1u;
-              const int64_t k = kbase + 16 * p + i;
-#pragma unroll
-              for (int tk = 0; tk < kAddSubTok; ++tk) {
-                const uint32_t xv = xs[tk * m_pad + k];
-                const float a = __uint_as_float((xv << 16) ^ sgn);
-                const float bb = __uint_as_float((xv & 0xFFFF0000u) ^ sgn);
-                acc[tk][0] += real ? a : 0.0f;
-                acc[tk][1] += real ? bb : 0.0f;
-                acc[tk][2] += real ? 0.0f : a;
-                acc[tk][3] += real ? 0.0f : bb;
-              }
+            for (int tk = 0; tk < kAddSubTok; ++tk) {
+              const uint32_t xv = xs[tk * m_pad + k];
+              const float a = __uint_as_float((xv << 16) ^ sgn);
+              const float bb = __uint_as_float((xv & 0xFFFF0000u) ^ sgn);
+              acc[tk][0] += real ? a : 0.0f;
+              acc[tk][1] += real ? bb : 0.0f;
+              acc[tk][2] += real ? 0.0f : a;
+              acc[tk][3] += real ? 0.0f : bb;
             }
           }
         }
@@ -193,322 +185,259 @@ __global__ void __launch_bounds__(kAddSubWarps * 32) linear_addsub_kernel(const 
 }
 
 // ---------------------------------------------------------------------------
-// ALGO_MMA_FP8: tensor-core decode.  The same signed sums, computed by
-// mma.sync m16n8k32 with e4m3 operands:
-//   A (16 x 32): rows g = real-axis row of output 8 rg + g, rows g + 8 = its
-//     imaginary-axis row; entries {+2, -2, +0, -0} made from the packed codes
-//     by one LOP3 per four codes (bits (7,6) of a byte are (sign, real flag):
-//     `w & 0xC0C0C0C0` keeps +-2 on real-coded columns, the complementary
-//     LOP3 keeps +-2 on imaginary-coded ones).
-//   B (32 x 8): columns = (token, part in {a, b}, hi/lo) for two tokens; the
-//     bfloat16 x of each (token, part) is scaled by a power of two 2^s so its
-//     largest magnitude lands in [128, 256) and split exactly into
-//     hi = e4m3(x 2^s) and lo = e4m3(16 (x 2^s - hi)).
-//   D (16 x 8): fp32.  <row, x_part> = 2^-s (D_hi + D_lo / 16) / 2.
-//
-// Persistent partition: the host gives each problem of the launch a number of
-// CTAs proportional to its bytes, and each CTA a contiguous run of
-// `rg_per_cta` row groups of one problem, so one launch fills the GPU in a
-// single wave with balanced work and no output row split across CTAs.  Each
-// CTA builds its problem's x fragments once in shared memory, then walks its
-// row groups RGC at a time, the KS = 8 / RGC warps of a row group splitting
-// its column chunks and reducing through shared memory.
+// ALGO_MMA: tensor-core decode with mma.sync m16n8k16 bf16:
+//   A (16 x 16): row g = real-axis row of output 8 rg + g, row g + 8 its
+//     imaginary-axis row; entries {+2, -2, +0, -0} (bfloat16 2.0 = 0x4000),
+//     one shift and two LOP3 per pair of codes (see layout.cuh).
+//   B (16 x 8): column 2 q' + p = part p (0: a = Re x, 1: b = Im x) of token
+//     q' of the tile, taken unchanged from the bfloat16 activations.
+//   D (16 x 8): fp32; lane (g, q) ends with <re-row, a>, <re-row, b>,
+//     <im-row, a>, <im-row, b> of token q, each times 2.  Products of +-2 and
+//     a bfloat16 are exact, so only the fp32 accumulation rounds.
+// Partition: the host gives each problem of the launch a number of CTAs in
+// proportion to its bytes and each CTA a run of `rg_per_cta` row groups, so
+// that one wave fills the GPU with no output row split across CTAs.  The 8
+// warps of a CTA split its (row group, column chunk) items evenly, stream
+// the 2T code planes with 16-byte loads two items ahead, fold each row
+// group's share into per-warp partial outputs in shared memory, and one
+// fixed-order sum at the end writes y (bitwise reproducible).
 // ---------------------------------------------------------------------------
 constexpr int kMmaWarps = 8;
+constexpr int kMaxRowGroupsPerCta = 16;
 
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint2 b) {
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Imaginary-axis operand: keep the sign bit, set the 2.0 exponent bit where
-// the real-axis flag is clear (one LOP3).
-__device__ __forceinline__ uint32_t im_axis_operand(uint32_t w) {
-  return (w & 0x80808080u) | (~w & 0x40404040u);
-}
+// Real-axis operand of the code pair in bits (15,14) / (31,30).
+__device__ __forceinline__ uint32_t re_operand(uint32_t w) { return w & 0xC000C000u; }
+// Imaginary-axis operand: keep the sign, set the 2.0 exponent bit where the
+// real-axis flag is clear (one LOP3).
+__device__ __forceinline__ uint32_t im_operand(uint32_t w) { return (w & 0x80008000u) | (~w & 0x40004000u); }
 
-// Two floats -> two e4m3 (round to nearest even, saturating), low byte = a.
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
-  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-}
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
+// Row stride (bfloat16 elements) of the staged activations: 16 bytes of
+// padding make the 8 (token, part) rows of a tile hit distinct banks.
+__host__ __device__ __forceinline__ int64_t x_stride(int64_t m) { return col_blocks(m) * 64 + 8; }
 
-// hi/lo e4m3 split of 8 consecutive activations (already scaled by 2^s).
-__device__ __forceinline__ void split8(const float (&v)[8], uint32_t (&hi)[2], uint32_t (&lo)[2]) {
-#pragma unroll
-  for (int w = 0; w < 2; ++w) {
-    uint32_t h = 0, l = 0;
-#pragma unroll
-    for (int pr = 0; pr < 2; ++pr) {
-      const float a = v[4 * w + 2 * pr], b = v[4 * w + 2 * pr + 1];
-      const uint32_t hb = e4m3x2(a, b);
-      const float2 hf = e4m3x2_to_float2(hb);
-      const uint32_t lb = e4m3x2((a - hf.x) * 16.0f, (b - hf.y) * 16.0f);
-      h |= hb << (16 * pr);
-      l |= lb << (16 * pr);
-    }
-    hi[w] = h;
-    lo[w] = l;
-  }
-}
-
-template <int TILES>
-struct DecodeSmem {
-  uint32_t absmax[2 * TILES][2];
-  float inv[2 * TILES][2];  // 2^(-s-1) per (token, part)
-  float up[2 * TILES][2];   // 2^s
-};
-
-// Builds the B fragments of x for all column steps in shared memory.
-// xf (uint32 view): word h of lane (4g + q) of step st of tile tl at
-// ((tl * nsteps + st) * 32 + lane) * 2 + h holds column g at rows
-// 32 st + 16 h + 4 q + (0..3).
-template <int TILES>
-__device__ void build_x_fragments(const uint16_t* __restrict__ x, int64_t m, int M, int64_t nsteps,
-                                  uint32_t* xf, DecodeSmem<TILES>& S) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  constexpr int NT = kMmaWarps * 32;
-  const bool vec = (m & 7) == 0 && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
-  // zero fill (padding columns, padding tokens)
-  uint4* z = reinterpret_cast<uint4*>(xf);
-  const int64_t nz = (int64_t)TILES * nsteps * 32 * 2 / 4;
-  for (int64_t i = tid; i < nz; i += NT) z[i] = make_uint4(0, 0, 0, 0);
-  if (tid < 4 * TILES) S.absmax[tid >> 1][tid & 1] = 0;
-  __syncthreads();
-  // largest magnitude per (token, part)
-  for (int tp = 0; tp < 2 * M; ++tp) {
-    const uint16_t* xr = x + (int64_t)(tp >> 1) * 2 * m + (tp & 1) * m;
-    uint32_t mx = 0;
-    if (vec) {
-      for (int64_t k = (int64_t)tid * 8; k < m; k += NT * 8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) mx = max(mx, max(w[u] & 0x7FFFu, (w[u] >> 16) & 0x7FFFu));
-      }
-    } else {
-      for (int64_t k = tid; k < m; k += NT) mx = max(mx, (uint32_t)(xr[k] & 0x7FFFu));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) atomicMax(&S.absmax[tp >> 1][tp & 1], mx);
-  }
-  __syncthreads();
-  if (tid < 4 * TILES) {
-    const uint32_t mb = S.absmax[tid >> 1][tid & 1];
-    const int ef = (int)(mb >> 7);
-    int sh = ef > 0 ? 7 - (ef - 127) : 125;  // largest magnitude -> [128, 256)
-    sh = max(-126, min(125, sh));
-    S.inv[tid >> 1][tid & 1] = __uint_as_float((uint32_t)(126 - sh) << 23);  // 2^(-s-1)
-    S.up[tid >> 1][tid & 1] = __uint_as_float((uint32_t)(127 + sh) << 23);   // 2^s
-  }
-  __syncthreads();
-  // fragments: one work item = (token, part, 8 consecutive columns)
-  const int64_t groups = (m + 7) >> 3;
-  for (int64_t it = tid; it < (int64_t)2 * M * groups; it += NT) {
-    const int tp = (int)(it / groups);
-    const int64_t k0 = (it - (int64_t)tp * groups) << 3;
-    const int tok = tp >> 1, part = tp & 1;
-    const uint16_t* xr = x + (int64_t)tok * 2 * m + part * m;
-    const float up = S.up[tok][part];
-    float v[8];
-    if (vec) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(xr + k0);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        v[2 * u] = __uint_as_float(w[u] << 16) * up;
-        v[2 * u + 1] = __uint_as_float(w[u] & 0xFFFF0000u) * up;
-      }
-    } else {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = (k0 + u < m) ? __uint_as_float((uint32_t)xr[k0 + u] << 16) * up : 0.0f;
-    }
-    uint32_t hi[2], lo[2];
-    split8(v, hi, lo);
-    const int64_t st = k0 >> 5;
-    const int within = (int)(k0 & 31);
-    const int h = within >> 4, q0 = (within & 15) >> 2;
-    const int tl = tok >> 1;
-    const int ghi = 4 * (tok & 1) + 2 * part;
-    uint32_t* base = xf + ((int64_t)tl * nsteps + st) * 64 + h;
-    base[(4 * ghi + q0) * 2] = hi[0];
-    base[(4 * ghi + q0 + 1) * 2] = hi[1];
-    base[(4 * (ghi + 1) + q0) * 2] = lo[0];
-    base[(4 * (ghi + 1) + q0 + 1) * 2] = lo[1];
-  }
-  __syncthreads();
-}
-
-template <int NPL, int TILES, int RGC>
-__global__ void __launch_bounds__(kMmaWarps * 32) linear_mma_fp8_kernel(const __grid_constant__ LinearGroup G) {
-  constexpr int KS = kMmaWarps / RGC;
+template <int NPL, int TILES>
+__global__ void __launch_bounds__(kMmaWarps * 32, (NPL * TILES <= 4) ? 2 : 1)
+    linear_mma_kernel(const __grid_constant__ LinearGroup G) {
   extern __shared__ __align__(16) unsigned char msm[];
-  __shared__ DecodeSmem<TILES> S;
 
   const LinearProblem& P = G.p[find_problem(G)];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, q = lane & 3;
   const int64_t n = P.n, m = P.m;
   const int T = P.T, M = G.M;
-  const int64_t KB = col_blocks(m), m_pad = KB * 64, nsteps = m_pad / 32, RG = row_groups(n);
-  uint32_t* xf = reinterpret_cast<uint32_t*>(msm);  // [TILES][nsteps][32][2]
-  float* red = reinterpret_cast<float*>(msm + (size_t)TILES * nsteps * 32 * sizeof(uint2));
-  const uint2* xf2 = reinterpret_cast<const uint2*>(xf);
-
-  build_x_fragments<TILES>(P.x, m, M, nsteps, xf, S);
-
-  const int rgc = warp % RGC, ks = warp / RGC;
-  const int g = lane >> 2, q = lane & 3;
+  const int64_t KB = col_blocks(m), RG = row_groups(n);
   const int64_t pbytes = plane_bytes(n, m);
-  const int64_t nchunks = (KB + 3) >> 2;
-  const int64_t cps = (nchunks + KS - 1) / KS;
-  const int64_t c0 = ks * cps, c1 = min(nchunks, c0 + cps);
+  const int nch = (int)((KB + 3) >> 2);
   const int64_t rg_begin = (int64_t)(blockIdx.x - P.cta_begin) * P.rg_per_cta;
   const int64_t rg_end = min(RG, rg_begin + P.rg_per_cta);
+  const int niter = (int)(rg_end - rg_begin);
+  const int64_t xstr = x_stride(m);
 
-  // Flat per-warp sequence of (row-group step r, chunk c) items with a
-  // one-item prefetch that runs across row-group boundaries, so the loads of
-  // the next row group are in flight during this one's reduction.
-  const int64_t niter = (rg_end - rg_begin + RGC - 1) / RGC;
-  const bool has_work = c0 < c1;
-  uint4 cur[NPL];
-  int nb = 4;
-  if (has_work && niter > 0 && rg_begin + rgc < rg_end) {
+  uint16_t* xs = reinterpret_cast<uint16_t*>(msm);  // [M][2][xstr]
+  // red: [niter][kMmaWarps][TILES][32 lanes] x (re, im)
+  float2* red = reinterpret_cast<float2*>(msm + (((size_t)M * 2 * xstr * sizeof(uint16_t) + 15) & ~(size_t)15));
+
+  // This warp's contiguous share of the CTA's (row group, chunk) items,
+  // walked with incremental counters.
+  const int items = niter * nch;
+  const int i0 = (int)((int64_t)items * warp / kMmaWarps), i1 = (int)((int64_t)items * (warp + 1) / kMmaWarps);
+  const int full = (int)(KB >> 2);
+  const int tail = (int)(KB - 4 * full);
+  const uint32_t row_stride = (uint32_t)KB * kTileBytes;
+  const uint32_t lane16 = (uint32_t)lane * 16u;
+  const uint32_t tail_off = (uint32_t)full * 512u + (uint32_t)lane * 4u * (uint32_t)tail;
+  const uint8_t* plane0 = P.codes + rg_begin * (int64_t)row_stride;
+
+  auto load_at = [&](int r, int c, uint4 (&dst)[NPL]) {
+    const uint32_t off = (uint32_t)r * row_stride + (c < full ? (uint32_t)c * 512u + lane16 : tail_off);
 #pragma unroll
-    for (int pl = 0; pl < NPL; ++pl) cur[pl] = load_chunk(P.codes + pl * pbytes, rg_begin + rgc, c0, lane, KB, nb);
+    for (int pl = 0; pl < NPL; ++pl) {
+      const uint8_t* a = plane0 + pl * pbytes + off;
+      if (c < full) {
+        dst[pl] = __ldcs(reinterpret_cast<const uint4*>(a));
+      } else {
+        const uint32_t* t = reinterpret_cast<const uint32_t*>(a);
+        dst[pl].x = __ldcs(t);
+        dst[pl].y = tail > 1 ? __ldcs(t + 1) : 0u;
+        dst[pl].z = tail > 2 ? __ldcs(t + 2) : 0u;
+        dst[pl].w = 0u;
+      }
+    }
+  };
+  auto advance = [&](int& r, int& c) {
+    if (++c == nch) {
+      c = 0;
+      ++r;
+    }
+  };
+
+  // Start streaming codes before staging the activations.
+  int rc = i0 / nch, cc = i0 - (i0 / nch) * nch;  // item being processed
+  int rl = rc, cl = cc;                           // next item to load
+  uint4 cur[NPL], nx1[NPL];
+  if (i0 < i1) {
+    load_at(rl, cl, cur);
+    advance(rl, cl);
   }
-  for (int64_t r = 0; r < niter; ++r) {
-    const int64_t rg = rg_begin + r * RGC + rgc;
-    const int64_t j = rg * 8 + g;
-    const bool active = has_work && rg < rg_end;
-    float y_re[TILES], y_im[TILES];
-#pragma unroll
-    for (int tl = 0; tl < TILES; ++tl) y_re[tl] = y_im[tl] = 0.0f;
+  if (i0 + 1 < i1) {
+    load_at(rl, cl, nx1);
+    advance(rl, cl);
+  }
 
-    if (active) {
-      float acc[NPL][TILES][4];
-#pragma unroll
-      for (int pl = 0; pl < NPL; ++pl)
-#pragma unroll
-        for (int tl = 0; tl < TILES; ++tl) acc[pl][tl][0] = acc[pl][tl][1] = acc[pl][tl][2] = acc[pl][tl][3] = 0.0f;
-
-      for (int64_t c = c0; c < c1; ++c) {
-        // next item: (r, c + 1), else (r + 1, c0) when that row group exists
-        uint4 nxt[NPL];
-        int nbn = 4;
-        const bool more_here = c + 1 < c1;
-        const int64_t rg_next = rg + RGC;
-        const bool more_next = !more_here && r + 1 < niter && rg_next < rg_end;
-        if (more_here || more_next) {
-          const int64_t rr = more_here ? rg : rg_next;
-          const int64_t cc = more_here ? c + 1 : c0;
-#pragma unroll
-          for (int pl = 0; pl < NPL; ++pl) nxt[pl] = load_chunk(P.codes + pl * pbytes, rr, cc, lane, KB, nbn);
-        }
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          if (b >= nb) break;
-          const int64_t st = 2 * (4 * c + b);
-          uint2 bx0[TILES], bx1[TILES];
-#pragma unroll
-          for (int tl = 0; tl < TILES; ++tl) {
-            bx0[tl] = xf2[((int64_t)tl * nsteps + st) * 32 + lane];
-            bx1[tl] = xf2[((int64_t)tl * nsteps + st + 1) * 32 + lane];
-          }
-#pragma unroll
-          for (int pl = 0; pl < NPL; ++pl) {
-            const uint32_t w0 = word_of(cur[pl], b);
-            const uint32_t w1 = w0 << 2, w2 = w0 << 4, w3 = w0 << 6;
-            const uint32_t r0 = w0 & 0xC0C0C0C0u, r1 = w1 & 0xC0C0C0C0u;
-            const uint32_t r2 = w2 & 0xC0C0C0C0u, r3 = w3 & 0xC0C0C0C0u;
-            const uint32_t i0 = im_axis_operand(w0), i1 = im_axis_operand(w1);
-            const uint32_t i2 = im_axis_operand(w2), i3 = im_axis_operand(w3);
-#pragma unroll
-            for (int tl = 0; tl < TILES; ++tl) {
-              mma_e4m3(acc[pl][tl], r0, i0, r1, i1, bx0[tl]);
-              mma_e4m3(acc[pl][tl], r2, i2, r3, i3, bx1[tl]);
-            }
-          }
-        }
-        if (more_here || more_next) {
-#pragma unroll
-          for (int pl = 0; pl < NPL; ++pl) cur[pl] = nxt[pl];
-          nb = nbn;
-        }
+  // Stage x (bfloat16, unchanged) and clear the partial outputs.
+  {
+    const bool vec = (m & 7) == 0 && ((reinterpret_cast<uintptr_t>(P.x) & 15) == 0);
+    const int64_t rows = (int64_t)M * 2;
+    if (vec) {
+      const int64_t per_row = xstr >> 3;  // uint4 per staged row
+      for (int64_t idx = tid; idx < rows * per_row; idx += kMmaWarps * 32) {
+        const int64_t row = idx / per_row, k8 = (idx - row * per_row) << 3;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (k8 < m) v = *reinterpret_cast<const uint4*>(P.x + (row >> 1) * 2 * m + (row & 1) * m + k8);
+        *reinterpret_cast<uint4*>(xs + row * xstr + k8) = v;
       }
-
-      // per-plane epilogue; lane q holds token 2 tl + (q >> 1), part q & 1
-#pragma unroll
-      for (int pl = 0; pl < NPL; ++pl) {
-        const int X = pl / T, t = pl - X * T;
-        float s_re = 0.0f, s_im = 0.0f;
-        if (j < n) {
-          s_re = P.scales[((int64_t)(X * T + t) * 2 + 0) * n + j];
-          s_im = P.scales[((int64_t)(X * T + t) * 2 + 1) * n + j];
-        }
-#pragma unroll
-        for (int tl = 0; tl < TILES; ++tl) {
-          const int tok = 2 * tl + (q >> 1), part = q & 1;
-          const float inv = S.inv[tok][part];
-          const float vr = (acc[pl][tl][0] + acc[pl][tl][1] * 0.0625f) * inv;  // <re-row, x_part>
-          const float vi = (acc[pl][tl][2] + acc[pl][tl][3] * 0.0625f) * inv;  // <im-row, x_part>
-          if (part == 0) {
-            y_re[tl] += s_re * vr;
-            y_im[tl] += s_im * vi;
-          } else if (X == 0) {
-            y_re[tl] -= s_im * vi;
-            y_im[tl] += s_re * vr;
-          } else {
-            y_re[tl] += s_im * vi;
-            y_im[tl] -= s_re * vr;
-          }
-        }
+    } else {
+      for (int64_t idx = tid; idx < rows * xstr; idx += kMmaWarps * 32) {
+        const int64_t row = idx / xstr, k = idx - row * xstr;
+        xs[idx] = k < m ? P.x[(row >> 1) * 2 * m + (row & 1) * m + k] : (uint16_t)0;
       }
     }
-    // combine parts a and b (lanes q, q ^ 1), then the column splits
+    for (int z = tid; z < niter * kMmaWarps * TILES * 32; z += kMmaWarps * 32) red[z] = make_float2(0.0f, 0.0f);
+  }
+  __syncthreads();
+
+  // B rows of this lane: token 4 tl + (g >> 1), part g & 1 (zero past M).
+  const uint16_t* xrow[TILES];
+  uint32_t bmask[TILES];
 #pragma unroll
-    for (int tl = 0; tl < TILES; ++tl) {
-      y_re[tl] += __shfl_xor_sync(0xffffffffu, y_re[tl], 1);
-      y_im[tl] += __shfl_xor_sync(0xffffffffu, y_im[tl], 1);
+  for (int tl = 0; tl < TILES; ++tl) {
+    const int tok = 4 * tl + (g >> 1);
+    const int tc = min(tok, M - 1);
+    xrow[tl] = xs + ((int64_t)tc * 2 + (g & 1)) * xstr + 2 * q;
+    bmask[tl] = tok < M ? 0xFFFFFFFFu : 0u;
+  }
+
+  float sc[NPL][2];
+  auto load_scales = [&](int r) {
+    const int64_t j = (rg_begin + r) * 8 + g;
+#pragma unroll
+    for (int pl = 0; pl < NPL; ++pl) {
+      sc[pl][0] = j < n ? P.scales[((int64_t)pl * 2 + 0) * n + j] : 0.0f;
+      sc[pl][1] = j < n ? P.scales[((int64_t)pl * 2 + 1) * n + j] : 0.0f;
     }
-    if (KS > 1) {
-      // red: [KS][RGC][TILES][2][32]
-      if (ks > 0) {
+  };
+  float acc[NPL][TILES][4];
 #pragma unroll
-        for (int tl = 0; tl < TILES; ++tl) {
-          red[((((ks * RGC) + rgc) * TILES + tl) * 2 + 0) * 32 + lane] = y_re[tl];
-          red[((((ks * RGC) + rgc) * TILES + tl) * 2 + 1) * 32 + lane] = y_im[tl];
-        }
-      }
-      __syncthreads();
-      if (ks == 0) {
-        for (int s2 = 1; s2 < KS; ++s2) {
+  for (int pl = 0; pl < NPL; ++pl)
 #pragma unroll
-          for (int tl = 0; tl < TILES; ++tl) {
-            y_re[tl] += red[((((s2 * RGC) + rgc) * TILES + tl) * 2 + 0) * 32 + lane];
-            y_im[tl] += red[((((s2 * RGC) + rgc) * TILES + tl) * 2 + 1) * 32 + lane];
-          }
-        }
-      }
-      __syncthreads();  // red is reused by the next row groups
-    }
-    if (ks == 0 && rg < rg_end && j < n && (q & 1) == 0) {
+    for (int tl = 0; tl < TILES; ++tl) acc[pl][tl][0] = acc[pl][tl][1] = acc[pl][tl][2] = acc[pl][tl][3] = 0.0f;
+  if (i0 < i1) load_scales(rc);
+
+  // One 64-column block: four k16 steps, two code pairs per step.
+  auto mma_block = [&](const uint32_t (&w)[NPL], int kk0) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      uint32_t b01[TILES], b23[TILES];
 #pragma unroll
       for (int tl = 0; tl < TILES; ++tl) {
-        const int tok = 2 * tl + (q >> 1);
-        if (tok < M) {
-          float* yr = P.y + (int64_t)tok * 2 * n;
-          yr[j] = y_re[tl];
-          yr[n + j] = y_im[tl];
+        b01[tl] = *reinterpret_cast<const uint32_t*>(xrow[tl] + kk0 + 16 * s) & bmask[tl];
+        b23[tl] = *reinterpret_cast<const uint32_t*>(xrow[tl] + kk0 + 16 * s + 8) & bmask[tl];
+      }
+#pragma unroll
+      for (int pl = 0; pl < NPL; ++pl) {
+        const uint32_t w0 = w[pl] << (4 * s), w1 = w[pl] << (4 * s + 2);
+        const uint32_t re0 = re_operand(w0), im0 = im_operand(w0);
+        const uint32_t re1 = re_operand(w1), im1 = im_operand(w1);
+#pragma unroll
+        for (int tl = 0; tl < TILES; ++tl) mma_bf16(acc[pl][tl], re0, im0, re1, im1, b01[tl], b23[tl]);
+      }
+    }
+  };
+
+  for (int i = i0; i < i1; ++i) {
+    uint4 nx2[NPL];
+    if (i + 2 < i1) {
+      load_at(rl, cl, nx2);
+      advance(rl, cl);
+    }
+    const int kc = 256 * cc;  // first column of this chunk
+    if (cc < full) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        uint32_t w[NPL];
+#pragma unroll
+        for (int pl = 0; pl < NPL; ++pl) w[pl] = word_of(cur[pl], b);
+        mma_block(w, kc + 64 * b);
+      }
+    } else {
+#pragma unroll
+      for (int b = 0; b < 3; ++b) {
+        if (b < tail) {
+          uint32_t w[NPL];
+#pragma unroll
+          for (int pl = 0; pl < NPL; ++pl) w[pl] = word_of(cur[pl], b);
+          mma_block(w, kc + 64 * b);
         }
       }
+    }
+
+    // end of this warp's segment of row group rc: fold into y partials
+    const int r = rc;
+    advance(rc, cc);
+    if (i + 1 == i1 || rc != r) {
+      float y_re[TILES], y_im[TILES];
+#pragma unroll
+      for (int tl = 0; tl < TILES; ++tl) y_re[tl] = y_im[tl] = 0.0f;
+#pragma unroll
+      for (int pl = 0; pl < NPL; ++pl) {
+        const int X = pl / T;
+#pragma unroll
+        for (int tl = 0; tl < TILES; ++tl) {
+          plane_epilogue(X, sc[pl][0], sc[pl][1], 0.5f * acc[pl][tl][0], 0.5f * acc[pl][tl][1],
+                         0.5f * acc[pl][tl][2], 0.5f * acc[pl][tl][3], y_re[tl], y_im[tl]);
+          acc[pl][tl][0] = acc[pl][tl][1] = acc[pl][tl][2] = acc[pl][tl][3] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int tl = 0; tl < TILES; ++tl)
+        red[((r * kMmaWarps + warp) * TILES + tl) * 32 + lane] = make_float2(y_re[tl], y_im[tl]);
+      if (i + 1 < i1) load_scales(rc);
+    }
+#pragma unroll
+    for (int pl = 0; pl < NPL; ++pl) {
+      cur[pl] = nx1[pl];
+      nx1[pl] = nx2[pl];
+    }
+  }
+  __syncthreads();
+
+  // fixed-order sum over the warps' partials, then store
+  for (int e = tid; e < niter * TILES * 32; e += kMmaWarps * 32) {
+    const int ln = e & 31;
+    const int tl = (e >> 5) % TILES;
+    const int r = (e >> 5) / TILES;
+    const int tok = 4 * tl + (ln & 3);
+    const int64_t j = (rg_begin + r) * 8 + (ln >> 2);
+    float re = 0.0f, im = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w) {
+      const float2 v = red[((r * kMmaWarps + w) * TILES + tl) * 32 + ln];
+      re += v.x;
+      im += v.y;
+    }
+    if (tok < M && j < n) {
+      float* yr = P.y + (int64_t)tok * 2 * n;
+      yr[j] = re;
+      yr[n + j] = im;
     }
   }
 }

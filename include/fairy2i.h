@@ -58,14 +58,15 @@ typedef enum {
  *   ceil(n/8) * ceil(m/64) * 128.  Inside a plane, rows come in groups of 8
  *   and columns in blocks of 64; each (row group, column block) is 32
  *   little-endian 32-bit words, word (4g + q) holding 16 codes of row
- *   8*group + g: byte i, bit pair p (bits 7-2p and 6-2p) is the code of
- *   column 64*block + 16p + 4q + i as (sign, real-axis flag) -- sign 1 means
- *   negative, flag 1 means the code is +-1, flag 0 means +-i.  Within a row
- *   group, blocks are stored in chunks of four so that a thread's words for
- *   four consecutive blocks are 16 contiguous bytes (a tail chunk holds the
- *   remaining 1-3 blocks the same way).  Padding rows and columns hold zero
- *   bits.  The layout is opaque to callers; fairy2i_unpack_codes() gives the
- *   canonical view.
+ *   8*group + g, each as two bits (sign, real-axis flag) -- sign 1 means
+ *   negative, flag 1 means the code is +-1, flag 0 means +-i.  Code c of
+ *   the word (s = c/4, h = (c/2)%2, e = c%2) is column
+ *   64*block + 16s + 8h + 2q + e, in bits (15 + 16e - 2P, 14 + 16e - 2P)
+ *   with P = 2s + h.  Within a row group, blocks are stored in chunks of
+ *   four so that a thread's words for four consecutive blocks are 16
+ *   contiguous bytes (a tail chunk holds the remaining 1-3 blocks the same
+ *   way).  Padding rows and columns hold zero bits.  The layout is opaque to
+ *   callers; fairy2i_unpack_codes() gives the canonical view.
  * scales: fairy2i_scales_count(n, T) floats, [2 (U, W)][T][2 (real axis,
  *   imaginary axis)][n], 16-byte aligned. */
 typedef struct {
@@ -81,7 +82,7 @@ typedef struct {
 typedef enum {
     FAIRY2I_ALGO_AUTO = 0,    /* pick the fastest kernel for the token count */
     FAIRY2I_ALGO_ADDSUB = 1,  /* CUDA cores: adds/subtracts only, fp32 accumulation */
-    FAIRY2I_ALGO_MMA_FP8 = 2, /* decode: codes expanded to e4m3 {+-2, +-0} in registers, mma.sync */
+    FAIRY2I_ALGO_MMA = 2,     /* decode: codes expanded to bf16 {+-2, +-0} in registers, mma.sync */
     FAIRY2I_ALGO_TCGEN05 = 3  /* prefill: codes expanded to bf16 in shared memory, tcgen05.mma */
 } fairy2i_algo;
 

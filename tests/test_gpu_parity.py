@@ -14,7 +14,7 @@ from bit_complex_valued_fairy2i_b300 import inputs
 pytestmark = pytest.mark.gpu
 
 REL_L2 = 1e-3
-DECODE_ALGOS = ("addsub", "mma_fp8")
+DECODE_ALGOS = ("addsub", "mma")
 
 
 def rel_l2(got, want):
