@@ -248,7 +248,8 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     peaks = _peaks()
 
-    stack, offline = build_stack(f2i, BLOCKS, dev)
+    blocks = args.blocks
+    stack, offline = build_stack(f2i, blocks, dev)
     bytes_per_block = sum(q.nbytes for q in stack[0])
     bytes_per_step = sum(q.nbytes for layers in stack for q in layers)
 
@@ -256,15 +257,15 @@ def run_ours(args, world, rank, local):
     x_sizes = [2 * q.m for layers in stack for q in layers]
     y_sizes = [2 * q.n for layers in stack for q in layers]
     x_all = torch.cat([inputs.activations(5, 7 * b + pi, 1, inf, device=dev).reshape(-1)
-                       for b in range(BLOCKS) for pi, (_, _, inf) in enumerate(inputs.LLAMA2_7B_BLOCK)])
+                       for b in range(blocks) for pi, (_, _, inf) in enumerate(inputs.LLAMA2_7B_BLOCK)])
     y_all = torch.empty(sum(y_sizes), dtype=torch.float32, device=dev)
     xv = list(torch.split(x_all, x_sizes))
     yv = list(torch.split(y_all, y_sizes))
-    xs = [[xv[7 * b + i].view(1, -1) for i in range(7)] for b in range(BLOCKS)]
-    ys = [[yv[7 * b + i].view(1, -1) for i in range(7)] for b in range(BLOCKS)]
+    xs = [[xv[7 * b + i].view(1, -1) for i in range(7)] for b in range(blocks)]
+    ys = [[yv[7 * b + i].view(1, -1) for i in range(7)] for b in range(blocks)]
 
     def step():
-        for b in range(BLOCKS):
+        for b in range(blocks):
             f2i.linear_group(stack[b], xs[b], ys[b])
 
     step()  # outside capture: first-use setup (shared-memory attributes)
@@ -289,7 +290,7 @@ def run_ours(args, world, rank, local):
     _barrier(world)
     total_ms = _max_over_ranks(start.elapsed_time(stop), world)
     ms_per_step = total_ms / args.steps
-    launch_ms = ms_per_step / BLOCKS  # every launch of the step is the decode kernel
+    launch_ms = ms_per_step / blocks  # every launch of the step is the decode kernel
     value = bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
 
     # end to end: the step's activations from pinned host memory, its outputs back
@@ -315,11 +316,12 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 mma.sync (codes as bf16 {+-2,+-0}, bf16 x), fp32 accumulate",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": 1, "T": T_STAGES, "blocks": BLOCKS, "projections": 7 * BLOCKS,
+        "config": {"workload": WORKLOAD if blocks == BLOCKS else f"{blocks}-block cut of: {WORKLOAD}",
+                   "M": 1, "T": T_STAGES, "blocks": blocks, "projections": 7 * blocks,
                    "bytes_per_step": bytes_per_step, "l2": "inputs larger than L2 (1.64 GB working set)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": BLOCKS * args.steps,
+        "gpu_launches": blocks * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                      "kernel": "linear_mma_kernel<4,1> (mma.sync bf16)", "bytes_per_launch": bytes_per_block,
@@ -341,6 +343,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--blocks", type=int, default=BLOCKS,
+                    help="decoder blocks in the stack (32 = the full model; fewer only for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:
