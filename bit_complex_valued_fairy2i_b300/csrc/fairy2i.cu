@@ -1,6 +1,8 @@
 // Host side of the C ABI declared in include/fairy2i.h: argument checks,
 // launch configuration and error reporting.  All arithmetic of the layer runs
 // in the kernels included below.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -15,6 +17,7 @@
 #include "layout.cuh"
 #include "convert_quantize.cuh"
 #include "linear_decode.cuh"
+#include "linear_prefill.cuh"
 
 namespace {
 
@@ -189,6 +192,96 @@ fairy2i_status run_addsub(f2i::LinearGroup& G, cudaStream_t s) {
   return check_launch("addsub decode launch");
 }
 
+// --- prefill (tcgen05) launch helpers ---------------------------------------
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on libcuda).
+fairy2i_status tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000& out) {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+      return fail(FAIRY2I_ERR_CUDA, "cuTensorMapEncodeTiled unavailable: %s", cudaGetErrorString(e));
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  out = fn;
+  return FAIRY2I_OK;
+}
+
+// x [M][2m] bfloat16 seen as a [2M][m] tensor (row 2 * token + part), tiles of
+// 256 rows x 64 columns, 128-byte swizzle, zero fill outside.
+fairy2i_status make_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t m) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  fairy2i_status st = tensor_map_encoder(enc);
+  if (st != FAIRY2I_OK) return st;
+  const cuuint64_t dims[2] = {(cuuint64_t)m, (cuuint64_t)(2 * M)};
+  const cuuint64_t strides[1] = {(cuuint64_t)m * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)f2i::kPfBK, (cuuint32_t)f2i::kPfBN};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FAIRY2I_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return FAIRY2I_OK;
+}
+
+template <int RO>
+fairy2i_status launch_tcgen05_t(const f2i::PrefillParams& P, cudaStream_t s) {
+  auto k = f2i::linear_tcgen05_kernel<RO>;
+  const void* fn = reinterpret_cast<const void*>(k);
+  fairy2i_status st = ensure_smem(fn, f2i::kPfSmemBytes, "tcgen05 prefill");
+  if (st != FAIRY2I_OK) return st;
+  const int64_t grid = std::min<int64_t>(P.total_tiles, sm_count());
+  k<<<(unsigned)grid, f2i::kPfThreads, f2i::kPfSmemBytes, s>>>(P);
+  return check_launch("tcgen05 prefill launch");
+}
+
+// Code rows per output in a prefill tile: 4T rounded up to a power of two.
+int prefill_rows_per_output(int T) { return T == 1 ? 4 : T == 2 ? 8 : 16; }
+
+fairy2i_status run_tcgen05(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count, int64_t M,
+                           int T, cudaStream_t s) {
+  const int ro = prefill_rows_per_output(T);
+  const int J = f2i::kPfBM / ro;
+  for (int p0 = 0; p0 < count; p0 += f2i::kPfMaxGroup) {
+    const int cnt = std::min(f2i::kPfMaxGroup, count - p0);
+    f2i::PrefillParams P;
+    memset(&P, 0, sizeof(P));
+    P.count = cnt;
+    P.T = T;
+    P.M = (int32_t)M;
+    int64_t tiles = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const fairy2i_packed& q = qs[p0 + i];
+      fairy2i_status st = make_x_map(&P.tmap[i], xs[p0 + i], M, q.m);
+      if (st != FAIRY2I_OK) return st;
+      f2i::PrefillProblem& pr = P.p[i];
+      pr.codes = static_cast<const uint8_t*>(q.codes);
+      pr.scales = q.scales;
+      pr.y = ys[p0 + i];
+      pr.n = q.n;
+      pr.m = q.m;
+      pr.row_tiles = (q.n + J - 1) / J;
+      pr.tok_tiles = (int32_t)((M + f2i::kPfTokens - 1) / f2i::kPfTokens);
+      pr.kblocks = (int32_t)((q.m + f2i::kPfBK - 1) / f2i::kPfBK);
+      pr.tile_begin = tiles;
+      tiles += pr.row_tiles * pr.tok_tiles;
+    }
+    P.total_tiles = tiles;
+    fairy2i_status st = ro == 4 ? launch_tcgen05_t<4>(P, s) : ro == 8 ? launch_tcgen05_t<8>(P, s)
+                                                                       : launch_tcgen05_t<16>(P, s);
+    if (st != FAIRY2I_OK) return st;
+  }
+  return ok();
+}
+
+// Token count from which FAIRY2I_ALGO_AUTO takes the tcgen05 prefill path.
+constexpr int64_t kPrefillMinTokens = 65;
+
 fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int32_t count,
                                  int64_t M, fairy2i_algo algo, cudaStream_t s) {
   if (count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "count=%d outside [1, 256]", count);
@@ -209,10 +302,20 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
   }
   if (M > (int64_t)1 << 30) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
 
+  bool m_mult8 = true;
+  for (int i = 0; i < count; ++i) m_mult8 = m_mult8 && (qs[i].m % 8) == 0;
   fairy2i_algo a = algo;
-  if (a == FAIRY2I_ALGO_AUTO) a = (T <= 4) ? FAIRY2I_ALGO_MMA : FAIRY2I_ALGO_ADDSUB;
-  if (a == FAIRY2I_ALGO_TCGEN05) return fail(FAIRY2I_ERR_UNSUPPORTED, "tcgen05 prefill path not built yet");
+  if (a == FAIRY2I_ALGO_AUTO) {
+    if (T <= 4 && M >= kPrefillMinTokens && m_mult8) a = FAIRY2I_ALGO_TCGEN05;
+    else a = (T <= 4) ? FAIRY2I_ALGO_MMA : FAIRY2I_ALGO_ADDSUB;
+  }
   if (a == FAIRY2I_ALGO_MMA && T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode supports T <= 4");
+  if (a == FAIRY2I_ALGO_TCGEN05) {
+    if (T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "tcgen05 prefill supports T <= 4");
+    if (!m_mult8) return fail(FAIRY2I_ERR_UNSUPPORTED, "tcgen05 prefill needs m to be a multiple of 8");
+    if (M > ((int64_t)1 << 30) - 1) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
+    return run_tcgen05(qs, xs, ys, count, M, T, s);
+  }
 
   const int chunk = (a == FAIRY2I_ALGO_MMA) ? kMmaTokens : f2i::kAddSubTok * 1024;
   for (int p0 = 0; p0 < count; p0 += f2i::kMaxGroup) {
