@@ -239,6 +239,113 @@ def build_stack(f2i, blocks: int, dev):
                    "convert_ms_stack": conv_ms, "quantize_ms_stack": quant_ms}
 
 
+def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
+    """Prefill: the 7 projections of one block at M tokens (1 % outliers x10),
+    one grouped tcgen05 launch per step; executed and dense-equivalent TFLOP/s."""
+    qs, xs, ys = [], [], []
+    flops_exec = flops_dense = 0
+    for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
+        R = inputs.weight_R(4, pi, out_f, in_f, device=dev)
+        U, W = f2i.convert(R)
+        q = f2i.quantize(U, W, T_STAGES, check=False)
+        del R, U, W
+        qs.append(q)
+        xs.append(inputs.activations(4, pi, M, in_f, outliers=True, device=dev))
+        ys.append(torch.empty((M, out_f), dtype=torch.float32, device=dev))
+        n, m = out_f // 2, in_f // 2
+        flops_exec += 16 * n * m * T_STAGES * M
+        flops_dense += 8 * n * m * M
+    f2i.sync_status()
+    for _ in range(warmup):
+        f2i.linear_group(qs, xs, ys, algo="tcgen05")
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        f2i.linear_group(qs, xs, ys, algo="tcgen05")
+    stop.record(stream)
+    torch.cuda.synchronize()
+    f2i.sync_status()
+    ms = start.elapsed_time(stop) / steps
+    tflops = flops_exec / (ms * 1e-3) / 1e12
+    return {"workload": f"llama2-7b block prefill, 7 projections, M={M}, T={T_STAGES}, 1% outliers x10, "
+                        "one grouped launch", "kernel": "linear_tcgen05_kernel<8>", "ms_per_block": ms,
+            "executed_flops_per_block": flops_exec, "dense_equivalent_flops_per_block": flops_dense,
+            "tflops_executed": tflops, "tflops_dense_equivalent": flops_dense / (ms * 1e-3) / 1e12,
+            "peak_bf16_tflops": peaks["bf16_tflops"], "frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
+            "peak_source": peaks["source"], "tokens_per_s_per_block": M / (ms * 1e-3), "steps": steps}
+
+
+def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int = 4):
+    """Batched decode sweep: per token count M and per algorithm, the 7 projections of
+    `blocks` distinct blocks (205 MB at 4 blocks, above L2), one grouped launch per block;
+    time per block, weight GB/s and tokens/s-equivalent."""
+    stack, xs_full = [], []
+    for b in range(blocks):
+        qs, xb = [], []
+        for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
+            R = inputs.weight_R(3, 7 * b + pi, out_f, in_f, device=dev)
+            U, W = f2i.convert(R)
+            qs.append(f2i.quantize(U, W, T_STAGES, check=False))
+            del R, U, W
+            xb.append(inputs.activations(3, 7 * b + pi, max(Ms), in_f, device=dev))
+        stack.append(qs)
+        xs_full.append(xb)
+    f2i.sync_status()
+    nbytes = sum(q.nbytes for q in stack[0])
+    out = []
+    stream = torch.cuda.current_stream()
+    for M in Ms:
+        xs = [[x[:M].contiguous() for x in xb] for xb in xs_full]
+        ys = [[torch.empty((M, 2 * q.n), dtype=torch.float32, device=dev) for q in qs] for qs in stack]
+        row = {"M": M}
+        for algo in ("mma", "tcgen05", "auto"):
+            def step():
+                for b in range(blocks):
+                    f2i.linear_group(stack[b], xs[b], ys[b], algo=algo)
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+            start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for _ in range(reps):
+                step()
+            stop.record(stream)
+            torch.cuda.synchronize()
+            us = start.elapsed_time(stop) / reps / blocks * 1e3
+            row[algo] = {"us_per_block": round(us, 2), "weight_GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                         "tokens_per_s_per_block": round(M / (us * 1e-6))}
+        out.append(row)
+    f2i.sync_status()
+    return {"workload": f"llama2-7b blocks (7 projections each), T=2, {blocks} distinct blocks "
+                        f"({blocks * nbytes / 1e6:.0f} MB > L2), one grouped launch per block",
+            "bytes_per_block": nbytes, "rows": out}
+
+
+def run_sweep_only(args, world, rank, local):
+    import bit_complex_valued_fairy2i_b300 as f2i
+    from bit_complex_valued_fairy2i_b300 import build as f2i_build
+
+    f2i_build.build()
+    torch.cuda.set_device(local)
+    res = sweep_leg(f2i, torch.device("cuda", local))
+    if rank == 0:
+        print(json.dumps({"sweep": res}), flush=True)
+
+
+def run_prefill_only(args, world, rank, local):
+    import bit_complex_valued_fairy2i_b300 as f2i
+    from bit_complex_valued_fairy2i_b300 import build as f2i_build
+
+    f2i_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    res = prefill_leg(f2i, dev, _peaks(), args.steps, args.warmup, args.prefill_tokens)
+    if rank == 0:
+        print(json.dumps({"prefill": res}), flush=True)
+
+
 def run_ours(args, world, rank, local):
     import bit_complex_valued_fairy2i_b300 as f2i
     from bit_complex_valued_fairy2i_b300 import build as f2i_build
@@ -330,6 +437,9 @@ def run_ours(args, world, rank, local):
         "clocks": clk.summary(),
         "offline": offline,
     }
+    if not args.no_prefill:
+        del graph
+        result["prefill"] = prefill_leg(f2i, dev, peaks, max(3, min(args.steps, 20)), 3, args.prefill_tokens)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
@@ -343,6 +453,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["decode", "prefill", "sweep"], default="decode",
+                    help="prefill: time only the prefill leg (for profiling)")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-tokens", type=int, default=2048)
     ap.add_argument("--blocks", type=int, default=BLOCKS,
                     help="decoder blocks in the stack (32 = the full model; fewer only for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -352,6 +466,10 @@ def main():
     world, rank, local = _dist()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.mode == "prefill":
+        run_prefill_only(args, world, rank, local)
+    elif args.mode == "sweep":
+        run_sweep_only(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

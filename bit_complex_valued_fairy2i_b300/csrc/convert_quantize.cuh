@@ -107,119 +107,167 @@ __device__ __forceinline__ uint32_t warp_max(uint32_t v) {
   return v;
 }
 
-constexpr int kQuantThreads = 256;
+// One CTA per (output row j, matrix X).  Thread t owns WPT packed words of the
+// row; word w = 4 kb + q holds the 16 weights at columns 64 kb + code_col(c, q).
+// The weights stay in registers through all T stages, so HBM sees one read of
+// the row and one write of its codes and scales, and each word is assembled as
+// its codes are decided.  Row-wide maxima, counts and exact sums are block
+// reductions (warp shuffles, then one value per warp in shared memory).
+constexpr int kQuantThreads = 512;  // words per thread: 1 for m <= 8192, 2 up to 16384
 
-// Dynamic shared memory: m float2 residual entries, then m code bytes.
-__global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(
+template <typename Tv, typename Op>
+__device__ __forceinline__ void block_reduce2(Tv& a, Tv& b, Tv* sa, Tv* sb, Op op) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = op(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = op(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  if (lane == 0) {
+    sa[warp] = a;
+    sb[warp] = b;
+  }
+  __syncthreads();
+  a = sa[0];
+  b = sb[0];
+  for (int w = 1; w < nw; ++w) {
+    a = op(a, sa[w]);
+    b = op(b, sb[w]);
+  }
+  __syncthreads();  // sa / sb are reused by the next reduction
+}
+
+template <int WPT>
+__global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
     const float2* __restrict__ U, const float2* __restrict__ W, int64_t n, int64_t m, int T,
     uint8_t* __restrict__ codes, float* __restrict__ scales) {
-  extern __shared__ __align__(16) unsigned char qsmem[];
-  float2* row = reinterpret_cast<float2*>(qsmem);
-  uint8_t* cbits = qsmem + m * sizeof(float2);
-  constexpr int NW = kQuantThreads / 32;
-  __shared__ uint32_t s_max[2][NW];
-  __shared__ int s_cnt[2][NW];
-  __shared__ long long s_sum[2][NW];
+  constexpr int E = 16 * WPT;  // weights per thread
+  __shared__ uint32_t s_u[2][32];
+  __shared__ long long s_l[2][32];
   __shared__ float s_scale[2];
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int X = blockIdx.y;
   const int64_t j = blockIdx.x;
+  const int64_t KB = col_blocks(m);
   const float2* src = (X == 0 ? U : W) + j * m;
 
+  // column of weight e = 16 u + c of this thread (word u of WPT)
+  auto col_of = [&](int e) -> int64_t {
+    const int64_t w = (int64_t)tid * WPT + (e >> 4);
+    return (w >> 2) * 64 + code_col(e & 15, (int)(w & 3));
+  };
+  float re[E], im[E];
   bool bad = false;
-  for (int64_t k = tid; k < m; k += kQuantThreads) {
-    const float2 v = src[k];
+  uint32_t valid[WPT];
+#pragma unroll
+  for (int u = 0; u < WPT; ++u) valid[u] = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int64_t w = (int64_t)tid * WPT + (e >> 4);
+    const int64_t k = col_of(e);
+    float2 v = make_float2(0.0f, 0.0f);
+    if ((w >> 2) < KB && k < m) {
+      v = __ldcs(src + k);
+      valid[e >> 4] |= 1u << (e & 15);
+    }
     bad |= !(isfinite(v.x) && isfinite(v.y));
-    row[k] = v;
+    re[e] = v.x;
+    im[e] = v.y;
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0) f2i_raise(kErrNonFinite);
     return;  // whole CTA leaves together; the codes of this row stay unspecified
   }
 
-  const int64_t KB = col_blocks(m);
   const int64_t pbytes = plane_bytes(n, m);
-  const int64_t rg = j >> 3;
   const int g = (int)(j & 7);
 
   for (int t = 0; t < T; ++t) {
-    // codes, per-axis maxima and counts
-    uint32_t lmax0 = 0, lmax1 = 0;
-    int lcnt0 = 0, lcnt1 = 0;
-    for (int64_t k = tid; k < m; k += kQuantThreads) {
-      const float2 v = row[k];
-      const float ar = fabsf(v.x), ai = fabsf(v.y);
+    // codes: real axis iff |Re| >= |Im|; negative iff the chosen component is < 0
+    // (branch-free; columns outside the matrix keep zero code bits and count nowhere)
+    uint32_t word[WPT], realm[WPT];
+    uint32_t mx0 = 0, mx1 = 0, cnt0 = 0, cnt1 = 0;
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) word[u] = realm[u] = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int u = e >> 4, c = e & 15;
+      const bool in = (valid[u] >> c) & 1u;
+      const float ar = fabsf(re[e]), ai = fabsf(im[e]);
       const bool real = ar >= ai;
-      const bool neg = real ? (v.x < 0.0f) : (v.y < 0.0f);
-      cbits[k] = (uint8_t)(((neg ? 1 : 0) << 1) | (real ? 1 : 0));
-      if (real) { lmax0 = max(lmax0, __float_as_uint(ar)); ++lcnt0; }
-      else { lmax1 = max(lmax1, __float_as_uint(ai)); ++lcnt1; }
+      const bool neg = real ? (re[e] < 0.0f) : (im[e] < 0.0f);
+      const bool isr = in && real, isi = in && !real;
+      word[u] |= (in ? (((neg ? 1u : 0u) << 1) | (real ? 1u : 0u)) : 0u) << code_shift(c);
+      realm[u] |= (isr ? 1u : 0u) << c;
+      mx0 = max(mx0, isr ? __float_as_uint(ar) : 0u);
+      mx1 = max(mx1, isi ? __float_as_uint(ai) : 0u);
+      cnt0 += isr ? 1u : 0u;
+      cnt1 += isi ? 1u : 0u;
     }
-    lmax0 = warp_max(lmax0); lmax1 = warp_max(lmax1);
-    lcnt0 = warp_sum(lcnt0); lcnt1 = warp_sum(lcnt1);
-    if (lane == 0) { s_max[0][warp] = lmax0; s_max[1][warp] = lmax1; s_cnt[0][warp] = lcnt0; s_cnt[1][warp] = lcnt1; }
-    __syncthreads();
-    uint32_t mx[2] = {0, 0};
-    int cnt[2] = {0, 0};
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      mx[0] = max(mx[0], s_max[0][w]); mx[1] = max(mx[1], s_max[1][w]);
-      cnt[0] += s_cnt[0][w]; cnt[1] += s_cnt[1][w];
-    }
-    const int e0 = mx[0] ? float_exponent(mx[0]) : 0;
-    const int e1 = mx[1] ? float_exponent(mx[1]) : 0;
+    block_reduce2(mx0, mx1, s_u[0], s_u[1], [](uint32_t x, uint32_t y) { return max(x, y); });
+    block_reduce2(cnt0, cnt1, s_u[0], s_u[1], [](uint32_t x, uint32_t y) { return x + y; });
+    const int e0 = mx0 ? float_exponent(mx0) : 0;
+    const int e1 = mx1 ? float_exponent(mx1) : 0;
 
-    // exact integer sums of |v| 2^(48-e)
+    // exact integer sums of trunc(|v| 2^(48-e)).  With 48 - e <= 127 the
+    // power of two is a float, |v| 2^(48-e) < 2^49 is exact (an exponent
+    // change) and the truncating conversion to u64 is exact; rows whose
+    // maximum is below 2^-79 take the integer-shift path (block-uniform).
     long long ls0 = 0, ls1 = 0;
-    for (int64_t k = tid; k < m; k += kQuantThreads) {
-      const float2 v = row[k];
-      if (cbits[k] & 1u) ls0 += scaled_trunc(__float_as_uint(fabsf(v.x)), e0);
-      else ls1 += scaled_trunc(__float_as_uint(fabsf(v.y)), e1);
+    if (e0 >= -79 && e1 >= -79) {
+      const float sc0 = __int_as_float((48 - e0 + 127) << 23), sc1 = __int_as_float((48 - e1 + 127) << 23);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int u = e >> 4, c = e & 15;
+        const bool isr = (realm[u] >> c) & 1u, in = (valid[u] >> c) & 1u;
+        const float v = isr ? fabsf(re[e]) : fabsf(im[e]);
+        const long long val = (long long)__float2ull_rz(__fmul_rn(v, isr ? sc0 : sc1));
+        ls0 += isr ? val : 0ll;
+        ls1 += (in && !isr) ? val : 0ll;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int u = e >> 4, c = e & 15;
+        if (!((valid[u] >> c) & 1u)) continue;
+        if ((realm[u] >> c) & 1u) ls0 += scaled_trunc(__float_as_uint(fabsf(re[e])), e0);
+        else ls1 += scaled_trunc(__float_as_uint(fabsf(im[e])), e1);
+      }
     }
-    ls0 = warp_sum(ls0); ls1 = warp_sum(ls1);
-    if (lane == 0) { s_sum[0][warp] = ls0; s_sum[1][warp] = ls1; }
-    __syncthreads();
+    block_reduce2(ls0, ls1, s_l[0], s_l[1], [](long long x, long long y) { return x + y; });
     if (tid < 2) {
-      const int a = tid;
-      long long sum = 0;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) sum += s_sum[a][w];
-      float s = 0.0f;
-      if (cnt[a] > 0 && mx[a] != 0) {
-        const int e = a == 0 ? e0 : e1;
-        const double mean = ldexp(__ll2double_rn(sum), e - 48) / (double)cnt[a];
-        s = __double2float_rn(mean);
-      }
-      s_scale[a] = s;
-      scales[((int64_t)(X * T + t) * 2 + a) * n + j] = s;
+      const long long sum = tid == 0 ? ls0 : ls1;
+      const uint32_t cnt = tid == 0 ? cnt0 : cnt1;
+      const uint32_t mx = tid == 0 ? mx0 : mx1;
+      const int e = tid == 0 ? e0 : e1;
+      float sc = 0.0f;
+      if (cnt > 0 && mx != 0) sc = __double2float_rn(ldexp(__ll2double_rn(sum), e - 48) / (double)cnt);
+      s_scale[tid] = sc;
+      scales[((int64_t)(X * T + t) * 2 + tid) * n + j] = sc;
     }
     __syncthreads();
-
-    // residual update r <- r - (s_re b_re + i s_im b_im), one float32 rounding
     const float s_re = s_scale[0], s_im = s_scale[1];
-    for (int64_t k = tid; k < m; k += kQuantThreads) {
-      const uint32_t c = cbits[k];
-      float2 v = row[k];
-      if (c & 1u) v.x = __fsub_rn(v.x, (c & 2u) ? -s_re : s_re);
-      else v.y = __fsub_rn(v.y, (c & 2u) ? -s_im : s_im);
-      row[k] = v;
-    }
+    __syncthreads();  // s_scale is rewritten by the next stage
 
-    // pack: word (kb, q) of row g holds the 16 columns 64 kb + code_col(c, q)
-    uint8_t* plane = codes + (int64_t)(X * T + t) * pbytes;
-    for (int64_t w = tid; w < KB * 4; w += kQuantThreads) {
-      const int64_t kb = w >> 2;
-      const int q = (int)(w & 3);
-      uint32_t word = 0;
+    // residual r <- r - (s_re b_re + i s_im b_im), one float32 rounding
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int64_t k = kb * 64 + code_col(c, q);
-        if (k < m) word |= (uint32_t)cbits[k] << code_shift(c);
-      }
-      *reinterpret_cast<uint32_t*>(plane + word_offset(rg, kb, 4 * g + q, KB)) = word;
+    for (int e = 0; e < E; ++e) {
+      const int u = e >> 4, c = e & 15;
+      const bool neg = (word[u] >> (code_shift(c) + 1)) & 1u;
+      const bool isr = (realm[u] >> c) & 1u;
+      const float d = isr ? (neg ? -s_re : s_re) : (neg ? -s_im : s_im);
+      const float upd = __fsub_rn(isr ? re[e] : im[e], d);
+      re[e] = isr ? upd : re[e];
+      im[e] = isr ? im[e] : upd;
     }
-    __syncthreads();  // cbits and row are rewritten by the next stage
+    uint8_t* plane = codes + (int64_t)(X * T + t) * pbytes;
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) {
+      const int64_t w = (int64_t)tid * WPT + u;
+      if ((w >> 2) < KB)
+        *reinterpret_cast<uint32_t*>(plane + word_offset(j >> 3, w >> 2, 4 * g + (int)(w & 3), KB)) = word[u];
+    }
   }
 }
 

@@ -163,7 +163,9 @@ fairy2i_status run_mma(f2i::LinearGroup& G, int T, cudaStream_t s) {
   for (int i = 0; i < G.count; ++i) xstr_max = std::max(xstr_max, f2i::x_stride(G.p[i].m));
   const size_t xbytes = (((size_t)G.M * 2 * xstr_max * sizeof(uint16_t)) + 15) & ~(size_t)15;
   const size_t per_rg = (size_t)f2i::kMmaWarps * tiles * 32 * sizeof(float2);
-  const size_t limit = 200 * 1024;
+  // Two CTAs per SM when the staged activations leave room for at least four
+  // row groups of partial outputs; otherwise one CTA with up to 200 KB.
+  const size_t limit = xbytes + 4 * per_rg <= 110 * 1024 ? 110 * 1024 : 200 * 1024;
   if (xbytes + per_rg > limit)
     return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode: staged activations need %zu bytes of shared memory", xbytes);
   const int rpc_max = (int)std::min<size_t>(f2i::kMaxRowGroupsPerCta, (limit - xbytes) / per_rg);
@@ -280,7 +282,7 @@ fairy2i_status run_tcgen05(const fairy2i_packed* qs, const void* const* xs, floa
 }
 
 // Token count from which FAIRY2I_ALGO_AUTO takes the tcgen05 prefill path.
-constexpr int64_t kPrefillMinTokens = 65;
+constexpr int64_t kPrefillMinTokens = 17;
 
 fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int32_t count,
                                  int64_t M, fairy2i_algo algo, cudaStream_t s) {
@@ -394,13 +396,16 @@ fairy2i_status fairy2i_quantize(const void* U, const void* W, int64_t n, int64_t
     cudaError_t e = cudaMemsetAsync(out->codes, 0, fairy2i_codes_bytes(n, m, T), s);
     if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "memset codes: %s", cudaGetErrorString(e));
   }
-  const size_t smem = (size_t)m * (sizeof(float2) + 1);
-  st = ensure_smem(reinterpret_cast<const void*>(f2i::quantize_rows_kernel), smem, "quantize");
-  if (st != FAIRY2I_OK) return st;
+  const int64_t words = 4 * f2i::col_blocks(m);  // packed words per row
+  const int wpt = words <= f2i::kQuantThreads ? 1 : 2;
+  const int threads = (int)(((words + wpt - 1) / wpt + 31) / 32 * 32);
   dim3 grid((unsigned)n, 2);
-  f2i::quantize_rows_kernel<<<grid, f2i::kQuantThreads, smem, s>>>(
-      static_cast<const float2*>(U), static_cast<const float2*>(W), n, m, T, static_cast<uint8_t*>(out->codes),
-      out->scales);
+  if (wpt == 1)
+    f2i::quantize_words_kernel<1><<<grid, threads, 0, s>>>(static_cast<const float2*>(U), static_cast<const float2*>(W),
+                                                           n, m, T, static_cast<uint8_t*>(out->codes), out->scales);
+  else
+    f2i::quantize_words_kernel<2><<<grid, threads, 0, s>>>(static_cast<const float2*>(U), static_cast<const float2*>(W),
+                                                           n, m, T, static_cast<uint8_t*>(out->codes), out->scales);
   return check_launch("quantize launch");
 }
 

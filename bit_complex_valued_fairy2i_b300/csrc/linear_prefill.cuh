@@ -313,6 +313,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
     }
   } else if (warp == 2 || warp == 3) {
     // ---------------- A producers: codes -> bfloat16 {+-2, +-0} ----------------
+    // Thread i owns code plane p of output jj of every tile: rows RO*jj + 2p
+    // (real axis) and RO*jj + 2p + 1 (imaginary axis).  The packed words of a
+    // whole chunk of four 64-column blocks are one 16-byte load per word
+    // column q; the next chunk (of this tile or the next) is loaded while the
+    // current one is expanded, so the load latency overlaps the MMAs.
     const int i = tid - 64;
     const int planes = 2 * T;
     const bool active = i < J * planes;
@@ -321,62 +326,102 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
     const uint32_t r_re = (uint32_t)(RO * jj + 2 * p);
     const uint32_t row_re = r_re * 128u, row_im = (r_re + 1u) * 128u;
     const uint32_t sw_re = r_re & 7u, sw_im = (r_re + 1u) & 7u;
+
+    // chunk cursor over (tile, chunk) in this CTA's tile order
+    int64_t ld_tile = blockIdx.x;
+    int64_t ld_ch = 0;
+    uint4 nxt[4];
+    auto load_chunk = [&](int64_t tile, int64_t ch, uint4 (&dst)[4]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (tile >= P.total_tiles) return;
+      const PfTile c = pf_tile(P, tile);
+      const PrefillProblem& pr = P.p[c.pi];
+      const int64_t j = c.rt * J + jj;
+      if (!active || j >= pr.n) return;
+      const int64_t KB = col_blocks(pr.m);
+      const int64_t full = KB >> 2;
+      const int g = (int)(j & 7);
+      const uint8_t* rowp = pr.codes + (int64_t)p * plane_bytes(pr.n, pr.m) + (j >> 3) * KB * kTileBytes;
+      if (ch < full) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = __ldg(reinterpret_cast<const uint4*>(rowp + ch * 512 + (4 * g + q) * 16));
+      } else {
+        const int tail = (int)(KB - 4 * full);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t* t = reinterpret_cast<const uint32_t*>(rowp + full * 512 + (int64_t)(4 * g + q) * 4 * tail);
+          dst[q].x = __ldg(t);
+          dst[q].y = tail > 1 ? __ldg(t + 1) : 0u;
+          dst[q].z = tail > 2 ? __ldg(t + 2) : 0u;
+        }
+      }
+    };
+    auto advance = [&]() {
+      if (ld_tile >= P.total_tiles) return;
+      const PfTile c = pf_tile(P, ld_tile);
+      if (++ld_ch * 4 >= P.p[c.pi].kblocks) {
+        ld_ch = 0;
+        ld_tile += gridDim.x;
+      }
+    };
+    load_chunk(ld_tile, ld_ch, nxt);
+    advance();
+
     uint32_t it = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
       const PfTile c = pf_tile(P, tile);
       const PrefillProblem& pr = P.p[c.pi];
-      const int64_t j = c.rt * J + jj;
-      const bool live = active && j < pr.n;
-      const int64_t KB = col_blocks(pr.m);
-      const int64_t full = KB >> 2;
-      const int tail = (int)(KB - 4 * full);
-      const int g = (int)(j & 7);
-      const uint8_t* rowp = pr.codes + (int64_t)p * plane_bytes(pr.n, pr.m) + (j >> 3) * KB * kTileBytes;
-      for (int kb = 0; kb < pr.kblocks; ++kb, ++it) {
-        const int s = (int)(it % kPfStages);
-        const uint32_t ph = (it / kPfStages) & 1u;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (live) {
+      const bool live = active && (c.rt * J + jj) < pr.n;
+      for (int kb0 = 0; ok && kb0 < pr.kblocks; kb0 += 4) {
+        uint4 cur[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint8_t* a = (kb < 4 * full)
-                                   ? rowp + (int64_t)(kb >> 2) * 512 + (4 * g + q) * 16 + (kb & 3) * 4
-                                   : rowp + full * 512 + (int64_t)(4 * g + q) * 4 * tail + (kb - 4 * full) * 4;
-            w[q] = __ldg(reinterpret_cast<const uint32_t*>(a));
+        for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
+        load_chunk(ld_tile, ld_ch, nxt);
+        advance();
+        const int nb = min(4, pr.kblocks - kb0);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          if (b >= nb) break;
+          const int s = (int)(it % kPfStages);
+          const uint32_t ph = (it / kPfStages) & 1u;
+          ++it;
+          bool got = true;
+          if (lane == 0) got = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag);
+          got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+          if (!got) {
+            ok = false;
+            break;
           }
-        }
-        bool got = true;
-        if (lane == 0) got = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag);
-        got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-        if (!got) {
-          ok = false;
-          break;
-        }
-        if (live) {
-          const uint32_t st = sA + (uint32_t)s * kPfAStage;
+          if (live) {
+            const uint32_t st = sA + (uint32_t)s * kPfAStage;
+            uint32_t w[4];
 #pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            const uint32_t cc = (uint32_t)(c8 + lane) & 7u;  // rotate chunks across lanes (banks)
-            const uint32_t sh = 2u * cc;                     // pair cc sits at bits (15-2cc, 14-2cc)
-            uint32_t re[4], im[4];
+            for (int q = 0; q < 4; ++q) w[q] = b == 0 ? cur[q].x : b == 1 ? cur[q].y : b == 2 ? cur[q].z : cur[q].w;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t x = w[q] << sh;
-              re[q] = x & 0xC000C000u;
-              im[q] = (x & 0x80008000u) | (~x & 0x40004000u);
+            for (int c8 = 0; c8 < 8; ++c8) {
+              const uint32_t cc = (uint32_t)(c8 + lane) & 7u;  // rotate chunks across lanes (banks)
+              const uint32_t sh = 2u * cc;                     // pair cc sits at bits (15-2cc, 14-2cc)
+              uint32_t re[4], im[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t x = w[q] << sh;
+                re[q] = x & 0xC000C000u;
+                im[q] = (x & 0x80008000u) | (~x & 0x40004000u);
+              }
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_re + ((cc ^ sw_re) << 4)),
+                           "r"(re[0]), "r"(re[1]), "r"(re[2]), "r"(re[3])
+                           : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_im + ((cc ^ sw_im) << 4)),
+                           "r"(im[0]), "r"(im[1]), "r"(im[2]), "r"(im[3])
+                           : "memory");
             }
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_re + ((cc ^ sw_re) << 4)),
-                         "r"(re[0]), "r"(re[1]), "r"(re[2]), "r"(re[3])
-                         : "memory");
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_im + ((cc ^ sw_im) << 4)),
-                         "r"(im[0]), "r"(im[1]), "r"(im[2]), "r"(im[3])
-                         : "memory");
           }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_bar(s));
         }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full_bar(s));
       }
     }
   } else {
