@@ -107,8 +107,14 @@ __device__ __forceinline__ uint32_t warp_max(uint32_t v) {
   return v;
 }
 
-// One CTA per (output row j, matrix X).  Thread t owns WPT packed words of the
-// row; word w = 4 kb + q holds the 16 weights at columns 64 kb + code_col(c, q).
+// Column (inside its 64-column block) of weight c = 4 s + 2 h + e of the
+// thread word q: 16 s + 8 h + 2 q + e, the columns whose signs share the sign
+// word of lane (g, q) in the packed layout.
+__host__ __device__ __forceinline__ int word_col(int c, int q) { return 16 * (c >> 2) + 8 * ((c >> 1) & 1) + 2 * q + (c & 1); }
+
+// One CTA per (output row j, matrix X).  Thread t owns WPT words of the row;
+// word w = 4 kb + q holds the 16 weights at columns 64 kb + word_col(c, q),
+// each code as two bits (sign, real-axis flag) at bits (2c + 1, 2c).
 // The weights stay in registers through all T stages, so HBM sees one read of
 // the row and one write of its codes and scales, and each word is assembled as
 // its codes are decided.  Row-wide maxima, counts and exact sums are block
@@ -155,7 +161,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
   // column of weight e = 16 u + c of this thread (word u of WPT)
   auto col_of = [&](int e) -> int64_t {
     const int64_t w = (int64_t)tid * WPT + (e >> 4);
-    return (w >> 2) * 64 + code_col(e & 15, (int)(w & 3));
+    return (w >> 2) * 64 + word_col(e & 15, (int)(w & 3));
   };
   float re[E], im[E];
   bool bad = false;
@@ -181,7 +187,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
   }
 
   const int64_t pbytes = plane_bytes(n, m);
-  const int g = (int)(j & 7);
+  const int g = (int)(j & 7), rho = (int)((j >> 3) & 1);
+  const int64_t rt = j >> 4;
 
   for (int t = 0; t < T; ++t) {
     // codes: real axis iff |Re| >= |Im|; negative iff the chosen component is < 0
@@ -198,7 +205,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
       const bool real = ar >= ai;
       const bool neg = real ? (re[e] < 0.0f) : (im[e] < 0.0f);
       const bool isr = in && real, isi = in && !real;
-      word[u] |= (in ? (((neg ? 1u : 0u) << 1) | (real ? 1u : 0u)) : 0u) << code_shift(c);
+      word[u] |= (in ? (((neg ? 1u : 0u) << 1) | (real ? 1u : 0u)) : 0u) << (2 * c);
       realm[u] |= (isr ? 1u : 0u) << c;
       mx0 = max(mx0, isr ? __float_as_uint(ar) : 0u);
       mx1 = max(mx1, isi ? __float_as_uint(ai) : 0u);
@@ -254,50 +261,80 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int u = e >> 4, c = e & 15;
-      const bool neg = (word[u] >> (code_shift(c) + 1)) & 1u;
+      const bool neg = (word[u] >> (2 * c + 1)) & 1u;
       const bool isr = (realm[u] >> c) & 1u;
       const float d = isr ? (neg ? -s_re : s_re) : (neg ? -s_im : s_im);
       const float upd = __fsub_rn(isr ? re[e] : im[e], d);
       re[e] = isr ? upd : re[e];
       im[e] = isr ? im[e] : upd;
     }
+    // scatter the codes into the sign and flag words of the row's tile (the
+    // plane was zeroed; the other row of each lane pair ORs its own bits)
     uint8_t* plane = codes + (int64_t)(X * T + t) * pbytes;
 #pragma unroll
     for (int u = 0; u < WPT; ++u) {
       const int64_t w = (int64_t)tid * WPT + u;
-      if ((w >> 2) < KB)
-        *reinterpret_cast<uint32_t*>(plane + word_offset(j >> 3, w >> 2, 4 * g + (int)(w & 3), KB)) = word[u];
+      const int64_t kb = w >> 2;
+      if (kb >= KB) continue;
+      const int q = (int)(w & 3);
+      uint32_t sw = 0, fw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int sidx = c >> 2, h = (c >> 1) & 1, e = c & 1;
+        const uint32_t v = (word[u] >> (2 * c)) & 3u;  // (sign, real-axis flag)
+        const uint32_t imag = (valid[u] >> c) & 1u & ~v;       // padding columns stay zero
+        sw |= (v >> 1) << sign_bit(sidx, h, rho, e);
+        fw[flag_lane(sidx, h)] |= imag << flag_bit(sidx, q, rho, e);
+      }
+      if (sw) atomicOr(reinterpret_cast<unsigned int*>(plane + pair_offset(rt, kb, 4 * g + q, KB)), sw);
+#pragma unroll
+      for (int ql = 0; ql < 4; ++ql)
+        if (fw[ql]) atomicOr(reinterpret_cast<unsigned int*>(plane + pair_offset(rt, kb, 4 * g + ql, KB) + 4), fw[ql]);
     }
   }
 }
 
 // ---------------------------------------------------------------------------
 // Canonical view of the packed codes: out[X][t][j][k] in {0: +1, 1: -1,
-// 2: +i, 3: -i}.  One thread per packed word.
+// 2: +i, 3: -i}.  One thread per (plane, row tile, column block, lane).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) unpack_codes_kernel(const uint8_t* __restrict__ codes, int64_t n, int64_t m,
                                                            int T, uint8_t* __restrict__ out) {
-  const int64_t RG = row_groups(n), KB = col_blocks(m);
-  const int64_t wpp = RG * KB * 32;
-  const int64_t total = 2 * (int64_t)T * wpp;
+  const int64_t RT = row_tiles(n), KB = col_blocks(m);
+  const int64_t per_plane = RT * KB * 32;
+  const int64_t total = 2 * (int64_t)T * per_plane;
   const int64_t pbytes = plane_bytes(n, m);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-    const int64_t plane = idx / wpp;
-    const int64_t rem = idx - plane * wpp;
-    const int64_t rg = rem / (KB * 32);
-    const int64_t rem2 = rem - rg * KB * 32;
+    const int64_t plane = idx / per_plane;
+    const int64_t rem = idx - plane * per_plane;
+    const int64_t rt = rem / (KB * 32);
+    const int64_t rem2 = rem - rt * KB * 32;
     const int64_t kb = rem2 >> 5;
     const int lane = (int)(rem2 & 31);
-    const int64_t j = rg * 8 + (lane >> 2);
-    if (j >= n) continue;
-    const int q = lane & 3;
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + plane * pbytes + word_offset(rg, kb, lane, KB));
-    uint8_t* dst = out + (plane * n + j) * m;
+    const int g = lane >> 2, q = lane & 3;
+    const uint8_t* pl = codes + plane * pbytes;
+    const uint32_t sw = *reinterpret_cast<const uint32_t*>(pl + pair_offset(rt, kb, lane, KB));
+    uint32_t fw[4];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int64_t k = kb * 64 + code_col(c, q);
-      if (k < m) dst[k] = (uint8_t)canonical_from_bits((w >> code_shift(c)) & 3u);
+    for (int ql = 0; ql < 4; ++ql) fw[ql] = *reinterpret_cast<const uint32_t*>(pl + pair_offset(rt, kb, 4 * g + ql, KB) + 4);
+#pragma unroll
+    for (int rho = 0; rho < 2; ++rho) {
+      const int64_t j = rt * 16 + 8 * rho + g;
+      if (j >= n) continue;
+      uint8_t* dst = out + (plane * n + j) * m;
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int64_t k = kb * 64 + 16 * s + 8 * h + 2 * q + e;
+            if (k >= m) continue;
+            const uint32_t sign = (sw >> sign_bit(s, h, rho, e)) & 1u;
+            const uint32_t imag = (fw[flag_lane(s, h)] >> flag_bit(s, q, rho, e)) & 1u;
+            dst[k] = (uint8_t)(2u * imag + sign);
+          }
     }
   }
 }

@@ -116,67 +116,99 @@ int resident_ctas(const void* fn, int threads, size_t smem) {
 }
 
 // Decode partition: `slots` resident CTAs shared among the problems in
-// proportion to their bytes; every CTA of a problem owns rg_per_cta
-// (<= rpc_max) consecutive row groups.  Returns the number of CTAs.
-int partition(f2i::LinearGroup& G, int slots, int rpc_max) {
+// proportion to their bytes; every CTA of a problem owns tiles_per_cta
+// (<= tiles_max) consecutive row tiles.  Returns the number of CTAs.
+int partition(f2i::LinearGroup& G, int slots, int tiles_max) {
   double total = 0.0;
   for (int i = 0; i < G.count; ++i)
-    total += (double)f2i::row_groups(G.p[i].n) * (double)f2i::col_blocks(G.p[i].m);
+    total += (double)f2i::row_tiles(G.p[i].n) * (double)f2i::col_blocks(G.p[i].m);
   int ctas = 0;
   for (int i = 0; i < G.count; ++i) {
-    const int64_t RG = f2i::row_groups(G.p[i].n);
-    const double share = (double)RG * (double)f2i::col_blocks(G.p[i].m) / total;
+    const int64_t RT = f2i::row_tiles(G.p[i].n);
+    const double share = (double)RT * (double)f2i::col_blocks(G.p[i].m) / total;
     const int64_t want = std::max<int64_t>(1, (int64_t)(slots * share));
-    const int64_t rpc = std::max<int64_t>(1, std::min<int64_t>(rpc_max, (RG + want - 1) / want));
+    const int64_t tpc = std::max<int64_t>(1, std::min<int64_t>(tiles_max, (RT + want - 1) / want));
     G.p[i].cta_begin = ctas;
-    G.p[i].rg_per_cta = (int32_t)rpc;
-    ctas += (int)((RG + rpc - 1) / rpc);
+    G.p[i].tiles_per_cta = (int32_t)tpc;
+    ctas += (int)((RT + tpc - 1) / tpc);
   }
   return ctas;
 }
 
 template <int NPL, int TILES>
-fairy2i_status launch_mma_t(f2i::LinearGroup& G, size_t smem, int rpc_max, cudaStream_t s) {
+fairy2i_status launch_mma_t(f2i::LinearGroup& G, size_t smem, int tiles_max, cudaStream_t s) {
   auto k = f2i::linear_mma_kernel<NPL, TILES>;
   const void* fn = reinterpret_cast<const void*>(k);
   fairy2i_status st = ensure_smem(fn, smem, "mma decode");
   if (st != FAIRY2I_OK) return st;
   const int slots = sm_count() * resident_ctas(fn, f2i::kMmaWarps * 32, smem);
-  const int ctas = partition(G, slots, rpc_max);
+  const int ctas = partition(G, slots, tiles_max);
   k<<<ctas, f2i::kMmaWarps * 32, smem, s>>>(G);
   return check_launch("mma decode launch");
 }
 
 template <int NPL>
-fairy2i_status launch_mma_tiles(f2i::LinearGroup& G, int tiles, size_t smem, int rpc_max, cudaStream_t s) {
-  return tiles == 1 ? launch_mma_t<NPL, 1>(G, smem, rpc_max, s) : launch_mma_t<NPL, 2>(G, smem, rpc_max, s);
+fairy2i_status launch_mma_tiles(f2i::LinearGroup& G, int tiles, size_t smem, int tiles_max, cudaStream_t s) {
+  return tiles == 1   ? launch_mma_t<NPL, 1>(G, smem, tiles_max, s)
+         : tiles == 2 ? launch_mma_t<NPL, 2>(G, smem, tiles_max, s)
+                      : launch_mma_t<NPL, 4>(G, smem, tiles_max, s);
 }
 
-// One launch of the bf16 mma decode for up to 8 tokens of every problem in
-// G.  Shared memory: the staged activations ([M][2][x_stride] bfloat16) and
-// the per-warp partial outputs of up to rpc_max row groups.
+// One launch of the sparse mma decode for up to 8 tokens of every problem in
+// G (two tokens per mma).  Shared memory: the code rings, the staged
+// activations ([2M + 1][x_stride] bfloat16) and the per-warp partial outputs
+// of up to tiles_max row tiles.
 constexpr int kMmaTokens = 8;
 
 fairy2i_status run_mma(f2i::LinearGroup& G, int T, cudaStream_t s) {
-  const int tiles = G.M <= 4 ? 1 : 2;
+  const int tiles = G.M <= 2 ? 1 : G.M <= 4 ? 2 : 4;
+  const int npl = 2 * T;
   int64_t xstr_max = 0;
   for (int i = 0; i < G.count; ++i) xstr_max = std::max(xstr_max, f2i::x_stride(G.p[i].m));
-  const size_t xbytes = (((size_t)G.M * 2 * xstr_max * sizeof(uint16_t)) + 15) & ~(size_t)15;
-  const size_t per_rg = (size_t)f2i::kMmaWarps * tiles * 32 * sizeof(float2);
-  // Two CTAs per SM when the staged activations leave room for at least four
-  // row groups of partial outputs; otherwise one CTA with up to 200 KB.
-  const size_t limit = xbytes + 4 * per_rg <= 110 * 1024 ? 110 * 1024 : 200 * 1024;
-  if (xbytes + per_rg > limit)
-    return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode: staged activations need %zu bytes of shared memory", xbytes);
-  const int rpc_max = (int)std::min<size_t>(f2i::kMaxRowGroupsPerCta, (limit - xbytes) / per_rg);
-  const size_t smem = xbytes + (size_t)rpc_max * per_rg;
+  const size_t ring = (size_t)f2i::kMmaWarps * 2 * npl * 512;
+  const size_t xbytes = (((size_t)(2 * G.M + 1) * xstr_max * sizeof(uint16_t)) + 15) & ~(size_t)15;
+  const size_t per_tile = (size_t)f2i::kMmaWarps * tiles * 64 * sizeof(float2);
+  // Two CTAs per SM when the buffers leave room for at least four row tiles
+  // of partial outputs; otherwise one CTA with up to 200 KB.
+  const size_t fixed = ring + xbytes;
+  const size_t limit = fixed + 4 * per_tile <= 110 * 1024 ? 110 * 1024 : 200 * 1024;
+  if (fixed + per_tile > limit)
+    return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode: buffers need %zu bytes of shared memory", fixed + per_tile);
+  const int tiles_max = (int)std::min<size_t>(f2i::kMaxTilesPerCta, (limit - fixed) / per_tile);
+  const size_t smem = fixed + (size_t)tiles_max * per_tile;
   switch (T) {
-    case 1: return launch_mma_tiles<2>(G, tiles, smem, rpc_max, s);
-    case 2: return launch_mma_tiles<4>(G, tiles, smem, rpc_max, s);
-    case 3: return launch_mma_tiles<6>(G, tiles, smem, rpc_max, s);
-    case 4: return launch_mma_tiles<8>(G, tiles, smem, rpc_max, s);
+    case 1: return launch_mma_tiles<2>(G, tiles, smem, tiles_max, s);
+    case 2: return launch_mma_tiles<4>(G, tiles, smem, tiles_max, s);
+    case 3: return launch_mma_tiles<6>(G, tiles, smem, tiles_max, s);
+    case 4: return launch_mma_tiles<8>(G, tiles, smem, tiles_max, s);
     default: return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode supports T <= 4 (got %d)", T);
   }
+}
+
+// Tokens per sparse-mma launch: 8, or fewer when the staged activations of
+// the widest layer of the group would not fit in shared memory.
+int mma_chunk(const fairy2i_packed* qs, int count, int T) {
+  int64_t xstr_max = 0;
+  for (int i = 0; i < count; ++i) xstr_max = std::max(xstr_max, f2i::x_stride(qs[i].m));
+  const size_t ring = (size_t)f2i::kMmaWarps * 2 * (2 * T) * 512;
+  for (int mc = kMmaTokens; mc > 1; mc /= 2) {
+    const size_t xbytes = (((size_t)(2 * mc + 1) * xstr_max * sizeof(uint16_t)) + 15) & ~(size_t)15;
+    const int tiles = mc <= 2 ? 1 : mc <= 4 ? 2 : 4;
+    if (ring + xbytes + (size_t)f2i::kMmaWarps * tiles * 64 * sizeof(float2) <= 200 * 1024) return mc;
+  }
+  return 1;
+}
+
+// Whether a sparse-mma launch of these layers with mc tokens keeps two CTAs
+// per SM (the same rule run_mma applies).
+bool mma_two_ctas(const fairy2i_packed* qs, int count, int T, int mc) {
+  int64_t xstr_max = 0;
+  for (int i = 0; i < count; ++i) xstr_max = std::max(xstr_max, f2i::x_stride(qs[i].m));
+  const int tiles = mc <= 2 ? 1 : mc <= 4 ? 2 : 4;
+  const size_t ring = (size_t)f2i::kMmaWarps * 2 * (2 * T) * 512;
+  const size_t xbytes = (((size_t)(2 * mc + 1) * xstr_max * sizeof(uint16_t)) + 15) & ~(size_t)15;
+  const size_t per_tile = (size_t)f2i::kMmaWarps * tiles * 64 * sizeof(float2);
+  return ring + xbytes + 4 * per_tile <= 110 * 1024;
 }
 
 fairy2i_status run_addsub(f2i::LinearGroup& G, cudaStream_t s) {
@@ -184,7 +216,7 @@ fairy2i_status run_addsub(f2i::LinearGroup& G, cudaStream_t s) {
   int64_t m_pad_max = 0;
   for (int i = 0; i < G.count; ++i) {
     G.p[i].cta_begin = ctas;
-    ctas += (int)((f2i::row_groups(G.p[i].n) + f2i::kAddSubWarps - 1) / f2i::kAddSubWarps);
+    ctas += (int)((f2i::row_tiles(G.p[i].n) + f2i::kAddSubWarps - 1) / f2i::kAddSubWarps);
     m_pad_max = std::max(m_pad_max, f2i::col_blocks(G.p[i].m) * 64);
   }
   const size_t smem = (size_t)f2i::kAddSubTok * m_pad_max * sizeof(uint32_t);
@@ -319,21 +351,42 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
     return run_tcgen05(qs, xs, ys, count, M, T, s);
   }
 
-  const int chunk = (a == FAIRY2I_ALGO_MMA) ? kMmaTokens : f2i::kAddSubTok * 1024;
-  for (int p0 = 0; p0 < count; p0 += f2i::kMaxGroup) {
-    const int cnt = std::min(f2i::kMaxGroup, count - p0);
+  // Launch order: when the widest layer's staged activations would leave the
+  // mma decode one CTA per SM, layers are launched in groups of equal
+  // activation width (the buffer of a launch is sized for its widest layer),
+  // keeping the caller's order inside a width.
+  std::vector<int> order(count);
+  for (int i = 0; i < count; ++i) order[i] = i;
+  bool split = false;
+  if (a == FAIRY2I_ALGO_MMA) {
+    const int mc = (int)std::min<int64_t>(M, mma_chunk(qs, count, T));
+    split = !mma_two_ctas(qs, count, T, mc);
+    if (split)
+      std::stable_sort(order.begin(), order.end(),
+                       [&](int u, int v) { return f2i::x_stride(qs[u].m) < f2i::x_stride(qs[v].m); });
+  }
+  for (int b0 = 0; b0 < count;) {
+    int b1 = b0 + 1;
+    while (b1 < count && b1 - b0 < f2i::kMaxGroup &&
+           (!split || f2i::x_stride(qs[order[b1]].m) == f2i::x_stride(qs[order[b0]].m)))
+      ++b1;
+    const int cnt = b1 - b0;
+    std::vector<fairy2i_packed> sub(cnt);
+    for (int i = 0; i < cnt; ++i) sub[i] = qs[order[b0 + i]];
+    const int chunk = (a == FAIRY2I_ALGO_MMA) ? mma_chunk(sub.data(), cnt, T) : f2i::kAddSubTok * 1024;
     for (int64_t t0 = 0; t0 < M; t0 += chunk) {
       f2i::LinearGroup G;
       memset(&G, 0, sizeof(G));
       G.count = cnt;
       G.M = (int32_t)std::min<int64_t>(chunk, M - t0);
       for (int i = 0; i < cnt; ++i) {
-        const fairy2i_packed& q = qs[p0 + i];
+        const int li = order[b0 + i];
+        const fairy2i_packed& q = qs[li];
         f2i::LinearProblem& P = G.p[i];
         P.codes = static_cast<const uint8_t*>(q.codes);
         P.scales = q.scales;
-        P.x = static_cast<const uint16_t*>(xs[p0 + i]) + t0 * 2 * q.m;
-        P.y = ys[p0 + i] + t0 * 2 * q.n;
+        P.x = static_cast<const uint16_t*>(xs[li]) + t0 * 2 * q.m;
+        P.y = ys[li] + t0 * 2 * q.n;
         P.n = q.n;
         P.m = q.m;
         P.T = q.T;
@@ -341,6 +394,7 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
       fairy2i_status st = (a == FAIRY2I_ALGO_MMA) ? run_mma(G, T, s) : run_addsub(G, s);
       if (st != FAIRY2I_OK) return st;
     }
+    b0 = b1;
   }
   return ok();
 }
@@ -392,7 +446,7 @@ fairy2i_status fairy2i_quantize(const void* U, const void* W, int64_t n, int64_t
                 (long long)out->n, (long long)out->m, out->T, (long long)n, (long long)m, T);
   if (n > INT32_MAX) return fail(FAIRY2I_ERR_UNSUPPORTED, "n too large");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((n & 7) != 0) {  // padding rows of the last row group stay zero
+  {  // the kernel ORs each row's bits into words shared with the other row of its lane pair
     cudaError_t e = cudaMemsetAsync(out->codes, 0, fairy2i_codes_bytes(n, m, T), s);
     if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "memset codes: %s", cudaGetErrorString(e));
   }

@@ -1,64 +1,67 @@
-// Packed code layout (version 1) and small shared device helpers.
+// Packed code layout (version 2) and small shared device helpers.
 //
 // A code plane (one matrix U or W, one stage t) of an n x m layer:
-//   rows in groups of 8 (row group rg = j / 8, g = j % 8),
-//   columns in blocks of 64 (block kb = k / 64),
-//   one 128-byte tile of 32 words per (rg, kb); word (4g + q) holds 16 codes
-//   of row j, each as two bits (sign, real-axis flag).
-// Code c = 0..15 of a word, with s = c >> 2, h = (c >> 1) & 1, e = c & 1,
-// is column  64 kb + 16 s + 8 h + 2 q + e  and sits in bits
-// (15 + 16 e - 2 P, 14 + 16 e - 2 P) with P = 2 s + h.
-// Why: in an mma.sync m16n8k16 bf16 A fragment whose row g is the real-axis
-// row of output 8 rg + g and row g + 8 its imaginary-axis row, lane (g, q)
-// holds for step s the columns 16 s + 2 q + {0, 1} (P = 2 s) and
-// 16 s + 8 + 2 q + {0, 1} (P = 2 s + 1), two per register, low column in
-// the low half.  Shifting the word left by 2 P puts both codes of pair P in
-// bits (15, 14) and (31, 30); then `& 0xC000C000` is the real-axis register
-// and `(w & 0x80008000) | (~w & 0x40004000)` the imaginary-axis register,
-// as bfloat16 values in {+2, -2, +0, -0} (2.0 = 0x4000).
-// Within a row group the 128-byte tiles are stored in chunks of four blocks
-// so that lane (4g + q) finds its words of four consecutive blocks in 16
-// contiguous bytes; the last chunk holds the remaining r = KB % 4 blocks
-// with r words per lane.
+//   rows in tiles of 16 (row tile rt = j / 16; rows 16 rt + 8 rho + g with
+//   rho in {0, 1}, g in 0..7), columns in blocks of 64 (block kb = k / 64),
+//   one 256-byte tile per (rt, kb): 32 lanes, lane (g, q) = 4 g + q, each with
+//   a sign word S and a flag word F (sign 1 = the code is -1 or -i, flag 1 =
+//   the code is +i or -i).
+//
+// The words are laid out for the sparse tensor-core form of the layer.  With
+// each code's real-axis and imaginary-axis slots interleaved along K, every
+// two codes form a group of four K slots holding exactly two nonzeros, i.e.
+// 2:4 structured sparsity: `mma.sp m16n8k32` takes the nonzero values (the
+// signs, as bfloat16 +-2) from S and the slot indices (the axis flags) from F.
+//   S of lane (g, q): for step s = 0..3 (16 columns each) and fragment
+//     register i = 0..3 (rho = i & 1, h = i >> 1), r = 4 s + i: bit 15 - r is
+//     the sign of row rho, column 64 kb + 16 s + 8 h + 2 q, and bit 31 - r the
+//     sign of the next column.  Shifting S left by r puts the two signs of
+//     register i of step s at bits 15 and 31.
+//   F of lane (g, q): the lane supplies the metadata of steps
+//     sA = 2 (q >> 1) + d (d = 0, 1) for column groups grp = 4 (q & 1) + n'
+//     (n' = 0..3; group = columns 16 sA + 2 grp, + 1) of rows rho = 0, 1:
+//     nibble nb = n' + 4 rho holds the flag of the even column at bit
+//     4 nb + d and of the odd column at bit 4 nb + 2 + d.  The metadata word
+//     of step sA is then ((F >> d) & 0x55555555) | 0x88888888 (indices
+//     0/1 for the even code's real/imaginary slot, 2/3 for the odd code's).
+// Storage per row tile: blocks in chunks of two, lane-major, so that a lane's
+// (S, F) of two consecutive blocks are 16 contiguous bytes; an odd last block
+// stores 8 bytes per lane.  Padding rows and columns hold zero bits.
 #pragma once
 #include <cstdint>
 
 namespace f2i {
 
-constexpr int kRowsPerGroup = 8;
+constexpr int kRowsPerTile = 16;
 constexpr int kColsPerBlock = 64;
-constexpr int kTileBytes = 128;  // one (row group, column block)
+constexpr int kTileBytes = 256;  // one (row tile, column block)
 
-__host__ __device__ __forceinline__ int64_t row_groups(int64_t n) { return (n + 7) / 8; }
+__host__ __device__ __forceinline__ int64_t row_tiles(int64_t n) { return (n + 15) / 16; }
 __host__ __device__ __forceinline__ int64_t col_blocks(int64_t m) { return (m + 63) / 64; }
 __host__ __device__ __forceinline__ int64_t plane_bytes(int64_t n, int64_t m) {
-  return row_groups(n) * col_blocks(m) * kTileBytes;
+  return row_tiles(n) * col_blocks(m) * kTileBytes;
 }
 
-// Byte offset inside a plane of the word of lane `lane` (= 4g + q) for row
-// group rg and column block kb, in a plane with KB column blocks.
-__host__ __device__ __forceinline__ int64_t word_offset(int64_t rg, int64_t kb, int lane, int64_t KB) {
-  const int64_t base = rg * KB * kTileBytes;
-  const int64_t full = KB >> 2;
-  const int64_t c = kb >> 2;
-  if (c < full) return base + c * 512 + lane * 16 + (kb & 3) * 4;
-  const int64_t r = KB - (full << 2);
-  return base + full * 512 + lane * (4 * r) + (kb - (full << 2)) * 4;
+// Byte offset inside a plane of the (S, F) pair of lane `lane` for row tile
+// rt and column block kb, in a plane with KB column blocks.
+__host__ __device__ __forceinline__ int64_t pair_offset(int64_t rt, int64_t kb, int lane, int64_t KB) {
+  const int64_t base = rt * KB * kTileBytes;
+  const int64_t fullc = KB >> 1;
+  if ((kb >> 1) < fullc) return base + (kb >> 1) * 512 + lane * 16 + (kb & 1) * 8;
+  return base + fullc * 512 + lane * 8;
 }
 
-// Column offset inside the 64-column block of code c (0..15) of lane q.
-__host__ __device__ __forceinline__ int code_col(int c, int q) {
-  return 16 * (c >> 2) + 8 * ((c >> 1) & 1) + 2 * q + (c & 1);
+// Bit of the sign of (row rho, column 16 s + 8 h + 2 q + e of a block) in the
+// S word of lane (g, q).
+__host__ __device__ __forceinline__ int sign_bit(int s, int h, int rho, int e) {
+  return 15 + 16 * e - (4 * s + 2 * h + rho);
 }
-// Shift that brings code c (0..15) of a word to bits 1..0.
-__host__ __device__ __forceinline__ int code_shift(int c) {
-  return 14 + 16 * (c & 1) - 2 * (2 * (c >> 2) + ((c >> 1) & 1));
-}
-
-// 2-bit internal code (sign << 1 | real_flag)  <->  canonical 0..3
-// (0 = +1, 1 = -1, 2 = +i, 3 = -i).
-__host__ __device__ __forceinline__ uint32_t canonical_from_bits(uint32_t v) {
-  return ((v & 1u) ? 0u : 2u) + (v >> 1);
+// The lane q and the bit of the axis flag of (row rho, column 16 s + 8 h +
+// 2 q' + e) in an F word: group 4 h + q' of step s is supplied by lane
+// q = h + 2 (s >> 1), nibble q' + 4 rho, bit (s & 1) + 2 e of the nibble.
+__host__ __device__ __forceinline__ int flag_lane(int s, int h) { return h + 2 * (s >> 1); }
+__host__ __device__ __forceinline__ int flag_bit(int s, int qp, int rho, int e) {
+  return 4 * (qp + 4 * rho) + (s & 1) + 2 * e;
 }
 
 // Per-device error word (bit flags), read and cleared by fairy2i_sync_status.

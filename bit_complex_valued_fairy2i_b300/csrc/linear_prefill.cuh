@@ -21,11 +21,12 @@
 // Every product is exact (+-2 times a bfloat16); only the fp32 accumulation
 // rounds.  The factor 2 is removed with the scale (exact).
 //
-// Warp roles (8 warps, one CTA per SM, persistent over tiles):
+// Warp roles (14 warps, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer for B
 //   warp 1      TMEM allocation; one thread issues tcgen05.mma / commit
-//   warps 2-3   A producers: codes -> swizzled bfloat16 tiles
-//   warps 4-7   epilogue: tcgen05.ld, scales, reduction over the RO code
+//   warps 2-9   A producers: codes -> swizzled bfloat16 tiles (two groups of
+//               four warps, alternate k-blocks)
+//   warps 10-13 epilogue: tcgen05.ld, scales, reduction over the RO code
 //               rows of each output (lane shuffles), stores y
 // All mbarrier waits are bounded (about 2 s); a wait that gives up raises the
 // timeout flag of the device error word and every role winds down.
@@ -44,7 +45,10 @@ constexpr int kPfBK = 64;   // columns per k-block: one 128-byte swizzle row of 
 constexpr int kPfTokens = kPfBN / 2;
 constexpr int kPfAStage = kPfBM * kPfBK * 2;  // 16 KB
 constexpr int kPfBStage = kPfBN * kPfBK * 2;  // 32 KB
-constexpr int kPfThreads = 256;
+constexpr int kPfProducerWarps = 8;
+constexpr int kPfProducerGroups = 2;  // groups fill alternate k-blocks concurrently
+constexpr int kPfGroupWarps = kPfProducerWarps / kPfProducerGroups;
+constexpr int kPfThreads = 32 * (6 + kPfProducerWarps);
 constexpr uint32_t kPfTmemCols = 512;  // two 256-column fp32 accumulators
 constexpr size_t kPfSmemBytes =
     1024 /* alignment slack */ + (size_t)kPfStages * (kPfAStage + kPfBStage) + 256 /* barriers, TMEM address */;
@@ -91,24 +95,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As above, but the thread may be suspended for up to `ns` nanoseconds while
+// the phase is incomplete (it resumes as soon as the phase completes), so
+// waiting warps do not take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
 // Wait for the phase of `parity` to complete.  Gives up after about 2 s, or
-// at once when another role of the CTA has given up (`abort_flag`); then the
+// soon after another role of the CTA has given up (`abort_flag`); then the
 // device error word gets the timeout flag and false is returned.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > 2000000000ull) {
-      *abort_flag = 1;
-      f2i_raise(kErrTimeout);
-      return false;
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((i & 15) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > 2000000000ull) {
+        *abort_flag = 1;
+        f2i_raise(kErrTimeout);
+        return false;
+      }
     }
   }
 }
@@ -167,6 +187,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// (x & m) | 0x40004000 in one LOP3 (m held in a register): the signs at bits
+// 15 and 31 become bfloat16 +-2.
+__device__ __forceinline__ uint32_t sign_operand_pf(uint32_t x, uint32_t m) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, 0x40004000, 0xEA;" : "=r"(r) : "r"(x), "r"(m));
+  return r;
+}
+
+// (x & m) | f in one LOP3 (m = 0x80008000 held in a register; f has bits at
+// 14 and 30 only): the signs of x at 15 and 31 and the flags of f form
+// bfloat16 {+-2, +-0}.
+__device__ __forceinline__ uint32_t real_operand_pf(uint32_t x, uint32_t m, uint32_t f) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(m), "r"(f));  // (x & m) | f
+  return r;
+}
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes in 1024-byte groups of eight (stride byte offset 1024).
@@ -230,7 +267,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
 
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) {
-      mbar_init(full_bar(s), 3);  // TMA arrive.expect_tx + one arrive per A-producer warp
+      mbar_init(full_bar(s), 1 + kPfGroupWarps);  // TMA arrive.expect_tx + one arrive per warp of the producing group
       mbar_init(empty_bar(s), 1); // tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -246,10 +283,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
     tmem_alloc(smem_u32(tmem_slot), kPfTmemCols);
     tmem_relinquish();
   }
-  if (warp == 2 || warp == 3) {
+  if (warp >= 2 && warp < 2 + kPfProducerWarps) {
     // zero every A stage once: code rows that no output uses (T = 3) stay zero
     const int i = tid - 64;
-    for (uint32_t off = (uint32_t)i * 16u; off < (uint32_t)(kPfStages * kPfAStage); off += 64u * 16u)
+    for (uint32_t off = (uint32_t)i * 16u; off < (uint32_t)(kPfStages * kPfAStage); off += 32u * kPfProducerWarps * 16u)
       asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sA + off), "r"(0u) : "memory");
     fence_async_smem();
   }
@@ -311,61 +348,78 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
         if (ok) tc_commit(accf_bar(b));
       }
     }
-  } else if (warp == 2 || warp == 3) {
+  } else if (warp < 2 + kPfProducerWarps) {
     // ---------------- A producers: codes -> bfloat16 {+-2, +-0} ----------------
-    // Thread i owns code plane p of output jj of every tile: rows RO*jj + 2p
-    // (real axis) and RO*jj + 2p + 1 (imaginary axis).  The packed words of a
-    // whole chunk of four 64-column blocks are one 16-byte load per word
-    // column q; the next chunk (of this tile or the next) is loaded while the
-    // current one is expanded, so the load latency overlaps the MMAs.
-    const int i = tid - 64;
+    // Two groups of four warps fill alternate k-blocks, so two stages are
+    // being expanded at any time.  Inside a group, thread (i, hf) owns code
+    // plane p of output jj of every tile, steps 2 hf and 2 hf + 1: rows
+    // RO*jj + 2p (real axis) and RO*jj + 2p + 1 (imaginary axis), chunks
+    // 4 hf .. 4 hf + 3.  A 16-byte chunk is 8 columns 16 s + 8 h + 2 q' + e
+    // (q' = 0..3): the signs come from the sign words of the four lanes
+    // (g, q') of the output's lane quad, the axis flags from the flag word of
+    // lane (g, h + 2 (s >> 1)).  The quad's words of two blocks are 64
+    // contiguous bytes; the next pair of blocks (of this tile or the next) is
+    // loaded while the current one is expanded.
+    const int gt = tid - 64;
+    const int grp = gt / (32 * kPfGroupWarps);
+    const int lt = gt - grp * 32 * kPfGroupWarps;
+    const int pi = lt >> 1, hf = lt & 1;
     const int planes = 2 * T;
-    const bool active = i < J * planes;
-    const int jj = active ? i / planes : 0;
-    const int p = active ? i - jj * planes : 0;
+    const bool active = pi < J * planes;
+    const int jj = active ? pi / planes : 0;
+    const int p = active ? pi - jj * planes : 0;
     const uint32_t r_re = (uint32_t)(RO * jj + 2 * p);
     const uint32_t row_re = r_re * 128u, row_im = (r_re + 1u) * 128u;
     const uint32_t sw_re = r_re & 7u, sw_im = (r_re + 1u) & 7u;
+    const uint32_t smask = 0x80008000u + (uint32_t)(P.M >> 30);  // register-held mask (M < 2^30)
 
-    // chunk cursor over (tile, chunk) in this CTA's tile order
+    // loader cursor: tile, its problem's row base and pair count
     int64_t ld_tile = blockIdx.x;
-    int64_t ld_ch = 0;
-    uint4 nxt[4];
-    auto load_chunk = [&](int64_t tile, int64_t ch, uint4 (&dst)[4]) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-      if (tile >= P.total_tiles) return;
-      const PfTile c = pf_tile(P, tile);
+    int64_t ld_c2 = 0;
+    const uint8_t* ld_tp = nullptr;  // this thread's row tile of plane p (null: nothing to load)
+    int64_t ld_fullc = 0, ld_pairs = 0;
+    int ld_g = 0;
+    auto set_ld_tile = [&]() {
+      ld_tp = nullptr;
+      if (ld_tile >= P.total_tiles) return;
+      const PfTile c = pf_tile(P, ld_tile);
       const PrefillProblem& pr = P.p[c.pi];
+      const int64_t KB = col_blocks(pr.m);
+      ld_fullc = KB >> 1;
+      ld_pairs = (KB + 1) >> 1;
       const int64_t j = c.rt * J + jj;
       if (!active || j >= pr.n) return;
-      const int64_t KB = col_blocks(pr.m);
-      const int64_t full = KB >> 2;
-      const int g = (int)(j & 7);
-      const uint8_t* rowp = pr.codes + (int64_t)p * plane_bytes(pr.n, pr.m) + (j >> 3) * KB * kTileBytes;
-      if (ch < full) {
+      ld_g = (int)(j & 7);
+      ld_tp = pr.codes + (int64_t)p * plane_bytes(pr.n, pr.m) + (j >> 4) * KB * kTileBytes;
+    };
+    uint4 nxt[4];
+    auto load_pair = [&](uint4 (&dst)[4]) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = __ldg(reinterpret_cast<const uint4*>(rowp + ch * 512 + (4 * g + q) * 16));
+      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (!ld_tp) return;
+      if (ld_c2 < ld_fullc) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = __ldg(reinterpret_cast<const uint4*>(ld_tp + ld_c2 * 512 + (4 * ld_g + q) * 16));
       } else {
-        const int tail = (int)(KB - 4 * full);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t* t = reinterpret_cast<const uint32_t*>(rowp + full * 512 + (int64_t)(4 * g + q) * 4 * tail);
-          dst[q].x = __ldg(t);
-          dst[q].y = tail > 1 ? __ldg(t + 1) : 0u;
-          dst[q].z = tail > 2 ? __ldg(t + 2) : 0u;
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(ld_tp + ld_fullc * 512 + (4 * ld_g + q) * 8));
+          dst[q].x = v.x;
+          dst[q].y = v.y;
         }
       }
     };
     auto advance = [&]() {
       if (ld_tile >= P.total_tiles) return;
-      const PfTile c = pf_tile(P, ld_tile);
-      if (++ld_ch * 4 >= P.p[c.pi].kblocks) {
-        ld_ch = 0;
+      if (++ld_c2 == ld_pairs) {
+        ld_c2 = 0;
         ld_tile += gridDim.x;
+        set_ld_tile();
       }
     };
-    load_chunk(ld_tile, ld_ch, nxt);
+    set_ld_tile();
+    load_pair(nxt);
     advance();
 
     uint32_t it = 0;
@@ -373,20 +427,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
     for (int64_t tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
       const PfTile c = pf_tile(P, tile);
       const PrefillProblem& pr = P.p[c.pi];
-      const bool live = active && (c.rt * J + jj) < pr.n;
-      for (int kb0 = 0; ok && kb0 < pr.kblocks; kb0 += 4) {
+      const int64_t j = c.rt * J + jj;
+      const bool live = active && j < pr.n;
+      const int rho = (int)((j >> 3) & 1);
+      for (int kb0 = 0; ok && kb0 < pr.kblocks; kb0 += 2) {
         uint4 cur[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
-        load_chunk(ld_tile, ld_ch, nxt);
+        load_pair(nxt);
         advance();
-        const int nb = min(4, pr.kblocks - kb0);
+        const int nb = min(2, pr.kblocks - kb0);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
+        for (int b = 0; b < 2; ++b) {
           if (b >= nb) break;
           const int s = (int)(it % kPfStages);
           const uint32_t ph = (it / kPfStages) & 1u;
+          const bool mine = (int)(it % kPfProducerGroups) == grp;
           ++it;
+          if (!mine) continue;
           bool got = true;
           if (lane == 0) got = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag);
           got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
@@ -396,26 +454,34 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
           }
           if (live) {
             const uint32_t st = sA + (uint32_t)s * kPfAStage;
-            uint32_t w[4];
+            uint32_t S[4], F[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) w[q] = b == 0 ? cur[q].x : b == 1 ? cur[q].y : b == 2 ? cur[q].z : cur[q].w;
+            for (int q = 0; q < 4; ++q) {
+              S[q] = (b == 0 ? cur[q].x : cur[q].z) << rho;         // row rho's signs one bit up
+              F[q] = ~(b == 0 ? cur[q].y : cur[q].w) >> (16 * rho);  // real-axis flags of row rho in the low half
+            }
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-              const uint32_t cc = (uint32_t)(c8 + lane) & 7u;  // rotate chunks across lanes (banks)
-              const uint32_t sh = 2u * cc;                     // pair cc sits at bits (15-2cc, 14-2cc)
-              uint32_t re[4], im[4];
+            for (int ss = 0; ss < 2; ++ss) {
+              const int sstep = 2 * hf + ss;  // 16-column step of the block
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint32_t x = w[q] << sh;
-                re[q] = x & 0xC000C000u;
-                im[q] = (x & 0x80008000u) | (~x & 0x40004000u);
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t cc = (uint32_t)(2 * sstep + h);  // 16-byte chunk of the 128-byte row
+                const uint32_t fword = F[h + 2 * hf];           // flag word of lane (g, h + 2 (s >> 1))
+                uint32_t re[4], im[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  // real flags of columns (2q, 2q + 1) at bits 0 and 2, then at bits 14 and 30
+                  const uint32_t fr = (((fword >> (4 * q + (sstep & 1))) & 5u) * 0x10004000u) & 0x40004000u;
+                  re[q] = real_operand_pf(S[q] << (4 * sstep + 2 * h), smask, fr);  // (sign, real flag)
+                  im[q] = re[q] ^ 0x40004000u;                                      // (sign, imaginary flag)
+                }
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_re + ((cc ^ sw_re) << 4)),
+                             "r"(re[0]), "r"(re[1]), "r"(re[2]), "r"(re[3])
+                             : "memory");
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_im + ((cc ^ sw_im) << 4)),
+                             "r"(im[0]), "r"(im[1]), "r"(im[2]), "r"(im[3])
+                             : "memory");
               }
-              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_re + ((cc ^ sw_re) << 4)),
-                           "r"(re[0]), "r"(re[1]), "r"(re[2]), "r"(re[3])
-                           : "memory");
-              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_im + ((cc ^ sw_im) << 4)),
-                           "r"(im[0]), "r"(im[1]), "r"(im[2]), "r"(im[3])
-                           : "memory");
             }
           }
           fence_async_smem();

@@ -46,27 +46,29 @@ typedef enum {
     FAIRY2I_ERR_TIMEOUT = 6      /* a bounded device-side wait gave up */
 } fairy2i_status;
 
-#define FAIRY2I_LAYOUT_VERSION 1
+#define FAIRY2I_LAYOUT_VERSION 2
 #define FAIRY2I_MAX_T 8
 #define FAIRY2I_MAX_M 16384
 
 /* Packed quantized layer (both U and W).
  *
- * codes: FAIRY2I_LAYOUT_VERSION 1 layout, fairy2i_codes_bytes(n, m, T)
+ * codes: FAIRY2I_LAYOUT_VERSION 2 layout, fairy2i_codes_bytes(n, m, T)
  *   bytes, 256-byte aligned.  2T code planes, plane (X, t) for X = 0 (U),
  *   1 (W) at byte offset (X*T + t) * plane_bytes with plane_bytes =
- *   ceil(n/8) * ceil(m/64) * 128.  Inside a plane, rows come in groups of 8
- *   and columns in blocks of 64; each (row group, column block) is 32
- *   little-endian 32-bit words, word (4g + q) holding 16 codes of row
- *   8*group + g, each as two bits (sign, real-axis flag) -- sign 1 means
- *   negative, flag 1 means the code is +-1, flag 0 means +-i.  Code c of
- *   the word (s = c/4, h = (c/2)%2, e = c%2) is column
- *   64*block + 16s + 8h + 2q + e, in bits (15 + 16e - 2P, 14 + 16e - 2P)
- *   with P = 2s + h.  Within a row group, blocks are stored in chunks of
- *   four so that a thread's words for four consecutive blocks are 16
- *   contiguous bytes (a tail chunk holds the remaining 1-3 blocks the same
- *   way).  Padding rows and columns hold zero bits.  The layout is opaque to
- *   callers; fairy2i_unpack_codes() gives the canonical view.
+ *   ceil(n/16) * ceil(m/64) * 256.  Inside a plane, rows come in tiles of 16
+ *   and columns in blocks of 64; each (row tile, column block) holds 32 lanes
+ *   (g, q) = 4g + q of two little-endian 32-bit words: a sign word (bit set =
+ *   the code is -1 or -i) and an axis-flag word (bit set = the code is +i or
+ *   -i).  Lane (g, q) carries rows g and g + 8 of the tile:
+ *     sign of (row 8 rho + g, column 16 s + 8 h + 2 q + e) at bit
+ *       15 + 16 e - (4 s + 2 h + rho) of the sign word of lane (g, q);
+ *     flag of (row 8 rho + g, column 16 s + 8 h + 2 q' + e) at bit
+ *       4 (q' + 4 rho) + (s & 1) + 2 e of the flag word of lane
+ *       (g, h + 2 (s >> 1)).
+ *   Blocks are stored in chunks of two so that a lane's words of two
+ *   consecutive blocks are 16 contiguous bytes (an odd last block stores 8
+ *   bytes per lane).  Padding rows and columns hold zero bits.  The layout is
+ *   opaque to callers; fairy2i_unpack_codes() gives the canonical view.
  * scales: fairy2i_scales_count(n, T) floats, [2 (U, W)][T][2 (real axis,
  *   imaginary axis)][n], 16-byte aligned. */
 typedef struct {
@@ -82,7 +84,7 @@ typedef struct {
 typedef enum {
     FAIRY2I_ALGO_AUTO = 0,    /* pick the fastest kernel for the token count */
     FAIRY2I_ALGO_ADDSUB = 1,  /* CUDA cores: adds/subtracts only, fp32 accumulation */
-    FAIRY2I_ALGO_MMA = 2,     /* decode: codes expanded to bf16 {+-2, +-0} in registers, mma.sync */
+    FAIRY2I_ALGO_MMA = 2,     /* decode: 2:4-sparse mma.sync, signs as bf16 +-2, axis flags as metadata */
     FAIRY2I_ALGO_TCGEN05 = 3  /* prefill: codes expanded to bf16 in shared memory, tcgen05.mma */
 } fairy2i_algo;
 

@@ -43,9 +43,10 @@ def test_sizes(lib):
     assert f2i.codes_bytes(2048, 2048, 2) == 2 * 2 * 2048 * 2048 // 4
     assert f2i.codes_bytes(5504, 2048, 2) == 2 * 2 * 5504 * 2048 // 4
     assert f2i.codes_bytes(2048, 5504, 2) == 2 * 2 * 2048 * 5504 // 4
-    # padding to 8 rows x 64 columns
-    assert f2i.codes_bytes(1, 1, 1) == 2 * 128
-    assert f2i.codes_bytes(9, 65, 1) == 2 * 2 * 2 * 128
+    # padding to 16 rows x 64 columns
+    assert f2i.codes_bytes(1, 1, 1) == 2 * 256
+    assert f2i.codes_bytes(9, 65, 1) == 2 * 2 * 256
+    assert f2i.codes_bytes(17, 65, 1) == 2 * 2 * 2 * 256
     assert f2i.scales_count(100, 3) == 4 * 3 * 100
     assert f2i.codes_bytes(0, 4, 1) == 0 and f2i.codes_bytes(4, 4, 9) == 0
     assert lib.fairy2i_layout_version() == f2i.LAYOUT_VERSION
