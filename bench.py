@@ -39,6 +39,10 @@ METRIC = "2-bit WL-complex GEMV weight GB/s vs HBM peak; prefill GEMM TFLOP/s"
 UNIT = "GB/s"
 T_STAGES = 2
 BLOCKS = inputs.LLAMA2_7B_BLOCKS
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch
+# of this workload, from an ncu capture of linear_mma_kernel<4,1>; must be
+# re-measured whenever that kernel changes.
+DECODE_TRAFFIC_BYTES = 51_389_952 + 8_704
 WORKLOAD = ("llama2-7b decode GEMV, M=1, T=2: 7 projections per block x 32 distinct blocks "
             "(224 projections, 1.64 GB packed > L2), one grouped launch per block")
 
@@ -211,7 +215,7 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def build_stack(f2i, blocks: int, dev):
+def build_stack(f2i, blocks: int, dev, T: int = T_STAGES):
     """Convert + quantize the stack on the GPU; times both (events)."""
     stack = []
     conv_ms = quant_ms = 0.0
@@ -224,7 +228,7 @@ def build_stack(f2i, blocks: int, dev):
             e[0].record()
             U, W = f2i.convert(R)
             e[1].record()
-            q = f2i.quantize(U, W, T_STAGES, check=False)
+            q = f2i.quantize(U, W, T, check=False)
             e[2].record()
             e[2].synchronize()
             conv_ms += e[0].elapsed_time(e[1])
@@ -321,6 +325,56 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
     return {"workload": f"llama2-7b blocks (7 projections each), T=2, {blocks} distinct blocks "
                         f"({blocks * nbytes / 1e6:.0f} MB > L2), one grouped launch per block",
             "bytes_per_block": nbytes, "rows": out}
+
+
+def stack_leg(f2i, dev, T: int, blocks: int, steps: int, warmup: int):
+    """The full 32-block LLaMA-2-7B linear stack at T stages: convert + quantize of all
+    224 projections (timed per launch), then batch-1 decode of all of them per step
+    (CUDA graph of one grouped launch per block)."""
+    stack, offline = build_stack(f2i, blocks, dev, T)
+    nbytes = sum(q.nbytes for layers in stack for q in layers)
+    xs = [[inputs.activations(5, 7 * b + pi, 1, inf, device=dev) for pi, (_, _, inf) in enumerate(inputs.LLAMA2_7B_BLOCK)]
+          for b in range(blocks)]
+    ys = [[torch.empty((1, outf), dtype=torch.float32, device=dev) for (_, outf, _) in inputs.LLAMA2_7B_BLOCK]
+          for _ in range(blocks)]
+
+    def step():
+        for b in range(blocks):
+            f2i.linear_group(stack[b], xs[b], ys[b])
+
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    f2i.sync_status()
+    ms = start.elapsed_time(stop) / steps
+    del graph, stack
+    return {"T": T, "packed_bytes": nbytes, "decode_ms_per_token": ms, "decode_GBps": nbytes / (ms * 1e-3) / 1e9,
+            "tokens_per_s": 1e3 / ms, **offline}
+
+
+def run_stack_only(args, world, rank, local):
+    import bit_complex_valued_fairy2i_b300 as f2i
+    from bit_complex_valued_fairy2i_b300 import build as f2i_build
+
+    f2i_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rows = [stack_leg(f2i, dev, T, args.blocks, max(3, min(args.steps, 200)), args.warmup) for T in (1, 2, 3)]
+    if rank == 0:
+        print(json.dumps({"stack": {"workload": f"llama2-7b linear stack, {args.blocks} blocks x 7 projections, M=1",
+                                    "rows": rows}}), flush=True)
 
 
 def run_sweep_only(args, world, rank, local):
@@ -421,7 +475,7 @@ def run_ours(args, world, rank, local):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16 mma.sync (codes as bf16 {+-2,+-0}, bf16 x), fp32 accumulate",
+        "vs_baseline": None, "dtype": "bf16 (2:4-sparse mma.sync: code signs as bf16 +-2, bf16 x), fp32 accumulate",
         "data": "synthetic",
         "config": {"workload": WORKLOAD if blocks == BLOCKS else f"{blocks}-block cut of: {WORKLOAD}",
                    "M": 1, "T": T_STAGES, "blocks": blocks, "projections": 7 * blocks,
@@ -430,8 +484,8 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": blocks * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                     "kernel": "linear_mma_kernel<4,1> (mma.sync bf16)", "bytes_per_launch": bytes_per_block,
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": DECODE_TRAFFIC_BYTES,
+                     "kernel": "linear_mma_kernel<4,1> (2:4-sparse mma.sync)", "bytes_per_launch": bytes_per_block,
                      "launch_us": launch_ms * 1e3, "peak_source": peaks["source"],
                      "frac_of_nominal_8TBps": achieved / 8000.0},
         "clocks": clk.summary(),
@@ -453,7 +507,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["decode", "prefill", "sweep"], default="decode",
+    ap.add_argument("--mode", choices=["decode", "prefill", "sweep", "stack"], default="decode",
                     help="prefill: time only the prefill leg (for profiling)")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-tokens", type=int, default=2048)
@@ -470,6 +524,8 @@ def main():
         run_prefill_only(args, world, rank, local)
     elif args.mode == "sweep":
         run_sweep_only(args, world, rank, local)
+    elif args.mode == "stack":
+        run_stack_only(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:
