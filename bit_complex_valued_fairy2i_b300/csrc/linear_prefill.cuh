@@ -460,28 +460,31 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
               S[q] = (b == 0 ? cur[q].x : cur[q].z) << rho;         // row rho's signs one bit up
               F[q] = ~(b == 0 ? cur[q].y : cur[q].w) >> (16 * rho);  // real-axis flags of row rho in the low half
             }
+            // chunk order rotated by the plane index, so that the eight lanes of
+            // a quarter-warp store to eight different 16-byte bank groups
 #pragma unroll
-            for (int ss = 0; ss < 2; ++ss) {
-              const int sstep = 2 * hf + ss;  // 16-column step of the block
+            for (int t4 = 0; t4 < 4; ++t4) {
+              const int idx = (t4 + p) & 3;
+              const int ss = idx >> 1, h = idx & 1;
+              const int sstep = 2 * hf + ss;                  // 16-column step of the block
+              const uint32_t cc = (uint32_t)(2 * sstep + h);  // 16-byte chunk of the 128-byte row
+              const uint32_t fword = F[h + 2 * hf];           // flag word of lane (g, h + 2 (s >> 1))
+              const uint32_t fsh = (uint32_t)(sstep & 1);
+              const uint32_t ssh = (uint32_t)(4 * sstep + 2 * h);
+              uint32_t re[4], im[4];
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint32_t cc = (uint32_t)(2 * sstep + h);  // 16-byte chunk of the 128-byte row
-                const uint32_t fword = F[h + 2 * hf];           // flag word of lane (g, h + 2 (s >> 1))
-                uint32_t re[4], im[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  // real flags of columns (2q, 2q + 1) at bits 0 and 2, then at bits 14 and 30
-                  const uint32_t fr = (((fword >> (4 * q + (sstep & 1))) & 5u) * 0x10004000u) & 0x40004000u;
-                  re[q] = real_operand_pf(S[q] << (4 * sstep + 2 * h), smask, fr);  // (sign, real flag)
-                  im[q] = re[q] ^ 0x40004000u;                                      // (sign, imaginary flag)
-                }
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_re + ((cc ^ sw_re) << 4)),
-                             "r"(re[0]), "r"(re[1]), "r"(re[2]), "r"(re[3])
-                             : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_im + ((cc ^ sw_im) << 4)),
-                             "r"(im[0]), "r"(im[1]), "r"(im[2]), "r"(im[3])
-                             : "memory");
+              for (int q = 0; q < 4; ++q) {
+                // real flags of columns (2q, 2q + 1) at bits 0 and 2, then at bits 14 and 30
+                const uint32_t fr = (((fword >> (4 * q + fsh)) & 5u) * 0x10004000u) & 0x40004000u;
+                re[q] = real_operand_pf(S[q] << ssh, smask, fr);  // (sign, real flag)
+                im[q] = re[q] ^ 0x40004000u;                      // (sign, imaginary flag)
               }
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_re + ((cc ^ sw_re) << 4)),
+                           "r"(re[0]), "r"(re[1]), "r"(re[2]), "r"(re[3])
+                           : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + row_im + ((cc ^ sw_im) << 4)),
+                           "r"(im[0]), "r"(im[1]), "r"(im[2]), "r"(im[3])
+                           : "memory");
             }
           }
           fence_async_smem();
