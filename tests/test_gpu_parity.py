@@ -269,3 +269,38 @@ def test_full_size_block_group_decode_sampled():
         y = y.cpu().numpy()
         got = np.concatenate([y[:, rows], y[:, q.n + rows]], axis=1)
         assert rel_l2(got, want) <= REL_L2
+
+
+@pytest.mark.parametrize("T,M", [(3, 6), (4, 8), (1, 5), (2, 7)])
+def test_linear_parity_wide_variants(T, M):
+    """The decode instances with several token pairs per launch and 2T = 6 or 8
+    code planes (the largest register footprints)."""
+    n, m = 48, 384
+    R = _R(n, m, 80 + 10 * T + M)
+    _, _, q = _gpu_layer(R, T)
+    _, _, qU, qW = _oracle_layer(R, T)
+    x = _x(M, m, 90 + M)
+    want = oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x))
+    for algo in DECODE_ALGOS:
+        y = f2i.linear(q, x.cuda(), algo=algo).cpu().numpy()
+        assert rel_l2(y, want) <= REL_L2, algo
+
+
+def test_group_split_by_activation_width():
+    """At 4 tokens a 3000-column layer's staged activations would leave one CTA
+    per SM, so the group is launched per activation width; results must not
+    depend on it."""
+    shapes = [(40, 256), (13, 3000), (64, 64), (24, 3000)]
+    qs, xs, wants = [], [], []
+    for i, (n, m) in enumerate(shapes):
+        R = _R(n, m, 500 + i)
+        _, _, q = _gpu_layer(R, 2)
+        _, _, qU, qW = _oracle_layer(R, 2)
+        x = _x(4, m, 600 + i)
+        qs.append(q)
+        xs.append(x.cuda())
+        wants.append(oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x)))
+    ys = f2i.linear_group(qs, xs, algo="mma")
+    for q, x, y, want in zip(qs, xs, ys, wants):
+        assert rel_l2(y.cpu().numpy(), want) <= REL_L2
+        assert torch.equal(y, f2i.linear(q, x, algo="mma"))
