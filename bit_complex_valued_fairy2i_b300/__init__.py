@@ -31,7 +31,7 @@ LAYOUT_VERSION = 2
 EXPORTED = (
     "fairy2i_codes_bytes", "fairy2i_scales_count", "fairy2i_convert", "fairy2i_quantize",
     "fairy2i_linear", "fairy2i_linear_ex", "fairy2i_linear_group", "fairy2i_unpack_codes",
-    "fairy2i_sync_status", "fairy2i_last_error", "fairy2i_layout_version",
+    "fairy2i_sync_status", "fairy2i_last_error", "fairy2i_layout_version", "fairy2i_selftest_bounded_wait",
 )
 
 
@@ -72,6 +72,7 @@ def load_library(path: str = LIB_PATH):
         "fairy2i_sync_status": (ctypes.c_int, [P]),
         "fairy2i_last_error": (ctypes.c_char_p, []),
         "fairy2i_layout_version": (I32, []),
+        "fairy2i_selftest_bounded_wait": (ctypes.c_int, [I32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -203,6 +204,11 @@ def unpack_codes(q: Packed, stream=None) -> torch.Tensor:
     d = q.desc()
     _check(load_library().fairy2i_unpack_codes(ctypes.byref(d), out.data_ptr(), _stream(stream)))
     return out
+
+
+def selftest_bounded_wait(limit_us: int = 10000, stream=None):
+    """Run the bounded-wait self-test; a following sync_status() raises TIMEOUT."""
+    _check(load_library().fairy2i_selftest_bounded_wait(limit_us, _stream(stream)))
 
 
 def sync_status(stream=None):

@@ -489,6 +489,12 @@ fairy2i_status fairy2i_unpack_codes(const fairy2i_packed* q, uint8_t* codes_out,
   return check_launch("unpack launch");
 }
 
+fairy2i_status fairy2i_selftest_bounded_wait(int32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return fail(FAIRY2I_ERR_INVALID_ARG, "limit_us=%d outside [1, 1000000]", limit_us);
+  f2i::bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((uint64_t)limit_us * 1000ull);
+  return check_launch("bounded-wait self-test launch");
+}
+
 fairy2i_status fairy2i_sync_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));

@@ -114,17 +114,19 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the phase of `parity` to complete.  Gives up after about 2 s, or
-// soon after another role of the CTA has given up (`abort_flag`); then the
-// device error word gets the timeout flag and false is returned.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// Wait for the phase of `parity` to complete.  Gives up after `limit_ns`
+// (about 2 s by default), or soon after another role of the CTA has given up
+// (`abort_flag`); then the device error word gets the timeout flag and false
+// is returned.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if ((i & 15) == 0) {
       if (*abort_flag) return false;
-      if (global_ns() - t0 > 2000000000ull) {
+      if (global_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         f2i_raise(kErrTimeout);
         return false;
@@ -570,6 +572,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kPfTmemCols);
+  }
+}
+
+// Self-test of the bounded wait: one thread waits on a barrier that nothing
+// arrives at, with a short limit; the wait must give up, raise the timeout
+// flag and return, leaving the context usable.
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    mbar_wait(smem_u32(&bar), 0, &abort_flag, limit_ns);
   }
 }
 

@@ -155,6 +155,14 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
  * 0 = +1, 1 = -1, 2 = +i, 3 = -i. */
 fairy2i_status fairy2i_unpack_codes(const fairy2i_packed *q, uint8_t *codes_out, void *stream);
 
+/* Self-test of the failure-detection path: launches one thread that waits on
+ * a shared-memory barrier nothing arrives at, using the same bounded wait as
+ * the prefill kernel with a limit of `limit_us` microseconds (1..1000000).
+ * The wait gives up, sets FAIRY2I_ERR_TIMEOUT in the device error word and
+ * the kernel returns; fairy2i_sync_status() then reports FAIRY2I_ERR_TIMEOUT
+ * (and clears it).  No device fault is involved.  INVALID_ARG on a bad limit. */
+fairy2i_status fairy2i_selftest_bounded_wait(int32_t limit_us, void *stream);
+
 /* Synchronize `stream`, then read and clear this device's error word.
  * Returns FAIRY2I_OK, FAIRY2I_ERR_NONFINITE, FAIRY2I_ERR_TIMEOUT or
  * FAIRY2I_ERR_CUDA. */

@@ -112,6 +112,11 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.fairy2i_linear_group(descs, arr, arr, 300, 1, 0, None) == 1
 
 
+def test_selftest_rejects_bad_limit(lib):
+    assert lib.fairy2i_selftest_bounded_wait(0, None) == 1
+    assert lib.fairy2i_selftest_bounded_wait(2000000, None) == 1
+
+
 def test_unpack_rejects_bad_arguments(lib):
     d = _desc()
     assert lib.fairy2i_unpack_codes(ctypes.byref(d), None, None) == 1

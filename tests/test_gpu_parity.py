@@ -304,3 +304,20 @@ def test_group_split_by_activation_width():
     for q, x, y, want in zip(qs, xs, ys, wants):
         assert rel_l2(y.cpu().numpy(), want) <= REL_L2
         assert torch.equal(y, f2i.linear(q, x, algo="mma"))
+
+
+def test_bounded_wait_gives_up_and_reports_timeout():
+    """The bounded mbarrier wait used by the prefill kernel, run on a barrier that
+    nothing arrives at: it must give up after its limit, report TIMEOUT through the
+    error word, clear it, and leave the context usable."""
+    f2i.selftest_bounded_wait(10000)  # 10 ms
+    with pytest.raises(f2i.Fairy2iError) as e:
+        f2i.sync_status()
+    assert e.value.status == 6
+    f2i.sync_status()  # cleared
+    R = _R(8, 64, 1)
+    _, _, q = _gpu_layer(R, 2)
+    _, _, qU, qW = _oracle_layer(R, 2)
+    x = _x(200, 64, 2)
+    y = f2i.linear(q, x.cuda(), algo="tcgen05").cpu().numpy()
+    assert rel_l2(y, oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x))) <= REL_L2
