@@ -333,6 +333,21 @@ def stack_leg(f2i, dev, T: int, blocks: int, steps: int, warmup: int):
     (CUDA graph of one grouped launch per block)."""
     stack, offline = build_stack(f2i, blocks, dev, T)
     nbytes = sum(q.nbytes for layers in stack for q in layers)
+    # the same stack through the one-pass convert + quantize (codes written over the first ones)
+    fused_ms, e = 0.0, [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for b in range(blocks):
+        for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
+            R = inputs.weight_R(5, 7 * b + pi, out_f, in_f, device=dev)
+            e[0].record()
+            f2i.convert_quantize(R, T, out=stack[b][pi], check=False)
+            e[1].record()
+            e[1].synchronize()
+            fused_ms += e[0].elapsed_time(e[1])
+            del R
+    f2i.sync_status()
+    offline["convert_quantize_fused_ms_stack"] = fused_ms
+    offline["convert_quantize_fused_GBps"] = sum(4 * o * i for (_, o, i) in inputs.LLAMA2_7B_BLOCK) * blocks / (
+        fused_ms * 1e6) + nbytes / (fused_ms * 1e6)
     xs = [[inputs.activations(5, 7 * b + pi, 1, inf, device=dev) for pi, (_, _, inf) in enumerate(inputs.LLAMA2_7B_BLOCK)]
           for b in range(blocks)]
     ys = [[torch.empty((1, outf), dtype=torch.float32, device=dev) for (_, outf, _) in inputs.LLAMA2_7B_BLOCK]

@@ -32,6 +32,7 @@ EXPORTED = (
     "fairy2i_codes_bytes", "fairy2i_scales_count", "fairy2i_convert", "fairy2i_quantize",
     "fairy2i_linear", "fairy2i_linear_ex", "fairy2i_linear_group", "fairy2i_unpack_codes",
     "fairy2i_sync_status", "fairy2i_last_error", "fairy2i_layout_version", "fairy2i_selftest_bounded_wait",
+    "fairy2i_convert_quantize",
 )
 
 
@@ -73,6 +74,7 @@ def load_library(path: str = LIB_PATH):
         "fairy2i_last_error": (ctypes.c_char_p, []),
         "fairy2i_layout_version": (I32, []),
         "fairy2i_selftest_bounded_wait": (ctypes.c_int, [I32, P]),
+        "fairy2i_convert_quantize": (ctypes.c_int, [P, I64, I64, I32, PD, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -162,6 +164,23 @@ def quantize(U: torch.Tensor, W: torch.Tensor, T: int = 2, out: Packed | None = 
     q = out if out is not None else Packed.empty(n, m, T, U.device)
     d = q.desc()
     _check(load_library().fairy2i_quantize(U.data_ptr(), W.data_ptr(), n, m, T, ctypes.byref(d), _stream(stream)))
+    if check:
+        sync_status(stream)
+    return q
+
+
+def convert_quantize(R: torch.Tensor, T: int = 2, out: Packed | None = None, stream=None,
+                     check: bool = True) -> Packed:
+    """Real [2n, 2m] float32 weight -> packed layer, in one pass (the same codes and
+    scales as quantize(*convert(R), T))."""
+    _dev(R, "R")
+    if R.dtype != torch.float32 or R.dim() != 2:
+        raise ValueError("R must be a 2-D float32 tensor")
+    n, m = R.shape[0] // 2, R.shape[1] // 2
+    q = out if out is not None else Packed.empty(n, m, T, R.device)
+    d = q.desc()
+    _check(load_library().fairy2i_convert_quantize(R.data_ptr(), R.shape[0], R.shape[1], T, ctypes.byref(d),
+                                                   _stream(stream)))
     if check:
         sync_status(stream)
     return q

@@ -143,20 +143,27 @@ __device__ __forceinline__ void block_reduce2(Tv& a, Tv& b, Tv* sa, Tv* sb, Op o
   __syncthreads();  // sa / sb are reused by the next reduction
 }
 
-template <int WPT>
+// FUSED = false: weights from complex U, W [n][m] (grid (n, 2): row, matrix).
+// FUSED = true:  weights computed from the real R [2n][2m] with the same
+// float32 operations as the conversion kernel, so the codes and scales equal
+// those of convert-then-quantize bit for bit (grid (2, n): the two matrices
+// of a row are neighbouring CTAs and share the R rows through L2).
+template <int WPT, bool FUSED>
 __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
-    const float2* __restrict__ U, const float2* __restrict__ W, int64_t n, int64_t m, int T,
-    uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    const float2* __restrict__ U, const float2* __restrict__ W, const float* __restrict__ R, int64_t n, int64_t m,
+    int T, uint8_t* __restrict__ codes, float* __restrict__ scales) {
   constexpr int E = 16 * WPT;  // weights per thread
   __shared__ uint32_t s_u[2][32];
   __shared__ long long s_l[2][32];
   __shared__ float s_scale[2];
 
   const int tid = threadIdx.x;
-  const int X = blockIdx.y;
-  const int64_t j = blockIdx.x;
+  const int X = FUSED ? blockIdx.x : blockIdx.y;
+  const int64_t j = FUSED ? blockIdx.y : blockIdx.x;
   const int64_t KB = col_blocks(m);
-  const float2* src = (X == 0 ? U : W) + j * m;
+  const float2* src = FUSED ? nullptr : (X == 0 ? U : W) + j * m;
+  const float* top = FUSED ? R + j * 2 * m : nullptr;        // R11 | R12 row
+  const float* bot = FUSED ? R + (n + j) * 2 * m : nullptr;  // R21 | R22 row
 
   // column of weight e = 16 u + c of this thread (word u of WPT)
   auto col_of = [&](int e) -> int64_t {
@@ -174,7 +181,14 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
     const int64_t k = col_of(e);
     float2 v = make_float2(0.0f, 0.0f);
     if ((w >> 2) < KB && k < m) {
-      v = __ldcs(src + k);
+      if (FUSED) {
+        const float r11 = __ldcs(top + k), r12 = __ldcs(top + m + k);
+        const float r21 = __ldcs(bot + k), r22 = __ldcs(bot + m + k);
+        v = X == 0 ? make_float2(half_sum(r11, r22), half_diff(r21, r12))   // U
+                   : make_float2(half_diff(r11, r22), half_sum(r12, r21));  // W
+      } else {
+        v = __ldcs(src + k);
+      }
       valid[e >> 4] |= 1u << (e & 15);
     }
     bad |= !(isfinite(v.x) && isfinite(v.y));

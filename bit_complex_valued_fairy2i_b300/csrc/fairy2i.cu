@@ -316,6 +316,29 @@ fairy2i_status run_tcgen05(const fairy2i_packed* qs, const void* const* xs, floa
 // Token count from which FAIRY2I_ALGO_AUTO takes the tcgen05 prefill path.
 constexpr int64_t kPrefillMinTokens = 17;
 
+// The quantizer over U, W (FUSED = false) or straight from R (true); the
+// caller has checked the arguments.  Codes are zeroed first: each row ORs its
+// bits into words it shares with the other row of its lane pair.
+fairy2i_status launch_quantize(const float2* U, const float2* W, const float* R, int64_t n, int64_t m, int32_t T,
+                               const fairy2i_packed* out, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(out->codes, 0, fairy2i_codes_bytes(n, m, T), s);
+  if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "memset codes: %s", cudaGetErrorString(e));
+  const int64_t words = 4 * f2i::col_blocks(m);  // packed words per row
+  const int wpt = words <= f2i::kQuantThreads ? 1 : 2;
+  const int threads = (int)(((words + wpt - 1) / wpt + 31) / 32 * 32);
+  uint8_t* codes = static_cast<uint8_t*>(out->codes);
+  if (R == nullptr) {
+    const dim3 grid((unsigned)n, 2);
+    if (wpt == 1) f2i::quantize_words_kernel<1, false><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, out->scales);
+    else f2i::quantize_words_kernel<2, false><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, out->scales);
+  } else {
+    const dim3 grid(2, (unsigned)n);
+    if (wpt == 1) f2i::quantize_words_kernel<1, true><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, out->scales);
+    else f2i::quantize_words_kernel<2, true><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, out->scales);
+  }
+  return check_launch("quantize launch");
+}
+
 fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int32_t count,
                                  int64_t M, fairy2i_algo algo, cudaStream_t s) {
   if (count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "count=%d outside [1, 256]", count);
@@ -446,21 +469,24 @@ fairy2i_status fairy2i_quantize(const void* U, const void* W, int64_t n, int64_t
                 (long long)out->n, (long long)out->m, out->T, (long long)n, (long long)m, T);
   if (n > INT32_MAX) return fail(FAIRY2I_ERR_UNSUPPORTED, "n too large");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  {  // the kernel ORs each row's bits into words shared with the other row of its lane pair
-    cudaError_t e = cudaMemsetAsync(out->codes, 0, fairy2i_codes_bytes(n, m, T), s);
-    if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "memset codes: %s", cudaGetErrorString(e));
-  }
-  const int64_t words = 4 * f2i::col_blocks(m);  // packed words per row
-  const int wpt = words <= f2i::kQuantThreads ? 1 : 2;
-  const int threads = (int)(((words + wpt - 1) / wpt + 31) / 32 * 32);
-  dim3 grid((unsigned)n, 2);
-  if (wpt == 1)
-    f2i::quantize_words_kernel<1><<<grid, threads, 0, s>>>(static_cast<const float2*>(U), static_cast<const float2*>(W),
-                                                           n, m, T, static_cast<uint8_t*>(out->codes), out->scales);
-  else
-    f2i::quantize_words_kernel<2><<<grid, threads, 0, s>>>(static_cast<const float2*>(U), static_cast<const float2*>(W),
-                                                           n, m, T, static_cast<uint8_t*>(out->codes), out->scales);
-  return check_launch("quantize launch");
+  return launch_quantize(static_cast<const float2*>(U), static_cast<const float2*>(W), nullptr, n, m, T, out, s);
+}
+
+fairy2i_status fairy2i_convert_quantize(const float* R, int64_t rows, int64_t cols, int32_t T,
+                                        const fairy2i_packed* out, void* stream) {
+  if (!R) return fail(FAIRY2I_ERR_INVALID_ARG, "R is NULL");
+  if (rows < 2 || cols < 2 || (rows & 1) || (cols & 1))
+    return fail(FAIRY2I_ERR_SHAPE, "R is %lld x %lld; both dimensions must be even and >= 2", (long long)rows,
+                (long long)cols);
+  if (!aligned(R, 8)) return fail(FAIRY2I_ERR_INVALID_ARG, "R must be 8-byte aligned");
+  fairy2i_status st = check_packed(out);
+  if (st != FAIRY2I_OK) return st;
+  const int64_t n = rows / 2, m = cols / 2;
+  if (out->n != n || out->m != m || out->T != T)
+    return fail(FAIRY2I_ERR_SHAPE, "descriptor (n=%lld, m=%lld, T=%d) does not match R (n=%lld, m=%lld, T=%d)",
+                (long long)out->n, (long long)out->m, out->T, (long long)n, (long long)m, T);
+  if (n > 65535) return fail(FAIRY2I_ERR_UNSUPPORTED, "n=%lld above 65535 for the fused path", (long long)n);
+  return launch_quantize(nullptr, nullptr, R, n, m, T, out, static_cast<cudaStream_t>(stream));
 }
 
 fairy2i_status fairy2i_linear_ex(const fairy2i_packed* q, const void* x, int64_t M, float* y, fairy2i_algo algo,

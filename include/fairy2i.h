@@ -127,6 +127,16 @@ fairy2i_status fairy2i_convert(const float *R, int64_t rows, int64_t cols,
 fairy2i_status fairy2i_quantize(const void *U, const void *W, int64_t n, int64_t m,
                                 int32_t T, const fairy2i_packed *out, void *stream);
 
+/* Conversion and quantization in one pass: the same codes and scales as
+ * fairy2i_convert followed by fairy2i_quantize, bit for bit (each weight of U
+ * and W is formed from R with the conversion's float32 operations), without
+ * writing U and W to memory.
+ *   R   : device float32 [rows][cols] = [2n][2m], 8-byte aligned
+ *   out : host descriptor with out->n = rows/2, out->m = cols/2, out->T = T
+ * Errors: as fairy2i_convert and fairy2i_quantize; UNSUPPORTED for n > 65535. */
+fairy2i_status fairy2i_convert_quantize(const float *R, int64_t rows, int64_t cols, int32_t T,
+                                        const fairy2i_packed *out, void *stream);
+
 /* The layer on a batch of tokens ("Fairy2i-W2" card, y = Ux + W conj(x);
  * "Fairy2i: Ultra-Low-Bit ...", "Industry implications: multiplication-free
  * inference"):

@@ -112,6 +112,15 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.fairy2i_linear_group(descs, arr, arr, 300, 1, 0, None) == 1
 
 
+def test_convert_quantize_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    d = _desc(n=2, m=2, T=1)
+    assert lib.fairy2i_convert_quantize(None, 4, 4, 1, ctypes.byref(d), None) == 1
+    assert lib.fairy2i_convert_quantize(p, 3, 4, 1, ctypes.byref(d), None) == 2
+    assert lib.fairy2i_convert_quantize(p, 4, 4, 2, ctypes.byref(d), None) == 2  # T differs
+    assert lib.fairy2i_convert_quantize(p, 6, 4, 1, ctypes.byref(d), None) == 2  # n differs
+
+
 def test_selftest_rejects_bad_limit(lib):
     assert lib.fairy2i_selftest_bounded_wait(0, None) == 1
     assert lib.fairy2i_selftest_bounded_wait(2000000, None) == 1

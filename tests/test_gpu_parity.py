@@ -321,3 +321,26 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     x = _x(200, 64, 2)
     y = f2i.linear(q, x.cuda(), algo="tcgen05").cpu().numpy()
     assert rel_l2(y, oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x))) <= REL_L2
+
+
+@pytest.mark.parametrize("n,m", [(37, 130), (256, 256), (13, 2049), (300, 700)])
+@pytest.mark.parametrize("T", [1, 2, 3])
+def test_convert_quantize_fused_equals_two_pass(n, m, T):
+    """One pass from R gives the codes and scales of convert + quantize, bit for bit,
+    and the oracle's."""
+    R = _R(n, m, 40 + n + m)
+    q2 = f2i.convert_quantize(R.cuda(), T)
+    _, _, q1 = _gpu_layer(R, T)
+    assert torch.equal(f2i.unpack_codes(q2), f2i.unpack_codes(q1))
+    assert torch.equal(q2.scales, q1.scales)
+    _, _, qU, qW = _oracle_layer(R, T)
+    codes = f2i.unpack_codes(q2).cpu().numpy()
+    assert np.array_equal(codes[0], qU.codes) and np.array_equal(codes[1], qW.codes)
+
+
+def test_convert_quantize_nonfinite_reported():
+    R = torch.zeros((8, 16), dtype=torch.float32)
+    R[5, 3] = float("inf")
+    with pytest.raises(f2i.Fairy2iError) as e:
+        f2i.convert_quantize(R.cuda(), 1)
+    assert e.value.status == 3
