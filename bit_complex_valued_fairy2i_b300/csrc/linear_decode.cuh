@@ -283,17 +283,21 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (NPL * TILES <= 8) ? 2 : 1)
   const uint8_t* plane0 = P.codes + rt_begin * (int64_t)tile_row;
 
   int ir = i0 / nch, ic = i0 - (i0 / nch) * nch;  // next item to load
+  // byte offset of this lane's 16 bytes of the next item, inside plane 0
+  uint32_t src_off = (uint32_t)ir * tile_row + (uint32_t)ic * 512u + (uint32_t)lane * 16u;
+  const uint32_t pstride = (uint32_t)pbytes;  // a plane is below 4 GB
   auto issue = [&](int slot) {
     if (ic < fullc) {
-      const uint8_t* src = plane0 + (uint32_t)ir * tile_row + (uint32_t)ic * 512u + (uint32_t)lane * 16u;
+      const uint32_t dst = ring + (uint32_t)slot * kSlot + (uint32_t)lane * 16u;
 #pragma unroll
-      for (int pl = 0; pl < NPL; ++pl)
-        cp_async16(ring + (uint32_t)slot * kSlot + (uint32_t)(pl * 512 + lane * 16), src + pl * pbytes);
+      for (int pl = 0; pl < NPL; ++pl) cp_async16(dst + pl * 512u, plane0 + (src_off + (uint32_t)pl * pstride));
     }
     cp_commit();
+    src_off += 512u;
     if (++ic == nch) {
       ic = 0;
       ++ir;
+      src_off = (uint32_t)ir * tile_row + (uint32_t)lane * 16u;
     }
   };
   if (i0 < i1) issue(0);
@@ -366,29 +370,29 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (NPL * TILES <= 8) ? 2 : 1)
     } else {
       cp_wait<0>();
     }
-    const unsigned char* rs = msm + (ring - sbase) + slot * kSlot + lane * 16;
+    if (cc < fullc) {  // two blocks from the ring: (S, F) of block 2cc and 2cc + 1 per plane
+      const unsigned char* rs = msm + (ring - sbase) + slot * kSlot + lane * 16;
+      uint32_t S0[NPL], F0[NPL], S1[NPL], F1[NPL];
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const int kb = 2 * cc + b;
-      if (kb >= (int)KB) break;
-      uint32_t S[NPL], F[NPL];
-      if (cc < fullc) {
-#pragma unroll
-        for (int pl = 0; pl < NPL; ++pl) {
-          const uint2 v = *reinterpret_cast<const uint2*>(rs + pl * 512 + b * 8);
-          S[pl] = v.x;
-          F[pl] = v.y;
-        }
-      } else {  // odd last block: 8 bytes per lane
-#pragma unroll
-        for (int pl = 0; pl < NPL; ++pl) {
-          const uint2 v = __ldcs(reinterpret_cast<const uint2*>(plane0 + pl * pbytes + (uint32_t)rc * tile_row +
-                                                                (uint32_t)fullc * 512u + (uint32_t)lane * 8u));
-          S[pl] = v.x;
-          F[pl] = v.y;
-        }
+      for (int pl = 0; pl < NPL; ++pl) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rs + pl * 512);
+        S0[pl] = v.x;
+        F0[pl] = v.y;
+        S1[pl] = v.z;
+        F1[pl] = v.w;
       }
-      block(S, F, 64 * kb);
+      block(S0, F0, 128 * cc);
+      block(S1, F1, 128 * cc + 64);
+    } else {  // odd last block: 8 bytes per lane, read directly
+      uint32_t S[NPL], F[NPL];
+#pragma unroll
+      for (int pl = 0; pl < NPL; ++pl) {
+        const uint2 v = __ldcs(reinterpret_cast<const uint2*>(plane0 + (uint32_t)pl * pstride + (uint32_t)rc * tile_row +
+                                                              (uint32_t)fullc * 512u + (uint32_t)lane * 8u));
+        S[pl] = v.x;
+        F[pl] = v.y;
+      }
+      block(S, F, 128 * cc);
     }
     const int r = rc;
     if (++cc == nch) {
