@@ -42,7 +42,7 @@ BLOCKS = inputs.LLAMA2_7B_BLOCKS
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch
 # of this workload, from an ncu capture of linear_mma_kernel<4,1>; must be
 # re-measured whenever that kernel changes.
-DECODE_TRAFFIC_BYTES = 51_389_952 + 8_704
+DECODE_TRAFFIC_BYTES = 51_392_512
 WORKLOAD = ("llama2-7b decode GEMV, M=1, T=2: 7 projections per block x 32 distinct blocks "
             "(224 projections, 1.64 GB packed > L2), one grouped launch per block")
 
