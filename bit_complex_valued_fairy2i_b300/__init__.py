@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libfairy2i.so")
 OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "SHAPE", 3: "NONFINITE", 4: "UNSUPPORTED", 5: "CUDA",
                 6: "TIMEOUT"}
-ALGO = {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3}
+ALGO = {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4}
 LAYOUT_VERSION = 2
 
 # every extern "C" symbol declared in include/fairy2i.h

@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -18,6 +19,7 @@
 #include "convert_quantize.cuh"
 #include "linear_decode.cuh"
 #include "linear_prefill.cuh"
+#include "linear_tc_decode.cuh"
 
 namespace {
 
@@ -313,6 +315,136 @@ fairy2i_status run_tcgen05(const fairy2i_packed* qs, const void* const* xs, floa
   return ok();
 }
 
+// --- batch decode on the sparse tensor core (tcgen05.mma.sp) ---------------
+
+// Output rows per tile: 2T planes x R rows fill at most the 128 TMEM lanes.
+int tc_decode_rows(int T) { return T <= 2 ? 64 / T : 16; }
+
+// Code planes of layer q as TMA views: full two-block chunks as (u32 of a lane
+// quad, lane quad g, chunk, row tile, plane) with 64-byte swizzle, and an odd
+// last block as (u32, g, row tile, plane).  Boxes cover one chunk of R rows of
+// every plane.
+fairy2i_status make_code_maps(CUtensorMap* cmap, CUtensorMap* tmap, const fairy2i_packed& q, int R) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  fairy2i_status st = tensor_map_encoder(enc);
+  if (st != FAIRY2I_OK) return st;
+  const int64_t KB = f2i::col_blocks(q.m), rt = f2i::row_tiles(q.n), full = KB / 2;
+  const uint64_t plane = (uint64_t)f2i::plane_bytes(q.n, q.m);
+  const cuuint64_t planes = (cuuint64_t)(2 * q.T);
+  if (full > 0) {
+    const cuuint64_t dims[5] = {16, 8, (cuuint64_t)full, (cuuint64_t)rt, planes};
+    const cuuint64_t strides[4] = {64, 512, (cuuint64_t)(KB * 256), plane};
+    const cuuint32_t box[5] = {16, 8, 1, (cuuint32_t)(R / 16), (cuuint32_t)planes};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = enc(cmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, q.codes, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FAIRY2I_ERR_CUDA, "cuTensorMapEncodeTiled (code chunks) failed (%d)", (int)r);
+  }
+  if (KB & 1) {
+    void* tail = static_cast<uint8_t*>(q.codes) + full * 512;
+    const cuuint64_t dims[4] = {8, 8, (cuuint64_t)rt, planes};
+    const cuuint64_t strides[3] = {32, (cuuint64_t)(KB * 256), plane};
+    const cuuint32_t box[4] = {8, 8, (cuuint32_t)(R / 16), (cuuint32_t)planes};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, tail, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FAIRY2I_ERR_CUDA, "cuTensorMapEncodeTiled (code tail) failed (%d)", (int)r);
+  }
+  return FAIRY2I_OK;
+}
+
+// One launch over up to kTdMaxGroup layers: tiles of R output rows are given
+// to CTAs by longest-processing-time-first (cost = MMAs + a constant for the
+// epilogue), so every CTA gets nearly the same number of MMAs.
+fairy2i_status launch_tc_decode(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count,
+                                int64_t M, int T, cudaStream_t s) {
+  static_assert(sizeof(f2i::TdParams) <= 32000, "kernel parameters too large");
+  const int R = tc_decode_rows(T);
+  f2i::TdParams* Pp = new f2i::TdParams;
+  std::unique_ptr<f2i::TdParams> guard(Pp);
+  f2i::TdParams& P = *Pp;
+  memset(&P, 0, sizeof(P));
+  P.count = count;
+  P.T = T;
+  P.R = R;
+  P.M = (int32_t)M;
+  P.N = 16 * (int32_t)((M + 1) / 2);
+  P.nsub = P.N <= 32 ? 4 : 2;
+  P.bstage_bytes = 256 * P.N;
+  P.bstages = std::min(f2i::kTdMaxBStages, (96 * 1024) / P.bstage_bytes);
+  struct Tile {
+    int cost, prob, tile;
+  };
+  std::vector<Tile> tiles;
+  for (int i = 0; i < count; ++i) {
+    const fairy2i_packed& q = qs[i];
+    fairy2i_status st = make_code_maps(&P.cmap[i], &P.tmap[i], q, R);
+    if (st != FAIRY2I_OK) return st;
+    f2i::TdProblem& pr = P.p[i];
+    pr.scales = q.scales;
+    pr.x = static_cast<const uint16_t*>(xs[i]);
+    pr.y = ys[i];
+    pr.n = (int32_t)q.n;
+    pr.m = (int32_t)q.m;
+    pr.KB = (int32_t)f2i::col_blocks(q.m);
+    pr.tiles = (int32_t)((q.n + R - 1) / R);
+    for (int k = 0; k < pr.tiles; ++k) tiles.push_back({2 * pr.KB + 8, i, k});
+  }
+  const int ctas = (int)std::min<int64_t>({(int64_t)tiles.size(), (int64_t)sm_count(), (int64_t)f2i::kTdMaxCtas});
+  P.ctas = ctas;
+  std::stable_sort(tiles.begin(), tiles.end(), [](const Tile& a, const Tile& b) { return a.cost > b.cost; });
+  std::vector<int64_t> load(ctas, 0);
+  std::vector<std::vector<uint16_t>> per(ctas);
+  for (const Tile& t : tiles) {
+    const int c = (int)(std::min_element(load.begin(), load.end()) - load.begin());
+    load[c] += t.cost;
+    per[c].push_back((uint16_t)((t.prob << 13) | t.tile));
+  }
+  int e = 0;
+  for (int c = 0; c < ctas; ++c) {
+    std::sort(per[c].begin(), per[c].end());
+    P.off[c] = (uint16_t)e;
+    for (uint16_t v : per[c]) P.sched[e++] = v;
+  }
+  P.off[ctas] = (uint16_t)e;
+  const void* fn = reinterpret_cast<const void*>(f2i::linear_tc_decode_kernel);
+  const size_t smem = std::max<size_t>(
+      120 * 1024, 1024 + (size_t)f2i::kTdAStages * f2i::kTdAStageBytes + (size_t)P.bstages * P.bstage_bytes +
+                      f2i::kTdRedBytes + sizeof(f2i::TdSmem));
+  fairy2i_status st = ensure_smem(fn, smem, "sparse tensor-core decode");
+  if (st != FAIRY2I_OK) return st;
+  f2i::linear_tc_decode_kernel<<<ctas, f2i::kTdThreads, smem, s>>>(P);
+  return check_launch("sparse tensor-core decode launch");
+}
+
+fairy2i_status run_tc_decode(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count,
+                             int64_t M, int T, cudaStream_t s) {
+  const int R = tc_decode_rows(T);
+  for (int b0 = 0; b0 < count;) {
+    int b1 = b0;
+    int64_t t = 0;
+    while (b1 < count && b1 - b0 < f2i::kTdMaxGroup) {
+      const int64_t ti = (qs[b1].n + R - 1) / R;
+      if (ti > 8192) return fail(FAIRY2I_ERR_UNSUPPORTED, "n=%lld too large for the sparse tensor-core decode",
+                                 (long long)qs[b1].n);
+      if (b1 > b0 && t + ti > f2i::kTdMaxSched) break;
+      if (t + ti > f2i::kTdMaxSched) return fail(FAIRY2I_ERR_UNSUPPORTED, "layer with too many row tiles");
+      t += ti;
+      ++b1;
+    }
+    fairy2i_status st = launch_tc_decode(qs + b0, xs + b0, ys + b0, b1 - b0, M, T, s);
+    if (st != FAIRY2I_OK) return st;
+    b0 = b1;
+  }
+  return ok();
+}
+
+// Largest token count of the sparse tensor-core decode (N = 8 B columns per
+// token, at most 64).
+constexpr int64_t kTcDecodeMaxTokens = 8;
+
 // Token count from which FAIRY2I_ALGO_AUTO takes the tcgen05 prefill path.
 constexpr int64_t kPrefillMinTokens = 17;
 
@@ -344,7 +476,7 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
   if (count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "count=%d outside [1, 256]", count);
   if (!qs || !xs || !ys) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL array argument");
   if (M < 0) return fail(FAIRY2I_ERR_SHAPE, "M=%lld is negative", (long long)M);
-  if ((int)algo < 0 || (int)algo > 3) return fail(FAIRY2I_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
+  if ((int)algo < 0 || (int)algo > 4) return fail(FAIRY2I_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
   const int T = qs[0].T;
   for (int i = 0; i < count; ++i) {
     fairy2i_status st = check_packed(&qs[i]);
@@ -365,6 +497,11 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
   if (a == FAIRY2I_ALGO_AUTO) {
     if (T <= 4 && M >= kPrefillMinTokens && m_mult8) a = FAIRY2I_ALGO_TCGEN05;
     else a = (T <= 4) ? FAIRY2I_ALGO_MMA : FAIRY2I_ALGO_ADDSUB;
+  }
+  if (a == FAIRY2I_ALGO_TCGEN05_SP) {
+    if (T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "sparse tensor-core decode supports T <= 4");
+    if (M > kTcDecodeMaxTokens) return fail(FAIRY2I_ERR_UNSUPPORTED, "sparse tensor-core decode supports M <= 8");
+    return run_tc_decode(qs, xs, ys, count, M, T, s);
   }
   if (a == FAIRY2I_ALGO_MMA && T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode supports T <= 4");
   if (a == FAIRY2I_ALGO_TCGEN05) {

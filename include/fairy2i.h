@@ -85,7 +85,9 @@ typedef enum {
     FAIRY2I_ALGO_AUTO = 0,    /* pick the fastest kernel for the token count */
     FAIRY2I_ALGO_ADDSUB = 1,  /* CUDA cores: adds/subtracts only, fp32 accumulation */
     FAIRY2I_ALGO_MMA = 2,     /* decode: 2:4-sparse mma.sync, signs as bf16 +-2, axis flags as metadata */
-    FAIRY2I_ALGO_TCGEN05 = 3  /* prefill: codes expanded to bf16 in shared memory, tcgen05.mma */
+    FAIRY2I_ALGO_TCGEN05 = 3, /* prefill: codes expanded to bf16 in shared memory, tcgen05.mma */
+    FAIRY2I_ALGO_TCGEN05_SP = 4 /* decode, M <= 8, T <= 4: 2:4-sparse tcgen05.mma.sp (e4m3 signs and axis
+                                   flags as metadata in tensor memory; x as two exact e4m3 terms) */
 } fairy2i_algo;
 
 /* Bytes of the code planes of an n x m layer with T stages (0 on bad input). */

@@ -102,6 +102,11 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.fairy2i_linear(ctypes.byref(d), p, -1, p, None) == 2
     assert lib.fairy2i_linear(ctypes.byref(d), ctypes.c_void_p(258), 1, p, None) == 1
     assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 7, None) == 1
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 5, None) == 1
+    # the sparse tensor-core decode takes at most 8 tokens and 4 stages (checked before any launch)
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 9, p, 4, None) == 4
+    t5 = _desc(T=5)
+    assert lib.fairy2i_linear_ex(ctypes.byref(t5), p, 1, p, 4, None) == 4
     zero = _desc(n=0)
     assert lib.fairy2i_linear(ctypes.byref(zero), p, 1, p, None) == 2
     # M = 0 with valid arguments is a no-op that launches nothing

@@ -14,7 +14,7 @@ from bit_complex_valued_fairy2i_b300 import inputs
 pytestmark = pytest.mark.gpu
 
 REL_L2 = 1e-3
-DECODE_ALGOS = ("addsub", "mma")
+DECODE_ALGOS = ("addsub", "mma", "tcgen05_sp")
 
 
 def rel_l2(got, want):
@@ -155,7 +155,7 @@ def test_linear_addsub_many_stages():
     assert rel_l2(y, oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x))) <= 1e-5
 
 
-@pytest.mark.parametrize("algo", DECODE_ALGOS)
+@pytest.mark.parametrize("algo", ("addsub", "mma"))  # the sparse tensor-core decode takes M <= 8
 def test_linear_more_tokens_than_one_launch(algo):
     n, m, M = 40, 256, 19
     R = _R(n, m, 5)
