@@ -31,10 +31,10 @@
 // are already in metadata nibble form (bit 0 / bit 2 = the axis flags of the
 // two codes of a group).
 //
-// Roles (17 warps): 0 TMA loads of code chunks (8 lanes), 1 and 16 MMA issue
+// Roles (19 warps): 0 TMA loads of code chunks (8 lanes), 1 and 18 MMA issue
 // (alternate chunks; warp 1 also allocates TMEM), 2-9 expansion of codes into
 // A and metadata (two warps per lane quarter, alternate chunks), 10-13
-// epilogue, 14-15 construction of B from x (alternate chunks).
+// epilogue, 14-17 construction of B from x (every fourth chunk each).
 #pragma once
 #include <cuda.h>
 
@@ -50,7 +50,8 @@ constexpr int kTdMaxTokens = 8;
 constexpr int kTdAStages = 16;  // shared-memory ring of code chunks (4 KB each)
 constexpr int kTdTStages = 4;   // TMEM stages of A + metadata (one chunk each)
 constexpr int kTdMaxBStages = 8;
-constexpr int kTdThreads = 544;  // 17 warps
+constexpr int kTdThreads = 608;  // 19 warps
+constexpr int kTdBuilders = 4;   // B-construction warps (chunk c goes to builder c % 4)
 constexpr int kTdLoaders = 8;    // loader lanes, each with its own chunk in flight
 constexpr int kTdMaxCtas = 160;
 constexpr int kTdMaxSched = 6144;
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
         td_advance(P, cur, kTdLoaders, t_end);
       }
     }
-  } else if (warp == 1 || warp == 16) {
+  } else if (warp == 1 || warp == 18) {
     // ---- MMA issue: two issuing threads take alternate chunks, each accumulating into its own
     // sub-accumulators (a thread's barrier wait lets its own MMAs drain; the other thread's MMAs keep
     // the tensor core busy meanwhile).  Issuer q uses subs 2q, 2q + 1 (nsub = 4) or q (nsub = 2). ----
@@ -577,7 +578,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
         yr[pr.n + orow] = im;
       }
     }
-  } else if (warp < 16) {
+  } else if (warp < 14 + kTdBuilders) {
     // ---- B construction: x (bfloat16) -> hi/lo e4m3 columns, one chunk of 128 columns per stage.
     // Lane task: 4 consecutive columns of one token. ----
     const int par = warp - 14;
@@ -589,7 +590,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
       const int nch = (pr.KB + 1) >> 1;
       const bool vec = (pr.m & 3) == 0;
       for (int c = 0; c < nch; ++c, ++chunk) {
-        if ((int)(chunk & 1) != par) continue;
+        if ((int)(chunk % kTdBuilders) != par) continue;
         const uint32_t bs = chunk % (uint32_t)P.bstages, ts = chunk % kTdTStages;
         if (!mbar_wait_warp(smem_u32(&S.b_empty[bs]), ((chunk / P.bstages) & 1) ^ 1, abort_flag)) {
           ok = false;
