@@ -10,7 +10,8 @@ through all 224 projections, one grouped launch per block (7 layers each).
 value      = packed bytes streamed per step / device time per step (GB/s)
 e2e        = the same bytes / time per step including the host->device copy of
              every projection's activation row and the device->host copy of
-             every output row (pinned host buffers)
+             every output row (pinned host buffers), the host waiting for the
+             step's outputs; copies of a block overlap the other blocks' launches
 roofline   = the decode kernel's average launch: packed bytes of one block
              (51,273,728 B) / launch time, against the measured HBM copy peak
 cpu_baseline / --impl reference = the oracle (plain C, double precision,
@@ -43,6 +44,17 @@ BLOCKS = inputs.LLAMA2_7B_BLOCKS
 # of this workload, from an ncu capture of linear_mma_kernel<4,1>; must be
 # re-measured whenever that kernel changes.
 DECODE_TRAFFIC_BYTES = 51_392_512
+# decode kernel and arithmetic per --decode-algo (auto = the 2:4-sparse mma.sync decode at M = 1)
+DECODE_KERNELS = {
+    "auto": ("linear_mma_kernel<4,1> (2:4-sparse mma.sync)",
+             "bf16 (2:4-sparse mma.sync: code signs as bf16 +-2, bf16 x), fp32 accumulate"),
+    "mma": ("linear_mma_kernel<4,1> (2:4-sparse mma.sync)",
+            "bf16 (2:4-sparse mma.sync: code signs as bf16 +-2, bf16 x), fp32 accumulate"),
+    "tcgen05_sp": ("linear_tc_decode_kernel (2:4-sparse tcgen05.mma.sp)",
+                   "e4m3 (2:4-sparse tcgen05.mma.sp: code signs as e4m3 +-1, x as two exact e4m3 terms), "
+                   "fp32 accumulate"),
+    "addsub": ("linear_addsub_kernel (CUDA cores)", "fp32 adds/subtracts of bf16 x"),
+}
 WORKLOAD = ("llama2-7b decode GEMV, M=1, T=2: 7 projections per block x 32 distinct blocks "
             "(224 projections, 1.64 GB packed > L2), one grouped launch per block")
 
@@ -304,7 +316,7 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
         xs = [[x[:M].contiguous() for x in xb] for xb in xs_full]
         ys = [[torch.empty((M, 2 * q.n), dtype=torch.float32, device=dev) for q in qs] for qs in stack]
         row = {"M": M}
-        for algo in ("mma", "tcgen05", "auto"):
+        for algo in ("mma", "tcgen05", "auto") + (("tcgen05_sp",) if M <= 8 else ()):
             def step():
                 for b in range(blocks):
                     f2i.linear_group(stack[b], xs[b], ys[b], algo=algo)
@@ -440,9 +452,11 @@ def run_ours(args, world, rank, local):
     xs = [[xv[7 * b + i].view(1, -1) for i in range(7)] for b in range(blocks)]
     ys = [[yv[7 * b + i].view(1, -1) for i in range(7)] for b in range(blocks)]
 
+    algo = args.decode_algo
+
     def step():
         for b in range(blocks):
-            f2i.linear_group(stack[b], xs[b], ys[b])
+            f2i.linear_group(stack[b], xs[b], ys[b], algo=algo)
 
     step()  # outside capture: first-use setup (shared-memory attributes)
     torch.cuda.synchronize()
@@ -469,19 +483,48 @@ def run_ours(args, world, rank, local):
     launch_ms = ms_per_step / blocks  # every launch of the step is the decode kernel
     value = bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
 
-    # end to end: the step's activations from pinned host memory, its outputs back
+    # end to end: every step copies all activations in from pinned host memory and all outputs
+    # back, then waits for them on the host.  One graph per step: block b's launch waits only for
+    # its own activations (copy stream in), and its outputs go back (copy stream out) while the
+    # next blocks run.
     x_host = torch.empty_like(x_all, device="cpu").pin_memory()
     x_host.copy_(x_all.cpu())
     y_host = torch.empty_like(y_all, device="cpu").pin_memory()
     h2d = x_all.numel() * x_all.element_size()
     d2h = y_all.numel() * y_all.element_size()
+    xb_sizes = [sum(x_sizes[7 * b:7 * b + 7]) for b in range(blocks)]
+    yb_sizes = [sum(y_sizes[7 * b:7 * b + 7]) for b in range(blocks)]
+    x_dev_b, x_host_b = torch.split(x_all, xb_sizes), torch.split(x_host, xb_sizes)
+    y_dev_b, y_host_b = torch.split(y_all, yb_sizes), torch.split(y_host, yb_sizes)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(blocks)]
+    ev_out = [torch.cuda.Event() for _ in range(blocks)]
+    e2e_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(e2e_graph):
+        main = torch.cuda.current_stream()
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+        with torch.cuda.stream(s_in):
+            for b in range(blocks):
+                x_dev_b[b].copy_(x_host_b[b], non_blocking=True)
+                ev_in[b].record(s_in)
+        for b in range(blocks):
+            main.wait_event(ev_in[b])
+            f2i.linear_group(stack[b], xs[b], ys[b], algo=algo)
+            ev_out[b].record(main)
+        with torch.cuda.stream(s_out):
+            for b in range(blocks):
+                s_out.wait_event(ev_out[b])
+                y_host_b[b].copy_(y_dev_b[b], non_blocking=True)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
     e2e_steps = max(3, args.steps // 4)
+    for _ in range(3):
+        e2e_graph.replay()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        x_all.copy_(x_host, non_blocking=True)
-        graph.replay()
-        y_host.copy_(y_all, non_blocking=True)
+        e2e_graph.replay()
         torch.cuda.current_stream().synchronize()
     e2e_s = _max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
     e2e_value = bytes_per_step * world / e2e_s / 1e9
@@ -490,7 +533,7 @@ def run_ours(args, world, rank, local):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16 (2:4-sparse mma.sync: code signs as bf16 +-2, bf16 x), fp32 accumulate",
+        "vs_baseline": None, "dtype": DECODE_KERNELS[algo][1],
         "data": "synthetic",
         "config": {"workload": WORKLOAD if blocks == BLOCKS else f"{blocks}-block cut of: {WORKLOAD}",
                    "M": 1, "T": T_STAGES, "blocks": blocks, "projections": 7 * blocks,
@@ -499,8 +542,9 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": blocks * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": DECODE_TRAFFIC_BYTES,
-                     "kernel": "linear_mma_kernel<4,1> (2:4-sparse mma.sync)", "bytes_per_launch": bytes_per_block,
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": DECODE_TRAFFIC_BYTES if algo in ("auto", "mma") else None,
+                     "kernel": DECODE_KERNELS[algo][0], "bytes_per_launch": bytes_per_block,
                      "launch_us": launch_ms * 1e3, "peak_source": peaks["source"],
                      "frac_of_nominal_8TBps": achieved / 8000.0},
         "clocks": clk.summary(),
@@ -525,6 +569,8 @@ def main():
     ap.add_argument("--mode", choices=["decode", "prefill", "sweep", "stack"], default="decode",
                     help="prefill: time only the prefill leg (for profiling)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--decode-algo", choices=sorted(DECODE_KERNELS), default="auto",
+                    help="decode kernel of the default mode (auto = the library's choice)")
     ap.add_argument("--prefill-tokens", type=int, default=2048)
     ap.add_argument("--blocks", type=int, default=BLOCKS,
                     help="decoder blocks in the stack (32 = the full model; fewer only for profiling)")
