@@ -373,7 +373,6 @@ fairy2i_status launch_tc_decode(const fairy2i_packed* qs, const void* const* xs,
   P.N = 16 * (int32_t)((M + 1) / 2);
   P.nsub = P.N <= 32 ? 4 : 2;
   P.bstage_bytes = 256 * P.N;
-  P.bstages = std::min(f2i::kTdMaxBStages, (96 * 1024) / P.bstage_bytes);
   struct Tile {
     int cost, prob, tile;
   };
@@ -411,7 +410,7 @@ fairy2i_status launch_tc_decode(const fairy2i_packed* qs, const void* const* xs,
   P.off[ctas] = (uint16_t)e;
   const void* fn = reinterpret_cast<const void*>(f2i::linear_tc_decode_kernel);
   const size_t smem = std::max<size_t>(
-      120 * 1024, 1024 + (size_t)f2i::kTdAStages * f2i::kTdAStageBytes + (size_t)P.bstages * P.bstage_bytes +
+      120 * 1024, 1024 + (size_t)f2i::kTdAStages * f2i::kTdAStageBytes + (size_t)f2i::kTdTStages * P.bstage_bytes +
                       f2i::kTdRedBytes + sizeof(f2i::TdSmem));
   fairy2i_status st = ensure_smem(fn, smem, "sparse tensor-core decode");
   if (st != FAIRY2I_OK) return st;

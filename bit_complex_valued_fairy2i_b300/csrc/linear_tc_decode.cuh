@@ -49,7 +49,6 @@ constexpr int kTdMaxGroup = 8;
 constexpr int kTdMaxTokens = 8;
 constexpr int kTdAStages = 16;  // shared-memory ring of code chunks (4 KB each)
 constexpr int kTdTStages = 4;   // TMEM stages of A + metadata (one chunk each)
-constexpr int kTdMaxBStages = 8;
 constexpr int kTdThreads = 608;  // 19 warps
 constexpr int kTdBuilders = 4;   // B-construction warps (chunk c goes to builder c % 4)
 constexpr int kTdLoaders = 8;    // loader lanes, each with its own chunk in flight
@@ -72,7 +71,7 @@ struct TdParams {
   CUtensorMap tmap[kTdMaxGroup];  // odd last block: 4-D view (u32, g, row tile, plane)
   TdProblem p[kTdMaxGroup];
   int32_t count, T, R, M;
-  int32_t N, nsub, bstages, bstage_bytes;
+  int32_t N, nsub, bstage_bytes, pad0_;
   int32_t ctas, pad_;
   uint16_t off[kTdMaxCtas + 1];  // schedule of CTA i: sched[off[i] .. off[i + 1])
   uint16_t sched[kTdMaxSched];   // (problem << 13) | tile
@@ -203,9 +202,9 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
 
 struct TdSmem {
   uint64_t a_full[kTdAStages], a_empty[kTdAStages];  // code chunks in shared memory
-  uint64_t s_full[kTdTStages];   // TMEM A + metadata written (4 expander warps) and B built (1 builder warp)
-  uint64_t s_empty[kTdTStages];  // the chunk's MMAs are done with TMEM stage (commit)
-  uint64_t b_empty[kTdMaxBStages];  // the chunk's MMAs are done with B stage (commit)
+  // Stage ts (chunk c goes to stage c % 4) = TMEM A + metadata columns and a B buffer.
+  uint64_t s_full[kTdTStages];   // A + metadata written (4 expander warps) and B built (1 builder warp)
+  uint64_t s_empty[kTdTStages];  // the chunk's MMAs are done with the stage (one commit)
   uint64_t acc_full[2], acc_empty[2];
   uint64_t red_full[2];  // the four epilogue warps have written their plane sums of a tile
   uint64_t done[2];
@@ -238,8 +237,8 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
   extern __shared__ __align__(1024) uint8_t td_smem_raw[];
   uint8_t* base = td_smem_raw + ((1024 - (smem_u32(td_smem_raw) & 1023)) & 1023);
   uint8_t* a_ring = base;                                      // kTdAStages x 4 KB
-  uint8_t* b_ring = a_ring + kTdAStages * kTdAStageBytes;      // bstages x bstage_bytes
-  float2* red = reinterpret_cast<float2*>(b_ring + P.bstages * P.bstage_bytes);  // [2][128][8]
+  uint8_t* b_ring = a_ring + kTdAStages * kTdAStageBytes;      // kTdTStages x bstage_bytes
+  float2* red = reinterpret_cast<float2*>(b_ring + kTdTStages * P.bstage_bytes);  // [2][128][8]
   TdSmem& S = *reinterpret_cast<TdSmem*>(reinterpret_cast<uint8_t*>(red) + kTdRedBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -260,7 +259,6 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
       mbar_init(smem_u32(&S.s_full[i]), 5);
       mbar_init(smem_u32(&S.s_empty[i]), 1);
     }
-    for (int i = 0; i < kTdMaxBStages; ++i) mbar_init(smem_u32(&S.b_empty[i]), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&S.acc_full[i]), 2);
       mbar_init(smem_u32(&S.acc_empty[i]), 4);
@@ -292,12 +290,21 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
         uint32_t mx = 0;
         if ((pr.m & 7) == 0) {
           const uint4* x4 = reinterpret_cast<const uint4*>(xr);
-          for (int64_t k = tid; k < row / 8; k += kTdThreads) {
-            const uint4 v = __ldg(x4 + k);
-            mx = __vmaxu2(mx, v.x & 0x7fff7fffu);
-            mx = __vmaxu2(mx, v.y & 0x7fff7fffu);
-            mx = __vmaxu2(mx, v.z & 0x7fff7fffu);
-            mx = __vmaxu2(mx, v.w & 0x7fff7fffu);
+          const int64_t nv = row / 8;
+          for (int64_t k0 = tid; k0 < nv; k0 += 4 * kTdThreads) {  // four loads in flight per thread
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int64_t k = k0 + (int64_t)u * kTdThreads;
+              v[u] = k < nv ? __ldg(x4 + k) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              mx = __vmaxu2(mx, v[u].x & 0x7fff7fffu);
+              mx = __vmaxu2(mx, v[u].y & 0x7fff7fffu);
+              mx = __vmaxu2(mx, v[u].z & 0x7fff7fffu);
+              mx = __vmaxu2(mx, v[u].w & 0x7fff7fffu);
+            }
           }
         } else {
           for (int64_t k = tid; k < row; k += kTdThreads) mx = max(mx, (uint32_t)(__ldg(xr + k) & 0x7fffu));
@@ -377,14 +384,14 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
         uint32_t acc_flag = 0;
         for (int c = 0; c < nch; ++c, ++chunk) {
           if ((int)(chunk & 1) != q) continue;
-          const uint32_t ts = chunk % kTdTStages, bs = chunk % (uint32_t)P.bstages;
+          const uint32_t ts = chunk % kTdTStages;
           if (!mbar_wait(smem_u32(&S.s_full[ts]), (chunk / kTdTStages) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_col = tmem + 32u * ts, m_col = tmem + 128u + 8u * ts;
-          const uint64_t bd = bdesc_hi | (uint64_t)(bring16 + bs * bstage16);
+          const uint64_t bd = bdesc_hi | (uint64_t)(bring16 + ts * bstage16);
           tc_mma_sp_f8(d0, a_col, bd, m_col, idesc, acc_flag);
           tc_mma_sp_f8(d1, a_col + 8u, bd + kstep_b16, m_col + 2u, idesc, nsub == 4 ? acc_flag : 1u);
           if (c < full) {
@@ -393,7 +400,6 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
           }
           acc_flag = 1u;
           tc_commit(smem_u32(&S.s_empty[ts]));
-          tc_commit(smem_u32(&S.b_empty[bs]));
         }
         if (!ok) break;
         tc_commit(smem_u32(&S.acc_full[abuf]));
@@ -591,12 +597,12 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
       const bool vec = (pr.m & 3) == 0;
       for (int c = 0; c < nch; ++c, ++chunk) {
         if ((int)(chunk % kTdBuilders) != par) continue;
-        const uint32_t bs = chunk % (uint32_t)P.bstages, ts = chunk % kTdTStages;
-        if (!mbar_wait_warp(smem_u32(&S.b_empty[bs]), ((chunk / P.bstages) & 1) ^ 1, abort_flag)) {
+        const uint32_t ts = chunk % kTdTStages;
+        if (!mbar_wait_warp(smem_u32(&S.s_empty[ts]), ((chunk / kTdTStages) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
-        uint8_t* bst = b_ring + bs * P.bstage_bytes;
+        uint8_t* bst = b_ring + ts * P.bstage_bytes;
         for (int t = 0; t < M; ++t) {
           const int col0 = c * 128 + lane * 4;
           const uint16_t* xr = pr.x + (int64_t)t * 2 * pr.m;
