@@ -403,6 +403,8 @@ fairy2i_status launch_tc_decode(const fairy2i_packed* qs, const void* const* xs,
   }
   int e = 0;
   for (int c = 0; c < ctas; ++c) {
+    if (per[c].size() > (size_t)f2i::kTdMaxLocal)
+      return fail(FAIRY2I_ERR_UNSUPPORTED, "sparse tensor-core decode: %zu tiles on one CTA", per[c].size());
     std::sort(per[c].begin(), per[c].end());
     P.off[c] = (uint16_t)e;
     for (uint16_t v : per[c]) P.sched[e++] = v;

@@ -54,6 +54,7 @@ constexpr int kTdBuilders = 4;   // B-construction warps (chunk c goes to builde
 constexpr int kTdLoaders = 8;    // loader lanes, each with its own chunk in flight
 constexpr int kTdMaxCtas = 160;
 constexpr int kTdMaxSched = 6144;
+constexpr int kTdMaxLocal = 1024;  // tile entries of one CTA (copied to shared memory)
 constexpr uint32_t kTdTmemCols = 512;
 constexpr uint32_t kTdAccCol = 256;  // accumulators: 2 buffers x nsub x N columns
 constexpr int kTdAStageBytes = 4096;
@@ -211,6 +212,8 @@ struct TdSmem {
   uint32_t xmax[kTdMaxGroup][kTdMaxTokens];
   float scale[kTdMaxGroup][kTdMaxTokens];  // 2^s
   float inv[kTdMaxGroup][kTdMaxTokens];    // 2^-s (NaN when x has a non-finite entry)
+  uint16_t sched[kTdMaxLocal];  // this CTA's tile entries: (problem << 13) | tile
+  int32_t kb[kTdMaxGroup];      // column blocks per problem
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -219,10 +222,15 @@ struct TdSmem {
 struct TdCursor {
   int e, c;
 };
-__device__ __forceinline__ int td_nch(const TdParams& P, int e) { return (P.p[P.sched[e] >> 13].KB + 1) >> 1; }
-__device__ __forceinline__ void td_advance(const TdParams& P, TdCursor& cur, int steps, int t_end) {
+// Chunk counts come from the shared-memory copies of the schedule and of the column-block counts
+// (dynamically indexed kernel parameters would go through the constant cache).
+__device__ __forceinline__ int td_nch(const uint16_t* sched, const int32_t* kb, int e) {
+  return (kb[sched[e] >> 13] + 1) >> 1;
+}
+__device__ __forceinline__ void td_advance(const uint16_t* sched, const int32_t* kb, TdCursor& cur, int steps,
+                                           int t_end) {
   while (steps > 0 && cur.e < t_end) {
-    const int left = td_nch(P, cur.e) - cur.c;
+    const int left = td_nch(sched, kb, cur.e) - cur.c;
     if (steps < left) {
       cur.c += steps;
       return;
@@ -243,12 +251,14 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
-  const int t_begin = P.off[cta], t_end = P.off[cta + 1];
+  const int t_begin = 0, t_end = P.off[cta + 1] - P.off[cta];  // local tile entries in S.sched
   const int T = P.T, R = P.R, M = P.M, N = P.N, nsub = P.nsub;
   volatile int* abort_flag = &S.abort_flag;
 
   // ---- setup: barriers, TMEM, per-token scales of x ----
   if (tid < kTdMaxGroup * kTdMaxTokens) (&S.xmax[0][0])[tid] = 0u;
+  for (int i = tid; i < t_end; i += kTdThreads) S.sched[i] = P.sched[P.off[cta] + i];
+  if (tid < kTdMaxGroup) S.kb[tid] = tid < P.count ? P.p[tid].KB : 0;
   if (tid == 0) {
     S.abort_flag = 0;
     for (int i = 0; i < kTdAStages; ++i) {
@@ -280,7 +290,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
   // magnitudes compare as integers (v & 0x7fff), NaN above every finite value.
   {
     uint32_t used = 0;
-    for (int e = t_begin; e < t_end; ++e) used |= 1u << (P.sched[e] >> 13);
+    for (int e = t_begin; e < t_end; ++e) used |= 1u << (S.sched[e] >> 13);
     for (int i = 0; i < P.count; ++i) {
       if (!((used >> i) & 1u)) continue;
       const TdProblem& pr = P.p[i];
@@ -338,11 +348,11 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
       const int Rt = R >> 4;
       const uint32_t full_bytes = 512u * Rt * 2 * T, tail_bytes = 256u * Rt * 2 * T;
       TdCursor cur{t_begin, 0};
-      td_advance(P, cur, lane, t_end);
+      td_advance(S.sched, S.kb, cur, lane, t_end);
       for (uint32_t chunk = lane; cur.e < t_end; chunk += kTdLoaders) {
         if (*abort_flag) break;
-        const int pi = P.sched[cur.e] >> 13, tile = P.sched[cur.e] & 8191;
-        const int full = P.p[pi].KB >> 1;
+        const int pi = S.sched[cur.e] >> 13, tile = S.sched[cur.e] & 8191;
+        const int full = S.kb[pi] >> 1;
         const uint32_t s = chunk % kTdAStages;
         if (!mbar_wait(smem_u32(&S.a_empty[s]), ((chunk / kTdAStages) & 1) ^ 1, abort_flag)) break;
         const uint32_t bar = smem_u32(&S.a_full[s]);
@@ -354,7 +364,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
           mbar_arrive_expect_tx(bar, tail_bytes);
           tma_load_4d(dst, &P.tmap[pi], bar, 0, 0, tile * Rt, 0);
         }
-        td_advance(P, cur, kTdLoaders, t_end);
+        td_advance(S.sched, S.kb, cur, kTdLoaders, t_end);
       }
     }
   } else if (warp == 1 || warp == 18) {
@@ -374,8 +384,8 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
       int tl = 0;
       bool ok = true;
       for (int e = t_begin; e < t_end && ok; ++e, ++tl) {
-        const int pi = P.sched[e] >> 13;
-        const int KB = P.p[pi].KB, full = KB >> 1, nch = (KB + 1) >> 1;
+        const int pi = S.sched[e] >> 13;
+        const int KB = S.kb[pi], full = KB >> 1, nch = (KB + 1) >> 1;
         const int abuf = tl & 1;
         if (!mbar_wait(smem_u32(&S.acc_empty[abuf]), ((tl >> 1) & 1) ^ 1, abort_flag)) break;
         tc_fence_after();
@@ -424,8 +434,8 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
     uint32_t chunk = 0;
     bool ok = true;
     for (int e = t_begin; e < t_end && ok; ++e) {
-      const int pi = P.sched[e] >> 13;
-      const int KB = P.p[pi].KB, full = KB >> 1, nch = (KB + 1) >> 1;
+      const int pi = S.sched[e] >> 13;
+      const int KB = S.kb[pi], full = KB >> 1, nch = (KB + 1) >> 1;
       for (int c = 0; c < nch; ++c, ++chunk) {
         if ((int)(chunk & 1) != par) continue;
         const uint32_t s = chunk % kTdAStages, ts = chunk % kTdTStages;
@@ -508,7 +518,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
     int tl = 0;
     uint32_t chunk0 = 0;  // first chunk of the tile in the CTA's sequence
     for (int e = t_begin; e < t_end; ++e, ++tl) {
-      const int pi = P.sched[e] >> 13, tile = P.sched[e] & 8191;
+      const int pi = S.sched[e] >> 13, tile = S.sched[e] & 8191;
       const TdProblem& pr = P.p[pi];
       const int nch = (pr.KB + 1) >> 1;
       // Sub-accumulators written in this tile: issuer q took a chunk iff the tile has two chunks or
@@ -591,7 +601,7 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
     uint32_t chunk = 0;
     bool ok = true;
     for (int e = t_begin; e < t_end && ok; ++e) {
-      const int pi = P.sched[e] >> 13;
+      const int pi = S.sched[e] >> 13;
       const TdProblem& pr = P.p[pi];
       const int nch = (pr.KB + 1) >> 1;
       const bool vec = (pr.m & 3) == 0;
