@@ -346,3 +346,60 @@ int oracle_linear_dense(const double *Uhat, const double *What, int64_t n, int64
     }
     return ORACLE_OK;
 }
+
+/* ---- Gradient of the layer with respect to its input (for quantization-aware
+ * training with the straight-through estimator: [Note] Step 3 and the QAT
+ * paragraph; [W2 card] y = Ux + W conj(x)).
+ * For a real loss L and g = dL/dRe y + i dL/dIm y (per token, complex [n]),
+ *   dL/dRe x + i dL/dIm x = U^^H g + W^^T conj(g)
+ * (the real form of the layer is a real matrix; its transpose is the real
+ * form of (U^^H, W^^T)).  Multiplication-free in the codes: per row j and
+ * stage t the gradient is scaled once per axis,
+ *   U:  h_re = s_re g_j,          h_im = s_im (-i g_j)
+ *   W:  h_re = s_re conj(g_j),    h_im = s_im (i conj(g_j))
+ * and every code adds or subtracts the h of its axis into its column:
+ *   gx_k += sign(code_jk) * (code_jk real-axis ? h_re : h_im).
+ * g: float [M][2n] = [dRe y | dIm y];  gx: double [M][2m] = [dRe x | dIm x]. */
+int oracle_linear_grad_x(const uint8_t *codesU, const float *scalesU,
+                         const uint8_t *codesW, const float *scalesW,
+                         int64_t n, int64_t m, int32_t T,
+                         const float *g, int64_t M, double *gx)
+{
+    if (!codesU || !scalesU || !codesW || !scalesW || !g || !gx || n <= 0 || m <= 0 || T < 1 || M < 0)
+        return ORACLE_BAD_ARG;
+    const int64_t nm = n * m;
+    for (int64_t tok = 0; tok < M; ++tok) {
+        const float *gt = g + tok * 2 * n;
+        double *out = gx + tok * 2 * m;
+        for (int64_t k = 0; k < 2 * m; ++k) out[k] = 0.0;
+        for (int X = 0; X < 2; ++X) {
+            const uint8_t *codes = X == 0 ? codesU : codesW;
+            const float *scales = X == 0 ? scalesU : scalesW;
+            for (int32_t t = 0; t < T; ++t) {
+                for (int64_t j = 0; j < n; ++j) {
+                    const double ga = gt[j], gb = gt[n + j];   /* g_j = ga + i gb */
+                    const double s_re = scales[((int64_t)t * 2 + 0) * n + j];
+                    const double s_im = scales[((int64_t)t * 2 + 1) * n + j];
+                    double hre_a, hre_b, him_a, him_b;         /* h = a + i b */
+                    if (X == 0) {
+                        hre_a = s_re * ga;  hre_b = s_re * gb;     /* s_re g */
+                        him_a = s_im * gb;  him_b = -s_im * ga;    /* s_im (-i)(ga + i gb) */
+                    } else {
+                        hre_a = s_re * ga;  hre_b = -s_re * gb;    /* s_re (ga - i gb) */
+                        him_a = s_im * gb;  him_b = s_im * ga;     /* s_im i (ga - i gb) */
+                    }
+                    const uint8_t *c = codes + (int64_t)t * nm + j * m;
+                    for (int64_t k = 0; k < m; ++k) {
+                        switch (c[k]) {
+                        case 0: out[k] += hre_a; out[m + k] += hre_b; break;
+                        case 1: out[k] -= hre_a; out[m + k] -= hre_b; break;
+                        case 2: out[k] += him_a; out[m + k] += him_b; break;
+                        default: out[k] -= him_a; out[m + k] -= him_b; break;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}

@@ -67,8 +67,10 @@ def _lib():
         lib.oracle_dequantize.argtypes = [P, P, I64, I64, I32, P]
         lib.oracle_linear_mulfree.argtypes = [P, P, P, P, I64, I64, I32, P, I64, P]
         lib.oracle_linear_dense.argtypes = [P, P, I64, I64, P, I64, P]
+        lib.oracle_linear_grad_x.argtypes = [P, P, P, P, I64, I64, I32, P, I64, P]
         for f in (lib.oracle_convert_f64, lib.oracle_convert_f32, lib.oracle_quantize,
-                  lib.oracle_dequantize, lib.oracle_linear_mulfree, lib.oracle_linear_dense):
+                  lib.oracle_dequantize, lib.oracle_linear_mulfree, lib.oracle_linear_dense,
+                  lib.oracle_linear_grad_x):
             f.restype = ctypes.c_int
         _lib_handle = lib
     return _lib_handle
@@ -186,6 +188,35 @@ def linear_dense(Uhat: np.ndarray, What: np.ndarray, x: np.ndarray) -> np.ndarra
     y = np.empty((M, 2 * n), np.float64)
     _check(_lib().oracle_linear_dense(_ptr(Up), _ptr(Wp), n, m, _ptr(x), M, _ptr(y)))
     return y
+
+
+def linear_grad_x_mulfree(qU: Quantized, qW: Quantized, g: np.ndarray) -> np.ndarray:
+    """dL/dx = U^^H g + W^^T conj(g) for g = [dRe y | dIm y] float32 [M, 2n], by one scale multiply
+    per row, stage and axis and adds/subtracts over the codes; returns [dRe x | dIm x] [M, 2m]."""
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    if g.ndim == 1:
+        g = g[None, :]
+    T, n, m = qU.codes.shape
+    assert qW.codes.shape == (T, n, m) and g.shape[1] == 2 * n
+    M = g.shape[0]
+    gx = np.empty((M, 2 * m), np.float64)
+    cu = np.ascontiguousarray(qU.codes)
+    cw = np.ascontiguousarray(qW.codes)
+    su = np.ascontiguousarray(qU.scales, dtype=np.float32)
+    sw = np.ascontiguousarray(qW.scales, dtype=np.float32)
+    _check(_lib().oracle_linear_grad_x(_ptr(cu), _ptr(su), _ptr(cw), _ptr(sw), n, m, T, _ptr(g), M, _ptr(gx)))
+    return gx
+
+
+def linear_grad_x_dense(Uhat: np.ndarray, What: np.ndarray, g: np.ndarray) -> np.ndarray:
+    """The same gradient with complex matrix products of the dequantized U^, W^ (complex [n, m])."""
+    g = np.asarray(g, np.float64)
+    if g.ndim == 1:
+        g = g[None, :]
+    n, m = Uhat.shape
+    gc = g[:, :n] + 1j * g[:, n:]
+    gxc = gc @ np.conj(Uhat) + np.conj(gc) @ What  # row form of U^^H g + W^^T conj(g)
+    return np.concatenate([gxc.real, gxc.imag], axis=1)
 
 
 def bf16_bits_to_f64(x: np.ndarray) -> np.ndarray:
