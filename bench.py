@@ -404,6 +404,52 @@ def run_stack_only(args, world, rank, local):
                                     "rows": rows}}), flush=True)
 
 
+def run_grad_only(args, world, rank, local):
+    """Input gradient dL/dx = U^^H g + W^^T conj(g) of every projection of the stack, M = 1, T = 2,
+    one CUDA graph of all launches: packed bytes / device time."""
+    import bit_complex_valued_fairy2i_b300 as f2i
+    from bit_complex_valued_fairy2i_b300 import build as f2i_build
+
+    f2i_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    blocks = args.blocks
+    stack, _ = build_stack(f2i, blocks, dev)
+    nbytes = sum(q.nbytes for layers in stack for q in layers)
+    gs = [[torch.randn((1, 2 * q.n), device=dev) for q in layers] for layers in stack]
+    gxs = [[torch.empty((1, 2 * q.m), device=dev) for q in layers] for layers in stack]
+
+    def step():
+        for layers, gl, xl in zip(stack, gs, gxs):
+            for q, g, gx in zip(layers, gl, xl):
+                f2i.linear_grad_x(q, g, out=gx)
+
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(3, min(args.steps, 200))
+    start.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop) / steps
+    if rank == 0:
+        print(json.dumps({"grad_x": {
+            "workload": f"input gradient of llama2-7b projections, {blocks} blocks x 7, M=1, T={T_STAGES}, "
+                        "one launch per projection",
+            "kernel": "linear_grad_x_kernel (CUDA cores, 8-CTA clusters)",
+            "ms_per_step": ms, "GBps": nbytes / (ms * 1e-3) / 1e9, "bytes_per_step": nbytes,
+            "us_per_block": ms * 1e3 / blocks, "steps": steps}}), flush=True)
+
+
 def run_sweep_only(args, world, rank, local):
     import bit_complex_valued_fairy2i_b300 as f2i
     from bit_complex_valued_fairy2i_b300 import build as f2i_build
@@ -566,7 +612,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["decode", "prefill", "sweep", "stack"], default="decode",
+    ap.add_argument("--mode", choices=["decode", "prefill", "sweep", "stack", "grad"], default="decode",
                     help="prefill: time only the prefill leg (for profiling)")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--decode-algo", choices=sorted(DECODE_KERNELS), default="auto",
@@ -587,6 +633,8 @@ def main():
         run_sweep_only(args, world, rank, local)
     elif args.mode == "stack":
         run_stack_only(args, world, rank, local)
+    elif args.mode == "grad":
+        run_grad_only(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -32,7 +32,7 @@ EXPORTED = (
     "fairy2i_codes_bytes", "fairy2i_scales_count", "fairy2i_convert", "fairy2i_quantize",
     "fairy2i_linear", "fairy2i_linear_ex", "fairy2i_linear_group", "fairy2i_unpack_codes",
     "fairy2i_sync_status", "fairy2i_last_error", "fairy2i_layout_version", "fairy2i_selftest_bounded_wait",
-    "fairy2i_convert_quantize",
+    "fairy2i_convert_quantize", "fairy2i_linear_grad_x",
 )
 
 
@@ -75,6 +75,7 @@ def load_library(path: str = LIB_PATH):
         "fairy2i_layout_version": (I32, []),
         "fairy2i_selftest_bounded_wait": (ctypes.c_int, [I32, P]),
         "fairy2i_convert_quantize": (ctypes.c_int, [P, I64, I64, I32, PD, P]),
+        "fairy2i_linear_grad_x": (ctypes.c_int, [PD, P, I64, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -197,6 +198,18 @@ def linear(q: Packed, x: torch.Tensor, algo: str = "auto", out: torch.Tensor | N
     _check(load_library().fairy2i_linear_ex(ctypes.byref(d), x.data_ptr(), x.shape[0], y.data_ptr(), ALGO[algo],
                                             _stream(stream)))
     return y
+
+
+def linear_grad_x(q: Packed, gy: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dL/dx = U^^H g + W^^T conj(g) for gy float32 [M, 2n] ([dRe y | dIm y]) -> gx float32 [M, 2m]."""
+    _dev(gy, "gy")
+    if gy.dtype != torch.float32 or gy.dim() != 2 or gy.shape[1] != 2 * q.n:
+        raise ValueError(f"gy must be float32 [M, {2 * q.n}]")
+    gx = out if out is not None else torch.empty((gy.shape[0], 2 * q.m), dtype=torch.float32, device=gy.device)
+    d = q.desc()
+    _check(load_library().fairy2i_linear_grad_x(ctypes.byref(d), gy.data_ptr(), gy.shape[0], gx.data_ptr(),
+                                                _stream(stream)))
+    return gx
 
 
 def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None):

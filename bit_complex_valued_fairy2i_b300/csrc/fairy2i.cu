@@ -20,6 +20,7 @@
 #include "linear_decode.cuh"
 #include "linear_prefill.cuh"
 #include "linear_tc_decode.cuh"
+#include "linear_grad.cuh"
 
 namespace {
 
@@ -642,6 +643,30 @@ fairy2i_status fairy2i_linear(const fairy2i_packed* q, const void* x, int64_t M,
 fairy2i_status fairy2i_linear_group(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int32_t count,
                                     int64_t M, fairy2i_algo algo, void* stream) {
   return linear_group_impl(qs, xs, ys, count, M, algo, static_cast<cudaStream_t>(stream));
+}
+
+fairy2i_status fairy2i_linear_grad_x(const fairy2i_packed* q, const float* gy, int64_t M, float* gx, void* stream) {
+  fairy2i_status st = check_packed(q);
+  if (st != FAIRY2I_OK) return st;
+  if (M < 0) return fail(FAIRY2I_ERR_SHAPE, "M=%lld is negative", (long long)M);
+  if (M == 0) return ok();
+  if (!gy || !gx) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL gradient pointer");
+  if (!aligned(gy, 16) || !aligned(gx, 16)) return fail(FAIRY2I_ERR_INVALID_ARG, "gy and gx must be 16-byte aligned");
+  const int64_t pairs = (M + 1) / 2;  // tokens go two per CTA (one when M = 1)
+  if (pairs * f2i::kGxCluster > 65535) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
+  f2i::GradParams P;
+  P.codes = static_cast<const uint8_t*>(q->codes);
+  P.scales = q->scales;
+  P.g = gy;
+  P.gx = gx;
+  P.n = q->n;
+  P.m = q->m;
+  P.T = q->T;
+  P.M = (int32_t)M;
+  const dim3 grid((unsigned)f2i::col_blocks(q->m), (unsigned)(pairs * f2i::kGxCluster));
+  if (M == 1) f2i::linear_grad_x_kernel<1><<<grid, f2i::kGxWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(P);
+  else f2i::linear_grad_x_kernel<2><<<grid, f2i::kGxWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(P);
+  return check_launch("input-gradient launch");
 }
 
 fairy2i_status fairy2i_unpack_codes(const fairy2i_packed* q, uint8_t* codes_out, void* stream) {

@@ -163,6 +163,19 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
                                     float *const *ys, int32_t count, int64_t M,
                                     fairy2i_algo algo, void *stream);
 
+/* Input gradient of the layer for training through it with the
+ * straight-through estimator ("Fairy2i: Ultra-Low-Bit ...", quantization-aware
+ * training; "Fairy2i-W2" card, y = Ux + W conj(x)):
+ *   dL/dx = U^^H g + W^^T conj(g),   g = dL/dRe y + i dL/dIm y,
+ * the transpose of the layer's real form applied to [dL/dRe y | dL/dIm y].
+ * U^ and W^ are the dequantized sums of stages of q.
+ *   gy : device float32 [M][2n], each row [dL/dRe y | dL/dIm y], 16-byte aligned
+ *   gx : device float32 [M][2m], each row [dL/dRe x | dL/dIm x], 16-byte aligned
+ * Deterministic (fixed summation order); M = 0 is a no-op.
+ * Errors: INVALID_ARG (null/misaligned/bad version), SHAPE, UNSUPPORTED (M > 16382). */
+fairy2i_status fairy2i_linear_grad_x(const fairy2i_packed *q, const float *gy, int64_t M, float *gx,
+                                     void *stream);
+
 /* Canonical view of the codes: device uint8 [2 (U, W)][T][n][m] with values
  * 0 = +1, 1 = -1, 2 = +i, 3 = -i. */
 fairy2i_status fairy2i_unpack_codes(const fairy2i_packed *q, uint8_t *codes_out, void *stream);

@@ -117,6 +117,17 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.fairy2i_linear_group(descs, arr, arr, 300, 1, 0, None) == 1
 
 
+def test_linear_grad_x_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(256)
+    d = _desc()
+    assert lib.fairy2i_linear_grad_x(None, p, 1, p, None) == 1
+    assert lib.fairy2i_linear_grad_x(ctypes.byref(d), None, 1, p, None) == 1
+    assert lib.fairy2i_linear_grad_x(ctypes.byref(d), p, -1, p, None) == 2
+    assert lib.fairy2i_linear_grad_x(ctypes.byref(d), ctypes.c_void_p(260), 1, p, None) == 1
+    assert lib.fairy2i_linear_grad_x(ctypes.byref(d), p, 0, p, None) == 0  # no tokens: nothing launched
+    assert lib.fairy2i_linear_grad_x(ctypes.byref(d), p, 20000, p, None) == 4
+
+
 def test_convert_quantize_rejects_bad_arguments(lib):
     p = ctypes.c_void_p(256)
     d = _desc(n=2, m=2, T=1)
