@@ -81,58 +81,75 @@ __global__ void __cluster_dims__(1, kGxCluster, 1) __launch_bounds__(kGxWarps * 
         gb[rho][TOK - 1] = ok && has_t1 ? __ldg(g1 + n + j) : 0.0f;
       }
     }
-    for (int p = 0; p < 2 * T; ++p) {
-      const int X = p / T;
-      const uint2 w =
-          __ldcs(reinterpret_cast<const uint2*>(P.codes + p * pbytes + pair_offset(rt, kb, lane, KB)));
-      const uint32_t S = w.x;
-      uint32_t Fq[4];
+    // planes in groups of four: the group's code words and scales are loaded before any is used
+    for (int p0 = 0; p0 < 2 * T; p0 += 4) {
+      uint2 wv[4];
+      float sre[4][2], sim[4][2];
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq) Fq[qq] = __shfl_sync(0xffffffffu, w.y, (lane & ~3) | qq) >> (4 * q);
-      // per row: the two candidate values (real axis, imaginary axis) of each token, complex
-      float hre[2][TOK][2], him[2][TOK][2];  // [rho][token][re, im]
+      for (int pp = 0; pp < 4; ++pp) {
+        const int p = p0 + pp;
+        const bool pok = p < 2 * T;
+        wv[pp] = pok ? __ldcs(reinterpret_cast<const uint2*>(P.codes + p * pbytes + pair_offset(rt, kb, lane, KB)))
+                     : make_uint2(0u, 0u);
 #pragma unroll
-      for (int rho = 0; rho < 2; ++rho) {
-        const int64_t j = rho ? j1 : j0;
-        const bool ok = j < n;
-        const float s_re = ok ? __ldg(P.scales + (int64_t)(2 * p) * n + j) : 0.0f;
-        const float s_im = ok ? __ldg(P.scales + (int64_t)(2 * p + 1) * n + j) : 0.0f;
-#pragma unroll
-        for (int tk = 0; tk < TOK; ++tk) {
-          const float a = ga[rho][tk], b = gb[rho][tk];
-          if (X == 0) {
-            hre[rho][tk][0] = s_re * a;
-            hre[rho][tk][1] = s_re * b;
-            him[rho][tk][0] = s_im * b;
-            him[rho][tk][1] = -s_im * a;
-          } else {
-            hre[rho][tk][0] = s_re * a;
-            hre[rho][tk][1] = -s_re * b;
-            him[rho][tk][0] = s_im * b;
-            him[rho][tk][1] = s_im * a;
-          }
+        for (int rho = 0; rho < 2; ++rho) {
+          const int64_t j = rho ? j1 : j0;
+          const bool ok = pok && j < n;
+          sre[pp][rho] = ok ? __ldg(P.scales + (int64_t)(2 * p) * n + j) : 0.0f;
+          sim[pp][rho] = ok ? __ldg(P.scales + (int64_t)(2 * p + 1) * n + j) : 0.0f;
         }
       }
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
+      for (int pp = 0; pp < 4; ++pp) {
+        const int p = p0 + pp;
+        if (p >= 2 * T) break;
+        const int X = p / T;
+        const uint32_t S = wv[pp].x;
+        uint32_t Fq[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int qq = 0; qq < 4; ++qq) Fq[qq] = __shfl_sync(0xffffffffu, wv[pp].y, (lane & ~3) | qq) >> (4 * q);
+        // per row: the real-axis value hre and the difference him - hre of each token, complex
+        float hre[2][TOK][2], hd[2][TOK][2];  // [rho][token][re, im]
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = 4 * s + 2 * h + e;  // column 16 s + 8 h + 2 q + e of the block
+        for (int rho = 0; rho < 2; ++rho) {
+          const float s_re = sre[pp][rho], s_im = sim[pp][rho];
 #pragma unroll
-            for (int rho = 0; rho < 2; ++rho) {
-              const uint32_t neg = ((S >> (15 + 16 * e - (4 * s + 2 * h + rho))) & 1u) << 31;
-              const bool imag = (Fq[h + 2 * (s >> 1)] >> (16 * rho + (s & 1) + 2 * e)) & 1u;
+          for (int tk = 0; tk < TOK; ++tk) {
+            const float a = ga[rho][tk], b = gb[rho][tk];
+            const float him_re = s_im * b, him_im = X == 0 ? -s_im * a : s_im * a;
+            hre[rho][tk][0] = s_re * a;
+            hre[rho][tk][1] = X == 0 ? s_re * b : -s_re * b;
+            hd[rho][tk][0] = him_re - hre[rho][tk][0];
+            hd[rho][tk][1] = him_im - hre[rho][tk][1];
+          }
+        }
 #pragma unroll
-              for (int tk = 0; tk < TOK; ++tk) {
-                const float vr = imag ? him[rho][tk][0] : hre[rho][tk][0];
-                const float vi = imag ? him[rho][tk][1] : hre[rho][tk][1];
-                acc[c][tk][0] += __uint_as_float(__float_as_uint(vr) ^ neg);
-                acc[c][tk][1] += __uint_as_float(__float_as_uint(vi) ^ neg);
+        for (int s = 0; s < 4; ++s)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = 4 * s + 2 * h + e;  // column 16 s + 8 h + 2 q + e of the block
+#pragma unroll
+              for (int rho = 0; rho < 2; ++rho) {
+                // sign bit of the code moved to bit 31: sgn = +-1.0; axis flag spread to a word
+                // mask: sf = sgn for an imaginary-axis code, 0 otherwise.  The code then adds
+                // sgn * hre + sf * (him - hre), i.e. +-(its axis' value), on the FMA pipe.
+                const int kSign = 15 + 16 * e - (4 * s + 2 * h + rho);
+                const int kFlag = 16 * rho + (s & 1) + 2 * e;
+                const uint32_t sgn = ((S << (31 - kSign)) & 0x80000000u) | 0x3f800000u;
+                const uint32_t fmask = (uint32_t)((int32_t)(Fq[h + 2 * (s >> 1)] << (31 - kFlag)) >> 31);
+                const float fs = __uint_as_float(sgn), fsf = __uint_as_float(sgn & fmask);
+#pragma unroll
+                for (int tk = 0; tk < TOK; ++tk) {
+                  acc[c][tk][0] = fmaf(fs, hre[rho][tk][0], acc[c][tk][0]);
+                  acc[c][tk][0] = fmaf(fsf, hd[rho][tk][0], acc[c][tk][0]);
+                  acc[c][tk][1] = fmaf(fs, hre[rho][tk][1], acc[c][tk][1]);
+                  acc[c][tk][1] = fmaf(fsf, hd[rho][tk][1], acc[c][tk][1]);
+                }
               }
             }
-          }
+      }
     }
   }
   // over the 8 lanes g of each column (lane = 4 g + q), fixed butterfly order
