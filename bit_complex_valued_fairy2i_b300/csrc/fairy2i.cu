@@ -393,7 +393,6 @@ fairy2i_status launch_tc_decode(const fairy2i_packed* qs, const void* const* xs,
     for (int k = 0; k < pr.tiles; ++k) tiles.push_back({2 * pr.KB + 8, i, k});
   }
   const int ctas = (int)std::min<int64_t>({(int64_t)tiles.size(), (int64_t)sm_count(), (int64_t)f2i::kTdMaxCtas});
-  P.ctas = ctas;
   std::stable_sort(tiles.begin(), tiles.end(), [](const Tile& a, const Tile& b) { return a.cost > b.cost; });
   std::vector<int64_t> load(ctas, 0);
   std::vector<std::vector<uint16_t>> per(ctas);

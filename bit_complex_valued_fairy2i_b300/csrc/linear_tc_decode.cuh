@@ -72,8 +72,7 @@ struct TdParams {
   CUtensorMap tmap[kTdMaxGroup];  // odd last block: 4-D view (u32, g, row tile, plane)
   TdProblem p[kTdMaxGroup];
   int32_t count, T, R, M;
-  int32_t N, nsub, bstage_bytes, pad0_;
-  int32_t ctas, pad_;
+  int32_t N, nsub, bstage_bytes;
   uint16_t off[kTdMaxCtas + 1];  // schedule of CTA i: sched[off[i] .. off[i + 1])
   uint16_t sched[kTdMaxSched];   // (problem << 13) | tile
 };
