@@ -143,6 +143,38 @@ __device__ __forceinline__ void block_reduce2(Tv& a, Tv& b, Tv* sa, Tv* sb, Op o
   __syncthreads();  // sa / sb are reused by the next reduction
 }
 
+// Sums of two 64-bit and two 32-bit values over the block in one round (the
+// counts travel with the exact sums; both are needed only for the scale).
+__device__ __forceinline__ void block_sum_ll2_u2(long long& a, long long& b, uint32_t& c, uint32_t& d,
+                                                 long long* sa, long long* sb, uint32_t* sc, uint32_t* sd) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+    c += __shfl_xor_sync(0xffffffffu, c, o);
+    d += __shfl_xor_sync(0xffffffffu, d, o);
+  }
+  if (lane == 0) {
+    sa[warp] = a;
+    sb[warp] = b;
+    sc[warp] = c;
+    sd[warp] = d;
+  }
+  __syncthreads();
+  a = sa[0];
+  b = sb[0];
+  c = sc[0];
+  d = sd[0];
+  for (int w = 1; w < nw; ++w) {
+    a += sa[w];
+    b += sb[w];
+    c += sc[w];
+    d += sd[w];
+  }
+  __syncthreads();  // the buffers are reused by the next reduction
+}
+
 // FUSED = false: weights from complex U, W [n][m] (grid (n, 2): row, matrix).
 // FUSED = true:  weights computed from the real R [2n][2m] with the same
 // float32 operations as the conversion kernel, so the codes and scales equal
@@ -227,7 +259,6 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
       cnt1 += isi ? 1u : 0u;
     }
     block_reduce2(mx0, mx1, s_u[0], s_u[1], [](uint32_t x, uint32_t y) { return max(x, y); });
-    block_reduce2(cnt0, cnt1, s_u[0], s_u[1], [](uint32_t x, uint32_t y) { return x + y; });
     const int e0 = mx0 ? float_exponent(mx0) : 0;
     const int e1 = mx1 ? float_exponent(mx1) : 0;
 
@@ -256,7 +287,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
         else ls1 += scaled_trunc(__float_as_uint(fabsf(im[e])), e1);
       }
     }
-    block_reduce2(ls0, ls1, s_l[0], s_l[1], [](long long x, long long y) { return x + y; });
+    block_sum_ll2_u2(ls0, ls1, cnt0, cnt1, s_l[0], s_l[1], s_u[0], s_u[1]);
     if (tid < 2) {
       const long long sum = tid == 0 ? ls0 : ls1;
       const uint32_t cnt = tid == 0 ? cnt0 : cnt1;

@@ -447,7 +447,7 @@ fairy2i_status run_tc_decode(const fairy2i_packed* qs, const void* const* xs, fl
 constexpr int64_t kTcDecodeMaxTokens = 8;
 
 // Token count from which FAIRY2I_ALGO_AUTO takes the tcgen05 prefill path.
-constexpr int64_t kPrefillMinTokens = 17;
+constexpr int64_t kPrefillMinTokens = 16;
 
 // The quantizer over U, W (FUSED = false) or straight from R (true); the
 // caller has checked the arguments.  Codes are zeroed first: each row ORs its
