@@ -9,8 +9,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <memory>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -394,12 +396,15 @@ fairy2i_status launch_tc_decode(const fairy2i_packed* qs, const void* const* xs,
   }
   const int ctas = (int)std::min<int64_t>({(int64_t)tiles.size(), (int64_t)sm_count(), (int64_t)f2i::kTdMaxCtas});
   std::stable_sort(tiles.begin(), tiles.end(), [](const Tile& a, const Tile& b) { return a.cost > b.cost; });
-  std::vector<int64_t> load(ctas, 0);
+  // least-loaded CTA first (ties to the lower index): a min-heap of (load, cta)
   std::vector<std::vector<uint16_t>> per(ctas);
+  std::priority_queue<std::pair<int64_t, int>, std::vector<std::pair<int64_t, int>>, std::greater<>> heap;
+  for (int c = 0; c < ctas; ++c) heap.push({0, c});
   for (const Tile& t : tiles) {
-    const int c = (int)(std::min_element(load.begin(), load.end()) - load.begin());
-    load[c] += t.cost;
+    auto [load, c] = heap.top();
+    heap.pop();
     per[c].push_back((uint16_t)((t.prob << 13) | t.tile));
+    heap.push({load + t.cost, c});
   }
   int e = 0;
   for (int c = 0; c < ctas; ++c) {
