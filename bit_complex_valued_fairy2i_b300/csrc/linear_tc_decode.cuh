@@ -48,10 +48,10 @@ namespace f2i {
 constexpr int kTdMaxGroup = 8;
 constexpr int kTdMaxTokens = 8;
 constexpr int kTdAStages = 16;  // shared-memory ring of code chunks (4 KB each)
-constexpr int kTdTStages = 4;   // TMEM stages of A + metadata (one chunk each)
+constexpr int kTdTStages = 4;   // stages of A + metadata in TMEM and B in shared memory (one chunk each)
 constexpr int kTdThreads = 608;  // 19 warps
 constexpr int kTdBuilders = 4;   // B-construction warps (chunk c goes to builder c % 4)
-constexpr int kTdLoaders = 8;    // loader lanes, each with its own chunk in flight
+constexpr int kTdLoaders = 8;    // loader lanes (lane l issues chunks l, l + 8, ...)
 constexpr int kTdMaxCtas = 160;
 constexpr int kTdMaxSched = 6144;
 constexpr int kTdMaxLocal = 1024;  // tile entries of one CTA (copied to shared memory)
@@ -340,9 +340,8 @@ __global__ void __launch_bounds__(kTdThreads, 1) linear_tc_decode_kernel(const _
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
-    // ---- TMA producer: one code chunk (2T planes x R rows x 128 columns) per stage.  Loader lane l
-    // takes chunks l, l + 8, ...: a thread's shared-memory and barrier operations wait for the copies
-    // it has in flight, so several lanes keep several chunks in flight. ----
+    // ---- TMA producer: one code chunk (2T planes x R rows x 128 columns) per stage; loader lane l
+    // takes chunks l, l + 8, ... ----
     if (lane < kTdLoaders) {
       const int Rt = R >> 4;
       const uint32_t full_bytes = 512u * Rt * 2 * T, tail_bytes = 256u * Rt * 2 * T;
