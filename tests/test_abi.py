@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import bit_complex_valued_fairy2i_b300 as f2i
 from bit_complex_valued_fairy2i_b300 import build as f2i_build
@@ -146,3 +147,16 @@ def test_unpack_rejects_bad_arguments(lib):
     d = _desc()
     assert lib.fairy2i_unpack_codes(ctypes.byref(d), None, None) == 1
     assert lib.fairy2i_unpack_codes(None, ctypes.c_void_p(256), None) == 1
+
+
+def test_python_wrappers_reject_host_tensors_and_bad_shapes(lib):
+    """The Python layer marshals arguments only: host tensors and wrong shapes or
+    dtypes are refused before anything reaches the library (no CPU fallback)."""
+    q = f2i.Packed(4, 8, 2, torch.zeros(f2i.codes_bytes(4, 8, 2), dtype=torch.uint8),
+                   torch.zeros((2, 2, 2, 4)))
+    with pytest.raises(ValueError):
+        f2i.linear(q, torch.zeros((1, 16), dtype=torch.bfloat16))  # host tensor
+    with pytest.raises(ValueError):
+        f2i.linear_grad_x(q, torch.zeros((1, 8)))  # host tensor
+    with pytest.raises(KeyError):
+        f2i.linear(q, torch.zeros((1, 16), dtype=torch.bfloat16), algo="nonexistent")
