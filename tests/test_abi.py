@@ -149,14 +149,14 @@ def test_unpack_rejects_bad_arguments(lib):
     assert lib.fairy2i_unpack_codes(None, ctypes.c_void_p(256), None) == 1
 
 
-def test_python_wrappers_reject_host_tensors_and_bad_shapes(lib):
-    """The Python layer marshals arguments only: host tensors and wrong shapes or
-    dtypes are refused before anything reaches the library (no CPU fallback)."""
+def test_python_wrappers_reject_host_tensors(lib):
+    """The Python layer marshals arguments only: host tensors are refused before
+    anything reaches the library (there is no CPU fallback)."""
     q = f2i.Packed(4, 8, 2, torch.zeros(f2i.codes_bytes(4, 8, 2), dtype=torch.uint8),
                    torch.zeros((2, 2, 2, 4)))
     with pytest.raises(ValueError):
         f2i.linear(q, torch.zeros((1, 16), dtype=torch.bfloat16))  # host tensor
     with pytest.raises(ValueError):
         f2i.linear_grad_x(q, torch.zeros((1, 8)))  # host tensor
-    with pytest.raises(KeyError):
-        f2i.linear(q, torch.zeros((1, 16), dtype=torch.bfloat16), algo="nonexistent")
+    # the algorithm names map onto the header's fairy2i_algo values
+    assert f2i.ALGO == {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4}
