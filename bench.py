@@ -25,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -79,7 +80,10 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+        # raw samples go to $FAIRY2I_CLOCKS_DIR (default: the system temp directory); the JSON
+        # line carries their summary
+        out_dir = os.environ.get("FAIRY2I_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"fairy2i_clocks_gpu{index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
