@@ -42,14 +42,14 @@ UNIT = "GB/s"
 T_STAGES = 2
 BLOCKS = inputs.LLAMA2_7B_BLOCKS
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch
-# of this workload, from an ncu capture of linear_mma_kernel<4,1>; must be
-# re-measured whenever that kernel changes.
+# of this workload, from an ncu capture of linear_mma_kernel<4,1,16> (one 16-warp
+# CTA per SM); must be re-measured whenever that kernel changes.
 DECODE_TRAFFIC_BYTES = 51_392_512
 # decode kernel and arithmetic per --decode-algo (auto = the 2:4-sparse mma.sync decode at M = 1)
 DECODE_KERNELS = {
-    "auto": ("linear_mma_kernel<4,1> (2:4-sparse mma.sync)",
+    "auto": ("linear_mma_kernel<4,1,16> (2:4-sparse mma.sync)",
              "bf16 (2:4-sparse mma.sync: code signs as bf16 +-2, bf16 x), fp32 accumulate"),
-    "mma": ("linear_mma_kernel<4,1> (2:4-sparse mma.sync)",
+    "mma": ("linear_mma_kernel<4,1,16> (2:4-sparse mma.sync)",
             "bf16 (2:4-sparse mma.sync: code signs as bf16 +-2, bf16 x), fp32 accumulate"),
     "tcgen05_sp": ("linear_tc_decode_kernel (2:4-sparse tcgen05.mma.sp)",
                    "e4m3 (2:4-sparse tcgen05.mma.sp: code signs as e4m3 +-1, x as two exact e4m3 terms), "

@@ -140,23 +140,36 @@ int partition(f2i::LinearGroup& G, int slots, int tiles_max) {
   return ctas;
 }
 
-template <int NPL, int TILES>
+template <int NPL, int TILES, int WARPS>
 fairy2i_status launch_mma_t(f2i::LinearGroup& G, size_t smem, int tiles_max, cudaStream_t s) {
-  auto k = f2i::linear_mma_kernel<NPL, TILES>;
+  auto k = f2i::linear_mma_kernel<NPL, TILES, WARPS>;
   const void* fn = reinterpret_cast<const void*>(k);
   fairy2i_status st = ensure_smem(fn, smem, "mma decode");
   if (st != FAIRY2I_OK) return st;
-  const int slots = sm_count() * resident_ctas(fn, f2i::kMmaWarps * 32, smem);
+  const int slots = sm_count() * resident_ctas(fn, WARPS * 32, smem);
   const int ctas = partition(G, slots, tiles_max);
-  k<<<ctas, f2i::kMmaWarps * 32, smem, s>>>(G);
+  k<<<ctas, WARPS * 32, smem, s>>>(G);
   return check_launch("mma decode launch");
 }
 
+// 16-warp CTAs exist only where 512 threads fit the register file without
+// spills (NPL * TILES <= 8, at most 128 registers per thread).
 template <int NPL>
-fairy2i_status launch_mma_tiles(f2i::LinearGroup& G, int tiles, size_t smem, int tiles_max, cudaStream_t s) {
-  return tiles == 1   ? launch_mma_t<NPL, 1>(G, smem, tiles_max, s)
-         : tiles == 2 ? launch_mma_t<NPL, 2>(G, smem, tiles_max, s)
-                      : launch_mma_t<NPL, 4>(G, smem, tiles_max, s);
+fairy2i_status launch_mma_tiles(f2i::LinearGroup& G, int tiles, bool wide, size_t smem, int tiles_max,
+                                cudaStream_t s) {
+  constexpr int W = f2i::kMmaWarpsWide;
+  if (wide) {
+    if (tiles == 1) return launch_mma_t<NPL, 1, W>(G, smem, tiles_max, s);
+    if constexpr (NPL * 2 <= 8)
+      if (tiles == 2) return launch_mma_t<NPL, 2, W>(G, smem, tiles_max, s);
+    if constexpr (NPL * 4 <= 8)
+      if (tiles == 4) return launch_mma_t<NPL, 4, W>(G, smem, tiles_max, s);
+    return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode: no 16-warp form for %d planes x %d token pairs", NPL, tiles);
+  }
+  constexpr int N = f2i::kMmaWarps;
+  return tiles == 1   ? launch_mma_t<NPL, 1, N>(G, smem, tiles_max, s)
+         : tiles == 2 ? launch_mma_t<NPL, 2, N>(G, smem, tiles_max, s)
+                      : launch_mma_t<NPL, 4, N>(G, smem, tiles_max, s);
 }
 
 // One launch of the sparse mma decode for up to 8 tokens of every problem in
@@ -164,28 +177,55 @@ fairy2i_status launch_mma_tiles(f2i::LinearGroup& G, int tiles, size_t smem, int
 // activations ([2M + 1][x_stride] bfloat16) and the per-warp partial outputs
 // of up to tiles_max row tiles.
 constexpr int kMmaTokens = 8;
+constexpr size_t kMmaWideSmem = 220 * 1024;  // one CTA per SM
+
+int mma_token_pairs(int M) { return M <= 2 ? 1 : M <= 4 ? 2 : 4; }
+
+// Shared-memory bytes of a launch with `warps` warps: fixed part (code rings
+// and staged activations) and partial outputs per row tile.
+void mma_smem(int warps, int T, int M, int64_t xstr_max, size_t& fixed, size_t& per_tile) {
+  const size_t ring = (size_t)warps * 2 * (2 * T) * 512;
+  const size_t xbytes = (((size_t)(2 * M + 1) * xstr_max * sizeof(uint16_t)) + 15) & ~(size_t)15;
+  fixed = ring + xbytes;
+  per_tile = (size_t)warps * mma_token_pairs(M) * 64 * sizeof(float2);
+}
+
+// Whether a launch runs as one 16-warp CTA per SM.  Measured on the LLaMA-2-7B
+// block at T = 2 against two 8-warp CTAs per SM: 24.6 against 26.65 us at M = 1,
+// 55.7 against 65.8 us at M = 4 (the whole-row-tile partition balances better
+// over 148 large CTAs than over 296 small ones).  Needs the 16-warp form
+// (2T planes x token pairs <= 8) and room for two row tiles of partial outputs.
+bool mma_wide(int T, int M, int64_t xstr_max) {
+  if (2 * T * mma_token_pairs(M) > 8) return false;
+  size_t fixed, per_tile;
+  mma_smem(f2i::kMmaWarpsWide, T, M, xstr_max, fixed, per_tile);
+  return fixed + 2 * per_tile <= kMmaWideSmem;
+}
 
 fairy2i_status run_mma(f2i::LinearGroup& G, int T, cudaStream_t s) {
-  const int tiles = G.M <= 2 ? 1 : G.M <= 4 ? 2 : 4;
-  const int npl = 2 * T;
+  const int tiles = mma_token_pairs(G.M);
   int64_t xstr_max = 0;
   for (int i = 0; i < G.count; ++i) xstr_max = std::max(xstr_max, f2i::x_stride(G.p[i].m));
-  const size_t ring = (size_t)f2i::kMmaWarps * 2 * npl * 512;
-  const size_t xbytes = (((size_t)(2 * G.M + 1) * xstr_max * sizeof(uint16_t)) + 15) & ~(size_t)15;
-  const size_t per_tile = (size_t)f2i::kMmaWarps * tiles * 64 * sizeof(float2);
-  // Two CTAs per SM when the buffers leave room for at least four row tiles
-  // of partial outputs; otherwise one CTA with up to 200 KB.
-  const size_t fixed = ring + xbytes;
-  const size_t limit = fixed + 4 * per_tile <= 110 * 1024 ? 110 * 1024 : 200 * 1024;
+  const bool wide = mma_wide(T, G.M, xstr_max);
+  size_t fixed, per_tile, limit;
+  if (wide) {
+    mma_smem(f2i::kMmaWarpsWide, T, G.M, xstr_max, fixed, per_tile);
+    limit = kMmaWideSmem;
+  } else {
+    // Two 8-warp CTAs per SM when the buffers leave room for at least four row
+    // tiles of partial outputs; otherwise one CTA with up to 200 KB.
+    mma_smem(f2i::kMmaWarps, T, G.M, xstr_max, fixed, per_tile);
+    limit = fixed + 4 * per_tile <= 110 * 1024 ? 110 * 1024 : 200 * 1024;
+  }
   if (fixed + per_tile > limit)
     return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode: buffers need %zu bytes of shared memory", fixed + per_tile);
   const int tiles_max = (int)std::min<size_t>(f2i::kMaxTilesPerCta, (limit - fixed) / per_tile);
   const size_t smem = fixed + (size_t)tiles_max * per_tile;
   switch (T) {
-    case 1: return launch_mma_tiles<2>(G, tiles, smem, tiles_max, s);
-    case 2: return launch_mma_tiles<4>(G, tiles, smem, tiles_max, s);
-    case 3: return launch_mma_tiles<6>(G, tiles, smem, tiles_max, s);
-    case 4: return launch_mma_tiles<8>(G, tiles, smem, tiles_max, s);
+    case 1: return launch_mma_tiles<2>(G, tiles, wide, smem, tiles_max, s);
+    case 2: return launch_mma_tiles<4>(G, tiles, wide, smem, tiles_max, s);
+    case 3: return launch_mma_tiles<6>(G, tiles, wide, smem, tiles_max, s);
+    case 4: return launch_mma_tiles<8>(G, tiles, wide, smem, tiles_max, s);
     default: return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode supports T <= 4 (got %d)", T);
   }
 }
@@ -204,16 +244,16 @@ int mma_chunk(const fairy2i_packed* qs, int count, int T) {
   return 1;
 }
 
-// Whether a sparse-mma launch of these layers with mc tokens keeps two CTAs
-// per SM (the same rule run_mma applies).
-bool mma_two_ctas(const fairy2i_packed* qs, int count, int T, int mc) {
+// Whether a sparse-mma launch of these layers with mc tokens keeps all 16
+// warps per SM: one 16-warp CTA, or two 8-warp CTAs (the rules run_mma
+// applies).  If not, the caller launches the layers per activation width.
+bool mma_full_sm(const fairy2i_packed* qs, int count, int T, int mc) {
   int64_t xstr_max = 0;
   for (int i = 0; i < count; ++i) xstr_max = std::max(xstr_max, f2i::x_stride(qs[i].m));
-  const int tiles = mc <= 2 ? 1 : mc <= 4 ? 2 : 4;
-  const size_t ring = (size_t)f2i::kMmaWarps * 2 * (2 * T) * 512;
-  const size_t xbytes = (((size_t)(2 * mc + 1) * xstr_max * sizeof(uint16_t)) + 15) & ~(size_t)15;
-  const size_t per_tile = (size_t)f2i::kMmaWarps * tiles * 64 * sizeof(float2);
-  return ring + xbytes + 4 * per_tile <= 110 * 1024;
+  if (mma_wide(T, mc, xstr_max)) return true;
+  size_t fixed, per_tile;
+  mma_smem(f2i::kMmaWarps, T, mc, xstr_max, fixed, per_tile);
+  return fixed + 4 * per_tile <= 110 * 1024;
 }
 
 fairy2i_status run_addsub(f2i::LinearGroup& G, cudaStream_t s) {
@@ -518,15 +558,15 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
   }
 
   // Launch order: when the widest layer's staged activations would leave the
-  // mma decode one CTA per SM, layers are launched in groups of equal
-  // activation width (the buffer of a launch is sized for its widest layer),
-  // keeping the caller's order inside a width.
+  // mma decode fewer than 16 warps per SM, layers are launched in groups of
+  // equal activation width (the buffer of a launch is sized for its widest
+  // layer), keeping the caller's order inside a width.
   std::vector<int> order(count);
   for (int i = 0; i < count; ++i) order[i] = i;
   bool split = false;
   if (a == FAIRY2I_ALGO_MMA) {
     const int mc = (int)std::min<int64_t>(M, mma_chunk(qs, count, T));
-    split = !mma_two_ctas(qs, count, T, mc);
+    split = !mma_full_sm(qs, count, T, mc);
     if (split)
       std::stable_sort(order.begin(), order.end(),
                        [&](int u, int v) { return f2i::x_stride(qs[u].m) < f2i::x_stride(qs[v].m); });

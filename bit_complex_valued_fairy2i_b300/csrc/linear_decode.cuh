@@ -216,12 +216,16 @@ __global__ void __launch_bounds__(kAddSubWarps * 32) linear_addsub_kernel(const 
 //   2-3 from lanes 2-3 (selector 1), which is how the flag words are laid out.
 // Partition: the host gives each problem of the launch a number of CTAs in
 // proportion to its bytes and each CTA a run of `tiles_per_cta` row tiles.
-// The 8 warps of a CTA split its (row tile, two-block chunk) items evenly,
-// stream the 2T code planes through a per-warp cp.async double buffer, fold
-// each row tile's share into per-warp partial outputs in shared memory, and
-// one fixed-order sum at the end writes y (bitwise reproducible).
+// A CTA has WARPS = 8 warps (two CTAs per SM) or 16 (one CTA per SM: twice the
+// row tiles per CTA, so the whole-tile granularity of the partition costs less
+// imbalance between SMs).  The warps of a CTA split its (row tile, two-block
+// chunk) items evenly, stream the 2T code planes through a per-warp cp.async
+// double buffer, fold each row tile's share into per-warp partial outputs in
+// shared memory, and one fixed-order sum at the end writes y (bitwise
+// reproducible for a given launch shape).
 // ---------------------------------------------------------------------------
-constexpr int kMmaWarps = 8;
+constexpr int kMmaWarps = 8;       // two CTAs per SM
+constexpr int kMmaWarpsWide = 16;  // one CTA per SM
 constexpr int kMaxTilesPerCta = 16;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -249,11 +253,11 @@ __device__ __forceinline__ void mma_sp_bf16(float (&d)[4], const uint32_t (&a)[4
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(e), "n"(SEL));
 }
 
-// Shared memory: per-warp rings [kMmaWarps][2][NPL][32 lanes] x 16 bytes, then
+// Shared memory: per-warp rings [WARPS][2][NPL][32 lanes] x 16 bytes, then
 // x staged as [2M + 1][x_stride(m)] bfloat16 (last row zero), then partials
-// [tiles][kMmaWarps][TILES][32 lanes][2 rows] float2.
-template <int NPL, int TILES>
-__global__ void __launch_bounds__(kMmaWarps * 32, (NPL * TILES <= 8) ? 2 : 1)
+// [tiles][WARPS][TILES][32 lanes][2 rows] float2.
+template <int NPL, int TILES, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, (WARPS == kMmaWarps && NPL * TILES <= 8) ? 2 : 1)
     linear_mma_kernel(const __grid_constant__ LinearGroup G) {
   extern __shared__ __align__(16) unsigned char msm[];
   const LinearProblem& P = G.p[find_problem(G)];
@@ -272,12 +276,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (NPL * TILES <= 8) ? 2 : 1)
 
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(msm);
   const uint32_t ring = sbase + (uint32_t)warp * 2u * kSlot;
-  uint16_t* xs = reinterpret_cast<uint16_t*>(msm + kMmaWarps * 2 * kSlot);
-  float2* red = reinterpret_cast<float2*>(msm + kMmaWarps * 2 * kSlot +
+  uint16_t* xs = reinterpret_cast<uint16_t*>(msm + WARPS * 2 * kSlot);
+  float2* red = reinterpret_cast<float2*>(msm + WARPS * 2 * kSlot +
                                           (((size_t)(2 * M + 1) * xstr * sizeof(uint16_t) + 15) & ~(size_t)15));
 
   const int items = niter * nch;
-  const int i0 = (int)((int64_t)items * warp / kMmaWarps), i1 = (int)((int64_t)items * (warp + 1) / kMmaWarps);
+  const int i0 = (int)((int64_t)items * warp / WARPS), i1 = (int)((int64_t)items * (warp + 1) / WARPS);
   const int fullc = (int)(KB >> 1);
   const uint32_t tile_row = (uint32_t)KB * kTileBytes;
   const uint8_t* plane0 = P.codes + rt_begin * (int64_t)tile_row;
@@ -302,8 +306,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (NPL * TILES <= 8) ? 2 : 1)
   };
   if (i0 < i1) issue(0);
 
-  stage_x(xs, P.x, M, m, 1, kMmaWarps * 32);
-  for (int z = tid; z < niter * kMmaWarps * TILES * 64; z += kMmaWarps * 32) red[z] = make_float2(0.0f, 0.0f);
+  stage_x(xs, P.x, M, m, 1, WARPS * 32);
+  for (int z = tid; z < niter * WARPS * TILES * 64; z += WARPS * 32) red[z] = make_float2(0.0f, 0.0f);
   __syncthreads();
 
   // B of this lane: token 2 tl + (g >> 2), part (g >> 1) & 1, upper half iff g odd
@@ -425,7 +429,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (NPL * TILES <= 8) ? 2 : 1)
       }
 #pragma unroll
       for (int tl = 0; tl < TILES; ++tl) {
-        float2* dst = red + ((size_t)((r * kMmaWarps + warp) * TILES + tl) * 32 + lane) * 2;
+        float2* dst = red + ((size_t)((r * WARPS + warp) * TILES + tl) * 32 + lane) * 2;
         dst[0] = make_float2(yr[tl][0], yi[tl][0]);
         dst[1] = make_float2(yr[tl][1], yi[tl][1]);
       }
@@ -434,7 +438,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (NPL * TILES <= 8) ? 2 : 1)
   __syncthreads();
 
   // fixed-order sum over the warps' partials (even lanes), then store
-  for (int e = tid; e < niter * TILES * 32; e += kMmaWarps * 32) {
+  for (int e = tid; e < niter * TILES * 32; e += WARPS * 32) {
     const int ln = e & 31;
     if (ln & 1) continue;
     const int tl = (e >> 5) % TILES;
@@ -445,8 +449,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32, (NPL * TILES <= 8) ? 2 : 1)
       const int64_t j = (rt_begin + r) * 16 + 8 * rr + (ln >> 2);
       float re = 0.0f, im = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kMmaWarps; ++w) {
-        const float2 v = red[((size_t)((r * kMmaWarps + w) * TILES + tl) * 32 + ln) * 2 + rr];
+      for (int w = 0; w < WARPS; ++w) {
+        const float2 v = red[((size_t)((r * WARPS + w) * TILES + tl) * 32 + ln) * 2 + rr];
         re += v.x;
         im += v.y;
       }

@@ -287,10 +287,10 @@ def test_linear_parity_wide_variants(T, M):
 
 
 def test_group_split_by_activation_width():
-    """At 4 tokens a 3000-column layer's staged activations would leave one CTA
-    per SM, so the group is launched per activation width; results must not
-    depend on it."""
-    shapes = [(40, 256), (13, 3000), (64, 64), (24, 3000)]
+    """At 4 tokens a 7200-column layer's staged activations fit neither one
+    16-warp CTA nor two 8-warp CTAs per SM, so the group is launched per
+    activation width; results must not depend on it."""
+    shapes = [(40, 256), (13, 7200), (64, 64), (24, 7200)]
     qs, xs, wants = [], [], []
     for i, (n, m) in enumerate(shapes):
         R = _R(n, m, 500 + i)
@@ -304,6 +304,28 @@ def test_group_split_by_activation_width():
     for q, x, y, want in zip(qs, xs, ys, wants):
         assert rel_l2(y.cpu().numpy(), want) <= REL_L2
         assert torch.equal(y, f2i.linear(q, x, algo="mma"))
+
+
+@pytest.mark.parametrize("T,M", [(4, 2), (2, 2), (3, 2)])
+def test_decode_both_launch_shapes(T, M):
+    """The same call takes one 16-warp CTA per SM when the buffers fit and two
+    (or one) 8-warp CTAs when a wide layer's staged activations do not: both
+    against the oracle, in one group and alone."""
+    wide_m = {4: 9000, 2: 15000, 3: 14000}[T]  # within the quantizer's m <= 16384
+    shapes = [(40, 512), (24, wide_m)]
+    qs, xs, wants = [], [], []
+    for i, (n, m) in enumerate(shapes):
+        R = _R(n, m, 700 + 10 * T + i)
+        _, _, q = _gpu_layer(R, T)
+        _, _, qU, qW = _oracle_layer(R, T)
+        x = _x(M, m, 800 + i)
+        qs.append(q)
+        xs.append(x.cuda())
+        wants.append(oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x)))
+    ys = f2i.linear_group(qs, xs, algo="mma")
+    for q, x, y, want in zip(qs, xs, ys, wants):
+        assert rel_l2(y.cpu().numpy(), want) <= REL_L2
+        assert rel_l2(f2i.linear(q, x, algo="mma").cpu().numpy(), want) <= REL_L2
 
 
 def test_bounded_wait_gives_up_and_reports_timeout():
