@@ -32,7 +32,7 @@ EXPORTED = (
     "fairy2i_codes_bytes", "fairy2i_scales_count", "fairy2i_convert", "fairy2i_quantize",
     "fairy2i_linear", "fairy2i_linear_ex", "fairy2i_linear_group", "fairy2i_unpack_codes",
     "fairy2i_sync_status", "fairy2i_last_error", "fairy2i_layout_version", "fairy2i_selftest_bounded_wait",
-    "fairy2i_convert_quantize", "fairy2i_linear_grad_x",
+    "fairy2i_convert_quantize", "fairy2i_linear_grad_x", "fairy2i_linear_grad_x_group",
 )
 
 
@@ -76,6 +76,7 @@ def load_library(path: str = LIB_PATH):
         "fairy2i_selftest_bounded_wait": (ctypes.c_int, [I32, P]),
         "fairy2i_convert_quantize": (ctypes.c_int, [P, I64, I64, I32, PD, P]),
         "fairy2i_linear_grad_x": (ctypes.c_int, [PD, P, I64, P, P]),
+        "fairy2i_linear_grad_x_group": (ctypes.c_int, [PD, ctypes.POINTER(P), ctypes.POINTER(P), I32, I64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -210,6 +211,24 @@ def linear_grad_x(q: Packed, gy: torch.Tensor, out: torch.Tensor | None = None, 
     _check(load_library().fairy2i_linear_grad_x(ctypes.byref(d), gy.data_ptr(), gy.shape[0], gx.data_ptr(),
                                                 _stream(stream)))
     return gx
+
+
+def linear_grad_x_group(qs, gys, outs=None, stream=None):
+    """Input gradients of several layers (same T and token count) in one launch."""
+    count = len(qs)
+    M = gys[0].shape[0]
+    if outs is None:
+        outs = [torch.empty((M, 2 * q.m), dtype=torch.float32, device=g.device) for q, g in zip(qs, gys)]
+    for q, g, gx in zip(qs, gys, outs):
+        _dev(g, "gy")
+        _dev(gx, "gx")
+        if g.dtype != torch.float32 or g.shape != (M, 2 * q.n) or gx.shape != (M, 2 * q.m):
+            raise ValueError("group members need matching gy [M, 2n] and gx [M, 2m] float32")
+    descs = (PackedDesc * count)(*[q.desc() for q in qs])
+    gp = (ctypes.c_void_p * count)(*[g.data_ptr() for g in gys])
+    xp = (ctypes.c_void_p * count)(*[gx.data_ptr() for gx in outs])
+    _check(load_library().fairy2i_linear_grad_x_group(descs, gp, xp, count, M, _stream(stream)))
+    return outs
 
 
 def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None):

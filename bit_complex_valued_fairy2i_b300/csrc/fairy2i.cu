@@ -690,27 +690,55 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed* qs, const void* const*
 }
 
 fairy2i_status fairy2i_linear_grad_x(const fairy2i_packed* q, const float* gy, int64_t M, float* gx, void* stream) {
-  fairy2i_status st = check_packed(q);
-  if (st != FAIRY2I_OK) return st;
+  return fairy2i_linear_grad_x_group(q, &gy, &gx, 1, M, stream);
+}
+
+fairy2i_status fairy2i_linear_grad_x_group(const fairy2i_packed* qs, const float* const* gys, float* const* gxs,
+                                           int32_t count, int64_t M, void* stream) {
+  if (count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "count=%d outside [1, 256]", count);
+  if (!qs || !gys || !gxs) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL array argument");
+  for (int i = 0; i < count; ++i) {
+    fairy2i_status st = check_packed(&qs[i]);
+    if (st != FAIRY2I_OK) return st;
+    if (qs[i].T != qs[0].T) return fail(FAIRY2I_ERR_SHAPE, "all layers of a group need the same T");
+  }
   if (M < 0) return fail(FAIRY2I_ERR_SHAPE, "M=%lld is negative", (long long)M);
   if (M == 0) return ok();
-  if (!gy || !gx) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL gradient pointer");
-  if (!aligned(gy, 16) || !aligned(gx, 16)) return fail(FAIRY2I_ERR_INVALID_ARG, "gy and gx must be 16-byte aligned");
+  for (int i = 0; i < count; ++i) {
+    if (!gys[i] || !gxs[i]) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL gradient pointer (layer %d)", i);
+    if (!aligned(gys[i], 16) || !aligned(gxs[i], 16))
+      return fail(FAIRY2I_ERR_INVALID_ARG, "gy and gx must be 16-byte aligned (layer %d)", i);
+  }
   const int64_t pairs = (M + 1) / 2;  // tokens go two per CTA (one when M = 1)
   if (pairs * f2i::kGxCluster > 65535) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
-  f2i::GradParams P;
-  P.codes = static_cast<const uint8_t*>(q->codes);
-  P.scales = q->scales;
-  P.g = gy;
-  P.gx = gx;
-  P.n = q->n;
-  P.m = q->m;
-  P.T = q->T;
-  P.M = (int32_t)M;
-  const dim3 grid((unsigned)f2i::col_blocks(q->m), (unsigned)(pairs * f2i::kGxCluster));
-  if (M == 1) f2i::linear_grad_x_kernel<1><<<grid, f2i::kGxWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(P);
-  else f2i::linear_grad_x_kernel<2><<<grid, f2i::kGxWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(P);
-  return check_launch("input-gradient launch");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int b0 = 0; b0 < count; b0 += f2i::kGxMaxGroup) {
+    const int cnt = std::min(f2i::kGxMaxGroup, count - b0);
+    f2i::GradGroup G;
+    memset(&G, 0, sizeof(G));
+    G.count = cnt;
+    G.T = qs[0].T;
+    G.M = (int32_t)M;
+    int64_t blocks = 0;  // column blocks of the launch: one grid column each
+    for (int i = 0; i < cnt; ++i) {
+      const fairy2i_packed& q = qs[b0 + i];
+      f2i::GradProblem& P = G.p[i];
+      P.codes = static_cast<const uint8_t*>(q.codes);
+      P.scales = q.scales;
+      P.g = gys[b0 + i];
+      P.gx = gxs[b0 + i];
+      P.n = q.n;
+      P.m = q.m;
+      P.kb_begin = (int32_t)blocks;
+      blocks += f2i::col_blocks(q.m);
+    }
+    const dim3 grid((unsigned)blocks, (unsigned)(pairs * f2i::kGxCluster));
+    if (M == 1) f2i::linear_grad_x_kernel<1><<<grid, f2i::kGxWarps * 32, 0, s>>>(G);
+    else f2i::linear_grad_x_kernel<2><<<grid, f2i::kGxWarps * 32, 0, s>>>(G);
+    fairy2i_status st = check_launch("input-gradient launch");
+    if (st != FAIRY2I_OK) return st;
+  }
+  return ok();
 }
 
 fairy2i_status fairy2i_unpack_codes(const fairy2i_packed* q, uint8_t* codes_out, void* stream) {

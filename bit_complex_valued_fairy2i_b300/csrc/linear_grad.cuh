@@ -11,8 +11,9 @@
 //   W:  h_re = s_re conj(g_j),    h_im = s_im (i conj(g_j))
 // and every code adds or subtracts the h of its axis into its column.
 //
-// Work split: one CTA per (64-column block, eighth of the row tiles, token
-// pair).  A warp walks row tiles; lane (g, q) owns columns 16 s + 8 h + 2 q + e
+// Work split: one CTA per (layer, 64-column block, eighth of the row tiles,
+// token pair); one launch may carry several layers (a decoder block's
+// projections), each with its own codes, gradients and outputs.  A warp walks row tiles; lane (g, q) owns columns 16 s + 8 h + 2 q + e
 // of rows g and g + 8 (its sign word; the axis flags of its columns sit in the
 // flag words of the four lanes of its quad, exchanged by shuffles).  Partial
 // sums are reduced over the 8 lanes of a column, then over the warps in shared
@@ -31,28 +32,40 @@ namespace f2i {
 constexpr int kGxWarps = 8;
 constexpr int kGxCluster = 8;
 
-struct GradParams {
+constexpr int kGxMaxGroup = 32;
+
+struct GradProblem {
   const uint8_t* codes;
   const float* scales;
   const float* g;  // [M][2n]
   float* gx;       // [M][2m]
   int64_t n, m;
-  int32_t T, M;
+  int32_t kb_begin;  // first blockIdx.x of this layer (its column blocks follow)
+  int32_t pad_;
+};
+
+struct GradGroup {
+  int32_t count, T, M, pad_;
+  GradProblem p[kGxMaxGroup];
 };
 
 // TOK = tokens per CTA (1 or 2; a launch with more tokens uses TOK = 2 over token pairs).
 template <int TOK>
 __global__ void __cluster_dims__(1, kGxCluster, 1) __launch_bounds__(kGxWarps * 32)
-    linear_grad_x_kernel(const GradParams P) {
+    linear_grad_x_kernel(const __grid_constant__ GradGroup G) {
   namespace cg = cooperative_groups;
   __shared__ float red[kGxWarps][4][16][2][2];  // [warp][q][column][token][re, im]
   __shared__ float cta_sum[4][16][2][2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
+  int pi = 0;
+  for (int i = 1; i < G.count; ++i)
+    if ((int)blockIdx.x >= G.p[i].kb_begin) pi = i;
+  const GradProblem& P = G.p[pi];
   const int64_t n = P.n, m = P.m;
-  const int T = P.T, M = P.M;
+  const int T = G.T, M = G.M;
   const int64_t KB = col_blocks(m), RT = row_tiles(n), pbytes = plane_bytes(n, m);
-  const int kb = blockIdx.x;
+  const int kb = (int)blockIdx.x - P.kb_begin;
   const int rank = blockIdx.y % kGxCluster, tp = blockIdx.y / kGxCluster;
   const int t0 = TOK * tp;
   const bool has_t1 = TOK == 2 && t0 + 1 < M;

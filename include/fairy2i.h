@@ -176,6 +176,16 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
 fairy2i_status fairy2i_linear_grad_x(const fairy2i_packed *q, const float *gy, int64_t M, float *gx,
                                      void *stream);
 
+/* The input gradients of several independent layers (same T and token count M,
+ * each with its own gy and gx), e.g. the seven projections of a decoder block,
+ * in one launch per 32 layers.  qs, gys, gxs are HOST arrays of `count`
+ * entries (1..256); the per-layer arguments mean what they mean for
+ * fairy2i_linear_grad_x, and each layer's gx equals that call's bit for bit.
+ * Errors: as fairy2i_linear_grad_x; INVALID_ARG also for a bad count or a NULL
+ * array, SHAPE for mixed T. */
+fairy2i_status fairy2i_linear_grad_x_group(const fairy2i_packed *qs, const float *const *gys,
+                                           float *const *gxs, int32_t count, int64_t M, void *stream);
+
 /* Canonical view of the codes: device uint8 [2 (U, W)][T][n][m] with values
  * 0 = +1, 1 = -1, 2 = +i, 3 = -i. */
 fairy2i_status fairy2i_unpack_codes(const fairy2i_packed *q, uint8_t *codes_out, void *stream);

@@ -129,6 +129,20 @@ def test_linear_grad_x_rejects_bad_arguments(lib):
     assert lib.fairy2i_linear_grad_x(ctypes.byref(d), p, 20000, p, None) == 4
 
 
+def test_linear_grad_x_group_rejects_bad_arguments(lib):
+    d = _desc()
+    descs = (f2i.PackedDesc * 2)(d, _desc(T=3))
+    arr = (ctypes.c_void_p * 2)(256, 512)
+    assert lib.fairy2i_linear_grad_x_group(descs, arr, arr, 0, 1, None) == 1  # count 0
+    assert lib.fairy2i_linear_grad_x_group(descs, arr, arr, 300, 1, None) == 1  # count above 256
+    assert lib.fairy2i_linear_grad_x_group(descs, None, arr, 1, 1, None) == 1  # NULL array
+    assert lib.fairy2i_linear_grad_x_group(descs, arr, arr, 2, 1, None) == 2  # mixed T
+    assert lib.fairy2i_linear_grad_x_group(descs, arr, arr, 1, -1, None) == 2  # negative M
+    assert lib.fairy2i_linear_grad_x_group(descs, arr, arr, 1, 0, None) == 0  # no tokens: nothing launched
+    nulls = (ctypes.c_void_p * 1)(None)
+    assert lib.fairy2i_linear_grad_x_group(descs, nulls, arr, 1, 1, None) == 1  # NULL gradient
+
+
 def test_convert_quantize_rejects_bad_arguments(lib):
     p = ctypes.c_void_p(256)
     d = _desc(n=2, m=2, T=1)

@@ -94,3 +94,22 @@ def test_grad_x_deterministic_and_zero_tokens():
     g = _g(3, 300, 7).cuda()
     assert torch.equal(f2i.linear_grad_x(q, g), f2i.linear_grad_x(q, g))
     assert f2i.linear_grad_x(q, torch.zeros((0, 600), device="cuda")).shape == (0, 1400)
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_grad_x_group_equals_single_launches(M):
+    """One launch over layers of mixed shapes (partial row tiles, an odd column
+    block count, a ragged last block) gives each layer's single-launch result
+    bit for bit, and the oracle's."""
+    shapes = [(37, 130), (256, 256), (13, 2049), (70, 300), (8, 64)]
+    qs, gs, wants = [], [], []
+    for i, (n, m) in enumerate(shapes):
+        q, qU, qW = _layer(n, m, 2, 900 + i)
+        g = _g(M, n, 950 + i)
+        qs.append(q)
+        gs.append(g.cuda())
+        wants.append(oracle.linear_grad_x_mulfree(qU, qW, g.numpy()))
+    gxs = f2i.linear_grad_x_group(qs, gs)
+    for q, g, gx, want in zip(qs, gs, gxs, wants):
+        assert torch.equal(gx, f2i.linear_grad_x(q, g))
+        assert rel_l2(gx.cpu().numpy(), want) <= TIGHT
