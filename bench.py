@@ -459,7 +459,7 @@ def run_grad_only(args, world, rank, local):
         print(json.dumps({"grad_x": {
             "workload": f"input gradient of llama2-7b projections, {blocks} blocks x 7, M=1, T={T_STAGES}, "
                         "one grouped launch per block",
-            "kernel": "linear_grad_x_kernel (CUDA cores, 8-CTA clusters)",
+            "kernel": "linear_grad_x_kernel (CUDA cores, 4-CTA clusters)",
             "ms_per_step": ms, "GBps": nbytes / (ms * 1e-3) / 1e9, "bytes_per_step": nbytes,
             "us_per_block": ms * 1e3 / blocks, "steps": steps,
             "one_launch_per_projection": {"us_per_block": ms_proj * 1e3 / blocks,

@@ -710,7 +710,7 @@ fairy2i_status fairy2i_linear_grad_x_group(const fairy2i_packed* qs, const float
       return fail(FAIRY2I_ERR_INVALID_ARG, "gy and gx must be 16-byte aligned (layer %d)", i);
   }
   const int64_t pairs = (M + 1) / 2;  // tokens go two per CTA (one when M = 1)
-  if (pairs * f2i::kGxCluster > 65535) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
+  if (M > f2i::kGxMaxTokens) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld above %d", (long long)M, f2i::kGxMaxTokens);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int b0 = 0; b0 < count; b0 += f2i::kGxMaxGroup) {
     const int cnt = std::min(f2i::kGxMaxGroup, count - b0);

@@ -11,13 +11,14 @@
 //   W:  h_re = s_re conj(g_j),    h_im = s_im (i conj(g_j))
 // and every code adds or subtracts the h of its axis into its column.
 //
-// Work split: one CTA per (layer, 64-column block, eighth of the row tiles,
+// Work split: one CTA per (layer, 64-column block, quarter of the row tiles,
 // token pair); one launch may carry several layers (a decoder block's
-// projections), each with its own codes, gradients and outputs.  A warp walks row tiles; lane (g, q) owns columns 16 s + 8 h + 2 q + e
-// of rows g and g + 8 (its sign word; the axis flags of its columns sit in the
-// flag words of the four lanes of its quad, exchanged by shuffles).  Partial
+// projections), each with its own codes, gradients and outputs.  A warp walks
+// row tiles; lane (g, q) owns columns 16 s + 8 h + 2 q + e of rows g and g + 8
+// (its sign word; the axis flags of its columns sit in the flag words of the
+// four lanes of its quad, exchanged by shuffles).  Partial
 // sums are reduced over the 8 lanes of a column, then over the warps in shared
-// memory, then over the 8 CTAs of a thread-block cluster by rank 0 through
+// memory, then over the 4 CTAs of a thread-block cluster by rank 0 through
 // distributed shared memory, always in a fixed order: the result is
 // deterministic and no global scratch is used.
 #pragma once
@@ -30,7 +31,8 @@
 namespace f2i {
 
 constexpr int kGxWarps = 8;
-constexpr int kGxCluster = 8;
+constexpr int kGxCluster = 4;  // CTAs per column block (row split); 4 measured faster than 2 or 8
+constexpr int kGxMaxTokens = 16382;
 
 constexpr int kGxMaxGroup = 32;
 
