@@ -306,8 +306,24 @@ __global__ void __launch_bounds__(WARPS * 32, (WARPS == kMmaWarps && NPL * TILES
   };
   if (i0 < i1) issue(0);
 
-  stage_x(xs, P.x, M, m, 1, WARPS * 32);
+  // Staged activations: with 16-byte rows every piece is an asynchronous copy
+  // (zero-filled past m and in the extra row), so all of a thread's pieces are
+  // in flight at once instead of one load-store round trip each.
+  if ((m & 7) == 0 && (reinterpret_cast<uintptr_t>(P.x) & 15) == 0) {
+    const int64_t rows = (int64_t)M * 2, per_row = xstr >> 3;
+    for (int64_t idx = tid; idx < (rows + 1) * per_row; idx += WARPS * 32) {
+      const int64_t row = idx / per_row, k8 = (idx - row * per_row) << 3;
+      const bool in = row < rows && k8 < m;
+      const uint16_t* src = in ? P.x + (row >> 1) * 2 * m + (row & 1) * m + k8 : P.x;
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(xs + row * xstr + k8);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(in ? 16 : 0) : "memory");
+    }
+    cp_commit();
+  } else {
+    stage_x(xs, P.x, M, m, 1, WARPS * 32);
+  }
   for (int z = tid; z < niter * WARPS * TILES * 64; z += WARPS * 32) red[z] = make_float2(0.0f, 0.0f);
+  cp_wait<0>();  // the staged activations (and the first code item)
   __syncthreads();
 
   // B of this lane: token 2 tl + (g >> 2), part (g >> 1) & 1, upper half iff g odd
