@@ -45,8 +45,11 @@ BLOCKS = inputs.LLAMA2_7B_BLOCKS
 # of this workload, from an ncu capture of linear_mma_kernel<4,1,16> (one 16-warp
 # CTA per SM); must be re-measured whenever that kernel changes.
 DECODE_TRAFFIC_BYTES = 51_399_680
-# decode kernel and arithmetic per --decode-algo (auto = the 2:4-sparse mma.sync decode at M = 1)
+# decode kernel and arithmetic per --decode-algo (auto = the 2:4-sparse mma.sync decode at M = 1 on
+# layout 2; lut = the table-lookup decode on layout 3)
 DECODE_KERNELS = {
+    "lut": ("linear_lut_kernel<2,1> (table lookup, layout 3)",
+            "fp16 table entries (fp32 sums of 8 bf16 activations rounded once), fp32 accumulate"),
     "auto": ("linear_mma_kernel<4,1,16> (2:4-sparse mma.sync)",
              "bf16 (2:4-sparse mma.sync: code signs as bf16 +-2, bf16 x), fp32 accumulate"),
     "mma": ("linear_mma_kernel<4,1,16> (2:4-sparse mma.sync)",
@@ -231,7 +234,11 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def build_stack(f2i, blocks: int, dev, T: int = T_STAGES):
+def decode_layout(algo: str) -> int:
+    return 3 if algo == "lut" else 2
+
+
+def build_stack(f2i, blocks: int, dev, T: int = T_STAGES, layout: int = 2):
     """Convert + quantize the stack on the GPU; times both (events)."""
     stack = []
     conv_ms = quant_ms = 0.0
@@ -244,7 +251,7 @@ def build_stack(f2i, blocks: int, dev, T: int = T_STAGES):
             e[0].record()
             U, W = f2i.convert(R)
             e[1].record()
-            q = f2i.quantize(U, W, T, check=False)
+            q = f2i.quantize(U, W, T, check=False, layout=layout)
             e[2].record()
             e[2].synchronize()
             conv_ms += e[0].elapsed_time(e[1])
@@ -499,7 +506,8 @@ def run_ours(args, world, rank, local):
     peaks = _peaks()
 
     blocks = args.blocks
-    stack, offline = build_stack(f2i, blocks, dev)
+    algo = args.decode_algo
+    stack, offline = build_stack(f2i, blocks, dev, layout=decode_layout(algo))
     bytes_per_block = sum(q.nbytes for q in stack[0])
     bytes_per_step = sum(q.nbytes for layers in stack for q in layers)
 
@@ -513,8 +521,6 @@ def run_ours(args, world, rank, local):
     yv = list(torch.split(y_all, y_sizes))
     xs = [[xv[7 * b + i].view(1, -1) for i in range(7)] for b in range(blocks)]
     ys = [[yv[7 * b + i].view(1, -1) for i in range(7)] for b in range(blocks)]
-
-    algo = args.decode_algo
 
     def step():
         for b in range(blocks):
@@ -631,8 +637,9 @@ def main():
     ap.add_argument("--mode", choices=["decode", "prefill", "sweep", "stack", "grad"], default="decode",
                     help="prefill: time only the prefill leg (for profiling)")
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--decode-algo", choices=sorted(DECODE_KERNELS), default="auto",
-                    help="decode kernel of the default mode (auto = the library's choice)")
+    ap.add_argument("--decode-algo", choices=sorted(DECODE_KERNELS), default="lut",
+                    help="decode kernel of the default mode (lut = the table-lookup decode on layout 3; "
+                         "auto = the library's choice on layout 2)")
     ap.add_argument("--prefill-tokens", type=int, default=2048)
     ap.add_argument("--blocks", type=int, default=BLOCKS,
                     help="decoder blocks in the stack (32 = the full model; fewer only for profiling)")

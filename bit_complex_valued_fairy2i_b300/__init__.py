@@ -9,6 +9,9 @@ missing, calls raise.
     U, W = convert(R)                 # R: cuda float32 [2n, 2m]
     q = quantize(U, W, T=2)           # packed 2-bit codes + per-row scales
     y = linear(q, x)                  # x: cuda bfloat16 [M, 2m] -> y float32 [M, 2n]
+
+    q3 = quantize(U, W, T=2, layout=3)   # the table-lookup decode layout
+    y = linear(q3, x)                    # table-lookup decode; workspace kept per (device, stream)
 """
 from __future__ import annotations
 
@@ -24,8 +27,9 @@ LIB_PATH = os.path.join(_HERE, "libfairy2i.so")
 OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "SHAPE", 3: "NONFINITE", 4: "UNSUPPORTED", 5: "CUDA",
                 6: "TIMEOUT"}
-ALGO = {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4}
+ALGO = {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4, "lut": 5}
 LAYOUT_VERSION = 2
+LAYOUT_LUT = 3
 
 # every extern "C" symbol declared in include/fairy2i.h
 EXPORTED = (
@@ -33,6 +37,7 @@ EXPORTED = (
     "fairy2i_linear", "fairy2i_linear_ex", "fairy2i_linear_group", "fairy2i_unpack_codes",
     "fairy2i_sync_status", "fairy2i_last_error", "fairy2i_layout_version", "fairy2i_selftest_bounded_wait",
     "fairy2i_convert_quantize", "fairy2i_linear_grad_x", "fairy2i_linear_grad_x_group",
+    "fairy2i_codes_bytes_layout", "fairy2i_linear_ws", "fairy2i_linear_group_ws", "fairy2i_linear_workspace_bytes",
 )
 
 
@@ -77,6 +82,11 @@ def load_library(path: str = LIB_PATH):
         "fairy2i_convert_quantize": (ctypes.c_int, [P, I64, I64, I32, PD, P]),
         "fairy2i_linear_grad_x": (ctypes.c_int, [PD, P, I64, P, P]),
         "fairy2i_linear_grad_x_group": (ctypes.c_int, [PD, ctypes.POINTER(P), ctypes.POINTER(P), I32, I64, P]),
+        "fairy2i_codes_bytes_layout": (SZ, [I64, I64, I32, I32]),
+        "fairy2i_linear_ws": (ctypes.c_int, [PD, P, I64, P, ctypes.c_int, P, SZ, P]),
+        "fairy2i_linear_group_ws": (ctypes.c_int, [PD, ctypes.POINTER(P), ctypes.POINTER(P), I32, I64, ctypes.c_int,
+                                                   P, SZ, P]),
+        "fairy2i_linear_workspace_bytes": (SZ, [PD, I32, I64]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -105,8 +115,8 @@ def _dev(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be contiguous")
 
 
-def codes_bytes(n: int, m: int, T: int) -> int:
-    return int(load_library().fairy2i_codes_bytes(n, m, T))
+def codes_bytes(n: int, m: int, T: int, layout: int = LAYOUT_VERSION) -> int:
+    return int(load_library().fairy2i_codes_bytes_layout(n, m, T, layout))
 
 
 def scales_count(n: int, T: int) -> int:
@@ -115,15 +125,17 @@ def scales_count(n: int, T: int) -> int:
 
 @dataclass
 class Packed:
-    """Packed quantized layer: device codes (uint8) and scales [2][T][2][n]."""
+    """Packed quantized layer: device codes (uint8) and scales [2][T][2][n].
+    ``layout`` is the code layout version: 2 (every kernel) or 3 (the table-lookup decode)."""
     n: int
     m: int
     T: int
     codes: torch.Tensor
     scales: torch.Tensor
+    layout: int = LAYOUT_VERSION
 
     def desc(self) -> PackedDesc:
-        return PackedDesc(LAYOUT_VERSION, self.T, self.n, self.m, self.codes.data_ptr(), self.scales.data_ptr())
+        return PackedDesc(self.layout, self.T, self.n, self.m, self.codes.data_ptr(), self.scales.data_ptr())
 
     @property
     def nbytes(self) -> int:
@@ -131,14 +143,14 @@ class Packed:
         return self.codes.numel() + 4 * self.scales.numel()
 
     @staticmethod
-    def empty(n: int, m: int, T: int, device="cuda") -> "Packed":
-        nb = codes_bytes(n, m, T)
+    def empty(n: int, m: int, T: int, device="cuda", layout: int = LAYOUT_VERSION) -> "Packed":
+        nb = codes_bytes(n, m, T, layout)
         ns = scales_count(n, T)
         if nb == 0 or ns == 0:
-            raise Fairy2iError(4, f"unsupported shape n={n} m={m} T={T}")
+            raise Fairy2iError(4, f"unsupported shape n={n} m={m} T={T} layout={layout}")
         codes = torch.empty(nb, dtype=torch.uint8, device=device)
         scales = torch.empty(ns, dtype=torch.float32, device=device).view(2, T, 2, n)
-        return Packed(n, m, T, codes, scales)
+        return Packed(n, m, T, codes, scales, layout)
 
 
 def convert(R: torch.Tensor, stream=None):
@@ -155,15 +167,16 @@ def convert(R: torch.Tensor, stream=None):
 
 
 def quantize(U: torch.Tensor, W: torch.Tensor, T: int = 2, out: Packed | None = None, stream=None,
-             check: bool = True) -> Packed:
-    """Phase-aware recursive residual quantization of U and W (complex64 [n, m]).
+             check: bool = True, layout: int = LAYOUT_VERSION) -> Packed:
+    """Phase-aware recursive residual quantization of U and W (complex64 [n, m]) into
+    code layout ``layout`` (ignored when ``out`` is given: its own layout is written).
     With ``check`` the stream is synchronized and a non-finite weight raises."""
     _dev(U, "U")
     _dev(W, "W")
     if U.dtype != torch.complex64 or W.dtype != torch.complex64 or U.shape != W.shape or U.dim() != 2:
         raise ValueError("U and W must be complex64 tensors of the same 2-D shape")
     n, m = U.shape
-    q = out if out is not None else Packed.empty(n, m, T, U.device)
+    q = out if out is not None else Packed.empty(n, m, T, U.device, layout)
     d = q.desc()
     _check(load_library().fairy2i_quantize(U.data_ptr(), W.data_ptr(), n, m, T, ctypes.byref(d), _stream(stream)))
     if check:
@@ -172,14 +185,14 @@ def quantize(U: torch.Tensor, W: torch.Tensor, T: int = 2, out: Packed | None = 
 
 
 def convert_quantize(R: torch.Tensor, T: int = 2, out: Packed | None = None, stream=None,
-                     check: bool = True) -> Packed:
+                     check: bool = True, layout: int = LAYOUT_VERSION) -> Packed:
     """Real [2n, 2m] float32 weight -> packed layer, in one pass (the same codes and
     scales as quantize(*convert(R), T))."""
     _dev(R, "R")
     if R.dtype != torch.float32 or R.dim() != 2:
         raise ValueError("R must be a 2-D float32 tensor")
     n, m = R.shape[0] // 2, R.shape[1] // 2
-    q = out if out is not None else Packed.empty(n, m, T, R.device)
+    q = out if out is not None else Packed.empty(n, m, T, R.device, layout)
     d = q.desc()
     _check(load_library().fairy2i_convert_quantize(R.data_ptr(), R.shape[0], R.shape[1], T, ctypes.byref(d),
                                                    _stream(stream)))
@@ -188,14 +201,44 @@ def convert_quantize(R: torch.Tensor, T: int = 2, out: Packed | None = None, str
     return q
 
 
+_workspaces: dict = {}
+
+
+def workspace(qs, M: int, device, stream=None) -> torch.Tensor | None:
+    """The zeroed device workspace of the table-lookup decode for these layers and token
+    count, kept per (device, stream) and grown when a call needs more (None if none is
+    needed).  Calls on one stream run in order, so they can share it."""
+    count = len(qs)
+    descs = (PackedDesc * count)(*[q.desc() for q in qs])
+    need = int(load_library().fairy2i_linear_workspace_bytes(descs, count, M))
+    if need == 0:
+        return None
+    dev = torch.device(device)
+    key = (dev.index if dev.index is not None else torch.cuda.current_device(), _stream(stream))
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
+    return ws
+
+
 def linear(q: Packed, x: torch.Tensor, algo: str = "auto", out: torch.Tensor | None = None,
-           stream=None) -> torch.Tensor:
-    """y = U^ x + W^ conj(x) for x bfloat16 [M, 2m] ([Re x | Im x] rows) -> y float32 [M, 2n]."""
+           stream=None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    """y = U^ x + W^ conj(x) for x bfloat16 [M, 2m] ([Re x | Im x] rows) -> y float32 [M, 2n].
+    A layout-3 layer goes through the table-lookup decode with workspace ``ws`` (by default
+    the one kept for this device and stream)."""
     _dev(x, "x")
     if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != 2 * q.m:
         raise ValueError(f"x must be bfloat16 [M, {2 * q.m}]")
     y = out if out is not None else torch.empty((x.shape[0], 2 * q.n), dtype=torch.float32, device=x.device)
     d = q.desc()
+    if q.layout == LAYOUT_LUT:
+        if ws is None:
+            ws = workspace([q], x.shape[0], x.device, stream)
+        wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
+        _check(load_library().fairy2i_linear_ws(ctypes.byref(d), x.data_ptr(), x.shape[0], y.data_ptr(), ALGO[algo],
+                                                wp, wn, _stream(stream)))
+        return y
     _check(load_library().fairy2i_linear_ex(ctypes.byref(d), x.data_ptr(), x.shape[0], y.data_ptr(), ALGO[algo],
                                             _stream(stream)))
     return y
@@ -231,8 +274,9 @@ def linear_grad_x_group(qs, gys, outs=None, stream=None):
     return outs
 
 
-def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None):
-    """Evaluate several layers (same T and token count) in one launch."""
+def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None, ws: torch.Tensor | None = None):
+    """Evaluate several layers (same T, layout and token count) in one launch; layout-3 layers
+    use workspace ``ws`` (by default the one kept for this device and stream)."""
     count = len(qs)
     M = xs[0].shape[0]
     if ys is None:
@@ -245,11 +289,17 @@ def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None):
         _dev(y, "y")
         if x.dtype != torch.bfloat16 or x.shape != (M, 2 * q.m) or y.shape != (M, 2 * q.n):
             raise ValueError("group members need matching x [M, 2m] bfloat16 and y [M, 2n] float32")
+    if qs[0].layout == LAYOUT_LUT:
+        if ws is None:
+            ws = workspace(qs, M, xs[0].device, stream)
+        wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
+        _check(load_library().fairy2i_linear_group_ws(descs, xp, yp, count, M, ALGO[algo], wp, wn, _stream(stream)))
+        return ys
     _check(load_library().fairy2i_linear_group(descs, xp, yp, count, M, ALGO[algo], _stream(stream)))
     return ys
 
 
-def unpack_codes(q: Packed, stream=None) -> torch.Tensor:
+def unpack_codes(q: Packed, stream=None) -> torch.Tensor:  # either layout
     """Canonical codes uint8 [2, T, n, m] (0=+1, 1=-1, 2=+i, 3=-i) on the device."""
     out = torch.empty((2, q.T, q.n, q.m), dtype=torch.uint8, device=q.codes.device)
     d = q.desc()

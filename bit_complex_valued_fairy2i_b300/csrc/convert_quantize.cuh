@@ -175,12 +175,32 @@ __device__ __forceinline__ void block_sum_ll2_u2(long long& a, long long& b, uin
   __syncthreads();  // the buffers are reused by the next reduction
 }
 
-// FUSED = false: weights from complex U, W [n][m] (grid (n, 2): row, matrix).
+// Writes the zero 16-byte chunks of a padding row (j >= n) of layout 3: the
+// last row tile's rows past n must read as zero codes.
+__device__ __forceinline__ void l3_zero_row(uint8_t* codes, int64_t n, int64_t m, int T, int64_t j, int X) {
+  const int64_t tau = j >> 5;
+  const int r = (int)(j & 31);
+  const int64_t W3 = l3_windows(m);
+  for (int64_t idx = threadIdx.x; idx < W3 * 4 * T; idx += blockDim.x) {
+    const int64_t win = idx / (4 * T);
+    const int rem = (int)(idx - win * 4 * T);
+    const int t = rem >> 2, jj = rem & 3;
+    if (jj >= l3_slots(m, win)) continue;
+    *reinterpret_cast<uint4*>(codes + l3_offset(n, m, T, win, tau, X * T + t) + jj * kL3SlotBytes + r * 16) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// FUSED = false: weights from complex U, W [n][m] (grid (rows, 2): row, matrix).
 // FUSED = true:  weights computed from the real R [2n][2m] with the same
 // float32 operations as the conversion kernel, so the codes and scales equal
-// those of convert-then-quantize bit for bit (grid (2, n): the two matrices
+// those of convert-then-quantize bit for bit (grid (2, rows): the two matrices
 // of a row are neighbouring CTAs and share the R rows through L2).
-template <int WPT, bool FUSED>
+// LAYOUT 2 or 3 selects the packed code layout written (the arithmetic is the
+// same; only the column order of a thread's words and the final stores
+// differ).  For layout 3 the grid has a row for every row of the last tile,
+// and rows past n write zero chunks.
+template <int WPT, bool FUSED, int LAYOUT>
 __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
     const float2* __restrict__ U, const float2* __restrict__ W, const float* __restrict__ R, int64_t n, int64_t m,
     int T, uint8_t* __restrict__ codes, float* __restrict__ scales) {
@@ -192,14 +212,21 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
   const int tid = threadIdx.x;
   const int X = FUSED ? blockIdx.x : blockIdx.y;
   const int64_t j = FUSED ? blockIdx.y : blockIdx.x;
+  if (LAYOUT == 3 && j >= n) {  // padding row of the last tile (block-uniform)
+    l3_zero_row(codes, n, m, T, j, X);
+    return;
+  }
   const int64_t KB = col_blocks(m);
   const float2* src = FUSED ? nullptr : (X == 0 ? U : W) + j * m;
   const float* top = FUSED ? R + j * 2 * m : nullptr;        // R11 | R12 row
   const float* bot = FUSED ? R + (n + j) * 2 * m : nullptr;  // R21 | R22 row
 
-  // column of weight e = 16 u + c of this thread (word u of WPT)
+  // column of weight e = 16 u + c of this thread (word u of WPT): layout 2
+  // orders a word's columns as one sign word of the mma fragment, layout 3
+  // takes 16 consecutive columns (two groups of 8)
   auto col_of = [&](int e) -> int64_t {
     const int64_t w = (int64_t)tid * WPT + (e >> 4);
+    if (LAYOUT == 3) return w * 16 + (e & 15);
     return (w >> 2) * 64 + word_col(e & 15, (int)(w & 3));
   };
   float re[E], im[E];
@@ -214,8 +241,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
     float2 v = make_float2(0.0f, 0.0f);
     if ((w >> 2) < KB && k < m) {
       if (FUSED) {
-        const float r11 = __ldcs(top + k), r12 = __ldcs(top + m + k);
-        const float r21 = __ldcs(bot + k), r22 = __ldcs(bot + m + k);
+        // default caching: the row's other matrix (the neighbouring CTA) reads the same R
+        const float r11 = __ldg(top + k), r12 = __ldg(top + m + k);
+        const float r21 = __ldg(bot + k), r22 = __ldg(bot + m + k);
         v = X == 0 ? make_float2(half_sum(r11, r22), half_diff(r21, r12))   // U
                    : make_float2(half_diff(r11, r22), half_sum(r12, r21));  // W
       } else {
@@ -312,6 +340,40 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
       const float upd = __fsub_rn(isr ? re[e] : im[e], d);
       re[e] = isr ? upd : re[e];
       im[e] = isr ? im[e] : upd;
+    }
+    if (LAYOUT == 3) {
+      // layout 3: the (4 / WPT) threads of a 64-column block assemble its
+      // sign bytes and q bytes (q = sign XOR imaginary flag) into one 16-byte
+      // chunk of the row, written once (no other row shares it)
+      const int64_t w0 = (int64_t)tid * WPT;  // first word; all WPT words lie in block w0 >> 2
+      const int64_t blk = w0 >> 2, win = blk >> 2;
+      const int r = (int)(j & 31), nb = l3_slots(m, win < l3_windows(m) ? win : 0);
+      unsigned long long S = 0, Q = 0;
+#pragma unroll
+      for (int u = 0; u < WPT; ++u) {
+        uint32_t s16 = 0;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) s16 |= ((word[u] >> (2 * c + 1)) & 1u) << c;
+        const uint32_t q16 = s16 ^ (valid[u] & ~realm[u] & 0xFFFFu);
+        const int g0 = (int)(((w0 + u) & 15) * 2);  // group of the word's first 8 columns in its window
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int pos = 8 * l3_byte_of(g0 + h, r);
+          S |= (unsigned long long)((s16 >> (8 * h)) & 0xFFu) << pos;
+          Q |= (unsigned long long)((q16 >> (8 * h)) & 0xFFu) << pos;
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < 4 / WPT; o <<= 1) {
+        S |= __shfl_xor_sync(0xffffffffu, S, o);
+        Q |= __shfl_xor_sync(0xffffffffu, Q, o);
+      }
+      if ((tid & (4 / WPT - 1)) == 0 && win < l3_windows(m) && (blk & 3) < nb) {
+        const int jj = l3_slot_of((int)((blk & 3) << 3), r, nb);
+        *reinterpret_cast<uint4*>(codes + l3_offset(n, m, T, win, j >> 5, X * T + t) + jj * kL3SlotBytes + r * 16) =
+            make_uint4((uint32_t)S, (uint32_t)(S >> 32), (uint32_t)Q, (uint32_t)(Q >> 32));
+      }
+      continue;
     }
     // scatter the codes into the sign and flag words of the row's tile (the
     // plane was zeroed; the other row of each lane pair ORs its own bits)

@@ -23,6 +23,7 @@
 #include "linear_prefill.cuh"
 #include "linear_tc_decode.cuh"
 #include "linear_grad.cuh"
+#include "linear_lut.cuh"
 
 namespace {
 
@@ -83,9 +84,9 @@ int sm_count() {
 
 fairy2i_status check_packed(const fairy2i_packed* q) {
   if (!q) return fail(FAIRY2I_ERR_INVALID_ARG, "packed descriptor is NULL");
-  if (q->version != FAIRY2I_LAYOUT_VERSION)
-    return fail(FAIRY2I_ERR_INVALID_ARG, "packed layout version %d, library expects %d", q->version,
-                FAIRY2I_LAYOUT_VERSION);
+  if (q->version != FAIRY2I_LAYOUT_VERSION && q->version != FAIRY2I_LAYOUT_LUT)
+    return fail(FAIRY2I_ERR_INVALID_ARG, "packed layout version %d, library reads %d and %d", q->version,
+                FAIRY2I_LAYOUT_VERSION, FAIRY2I_LAYOUT_LUT);
   if (q->n < 1 || q->m < 1) return fail(FAIRY2I_ERR_SHAPE, "n=%lld m=%lld must be >= 1", (long long)q->n, (long long)q->m);
   if (q->T < 1 || q->T > FAIRY2I_MAX_T) return fail(FAIRY2I_ERR_UNSUPPORTED, "T=%d outside [1, %d]", q->T, FAIRY2I_MAX_T);
   if (q->m > FAIRY2I_MAX_M) return fail(FAIRY2I_ERR_UNSUPPORTED, "m=%lld above %d", (long long)q->m, FAIRY2I_MAX_M);
@@ -200,6 +201,13 @@ bool mma_wide(int T, int M, int64_t xstr_max) {
   size_t fixed, per_tile;
   mma_smem(f2i::kMmaWarpsWide, T, M, xstr_max, fixed, per_tile);
   return fixed + 2 * per_tile <= kMmaWideSmem;
+}
+
+// The mma decode forms a lane's code offsets inside a layer in 32 bits (plane
+// index x plane bytes + offset in the plane): all 2T planes of a layer must
+// lie within 4 GB.
+bool mma_offsets_fit(const fairy2i_packed& q) {
+  return (uint64_t)(2 * q.T) * (uint64_t)f2i::plane_bytes(q.n, q.m) <= 0xFFFFFFFFull;
 }
 
 fairy2i_status run_mma(f2i::LinearGroup& G, int T, cudaStream_t s) {
@@ -497,38 +505,214 @@ constexpr int64_t kPrefillMinTokens = 16;
 // The quantizer over U, W (FUSED = false) or straight from R (true); the
 // caller has checked the arguments.  Codes are zeroed first: each row ORs its
 // bits into words it shares with the other row of its lane pair.
+template <int LAYOUT>
+void quantize_kernels(const float2* U, const float2* W, const float* R, int64_t n, int64_t m, int32_t T, int64_t rows,
+                      int wpt, int threads, uint8_t* codes, float* scales, cudaStream_t s) {
+  if (R == nullptr) {
+    const dim3 grid((unsigned)rows, 2);
+    if (wpt == 1) f2i::quantize_words_kernel<1, false, LAYOUT><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, scales);
+    else f2i::quantize_words_kernel<2, false, LAYOUT><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, scales);
+  } else {
+    const dim3 grid(2, (unsigned)rows);
+    if (wpt == 1) f2i::quantize_words_kernel<1, true, LAYOUT><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, scales);
+    else f2i::quantize_words_kernel<2, true, LAYOUT><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, scales);
+  }
+}
+
 fairy2i_status launch_quantize(const float2* U, const float2* W, const float* R, int64_t n, int64_t m, int32_t T,
                                const fairy2i_packed* out, cudaStream_t s) {
+  uint8_t* codes = static_cast<uint8_t*>(out->codes);
+  if (out->version == FAIRY2I_LAYOUT_LUT) {
+    // layout 3: every 16-byte chunk of a row is written once by the row's CTA
+    // (rows past n in the last tile write zeros), so nothing is cleared first
+    const int64_t words = 4 * f2i::l3_row_slots(m);
+    const int wpt = words <= f2i::kQuantThreads ? 1 : 2;
+    const int threads = (int)(((words + wpt - 1) / wpt + 31) / 32 * 32);
+    const int64_t rows = f2i::l3_tiles(n) * 32;
+    if (R != nullptr && rows > 65535) return fail(FAIRY2I_ERR_UNSUPPORTED, "n=%lld too large for the fused path", (long long)n);
+    quantize_kernels<3>(U, W, R, n, m, T, rows, wpt, threads, codes, out->scales, s);
+    return check_launch("quantize launch");
+  }
   cudaError_t e = cudaMemsetAsync(out->codes, 0, fairy2i_codes_bytes(n, m, T), s);
   if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "memset codes: %s", cudaGetErrorString(e));
   const int64_t words = 4 * f2i::col_blocks(m);  // packed words per row
   const int wpt = words <= f2i::kQuantThreads ? 1 : 2;
   const int threads = (int)(((words + wpt - 1) / wpt + 31) / 32 * 32);
-  uint8_t* codes = static_cast<uint8_t*>(out->codes);
-  if (R == nullptr) {
-    const dim3 grid((unsigned)n, 2);
-    if (wpt == 1) f2i::quantize_words_kernel<1, false><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, out->scales);
-    else f2i::quantize_words_kernel<2, false><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, out->scales);
-  } else {
-    const dim3 grid(2, (unsigned)n);
-    if (wpt == 1) f2i::quantize_words_kernel<1, true><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, out->scales);
-    else f2i::quantize_words_kernel<2, true><<<grid, threads, 0, s>>>(U, W, R, n, m, T, codes, out->scales);
-  }
+  quantize_kernels<2>(U, W, R, n, m, T, n, wpt, threads, codes, out->scales, s);
   return check_launch("quantize launch");
 }
 
+// --- table-lookup decode (layout 3) ------------------------------------------
+
+// Layers of one launch: consecutive runs of at most kLutMaxGroup layers.
+// Workspace of a launch with mc tokens: one counter per row tile of every
+// layer with more than one window (256-byte aligned block), then a float2
+// partial output per (unit, token, row of the tile).
+size_t lut_launch_workspace(const fairy2i_packed* qs, int cnt, int mc, size_t* ctr_bytes) {
+  size_t ctr = 0, parts = 0;
+  for (int i = 0; i < cnt; ++i) {
+    const int64_t tiles = f2i::l3_tiles(qs[i].n), windows = f2i::l3_windows(qs[i].m);
+    if (windows > 1) {
+      ctr += (size_t)tiles;
+      parts += (size_t)(tiles * windows) * (size_t)mc * 32;
+    }
+  }
+  const size_t cb = (ctr * sizeof(unsigned) + 255) & ~(size_t)255;
+  if (ctr_bytes) *ctr_bytes = cb;
+  return parts ? cb + parts * sizeof(float2) : (ctr ? cb : 0);
+}
+
+size_t lut_workspace(const fairy2i_packed* qs, int count, int64_t M, int T) {
+  const int mc = (int)std::min<int64_t>(M, f2i::lut_max_tokens(T));
+  size_t need = 0;
+  for (int p0 = 0; p0 < count; p0 += f2i::kLutMaxGroup)
+    need = std::max(need, lut_launch_workspace(qs + p0, std::min(f2i::kLutMaxGroup, count - p0), mc, nullptr));
+  return need;
+}
+
+template <int T, int M>
+fairy2i_status launch_lut_t(const f2i::LutParams& P, int ctas, cudaStream_t s) {
+  auto k = f2i::linear_lut_kernel<T, M>;
+  fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(k), f2i::kLutSmemBytes, "table-lookup decode");
+  if (st != FAIRY2I_OK) return st;
+  k<<<ctas, f2i::kLutThreads, f2i::kLutSmemBytes, s>>>(P);
+  return check_launch("table-lookup decode launch");
+}
+
+fairy2i_status launch_lut(const f2i::LutParams& P, int T, int mc, int ctas, cudaStream_t s) {
+  switch (T * 8 + mc) {
+    case 9: return launch_lut_t<1, 1>(P, ctas, s);
+    case 10: return launch_lut_t<1, 2>(P, ctas, s);
+    case 11: return launch_lut_t<1, 3>(P, ctas, s);
+    case 12: return launch_lut_t<1, 4>(P, ctas, s);
+    case 17: return launch_lut_t<2, 1>(P, ctas, s);
+    case 18: return launch_lut_t<2, 2>(P, ctas, s);
+    case 19: return launch_lut_t<2, 3>(P, ctas, s);
+    case 20: return launch_lut_t<2, 4>(P, ctas, s);
+    case 25: return launch_lut_t<3, 1>(P, ctas, s);
+    case 26: return launch_lut_t<3, 2>(P, ctas, s);
+    case 33: return launch_lut_t<4, 1>(P, ctas, s);
+    default: return fail(FAIRY2I_ERR_UNSUPPORTED, "table-lookup decode: no kernel for T=%d with %d tokens", T, mc);
+  }
+}
+
+// One launch per kLutMaxGroup layers and per lut_max_tokens(T) tokens.  Units
+// (layer, window, row tile) are split over one CTA per SM by their cost, in
+// launch order: 8 per slot of codes plus 3 for the unit's epilogue.
+fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count, int64_t M, int T,
+                       void* ws, size_t ws_bytes, cudaStream_t s) {
+  const size_t need = lut_workspace(qs, count, M, T);
+  if (need > 0) {
+    if (!ws) return fail(FAIRY2I_ERR_INVALID_ARG, "table-lookup decode needs a workspace of %zu bytes", need);
+    if (ws_bytes < need)
+      return fail(FAIRY2I_ERR_INVALID_ARG, "workspace of %zu bytes, the table-lookup decode needs %zu", ws_bytes, need);
+    if (!aligned(ws, 256)) return fail(FAIRY2I_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  }
+  for (int i = 0; i < count; ++i)
+    if (f2i::l3_tiles(qs[i].n) * f2i::l3_windows(qs[i].m) > (int64_t)1 << 30)
+      return fail(FAIRY2I_ERR_UNSUPPORTED, "layer %d too large for the table-lookup decode", i);
+  const int mcmax = f2i::lut_max_tokens(T);
+  std::unique_ptr<f2i::LutParams> holder(new f2i::LutParams);
+  f2i::LutParams& P = *holder;
+  for (int p0 = 0; p0 < count; p0 += f2i::kLutMaxGroup) {
+    const int cnt = std::min(f2i::kLutMaxGroup, count - p0);
+    for (int64_t t0 = 0; t0 < M; t0 += mcmax) {
+      const int mc = (int)std::min<int64_t>(mcmax, M - t0);
+      memset(&P, 0, sizeof(P));
+      size_t cb = 0;
+      const size_t wsn = lut_launch_workspace(qs + p0, cnt, mc, &cb);
+      P.count = cnt;
+      P.M = mc;
+      P.counters = wsn ? static_cast<unsigned*>(ws) : nullptr;
+      P.partials = wsn ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + cb) : nullptr;
+      int64_t units = 0, ctr = 0, part = 0;
+      for (int i = 0; i < cnt; ++i) {
+        const fairy2i_packed& q = qs[p0 + i];
+        f2i::LutProblem& L = P.p[i];
+        L.codes = static_cast<const uint8_t*>(q.codes);
+        L.scales = q.scales;
+        L.x = static_cast<const uint16_t*>(xs[p0 + i]) + t0 * 2 * q.m;
+        L.y = ys[p0 + i] + t0 * 2 * q.n;
+        L.n = (int32_t)q.n;
+        L.m = (int32_t)q.m;
+        L.tiles = (int32_t)f2i::l3_tiles(q.n);
+        L.windows = (int32_t)f2i::l3_windows(q.m);
+        L.unit_begin = (int32_t)units;
+        L.ctr_begin = L.windows > 1 ? (int32_t)ctr : -1;
+        L.part_begin = part;
+        units += (int64_t)L.tiles * L.windows;
+        if (L.windows > 1) {
+          ctr += L.tiles;
+          part += (int64_t)L.tiles * L.windows * mc * 32;
+        }
+      }
+      if (units > INT32_MAX / 2) return fail(FAIRY2I_ERR_UNSUPPORTED, "too many units for one launch");
+      P.total_units = (int32_t)units;
+      const int ctas = (int)std::min<int64_t>({units, (int64_t)sm_count(), (int64_t)f2i::kLutMaxCtas});
+      // cost-balanced split of the units, in order
+      int64_t total = 0;
+      for (int i = 0; i < cnt; ++i) {
+        const f2i::LutProblem& L = P.p[i];
+        for (int w = 0; w < L.windows; ++w) total += (int64_t)L.tiles * (8 * f2i::l3_slots(L.m, w) + 3);
+      }
+      int c = 1;
+      int64_t cum = 0;
+      P.cta_begin[0] = 0;
+      for (int i = 0; i < cnt && c < ctas; ++i) {
+        const f2i::LutProblem& L = P.p[i];
+        for (int w = 0; w < L.windows && c < ctas; ++w) {
+          const int64_t cost = 8 * f2i::l3_slots(L.m, w) + 3;
+          for (int tau = 0; tau < L.tiles && c < ctas; ++tau) {
+            // unit u starts CTA c when the cost before it reaches c / ctas of the total
+            while (c < ctas && cum * ctas >= total * c) P.cta_begin[c++] = L.unit_begin + w * L.tiles + tau;
+            cum += cost;
+          }
+        }
+      }
+      while (c < ctas) P.cta_begin[c++] = (int32_t)units;
+      P.cta_begin[ctas] = (int32_t)units;
+      fairy2i_status st = launch_lut(P, T, mc, ctas, s);
+      if (st != FAIRY2I_OK) return st;
+    }
+  }
+  return ok();
+}
+
+// with_ws: the call came through a *_ws entry point (workspace may still be
+// NULL when none is needed).
 fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int32_t count,
-                                 int64_t M, fairy2i_algo algo, cudaStream_t s) {
+                                 int64_t M, fairy2i_algo algo, bool with_ws, void* ws, size_t ws_bytes,
+                                 cudaStream_t s) {
   if (count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "count=%d outside [1, 256]", count);
   if (!qs || !xs || !ys) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL array argument");
   if (M < 0) return fail(FAIRY2I_ERR_SHAPE, "M=%lld is negative", (long long)M);
-  if ((int)algo < 0 || (int)algo > 4) return fail(FAIRY2I_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
+  if ((int)algo < 0 || (int)algo > 5) return fail(FAIRY2I_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
+  if (!qs) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL descriptor array");
   const int T = qs[0].T;
   for (int i = 0; i < count; ++i) {
     fairy2i_status st = check_packed(&qs[i]);
     if (st != FAIRY2I_OK) return st;
     if (qs[i].T != T) return fail(FAIRY2I_ERR_SHAPE, "all layers of a group need the same T");
+    if (qs[i].version != qs[0].version) return fail(FAIRY2I_ERR_SHAPE, "all layers of a group need the same layout");
   }
+  if (qs[0].version == FAIRY2I_LAYOUT_LUT) {
+    if (algo != FAIRY2I_ALGO_AUTO && algo != FAIRY2I_ALGO_LUT)
+      return fail(FAIRY2I_ERR_UNSUPPORTED, "layout 3 is read by the table-lookup decode only (algo AUTO or LUT)");
+    if (T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "table-lookup decode supports T <= 4");
+    if (!with_ws)
+      return fail(FAIRY2I_ERR_UNSUPPORTED, "layout 3 needs a workspace: call fairy2i_linear_ws / fairy2i_linear_group_ws");
+    if (M == 0) return ok();
+    for (int i = 0; i < count; ++i) {
+      if (!xs[i] || !ys[i]) return fail(FAIRY2I_ERR_INVALID_ARG, "x or y of layer %d is NULL", i);
+      if (!aligned(xs[i], 16) || !aligned(ys[i], 16))
+        return fail(FAIRY2I_ERR_INVALID_ARG, "x and y must be 16-byte aligned (layer %d)", i);
+    }
+    if (M > (int64_t)1 << 30) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
+    return run_lut(qs, xs, ys, count, M, T, ws, ws_bytes, s);
+  }
+  if (algo == FAIRY2I_ALGO_LUT) return fail(FAIRY2I_ERR_UNSUPPORTED, "the table-lookup decode reads layout 3 only");
+  (void)ws;
+  (void)ws_bytes;
   if (M == 0) return ok();  // no tokens: nothing is read or written
   for (int i = 0; i < count; ++i) {
     if (!xs[i] || !ys[i]) return fail(FAIRY2I_ERR_INVALID_ARG, "x or y of layer %d is NULL", i);
@@ -539,11 +723,15 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
 
   bool m_mult8 = true;
   for (int i = 0; i < count; ++i) m_mult8 = m_mult8 && (qs[i].m % 8) == 0;
+  bool offsets32 = true;
+  for (int i = 0; i < count; ++i) offsets32 = offsets32 && mma_offsets_fit(qs[i]);
   fairy2i_algo a = algo;
   if (a == FAIRY2I_ALGO_AUTO) {
     if (T <= 4 && M >= kPrefillMinTokens && m_mult8) a = FAIRY2I_ALGO_TCGEN05;
-    else a = (T <= 4) ? FAIRY2I_ALGO_MMA : FAIRY2I_ALGO_ADDSUB;
+    else a = (T <= 4 && offsets32) ? FAIRY2I_ALGO_MMA : FAIRY2I_ALGO_ADDSUB;
   }
+  if (a == FAIRY2I_ALGO_MMA && !offsets32)
+    return fail(FAIRY2I_ERR_UNSUPPORTED, "mma decode: a layer's code planes exceed 4 GB (32-bit offsets)");
   if (a == FAIRY2I_ALGO_TCGEN05_SP) {
     if (T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "sparse tensor-core decode supports T <= 4");
     if (M > kTcDecodeMaxTokens) return fail(FAIRY2I_ERR_UNSUPPORTED, "sparse tensor-core decode supports M <= 8");
@@ -605,6 +793,10 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
   return ok();
 }
 
+__device__ unsigned int g_fairy2i_error_taken;
+
+__global__ void take_error_word_kernel() { g_fairy2i_error_taken = atomicExch(&g_fairy2i_error_word, 0u); }
+
 }  // namespace
 
 extern "C" {
@@ -616,6 +808,13 @@ const char* fairy2i_last_error(void) { return g_last_error.c_str(); }
 size_t fairy2i_codes_bytes(int64_t n, int64_t m, int32_t T) {
   if (n < 1 || m < 1 || T < 1 || T > FAIRY2I_MAX_T) return 0;
   return (size_t)(2 * T) * (size_t)f2i::plane_bytes(n, m);
+}
+
+size_t fairy2i_codes_bytes_layout(int64_t n, int64_t m, int32_t T, int32_t version) {
+  if (n < 1 || m < 1 || T < 1 || T > FAIRY2I_MAX_T) return 0;
+  if (version == FAIRY2I_LAYOUT_VERSION) return (size_t)(2 * T) * (size_t)f2i::plane_bytes(n, m);
+  if (version == FAIRY2I_LAYOUT_LUT) return (size_t)f2i::l3_codes_bytes(n, m, T);
+  return 0;
 }
 
 size_t fairy2i_scales_count(int64_t n, int32_t T) {
@@ -677,7 +876,31 @@ fairy2i_status fairy2i_linear_ex(const fairy2i_packed* q, const void* x, int64_t
   if (!q) return fail(FAIRY2I_ERR_INVALID_ARG, "packed descriptor is NULL");
   const void* xs[1] = {x};
   float* ys[1] = {y};
-  return linear_group_impl(q, xs, ys, 1, M, algo, static_cast<cudaStream_t>(stream));
+  return linear_group_impl(q, xs, ys, 1, M, algo, false, nullptr, 0, static_cast<cudaStream_t>(stream));
+}
+
+size_t fairy2i_linear_workspace_bytes(const fairy2i_packed* qs, int32_t count, int64_t M) {
+  if (!qs || count < 1 || count > 256 || M < 1) return 0;
+  for (int i = 0; i < count; ++i)
+    if (qs[i].version != FAIRY2I_LAYOUT_LUT || qs[i].T < 1 || qs[i].T > 4 || qs[i].T != qs[0].T || qs[i].n < 1 ||
+        qs[i].m < 1)
+      return 0;
+  return lut_workspace(qs, count, M, qs[0].T);
+}
+
+fairy2i_status fairy2i_linear_ws(const fairy2i_packed* q, const void* x, int64_t M, float* y, fairy2i_algo algo,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q) return fail(FAIRY2I_ERR_INVALID_ARG, "packed descriptor is NULL");
+  const void* xs[1] = {x};
+  float* ys[1] = {y};
+  return linear_group_impl(q, xs, ys, 1, M, algo, true, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+fairy2i_status fairy2i_linear_group_ws(const fairy2i_packed* qs, const void* const* xs, float* const* ys,
+                                       int32_t count, int64_t M, fairy2i_algo algo, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  return linear_group_impl(qs, xs, ys, count, M, algo, true, workspace, workspace_bytes,
+                           static_cast<cudaStream_t>(stream));
 }
 
 fairy2i_status fairy2i_linear(const fairy2i_packed* q, const void* x, int64_t M, float* y, void* stream) {
@@ -686,7 +909,7 @@ fairy2i_status fairy2i_linear(const fairy2i_packed* q, const void* x, int64_t M,
 
 fairy2i_status fairy2i_linear_group(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int32_t count,
                                     int64_t M, fairy2i_algo algo, void* stream) {
-  return linear_group_impl(qs, xs, ys, count, M, algo, static_cast<cudaStream_t>(stream));
+  return linear_group_impl(qs, xs, ys, count, M, algo, false, nullptr, 0, static_cast<cudaStream_t>(stream));
 }
 
 fairy2i_status fairy2i_linear_grad_x(const fairy2i_packed* q, const float* gy, int64_t M, float* gx, void* stream) {
@@ -701,6 +924,8 @@ fairy2i_status fairy2i_linear_grad_x_group(const fairy2i_packed* qs, const float
     fairy2i_status st = check_packed(&qs[i]);
     if (st != FAIRY2I_OK) return st;
     if (qs[i].T != qs[0].T) return fail(FAIRY2I_ERR_SHAPE, "all layers of a group need the same T");
+    if (qs[i].version != FAIRY2I_LAYOUT_VERSION)
+      return fail(FAIRY2I_ERR_UNSUPPORTED, "the input gradient reads layout %d only", FAIRY2I_LAYOUT_VERSION);
   }
   if (M < 0) return fail(FAIRY2I_ERR_SHAPE, "M=%lld is negative", (long long)M);
   if (M == 0) return ok();
@@ -745,8 +970,12 @@ fairy2i_status fairy2i_unpack_codes(const fairy2i_packed* q, uint8_t* codes_out,
   fairy2i_status st = check_packed(q);
   if (st != FAIRY2I_OK) return st;
   if (!codes_out) return fail(FAIRY2I_ERR_INVALID_ARG, "codes_out is NULL");
-  f2i::unpack_codes_kernel<<<sm_count() * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint8_t*>(q->codes), q->n, q->m, q->T, codes_out);
+  if (q->version == FAIRY2I_LAYOUT_LUT)
+    f2i::unpack_codes_l3_kernel<<<sm_count() * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t*>(q->codes), q->n, q->m, q->T, codes_out);
+  else
+    f2i::unpack_codes_kernel<<<sm_count() * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t*>(q->codes), q->n, q->m, q->T, codes_out);
   return check_launch("unpack launch");
 }
 
@@ -757,18 +986,20 @@ fairy2i_status fairy2i_selftest_bounded_wait(int32_t limit_us, void* stream) {
 }
 
 fairy2i_status fairy2i_sync_status(void* stream) {
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  // read and clear in one atomic step on the device, so that a flag raised by
+  // a kernel on another stream in between is kept for the next call
+  take_error_word_kernel<<<1, 1, 0, s>>>();
   unsigned word = 0;
-  e = cudaMemcpyFromSymbol(&word, g_fairy2i_error_word, sizeof(word));
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(&word, g_fairy2i_error_taken, sizeof(word), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "read error word: %s", cudaGetErrorString(e));
-  if (word != 0) {
-    const unsigned zero = 0;
-    e = cudaMemcpyToSymbol(g_fairy2i_error_word, &zero, sizeof(zero));
-    if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "clear error word: %s", cudaGetErrorString(e));
-  }
   if (word & f2i::kErrNonFinite) return fail(FAIRY2I_ERR_NONFINITE, "non-finite weight seen by quantize");
   if (word & f2i::kErrTimeout) return fail(FAIRY2I_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (word & f2i::kErrConfig) return fail(FAIRY2I_ERR_CUDA, "a kernel refused its shared-memory placement");
   return ok();
 }
 

@@ -64,8 +64,65 @@ __host__ __device__ __forceinline__ int flag_bit(int s, int qp, int rho, int e) 
   return 4 * (qp + 4 * rho) + (s & 1) + 2 * e;
 }
 
+// ---------------------------------------------------------------------------
+// Layout version 3: the table-lookup decode layout.
+//
+// The decode evaluates each plane's two signed sums per row, P = sum of
+// sigma x and Q = sum of sigma tau x (sigma = the code's sign, tau = +1 on the
+// real axis and -1 on the imaginary axis; A_re = (P + Q) / 2 and
+// A_im = (P - Q) / 2), by looking up, for every group of 8 columns, the signed
+// sum of those 8 activations selected by one byte of code bits.  A code plane
+// therefore stores, per (row, group of 8 columns), a sign byte (bit c = sign
+// of column 8 G + c, 1 = -1 or -i) and a q byte (sign XOR imaginary-axis
+// flag).
+//
+// Rows come in tiles of 32 (row j = 32 tau + r, lane r of the decode) and
+// columns in windows of 256 (32 groups; window w).  Inside a window the
+// groups form blocks of 8 (block b = G >> 3, 64 columns); a window stores
+// nb blocks (4, or for a last partial window 1, 2 or 4 with zero padding),
+// as nb slots of 512 bytes: 32 rows x 16 bytes, sign bytes 0..7 then q bytes
+// 8..15.  Slot jj of row r holds block b = jj ^ (a & (nb - 1)), a =
+// (r >> 3) & 3, its group 8 b + ((r & 7) ^ i) in byte i.  Equivalently the
+// byte (jj, i) of row r is group (r & (8 nb - 1)) ^ (8 jj + i): at every byte
+// position the 32 rows of a full window name 32 different groups, so the 32
+// lanes of a warp read 32 different tables.
+// Byte order: [window][row tile][plane (X, t)][slot][row][16 bytes].
+// ---------------------------------------------------------------------------
+constexpr int kL3Rows = 32;
+constexpr int kL3Cols = 256;
+constexpr int kL3SlotBytes = 512;
+
+__host__ __device__ __forceinline__ int64_t l3_tiles(int64_t n) { return (n + 31) / 32; }
+__host__ __device__ __forceinline__ int64_t l3_windows(int64_t m) { return (m + 255) / 256; }
+// Slots (blocks of 64 columns) stored for window w: 4, or 1, 2, 4 for a last
+// partial window (3 blocks are padded to 4).
+__host__ __device__ __forceinline__ int l3_slots(int64_t m, int64_t w) {
+  const int64_t rest = m - 256 * w;
+  if (rest >= 256) return 4;
+  const int nc = (int)((rest + 63) / 64);
+  return nc == 3 ? 4 : nc;
+}
+// Slots of all windows of one row tile and plane.
+__host__ __device__ __forceinline__ int64_t l3_row_slots(int64_t m) {
+  return 4 * (m / 256) + ((m % 256) ? l3_slots(m, m / 256) : 0);
+}
+__host__ __device__ __forceinline__ int64_t l3_codes_bytes(int64_t n, int64_t m, int T) {
+  return l3_tiles(n) * 2 * T * kL3SlotBytes * l3_row_slots(m);
+}
+// Byte offset of slot 0 of (window w, row tile tau, plane p).
+__host__ __device__ __forceinline__ int64_t l3_offset(int64_t n, int64_t m, int T, int64_t w, int64_t tau, int p) {
+  const int nb = l3_slots(m, w);
+  return w * l3_tiles(n) * 2 * T * 4 * kL3SlotBytes + (tau * 2 * T + p) * (int64_t)nb * kL3SlotBytes;
+}
+// Byte (within the 16 bytes of row r in slot jj) of group g of a window with
+// nb slots, and the slot: the inverse of the rule above.
+__host__ __device__ __forceinline__ int l3_slot_of(int g, int r, int nb) { return (g >> 3) ^ ((r >> 3) & (nb - 1)); }
+__host__ __device__ __forceinline__ int l3_byte_of(int g, int r) { return (g & 7) ^ (r & 7); }
+
 // Per-device error word (bit flags), read and cleared by fairy2i_sync_status.
-enum : unsigned { kErrNonFinite = 1u, kErrTimeout = 2u };
+// kErrConfig: a kernel found its launch configuration unusable (shared-memory
+// placement) and did nothing.
+enum : unsigned { kErrNonFinite = 1u, kErrTimeout = 2u, kErrConfig = 4u };
 
 }  // namespace f2i
 

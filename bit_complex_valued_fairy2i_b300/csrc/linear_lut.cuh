@@ -1,0 +1,484 @@
+// Layer evaluation by table lookup over layout 3 (decode token counts).
+//
+// The layer ("Fairy2i-W2" model card, y = Ux + W conj(x); "Fairy2i: Ultra-Low-
+// Bit LLM Quantization Using Complex Weights {±1, ±i}", "Industry
+// implications: multiplication-free inference") needs, per output row and
+// code plane (matrix X, stage t), the two signed sums A_re (real-coded
+// columns) and A_im (imaginary-coded columns) of x.  With sigma the code's
+// sign and tau = +1 (real axis) or -1 (imaginary axis):
+//   P = sum sigma x,  Q = sum sigma tau x,  A_re = (P + Q) / 2,  A_im = (P - Q) / 2.
+// Both P and Q are sums of +-x only, so they are read from tables: for every
+// group of 8 columns the 256 signed sums of its 8 activations, indexed by a
+// byte of sign bits (P) or of sign-XOR-axis bits (Q).  Each lookup replaces 8
+// complex adds; the inner loop per byte is one byte permute (the shared-memory
+// address), one shared load and two fp32 adds of the fp16 table entry.
+//
+// Tables: one per (window of 256 columns, token), 32 groups x 256 entries of
+// packed fp16 (re, im), entry e of group G at byte e * 256 + 4 G of a 64 KB
+// region (two tables share a region, offset by 128 bytes).  Lane r of a warp
+// owns row r of a 32-row tile; at each byte position of layout 3 the 32 rows
+// name 32 different groups, so the 32 lanes hit 32 different banks.  The
+// activations of a table are scaled by a power of two (the window maximum
+// lands in [2^11, 2^12)) so that every entry is a normal fp16 number; each
+// entry is the fp32 sum of its 8 terms rounded once to fp16.
+//
+// Work: a unit is (layer, window, row tile) = 32 rows x 256 columns x 2T
+// planes.  Units are numbered window-major inside a layer and split evenly
+// (by slot count) over one CTA per SM.  A CTA builds the tables of the
+// windows its units touch, then its 16 warps take units in turn.  A unit's
+// fp32 accumulators become a partial output (scales applied) in the
+// caller's workspace; the last warp to finish a row tile (an atomic counter
+// per tile) adds the partials of all windows in window order and writes y.
+// Results are deterministic: every sum has a fixed order.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+#include "layout.cuh"
+
+namespace f2i {
+
+constexpr int kLutWarps = 16;
+constexpr int kLutThreads = kLutWarps * 32;
+constexpr int kLutMaxGroup = 32;
+constexpr int kLutMaxCtas = 1024;
+constexpr uint32_t kLutTableBase = 65536;          // shared address of the first 64 KB table region
+constexpr uint32_t kLutSmemBytes = 3u * 65536u;    // dynamic shared memory: covers [64 KB, 192 KB) for any base
+
+// Largest token count of one launch for T stages (fp32 accumulators and the
+// double-buffered code words stay within 128 registers).
+__host__ __device__ constexpr int lut_max_tokens(int T) { return T <= 2 ? 4 : T == 3 ? 2 : 1; }
+
+struct LutProblem {
+  const uint8_t* codes;
+  const float* scales;
+  const uint16_t* x;  // bfloat16 [M][2m] (this launch's tokens)
+  float* y;           // [M][2n]
+  int32_t n, m;
+  int32_t tiles;       // row tiles of 32 rows
+  int32_t windows;     // column windows of 256
+  int32_t unit_begin;  // first unit of the layer in the launch
+  int32_t ctr_begin;   // first row-tile counter in the workspace (layers with more than one window)
+  int64_t part_begin;  // first partial output (float2) in the workspace
+};
+
+struct LutParams {
+  int32_t count, M, total_units, pad_;
+  unsigned* counters;
+  float2* partials;
+  LutProblem p[kLutMaxGroup];
+  int32_t cta_begin[kLutMaxCtas + 1];
+};
+
+__device__ __forceinline__ uint32_t lut_prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+template <uint32_t OFF>
+__device__ __forceinline__ uint32_t lut_lds(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF));
+  return v;
+}
+// acc_re += lo(e), acc_im += hi(e): fp16 table entry added in fp32 (one rounding each)
+__device__ __forceinline__ void lut_add(float& re, float& im, uint32_t e) {
+  unsigned short lo, hi;
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(e));
+  asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(re) : "h"(lo));
+  asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(im) : "h"(hi));
+}
+
+__device__ __forceinline__ int lut_problem_of(const LutParams& P, int u) {
+  int pi = 0;
+  for (int i = 1; i < P.count; ++i)
+    if (u >= P.p[i].unit_begin) pi = i;
+  return pi;
+}
+
+// Table set z of a resident segment s and token t (M tokens per launch):
+// region z >> 1 (64 KB each, from kLutTableBase), half z & 1 (+128 bytes).
+template <int M>
+__host__ __device__ constexpr int lut_segments() { return M == 1 ? 4 : M == 2 ? 2 : 1; }
+template <int M>
+__device__ __forceinline__ int lut_set(int s, int t) { return M == 1 ? s : M == 2 ? 2 * s + t : t; }
+// Shared-address part of set z that the lane's B word carries (bits 7 and
+// 16..23) and the part given as an immediate offset of the loads.
+template <int M>
+__device__ __forceinline__ uint32_t lut_b_bits(int s) {
+  return M == 1 ? (((uint32_t)s & 1u) << 7) | (((uint32_t)s >> 1) << 16) : M == 2 ? ((uint32_t)s << 16) : 0u;
+}
+template <int M, int t>
+__host__ __device__ constexpr uint32_t lut_imm() {
+  return M == 1 ? kLutTableBase : M == 2 ? kLutTableBase + 128u * t : kLutTableBase + 65536u * (t >> 1) + 128u * (t & 1);
+}
+
+// Builds the table of (window w of layer L, token t) into set z: warp h
+// writes entries 16 h .. 16 h + 15 of every slot (lane = slot).  Slot S holds
+// group S & (8 nb - 1): a partial window's groups are repeated over all 32
+// slots, so that the lanes that share a group read different banks.  Returns
+// the factor 2^e that undoes the activation scaling.
+__device__ __forceinline__ float lut_build(const LutProblem& L, int w, int t, int z) {
+  const int lane = threadIdx.x & 31, h = threadIdx.x >> 5;
+  const int64_t m = L.m;
+  const int grp = lane & (8 * l3_slots(m, w) - 1);
+  const int64_t k0 = 256 * (int64_t)w + 8 * grp;
+  const uint16_t* xa = L.x + (int64_t)t * 2 * m;
+  float a[8], b[8];
+  if ((m & 7) == 0 && (reinterpret_cast<uintptr_t>(L.x) & 15) == 0 && k0 < m) {
+    const uint4 va = *reinterpret_cast<const uint4*>(xa + k0);
+    const uint4 vb = *reinterpret_cast<const uint4*>(xa + m + k0);
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      a[2 * c] = __uint_as_float(wa[c] << 16);
+      a[2 * c + 1] = __uint_as_float(wa[c] & 0xFFFF0000u);
+      b[2 * c] = __uint_as_float(wb[c] << 16);
+      b[2 * c + 1] = __uint_as_float(wb[c] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const bool in = k0 + c < m;
+      a[c] = in ? __uint_as_float((uint32_t)xa[k0 + c] << 16) : 0.0f;
+      b[c] = in ? __uint_as_float((uint32_t)xa[m + k0 + c] << 16) : 0.0f;
+    }
+  }
+  // window maximum over finite magnitudes (every warp holds the whole window)
+  float mx = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float fa = fabsf(a[c]), fb = fabsf(b[c]);
+    mx = fmaxf(mx, isfinite(fa) ? fa : 0.0f);
+    mx = fmaxf(mx, isfinite(fb) ? fb : 0.0f);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  // e: mx 2^-e in [2^11, 2^12); clamped so that 2^-e and 2^e are normal floats
+  int e = 0;
+  if (mx > 0.0f) {
+    const int ex = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // a subnormal maximum gives -127, then the clamp
+    e = max(ex - 11, -126);
+  }
+  const float down = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    a[c] *= down;
+    b[c] *= down;
+  }
+  // entry (16 h + l) = sum over c of (bit c set ? -1 : +1) (a_c, b_c)
+  float hr = 0.0f, hi = 0.0f;
+#pragma unroll
+  for (int c = 4; c < 8; ++c) {
+    const bool neg = (h >> (c - 4)) & 1;
+    hr += neg ? -a[c] : a[c];
+    hi += neg ? -b[c] : b[c];
+  }
+  float pr[4], pi[4], qr[4], qi[4];  // +-x0 +-x1 and +-x2 +-x3, index = the two sign bits
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    pr[v] = ((v & 1) ? -a[0] : a[0]) + ((v & 2) ? -a[1] : a[1]);
+    pi[v] = ((v & 1) ? -b[0] : b[0]) + ((v & 2) ? -b[1] : b[1]);
+    qr[v] = ((v & 1) ? -a[2] : a[2]) + ((v & 2) ? -a[3] : a[3]) + hr;
+    qi[v] = ((v & 1) ? -b[2] : b[2]) + ((v & 2) ? -b[3] : b[3]) + hi;
+  }
+  const uint32_t set_addr = kLutTableBase + ((uint32_t)z >> 1) * 65536u + ((uint32_t)z & 1u) * 128u;
+#pragma unroll
+  for (int l = 0; l < 16; ++l) {
+    const float er = pr[l & 3] + qr[l >> 2], ei = pi[l & 3] + qi[l >> 2];
+    const __half2 hv = __floats2half2_rn(er, ei);
+    const uint32_t addr = set_addr + (uint32_t)(16 * h + l) * 256u + 4u * (uint32_t)lane;
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(*reinterpret_cast<const uint32_t*>(&hv)) : "memory");
+  }
+  return __uint_as_float((uint32_t)(127 + e) << 23);  // 2^e
+}
+
+template <int T, int M>
+__global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid_constant__ LutParams P) {
+  extern __shared__ __align__(16) uint8_t lsm[];
+  constexpr int NP = 2 * T;
+  constexpr int S = lut_segments<M>();
+  __shared__ int s_nseg;
+  __shared__ int s_unit[S + 1];  // unit range of each resident segment
+  __shared__ int s_prob[S], s_win[S];
+  __shared__ float s_pow[S][M];  // 2^e per (segment, token)
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the table regions must lie inside this CTA's dynamic shared memory
+  const uint32_t base = (uint32_t)__cvta_generic_to_shared(lsm);
+  if (base + (uint32_t)(kLutWarps * 2 * NP * 32 * 4) > kLutTableBase || base + kLutSmemBytes < kLutTableBase + 2u * 65536u) {
+    if (tid == 0) f2i_raise(kErrConfig);  // refuse rather than address memory outside the CTA's buffer
+    return;
+  }
+  const int u_end = P.cta_begin[blockIdx.x + 1];
+  int u = P.cta_begin[blockIdx.x];
+  while (u < u_end) {
+    if (tid == 0) {
+      int s = 0, uu = u;
+      while (s < S && uu < u_end) {
+        const int pi = lut_problem_of(P, uu);
+        const LutProblem& L = P.p[pi];
+        const int w = (uu - L.unit_begin) / L.tiles;
+        s_unit[s] = uu;
+        s_prob[s] = pi;
+        s_win[s] = w;
+        uu = min(u_end, L.unit_begin + (w + 1) * L.tiles);
+        ++s;
+      }
+      s_nseg = s;
+      s_unit[s] = uu;
+    }
+    __syncthreads();
+    const int nseg = s_nseg;
+    const int ub = s_unit[0], ue = s_unit[nseg];
+    // a unit's codes (2T planes x nb slots, contiguous) as (pointer to lane 0's bytes, slots)
+    auto unit_codes = [&](int uu, int& seg, int& nb) -> const uint8_t* {
+      seg = 0;
+#pragma unroll
+      for (int k = 1; k < S; ++k)
+        if (k < nseg && uu >= s_unit[k]) seg = k;
+      const LutProblem& L = P.p[s_prob[seg]];
+      const int w = s_win[seg];
+      nb = l3_slots(L.m, w);
+      return L.codes + l3_offset(L.n, L.m, T, w, uu - L.unit_begin - w * L.tiles, 0);
+    };
+    // every unit this warp will take, into L2 now: HBM streams while the tables are built
+    if (lane == 0)
+      for (int uu = ub + warp; uu < ue; uu += kLutWarps) {
+        int sg, nbu;
+        const uint8_t* cp0 = unit_codes(uu, sg, nbu);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cp0), "r"((uint32_t)(NP * nbu * kL3SlotBytes))
+                     : "memory");
+      }
+    for (int s = 0; s < nseg; ++s) {
+#pragma unroll
+      for (int t = 0; t < M; ++t) {
+        const float pw = lut_build(P.p[s_prob[s]], s_win[s], t, lut_set<M>(s, t));
+        if (tid == 0) s_pow[s][t] = pw;
+      }
+    }
+    __syncthreads();
+
+    // this warp's scale buffer: [2T planes x 2 axes][32 rows] floats
+    float* sscale = reinterpret_cast<float*>(lsm) + warp * (2 * NP * 32);
+    const uint32_t sscale_addr = base + (uint32_t)(warp * 2 * NP * 32 + lane) * 4u;
+    uint4 cw[2][NP];
+    int uu = ub + warp, s = 0, nb = 4;
+    const uint8_t* cp = nullptr;
+    if (uu < ue) {
+      cp = unit_codes(uu, s, nb) + lane * 16;
+#pragma unroll
+      for (int p = 0; p < NP; ++p) cw[0][p] = __ldcg(reinterpret_cast<const uint4*>(cp + p * nb * kL3SlotBytes));
+    }
+    while (uu < ue) {
+      const int pi = s_prob[s], w = s_win[s];
+      const LutProblem& L = P.p[pi];
+      const int tau = uu - L.unit_begin - w * L.tiles;
+      const int64_t j = 32 * (int64_t)tau + lane;
+      const bool row_in = j < L.n;
+      // the row's scales into shared memory (zero past n), used by the epilogue
+#pragma unroll
+      for (int k = 0; k < 2 * NP; ++k) {
+        const float* src = row_in ? L.scales + (int64_t)k * L.n + j : L.scales;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(sscale_addr + (uint32_t)k * 128u), "l"(src),
+                     "r"(row_in ? 4 : 0)
+                     : "memory");
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      const int un = uu + kLutWarps;
+      int sn = 0, nbn = 4;
+      const uint8_t* cpn = un < ue ? unit_codes(un, sn, nbn) + lane * 16 : nullptr;
+      const uint32_t pstride = (uint32_t)nb * kL3SlotBytes;
+      // slot lane ^ (8 jj + i): group (lane & (8 nb - 1)) ^ (8 jj + i), bank = slot
+      const uint32_t bbase = 4u * (uint32_t)lane | lut_b_bits<M>(s);
+
+      float acc[M][NP][4];
+#pragma unroll
+      for (int t = 0; t < M; ++t)
+#pragma unroll
+        for (int p = 0; p < NP; ++p) acc[t][p][0] = acc[t][p][1] = acc[t][p][2] = acc[t][p][3] = 0.0f;
+
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        if (jj < nb) {
+          // next slot of this unit, or after the last slot the next unit's first
+          if (jj + 1 < nb) {
+#pragma unroll
+            for (int p = 0; p < NP; ++p)
+              cw[(jj + 1) & 1][p] = __ldcg(reinterpret_cast<const uint4*>(cp + p * pstride + (jj + 1) * kL3SlotBytes));
+          } else if (cpn != nullptr) {
+#pragma unroll
+            for (int p = 0; p < NP; ++p)
+              cw[(jj + 1) & 1][p] = __ldcg(reinterpret_cast<const uint4*>(cpn + p * nbn * kL3SlotBytes));
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t bi = bbase ^ (uint32_t)(4 * (8 * jj + i));
+            const uint32_t sel = 0x7604u | ((uint32_t)(i & 3) << 4);
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+              const uint4 v = cw[jj & 1][p];
+              const uint32_t aP = lut_prmt(i < 4 ? v.x : v.y, bi, sel);
+              const uint32_t aQ = lut_prmt(i < 4 ? v.z : v.w, bi, sel);
+              lut_add(acc[0][p][0], acc[0][p][1], lut_lds<lut_imm<M, 0>()>(aP));
+              lut_add(acc[0][p][2], acc[0][p][3], lut_lds<lut_imm<M, 0>()>(aQ));
+              if constexpr (M > 1) {
+                lut_add(acc[1][p][0], acc[1][p][1], lut_lds<lut_imm<M, 1>()>(aP));
+                lut_add(acc[1][p][2], acc[1][p][3], lut_lds<lut_imm<M, 1>()>(aQ));
+              }
+              if constexpr (M > 2) {
+                lut_add(acc[2][p][0], acc[2][p][1], lut_lds<lut_imm<M, 2>()>(aP));
+                lut_add(acc[2][p][2], acc[2][p][3], lut_lds<lut_imm<M, 2>()>(aQ));
+              }
+              if constexpr (M > 3) {
+                lut_add(acc[3][p][0], acc[3][p][1], lut_lds<lut_imm<M, 3>()>(aP));
+                lut_add(acc[3][p][2], acc[3][p][3], lut_lds<lut_imm<M, 3>()>(aQ));
+              }
+            }
+          }
+        }
+      }
+      // the next unit's first slot went to buffer nb & 1; it is read from buffer 0
+      if (nb & 1) {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) cw[0][p] = cw[1][p];
+      }
+
+      // epilogue: A_re = (P + Q) / 2, A_im = (P - Q) / 2 per plane, the row's
+      // axis scales, then the window's 2^e (the 1/2 folded in)
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      float yre[M], yim[M];
+#pragma unroll
+      for (int t = 0; t < M; ++t) yre[t] = yim[t] = 0.0f;
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        const int X = p / T;
+        const float s_re = sscale[(2 * p) * 32 + lane], s_im = sscale[(2 * p + 1) * 32 + lane];
+#pragma unroll
+        for (int t = 0; t < M; ++t) {
+          const float ra = acc[t][p][0] + acc[t][p][2], rb = acc[t][p][1] + acc[t][p][3];  // 2 A_re
+          const float ia = acc[t][p][0] - acc[t][p][2], ib = acc[t][p][1] - acc[t][p][3];  // 2 A_im
+          if (X == 0) {
+            yre[t] += s_re * ra - s_im * ib;
+            yim[t] += s_re * rb + s_im * ia;
+          } else {
+            yre[t] += s_re * ra + s_im * ib;
+            yim[t] += -s_re * rb + s_im * ia;
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < M; ++t) {
+        const float f = 0.5f * s_pow[s][t];
+        yre[t] *= f;
+        yim[t] *= f;
+      }
+      const int64_t n2 = 2 * (int64_t)L.n;
+      if (L.windows == 1) {
+        if (row_in)
+#pragma unroll
+          for (int t = 0; t < M; ++t) {
+            L.y[t * n2 + j] = yre[t];
+            L.y[t * n2 + L.n + j] = yim[t];
+          }
+      } else {  // a partial output; the tile's counter is taken after the warp's last unit
+        float2* part = P.partials + L.part_begin;
+#pragma unroll
+        for (int t = 0; t < M; ++t)
+          __stcg(part + (((int64_t)w * L.tiles + tau) * M + t) * 32 + lane, make_float2(yre[t], yim[t]));
+      }
+      __syncwarp();  // the scale buffer is refilled for the next unit
+      uu = un;
+      s = sn;
+      nb = nbn;
+      cp = cpn;
+    }
+    // Row tiles finished: one fence for all of the warp's partial outputs, then
+    // the counters of up to 32 units at once (lane k takes the warp's k-th
+    // unit); the last window to arrive at a tile sums its partials in window
+    // order and writes y.
+    const int nunits = ue > ub + warp ? (ue - ub - warp + kLutWarps - 1) / kLutWarps : 0;
+    if (nunits > 0) {
+      __threadfence();  // each lane's partial outputs, then all lanes past this point
+      __syncwarp();
+    }
+    for (int k0 = 0; k0 < nunits; k0 += 32) {
+      bool last = false;
+      if (k0 + lane < nunits) {
+        const int uk = ub + warp + (k0 + lane) * kLutWarps;
+        int sk = 0;
+#pragma unroll
+        for (int k = 1; k < S; ++k)
+          if (k < nseg && uk >= s_unit[k]) sk = k;
+        const LutProblem& L = P.p[s_prob[sk]];
+        if (L.windows > 1) {
+          const int tau = uk - L.unit_begin - s_win[sk] * L.tiles;
+          last = atomicAdd(P.counters + L.ctr_begin + tau, 1u) == (unsigned)(L.windows - 1);
+        }
+      }
+      unsigned lastmask = __ballot_sync(0xffffffffu, last);
+      if (lastmask) __threadfence();
+      while (lastmask) {
+        const int k = __ffs(lastmask) - 1;
+        lastmask &= lastmask - 1;
+        const int uk = ub + warp + (k0 + k) * kLutWarps;
+        int sk = 0;
+#pragma unroll
+        for (int kk = 1; kk < S; ++kk)
+          if (kk < nseg && uk >= s_unit[kk]) sk = kk;
+        const LutProblem& L = P.p[s_prob[sk]];
+        const int tau = uk - L.unit_begin - s_win[sk] * L.tiles;
+        const int64_t j = 32 * (int64_t)tau + lane, n2 = 2 * (int64_t)L.n;
+        const float2* part = P.partials + L.part_begin;
+#pragma unroll
+        for (int t = 0; t < M; ++t) {
+          // window order; eight independent loads in flight at a time
+          float sr = 0.0f, si = 0.0f;
+          for (int w0 = 0; w0 < L.windows; w0 += 8) {
+            float2 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              v[k] = w0 + k < L.windows ? __ldcg(part + (((int64_t)(w0 + k) * L.tiles + tau) * M + t) * 32 + lane)
+                                        : make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (w0 + k < L.windows) {
+                sr += v[k].x;
+                si += v[k].y;
+              }
+          }
+          if (j < L.n) {
+            L.y[t * n2 + j] = sr;
+            L.y[t * n2 + L.n + j] = si;
+          }
+        }
+        if (lane == 0) atomicExch(P.counters + L.ctr_begin + tau, 0u);  // ready for the next launch
+      }
+    }
+    u = ue;
+    if (u < u_end) __syncthreads();  // the tables are rebuilt for the next segments
+  }
+}
+
+// Canonical codes of a layout-3 layer: out[plane][j][k] = 2 imag + sign.
+__global__ void __launch_bounds__(256) unpack_codes_l3_kernel(const uint8_t* __restrict__ codes, int64_t n, int64_t m,
+                                                              int T, uint8_t* __restrict__ out) {
+  const int64_t G = (m + 7) / 8;
+  const int64_t total = 2 * (int64_t)T * n * G;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int64_t plane = idx / (n * G);
+    const int64_t rem = idx - plane * n * G;
+    const int64_t j = rem / G, g8 = rem - (rem / G) * G;
+    const int64_t win = g8 >> 5;
+    const int g = (int)(g8 & 31), r = (int)(j & 31), nb = l3_slots(m, win);
+    const uint8_t* c = codes + l3_offset(n, m, T, win, j >> 5, (int)plane) + l3_slot_of(g, r, nb) * kL3SlotBytes +
+                       r * 16 + l3_byte_of(g, r);
+    const uint32_t s = c[0], q = c[8];
+    uint8_t* dst = out + (plane * n + j) * m + 8 * g8;
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+      if (8 * g8 + b < m) dst[b] = (uint8_t)(2u * (((s ^ q) >> b) & 1u) + ((s >> b) & 1u));
+  }
+}
+
+}  // namespace f2i

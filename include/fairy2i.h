@@ -47,6 +47,7 @@ typedef enum {
 } fairy2i_status;
 
 #define FAIRY2I_LAYOUT_VERSION 2
+#define FAIRY2I_LAYOUT_LUT 3
 #define FAIRY2I_MAX_T 8
 #define FAIRY2I_MAX_M 16384
 
@@ -70,9 +71,25 @@ typedef enum {
  *   bytes per lane).  Padding rows and columns hold zero bits.  The layout is
  *   opaque to callers; fairy2i_unpack_codes() gives the canonical view.
  * scales: fairy2i_scales_count(n, T) floats, [2 (U, W)][T][2 (real axis,
- *   imaginary axis)][n], 16-byte aligned. */
+ *   imaginary axis)][n], 16-byte aligned.
+ *
+ * codes, FAIRY2I_LAYOUT_LUT (version 3), the table-lookup decode layout:
+ *   fairy2i_codes_bytes_layout(n, m, T, 3) bytes, 256-byte aligned.  Per
+ *   (row, group of 8 columns) a sign byte (bit c: the code of column 8 G + c
+ *   is -1 or -i) and a q byte (sign XOR imaginary-axis flag).  Rows in tiles
+ *   of 32 (row 32 tau + r), columns in windows of 256; a window stores nb
+ *   slots of 512 bytes (nb = 4, or 1, 2 or 4 for a last partial window; 3 is
+ *   padded to 4), each 32 rows x (8 sign bytes, 8 q bytes).  Byte i of row r
+ *   in slot jj holds group (r & (8 nb - 1)) ^ (8 jj + i) of the window.
+ *   Order: [window][row tile][plane (X * T + t)][slot][row][16 bytes], so
+ *   window w, tile tau, plane p starts at byte w * tiles * 2T * 2048 +
+ *   (tau * 2T + p) * nb * 512.  Padding rows and columns hold zero bits.
+ *   Scales as for version 2.  Read by the table-lookup decode
+ *   (FAIRY2I_ALGO_LUT, through fairy2i_linear_ws / fairy2i_linear_group_ws)
+ *   and by fairy2i_unpack_codes; written by fairy2i_quantize and
+ *   fairy2i_convert_quantize when out->version is 3. */
 typedef struct {
-    int32_t version; /* must be FAIRY2I_LAYOUT_VERSION */
+    int32_t version; /* FAIRY2I_LAYOUT_VERSION (2) or FAIRY2I_LAYOUT_LUT (3) */
     int32_t T;       /* number of residual stages, 1..FAIRY2I_MAX_T */
     int64_t n;       /* complex output rows (real rows 2n) */
     int64_t m;       /* complex input columns (real columns 2m), 1..FAIRY2I_MAX_M */
@@ -86,12 +103,20 @@ typedef enum {
     FAIRY2I_ALGO_ADDSUB = 1,  /* CUDA cores: adds/subtracts only, fp32 accumulation */
     FAIRY2I_ALGO_MMA = 2,     /* decode: 2:4-sparse mma.sync, signs as bf16 +-2, axis flags as metadata */
     FAIRY2I_ALGO_TCGEN05 = 3, /* prefill: codes expanded to bf16 in shared memory, tcgen05.mma */
-    FAIRY2I_ALGO_TCGEN05_SP = 4 /* decode, M <= 8, T <= 4: 2:4-sparse tcgen05.mma.sp (e4m3 signs and axis
+    FAIRY2I_ALGO_TCGEN05_SP = 4, /* decode, M <= 8, T <= 4: 2:4-sparse tcgen05.mma.sp (e4m3 signs and axis
                                    flags as metadata in tensor memory; x as two exact e4m3 terms) */
+    FAIRY2I_ALGO_LUT = 5      /* layout 3, T <= 4: per window of 256 columns and token, tables of the
+                                 256 signed sums of every 8 activations (fp16 entries, each the fp32 sum
+                                 rounded once, activations scaled by a power of two per window); per
+                                 code byte one shared-memory lookup and two fp32 adds */
 } fairy2i_algo;
 
-/* Bytes of the code planes of an n x m layer with T stages (0 on bad input). */
+/* Bytes of the code planes of an n x m layer with T stages in layout
+ * version 2 (0 on bad input). */
 size_t fairy2i_codes_bytes(int64_t n, int64_t m, int32_t T);
+
+/* Bytes of the code planes in layout `version` (2 or 3); 0 on bad input. */
+size_t fairy2i_codes_bytes_layout(int64_t n, int64_t m, int32_t T, int32_t version);
 
 /* Number of fp32 scales, 4 * T * n (0 on bad input). */
 size_t fairy2i_scales_count(int64_t n, int32_t T);
@@ -162,6 +187,44 @@ fairy2i_status fairy2i_linear_ex(const fairy2i_packed *q, const void *x, int64_t
 fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const *xs,
                                     float *const *ys, int32_t count, int64_t M,
                                     fairy2i_algo algo, void *stream);
+
+/* The layer through the table-lookup decode (same y as fairy2i_linear; "Fairy2i:
+ * Ultra-Low-Bit ...", "Industry implications: multiplication-free inference":
+ * each code contributes a signed activation, here eight codes at a time read
+ * from a table of signed sums).  For layout-3 descriptors (all layers of a
+ * group the same layout and T <= 4); layout-2 descriptors are evaluated as by
+ * fairy2i_linear_ex / fairy2i_linear_group and the workspace is unused.
+ *   workspace : device, caller-owned, at least
+ *               fairy2i_linear_workspace_bytes(qs, count, M) bytes, 256-byte
+ *               aligned, ALL ZERO before its first use (e.g. cudaMemset once);
+ *               every call leaves it zero again.  It holds one counter per
+ *               32-row tile and one partial output per (row, window of 256
+ *               columns, token); the last window to finish a tile sums the
+ *               partials in window order, so results are deterministic.  Calls
+ *               that may run at the same time need separate workspaces.
+ *               NULL is allowed when the size query returns 0 (every layer
+ *               has m <= 256).
+ * Tokens go in launches of up to 4 (T <= 2), 2 (T = 3) or 1 (T = 4); each
+ * launch streams the codes once.  Precision: each table entry is the fp32 sum
+ * of 8 scaled activations rounded once to fp16 (relative error <= 2^-11 per
+ * entry), accumulated in fp32; outputs agree with the exact sum to about
+ * 3e-4 relative (L2) for Gaussian activations.  A token with a non-finite
+ * activation gives non-finite outputs.
+ * Errors: as fairy2i_linear_ex; INVALID_ARG for a missing, short or
+ * misaligned workspace; UNSUPPORTED for layout 3 with another algo than AUTO
+ * or LUT, or T > 4. */
+fairy2i_status fairy2i_linear_ws(const fairy2i_packed *q, const void *x, int64_t M, float *y,
+                                 fairy2i_algo algo, void *workspace, size_t workspace_bytes,
+                                 void *stream);
+fairy2i_status fairy2i_linear_group_ws(const fairy2i_packed *qs, const void *const *xs,
+                                       float *const *ys, int32_t count, int64_t M,
+                                       fairy2i_algo algo, void *workspace,
+                                       size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of fairy2i_linear_ws / fairy2i_linear_group_ws for these
+ * layers and token count: 0 if none is needed or the descriptors are not
+ * layout 3 (or invalid). */
+size_t fairy2i_linear_workspace_bytes(const fairy2i_packed *qs, int32_t count, int64_t M);
 
 /* Input gradient of the layer for training through it with the
  * straight-through estimator ("Fairy2i: Ultra-Low-Bit ...", quantization-aware

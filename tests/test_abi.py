@@ -103,7 +103,8 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.fairy2i_linear(ctypes.byref(d), p, -1, p, None) == 2
     assert lib.fairy2i_linear(ctypes.byref(d), ctypes.c_void_p(258), 1, p, None) == 1
     assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 7, None) == 1
-    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 5, None) == 1
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 6, None) == 1
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 5, None) == 4  # the table lookup reads layout 3 only
     # the sparse tensor-core decode takes at most 8 tokens and 4 stages (checked before any launch)
     assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 9, p, 4, None) == 4
     t5 = _desc(T=5)
@@ -173,4 +174,63 @@ def test_python_wrappers_reject_host_tensors(lib):
     with pytest.raises(ValueError):
         f2i.linear_grad_x(q, torch.zeros((1, 8)))  # host tensor
     # the algorithm names map onto the header's fairy2i_algo values
-    assert f2i.ALGO == {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4}
+    assert f2i.ALGO == {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4, "lut": 5}
+
+
+def test_layout3_sizes(lib):
+    L3 = f2i.LAYOUT_LUT
+    # 2 bits per code for every LLaMA-2-7B projection (n a multiple of 32, m of 64)
+    for n, m in [(2048, 2048), (5504, 2048), (2048, 5504)]:
+        assert f2i.codes_bytes(n, m, 2, L3) == 2 * 2 * n * m // 4
+    # padding: rows to 32; a last partial window keeps 1, 2 or 4 blocks of 64 columns (3 -> 4)
+    assert f2i.codes_bytes(1, 1, 1, L3) == 2 * 512
+    assert f2i.codes_bytes(1, 129, 1, L3) == 2 * 512 * 4
+    assert f2i.codes_bytes(1, 100, 1, L3) == 2 * 512 * 2
+    assert f2i.codes_bytes(33, 256, 1, L3) == 2 * 2 * 512 * 4
+    assert f2i.codes_bytes(1, 257, 3, L3) == 6 * 512 * 5
+    assert f2i.codes_bytes(4, 4, 1, 7) == 0
+
+
+def test_layout3_workspace_bytes(lib):
+    """One counter per 32-row tile (a 256-byte block) and one float2 partial per
+    (row, window of 256 columns, token of a launch) for layers with several windows."""
+    def ws(descs, M):
+        arr = (f2i.PackedDesc * len(descs))(*descs)
+        return lib.fairy2i_linear_workspace_bytes(arr, len(descs), M)
+    L3 = f2i.LAYOUT_LUT
+    q = _desc(n=2048, m=2048, T=2, version=L3)
+    assert ws([q], 1) == 256 + 64 * 8 * 32 * 8
+    assert ws([q], 4) == 256 + 64 * 8 * 4 * 32 * 8
+    assert ws([q], 9) == ws([q], 4)  # launches of at most 4 tokens at T = 2 share it
+    assert ws([_desc(n=2048, m=2048, T=3, version=L3)], 9) == 256 + 64 * 8 * 2 * 32 * 8
+    assert ws([_desc(n=100, m=256, T=2, version=L3)], 1) == 0  # one window: written directly
+    assert ws([_desc(n=2048, m=2048, T=2)], 1) == 0  # layout 2
+    assert ws([q], 0) == 0
+
+
+def test_layout3_host_errors(lib):
+    p = ctypes.c_void_p(256)
+    L3 = f2i.LAYOUT_LUT
+    d = _desc(n=4, m=600, T=2, version=L3)
+    assert lib.fairy2i_linear(ctypes.byref(d), p, 1, p, None) == 4  # needs the workspace entry point
+    assert "workspace" in _err(lib)
+    assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 1, p, 0, None, 0, None) == 1  # workspace missing
+    assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 1, p, 0, p, 16, None) == 1  # workspace too small
+    assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 1, p, 0, ctypes.c_void_p(272), 1 << 20, None) == 1  # misaligned
+    assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 1, p, 2, p, 1 << 20, None) == 4  # mma does not read layout 3
+    t5 = _desc(n=4, m=600, T=5, version=L3)
+    assert lib.fairy2i_linear_ws(ctypes.byref(t5), p, 1, p, 0, p, 1 << 20, None) == 4
+    assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 0, p, 0, None, 0, None) == 0  # no tokens
+    descs = (f2i.PackedDesc * 2)(d, _desc(n=4, m=600, T=2))
+    arr = (ctypes.c_void_p * 2)(256, 512)
+    assert lib.fairy2i_linear_group_ws(descs, arr, arr, 2, 1, 0, p, 1 << 20, None) == 2  # mixed layouts
+    assert lib.fairy2i_linear_grad_x(ctypes.byref(d), p, 1, p, None) == 4  # the gradient reads layout 2
+
+
+def test_mma_decode_rejects_code_planes_beyond_32bit_offsets(lib):
+    """The mma decode addresses a layer's planes with 32-bit offsets: a layer whose
+    2T planes exceed 4 GB is refused on the host (AUTO takes the add/subtract path)."""
+    p = ctypes.c_void_p(256)
+    big = _desc(n=300000, m=16384, T=2)
+    assert lib.fairy2i_linear_ex(ctypes.byref(big), p, 1, p, 2, None) == 4
+    assert "32-bit" in _err(lib)

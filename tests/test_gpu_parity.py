@@ -229,12 +229,13 @@ def _oracle_rows(R, rows, T):
     return _oracle_layer(torch.from_numpy(Rs), T)
 
 
+@pytest.mark.parametrize("T", [1, 2, 3])
 @pytest.mark.parametrize("name,out_f,in_f", inputs.LLAMA2_7B_BLOCK[3:])  # o, gate, up, down
-def test_full_size_projection_sampled(name, out_f, in_f):
-    """LLaMA-2-7B-shaped projection at full size: codes and scales bit-exact
-    and outputs within the bar on sampled rows."""
+def test_full_size_projection_sampled(name, out_f, in_f, T):
+    """LLaMA-2-7B-shaped projection at full size, T = 1, 2, 3 (the stack's stage
+    counts): codes and scales bit-exact and outputs within the bar on sampled rows."""
     pi = [p[0] for p in inputs.LLAMA2_7B_BLOCK].index(name)
-    n, m, T = out_f // 2, in_f // 2, 2
+    n, m = out_f // 2, in_f // 2
     R = inputs.weight_R(2, pi, out_f, in_f)
     _, _, q = _gpu_layer(R, T)
     rows = _sample_rows(n, seed=pi)
@@ -251,24 +252,43 @@ def test_full_size_projection_sampled(name, out_f, in_f):
         assert rel_l2(got, want) <= REL_L2, algo
 
 
-def test_full_size_block_group_decode_sampled():
-    """The seven projections of a block in one grouped launch, M = 1."""
+@pytest.mark.parametrize("T", [1, 2, 3])
+def test_full_size_block_group_decode_sampled(T):
+    """The seven projections of a block in one grouped launch, M = 1, T = 1, 2, 3."""
     qs, xs, samples = [], [], []
     for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
         n = out_f // 2
         R = inputs.weight_R(2, pi, out_f, in_f)
-        _, _, q = _gpu_layer(R, 2)
+        q = f2i.convert_quantize(R.cuda(), T)
         qs.append(q)
         x = inputs.activations(2, pi, 1, in_f)
         xs.append(x.cuda())
         rows = _sample_rows(n, count=8, seed=pi)
-        _, _, qU, qW = _oracle_rows(R, rows, 2)
+        _, _, qU, qW = _oracle_rows(R, rows, T)
         samples.append((rows, oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x))))
     ys = f2i.linear_group(qs, xs)
     for q, y, (rows, want) in zip(qs, ys, samples):
         y = y.cpu().numpy()
         got = np.concatenate([y[:, rows], y[:, q.n + rows]], axis=1)
         assert rel_l2(got, want) <= REL_L2
+
+
+@pytest.mark.parametrize("M", [16, 32, 64])
+@pytest.mark.parametrize("name,out_f,in_f", [inputs.LLAMA2_7B_BLOCK[4], inputs.LLAMA2_7B_BLOCK[6]])  # gate, down
+def test_full_size_auto_batched_decode_sampled(name, out_f, in_f, M):
+    """Batched decode at M = 16, 32, 64 through AUTO on full-size gate and down
+    projections: the tcgen05 path with one partial 128-token tile at real m."""
+    pi = [p[0] for p in inputs.LLAMA2_7B_BLOCK].index(name)
+    n = out_f // 2
+    R = inputs.weight_R(3, pi, out_f, in_f)
+    q = f2i.convert_quantize(R.cuda(), 2)
+    rows = _sample_rows(n, count=12, seed=M + pi)
+    _, _, qU, qW = _oracle_rows(R, rows, 2)
+    x = inputs.activations(3, pi, M, in_f)
+    want = oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x))
+    y = f2i.linear(q, x.cuda()).cpu().numpy()
+    got = np.concatenate([y[:, rows], y[:, n + rows]], axis=1)
+    assert rel_l2(got, want) <= REL_L2
 
 
 @pytest.mark.parametrize("T,M", [(3, 6), (4, 8), (1, 5), (2, 7)])
