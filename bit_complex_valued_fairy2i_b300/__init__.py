@@ -205,9 +205,9 @@ _workspaces: dict = {}
 
 
 def workspace(qs, M: int, device, stream=None) -> torch.Tensor | None:
-    """The zeroed device workspace of the table-lookup decode for these layers and token
-    count, kept per (device, stream) and grown when a call needs more (None if none is
-    needed).  Calls on one stream run in order, so they can share it."""
+    """The device scratch of the table-lookup decode for these layers and token count,
+    kept per (device, stream) and grown when a call needs more (None if none is needed).
+    Calls on one stream run in order, so they can share it."""
     count = len(qs)
     descs = (PackedDesc * count)(*[q.desc() for q in qs])
     need = int(load_library().fairy2i_linear_workspace_bytes(descs, count, M))
@@ -217,7 +217,7 @@ def workspace(qs, M: int, device, stream=None) -> torch.Tensor | None:
     key = (dev.index if dev.index is not None else torch.cuda.current_device(), _stream(stream))
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < need:
-        ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
         _workspaces[key] = ws
     return ws
 

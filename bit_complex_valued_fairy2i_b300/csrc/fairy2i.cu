@@ -545,29 +545,41 @@ fairy2i_status launch_quantize(const float2* U, const float2* W, const float* R,
 // --- table-lookup decode (layout 3) ------------------------------------------
 
 // Layers of one launch: consecutive runs of at most kLutMaxGroup layers.
-// Workspace of a launch with mc tokens: one counter per row tile of every
-// layer with more than one window (256-byte aligned block), then a float2
-// partial output per (unit, token, row of the tile).
-size_t lut_launch_workspace(const fairy2i_packed* qs, int cnt, int mc, size_t* ctr_bytes) {
-  size_t ctr = 0, parts = 0;
+// Workspace of a launch with mc tokens: a float2 partial output per (unit,
+// token, row of the tile) of every layer with more than one window.
+size_t lut_launch_workspace(const fairy2i_packed* qs, int cnt, int mc) {
+  size_t parts = 0;
   for (int i = 0; i < cnt; ++i) {
     const int64_t tiles = f2i::l3_tiles(qs[i].n), windows = f2i::l3_windows(qs[i].m);
-    if (windows > 1) {
-      ctr += (size_t)tiles;
-      parts += (size_t)(tiles * windows) * (size_t)mc * 32;
-    }
+    if (windows > 1) parts += (size_t)(tiles * windows) * (size_t)mc * 32;
   }
-  const size_t cb = (ctr * sizeof(unsigned) + 255) & ~(size_t)255;
-  if (ctr_bytes) *ctr_bytes = cb;
-  return parts ? cb + parts * sizeof(float2) : (ctr ? cb : 0);
+  return parts * sizeof(float2);
 }
 
 size_t lut_workspace(const fairy2i_packed* qs, int count, int64_t M, int T) {
   const int mc = (int)std::min<int64_t>(M, f2i::lut_max_tokens(T));
   size_t need = 0;
   for (int p0 = 0; p0 < count; p0 += f2i::kLutMaxGroup)
-    need = std::max(need, lut_launch_workspace(qs + p0, std::min(f2i::kLutMaxGroup, count - p0), mc, nullptr));
+    need = std::max(need, lut_launch_workspace(qs + p0, std::min(f2i::kLutMaxGroup, count - p0), mc));
   return need;
+}
+
+// Launches a kernel as a programmatic dependent of the previous work in the
+// stream (it may start while that work finishes; its griddepcontrol.wait
+// orders everything that depends on it).
+template <typename Kernel, typename Params>
+cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Params& P) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, P);
 }
 
 template <int T, int M>
@@ -575,7 +587,8 @@ fairy2i_status launch_lut_t(const f2i::LutParams& P, int ctas, cudaStream_t s) {
   auto k = f2i::linear_lut_kernel<T, M>;
   fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(k), f2i::kLutSmemBytes, "table-lookup decode");
   if (st != FAIRY2I_OK) return st;
-  k<<<ctas, f2i::kLutThreads, f2i::kLutSmemBytes, s>>>(P);
+  const cudaError_t e = launch_pdl(k, dim3(ctas), dim3(f2i::kLutThreads), f2i::kLutSmemBytes, s, P);
+  if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "table-lookup decode launch: %s", cudaGetErrorString(e));
   return check_launch("table-lookup decode launch");
 }
 
@@ -614,18 +627,19 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
   const int mcmax = f2i::lut_max_tokens(T);
   std::unique_ptr<f2i::LutParams> holder(new f2i::LutParams);
   f2i::LutParams& P = *holder;
+  f2i::LutReduceParams RP;
   for (int p0 = 0; p0 < count; p0 += f2i::kLutMaxGroup) {
     const int cnt = std::min(f2i::kLutMaxGroup, count - p0);
     for (int64_t t0 = 0; t0 < M; t0 += mcmax) {
       const int mc = (int)std::min<int64_t>(mcmax, M - t0);
       memset(&P, 0, sizeof(P));
-      size_t cb = 0;
-      const size_t wsn = lut_launch_workspace(qs + p0, cnt, mc, &cb);
+      memset(&RP, 0, sizeof(RP));
+      const size_t wsn = lut_launch_workspace(qs + p0, cnt, mc);
       P.count = cnt;
       P.M = mc;
-      P.counters = wsn ? static_cast<unsigned*>(ws) : nullptr;
-      P.partials = wsn ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + cb) : nullptr;
-      int64_t units = 0, ctr = 0, part = 0;
+      P.partials = wsn ? static_cast<float2*>(ws) : nullptr;
+      RP.M = mc;
+      int64_t units = 0, part = 0, rrows = 0;
       for (int i = 0; i < cnt; ++i) {
         const fairy2i_packed& q = qs[p0 + i];
         f2i::LutProblem& L = P.p[i];
@@ -638,15 +652,22 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
         L.tiles = (int32_t)f2i::l3_tiles(q.n);
         L.windows = (int32_t)f2i::l3_windows(q.m);
         L.unit_begin = (int32_t)units;
-        L.ctr_begin = L.windows > 1 ? (int32_t)ctr : -1;
         L.part_begin = part;
         units += (int64_t)L.tiles * L.windows;
         if (L.windows > 1) {
-          ctr += L.tiles;
+          f2i::LutReduceProblem& Rp = RP.p[RP.count++];
+          Rp.y = L.y;
+          Rp.part = P.partials + part;
+          Rp.n = L.n;
+          Rp.tiles = L.tiles;
+          Rp.windows = L.windows;
+          Rp.row_begin = (int32_t)rrows;
+          rrows += 32 * (int64_t)L.tiles;
           part += (int64_t)L.tiles * L.windows * mc * 32;
         }
       }
-      if (units > INT32_MAX / 2) return fail(FAIRY2I_ERR_UNSUPPORTED, "too many units for one launch");
+      if (units > INT32_MAX / 2 || rrows > INT32_MAX / 8)
+        return fail(FAIRY2I_ERR_UNSUPPORTED, "too many units for one launch");
       P.total_units = (int32_t)units;
       const int ctas = (int)std::min<int64_t>({units, (int64_t)sm_count(), (int64_t)f2i::kLutMaxCtas});
       // cost-balanced split of the units, in order
@@ -673,6 +694,15 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
       P.cta_begin[ctas] = (int32_t)units;
       fairy2i_status st = launch_lut(P, T, mc, ctas, s);
       if (st != FAIRY2I_OK) return st;
+      if (RP.count > 0) {
+        RP.total_rows = (int32_t)rrows;
+        const int64_t work = rrows * mc;
+        const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 8 * (int64_t)sm_count()));
+        const cudaError_t e = launch_pdl(f2i::lut_reduce_kernel, dim3(rgrid), dim3(256), 0, s, RP);
+        if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "table-lookup reduction launch: %s", cudaGetErrorString(e));
+        st = check_launch("table-lookup reduction launch");
+        if (st != FAIRY2I_OK) return st;
+      }
     }
   }
   return ok();

@@ -25,11 +25,17 @@
 // Work: a unit is (layer, window, row tile) = 32 rows x 256 columns x 2T
 // planes.  Units are numbered window-major inside a layer and split evenly
 // (by slot count) over one CTA per SM.  A CTA builds the tables of the
-// windows its units touch, then its 16 warps take units in turn.  A unit's
-// fp32 accumulators become a partial output (scales applied) in the
-// caller's workspace; the last warp to finish a row tile (an atomic counter
-// per tile) adds the partials of all windows in window order and writes y.
-// Results are deterministic: every sum has a fixed order.
+// windows its units touch, then its 16 warps take units in turn, streaming
+// the codes through per-warp shared-memory rings (cp.async).  A unit's fp32
+// accumulators become a partial output (scales applied): written to y for a
+// layer of one window, otherwise to the caller's workspace, where a second
+// kernel adds the windows of every row in window order.  Results are
+// deterministic: every sum has a fixed order.
+//
+// Both kernels are launched as programmatic dependents of the previous
+// kernel in the stream: before griddepcontrol.wait a CTA only issues L2
+// prefetches of its codes (weights, never written by the decode); every read
+// of activations, codes into shared memory, and every write comes after it.
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -41,8 +47,7 @@ constexpr int kLutWarps = 16;
 constexpr int kLutThreads = kLutWarps * 32;
 constexpr int kLutMaxGroup = 32;
 constexpr int kLutMaxCtas = 1024;
-constexpr uint32_t kLutTableBase = 65536;          // shared address of the first 64 KB table region
-constexpr uint32_t kLutSmemBytes = 3u * 65536u;    // dynamic shared memory: covers [64 KB, 192 KB) for any base
+constexpr uint32_t kLutSmemBytes = 224u * 1024u;  // dynamic shared memory: covers [base, 224 KB) for any base
 
 // Largest token count of one launch for T stages (fp32 accumulators and the
 // double-buffered code words stay within 128 registers).
@@ -57,17 +62,31 @@ struct LutProblem {
   int32_t tiles;       // row tiles of 32 rows
   int32_t windows;     // column windows of 256
   int32_t unit_begin;  // first unit of the layer in the launch
-  int32_t ctr_begin;   // first row-tile counter in the workspace (layers with more than one window)
+  int32_t pad_;
   int64_t part_begin;  // first partial output (float2) in the workspace
 };
 
 struct LutParams {
   int32_t count, M, total_units, pad_;
-  unsigned* counters;
   float2* partials;
   LutProblem p[kLutMaxGroup];
   int32_t cta_begin[kLutMaxCtas + 1];
 };
+
+// The window-combining pass: one thread per (row of a 32-row tile, token) of
+// every layer with more than one window.
+struct LutReduceProblem {
+  float* y;
+  const float2* part;  // [window][tile][token][32]
+  int32_t n, tiles, windows, row_begin;  // row_begin: first padded row of the layer in the pass
+};
+struct LutReduceParams {
+  int32_t count, M, total_rows, pad_;
+  LutReduceProblem p[kLutMaxGroup];
+};
+
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t lut_prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -95,21 +114,63 @@ __device__ __forceinline__ int lut_problem_of(const LutParams& P, int u) {
   return pi;
 }
 
-// Table set z of a resident segment s and token t (M tokens per launch):
-// region z >> 1 (64 KB each, from kLutTableBase), half z & 1 (+128 bytes).
+// Shared-memory map: the warps' code rings from the bottom, the tables in the
+// top one (M <= 2) or two (M = 3, 4) 64 KB regions below 224 KB.  Table set z
+// of a resident segment s and token t: region z >> 1, half z & 1 (+128 bytes);
+// M = 1 keeps two windows (one region), M = 2 one window (both tokens in one
+// region), M = 3, 4 one window (four sets, two regions).
 template <int M>
-__host__ __device__ constexpr int lut_segments() { return M == 1 ? 4 : M == 2 ? 2 : 1; }
+__host__ __device__ constexpr uint32_t lut_table_base() { return M <= 2 ? 160u * 1024u : 96u * 1024u; }
 template <int M>
-__device__ __forceinline__ int lut_set(int s, int t) { return M == 1 ? s : M == 2 ? 2 * s + t : t; }
-// Shared-address part of set z that the lane's B word carries (bits 7 and
-// 16..23) and the part given as an immediate offset of the loads.
+__host__ __device__ constexpr int lut_segments() { return M == 1 ? 2 : 1; }
 template <int M>
-__device__ __forceinline__ uint32_t lut_b_bits(int s) {
-  return M == 1 ? (((uint32_t)s & 1u) << 7) | (((uint32_t)s >> 1) << 16) : M == 2 ? ((uint32_t)s << 16) : 0u;
-}
+__device__ __forceinline__ int lut_set(int s, int t) { return M == 1 ? s : t; }
+// Shared-address part of set z that the lane's B word carries (bit 7 = the
+// half) and the part given as an immediate offset of the loads.
+template <int M>
+__device__ __forceinline__ uint32_t lut_b_bits(int s) { return M == 1 ? ((uint32_t)s & 1u) << 7 : 0u; }
 template <int M, int t>
-__host__ __device__ constexpr uint32_t lut_imm() {
-  return M == 1 ? kLutTableBase : M == 2 ? kLutTableBase + 128u * t : kLutTableBase + 65536u * (t >> 1) + 128u * (t & 1);
+__host__ __device__ constexpr uint32_t lut_imm() { return lut_table_base<M>() + 65536u * (t >> 1) + 128u * (t & 1); }
+// Code ring of a warp: RING slots of 2T planes x 512 bytes (32 lanes x 16
+// bytes) filled by cp.async; a slot is refilled after the evaluation that
+// read it, so RING - 1 slots are in flight (at most 4 slots; the rings of the
+// 16 warps stay below the tables with 2 KB to spare for the base).
+__host__ __device__ constexpr uint32_t lut_slot_bytes(int T) { return 2u * T * 512u; }
+template <int T, int M>
+__host__ __device__ constexpr int lut_ring() {
+  return (lut_table_base<M>() - 2048u) / (kLutWarps * lut_slot_bytes(T)) >= 4
+             ? 4
+             : (int)((lut_table_base<M>() - 2048u) / (kLutWarps * lut_slot_bytes(T)));
+}
+
+// One slot (8 groups x 2T planes) of a unit: for step i the lane reads group
+// slot bj ^ 4 i of every plane's table (P from the sign byte, Q from the q byte).
+template <int T, int M>
+__device__ __forceinline__ void lut_slot(const uint4 (&c)[2 * T], uint32_t bj, float (&acc)[M][2 * T][4]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t bi = bj ^ (uint32_t)(4 * i);
+    const uint32_t sel = 0x7604u | ((uint32_t)(i & 3) << 4);
+#pragma unroll
+    for (int p = 0; p < 2 * T; ++p) {
+      const uint32_t aP = lut_prmt(i < 4 ? c[p].x : c[p].y, bi, sel);
+      const uint32_t aQ = lut_prmt(i < 4 ? c[p].z : c[p].w, bi, sel);
+      lut_add(acc[0][p][0], acc[0][p][1], lut_lds<lut_imm<M, 0>()>(aP));
+      lut_add(acc[0][p][2], acc[0][p][3], lut_lds<lut_imm<M, 0>()>(aQ));
+      if constexpr (M > 1) {
+        lut_add(acc[1][p][0], acc[1][p][1], lut_lds<lut_imm<M, 1>()>(aP));
+        lut_add(acc[1][p][2], acc[1][p][3], lut_lds<lut_imm<M, 1>()>(aQ));
+      }
+      if constexpr (M > 2) {
+        lut_add(acc[2][p][0], acc[2][p][1], lut_lds<lut_imm<M, 2>()>(aP));
+        lut_add(acc[2][p][2], acc[2][p][3], lut_lds<lut_imm<M, 2>()>(aQ));
+      }
+      if constexpr (M > 3) {
+        lut_add(acc[3][p][0], acc[3][p][1], lut_lds<lut_imm<M, 3>()>(aP));
+        lut_add(acc[3][p][2], acc[3][p][3], lut_lds<lut_imm<M, 3>()>(aQ));
+      }
+    }
+  }
 }
 
 // Builds the table of (window w of layer L, token t) into set z: warp h
@@ -117,7 +178,7 @@ __host__ __device__ constexpr uint32_t lut_imm() {
 // group S & (8 nb - 1): a partial window's groups are repeated over all 32
 // slots, so that the lanes that share a group read different banks.  Returns
 // the factor 2^e that undoes the activation scaling.
-__device__ __forceinline__ float lut_build(const LutProblem& L, int w, int t, int z) {
+__device__ __forceinline__ float lut_build(const LutProblem& L, int w, int t, int z, uint32_t tbase) {
   const int lane = threadIdx.x & 31, h = threadIdx.x >> 5;
   const int64_t m = L.m;
   const int grp = lane & (8 * l3_slots(m, w) - 1);
@@ -181,7 +242,7 @@ __device__ __forceinline__ float lut_build(const LutProblem& L, int w, int t, in
     qr[v] = ((v & 1) ? -a[2] : a[2]) + ((v & 2) ? -a[3] : a[3]) + hr;
     qi[v] = ((v & 1) ? -b[2] : b[2]) + ((v & 2) ? -b[3] : b[3]) + hi;
   }
-  const uint32_t set_addr = kLutTableBase + ((uint32_t)z >> 1) * 65536u + ((uint32_t)z & 1u) * 128u;
+  const uint32_t set_addr = tbase + ((uint32_t)z >> 1) * 65536u + ((uint32_t)z & 1u) * 128u;
 #pragma unroll
   for (int l = 0; l < 16; ++l) {
     const float er = pr[l & 3] + qr[l >> 2], ei = pi[l & 3] + qi[l >> 2];
@@ -197,20 +258,38 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
   extern __shared__ __align__(16) uint8_t lsm[];
   constexpr int NP = 2 * T;
   constexpr int S = lut_segments<M>();
+  constexpr int RING = lut_ring<T, M>();
+  constexpr uint32_t SLOT = lut_slot_bytes(T);
   __shared__ int s_nseg;
   __shared__ int s_unit[S + 1];  // unit range of each resident segment
   __shared__ int s_prob[S], s_win[S];
   __shared__ float s_pow[S][M];  // 2^e per (segment, token)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the table regions must lie inside this CTA's dynamic shared memory
+  // rings at [base, ...), tables at [lut_table_base, 224 KB): all inside this
+  // CTA's dynamic shared memory
   const uint32_t base = (uint32_t)__cvta_generic_to_shared(lsm);
-  if (base + (uint32_t)(kLutWarps * 2 * NP * 32 * 4) > kLutTableBase || base + kLutSmemBytes < kLutTableBase + 2u * 65536u) {
+  const uint32_t ring_base = (base + 15u) & ~15u;
+  if (base + kLutSmemBytes < 224u * 1024u || ring_base + kLutWarps * RING * SLOT > lut_table_base<M>()) {
     if (tid == 0) f2i_raise(kErrConfig);  // refuse rather than address memory outside the CTA's buffer
     return;
   }
+  const uint32_t ring0 = ring_base + (uint32_t)warp * RING * SLOT + (uint32_t)lane * 16u;
   const int u_end = P.cta_begin[blockIdx.x + 1];
   int u = P.cta_begin[blockIdx.x];
+  pdl_launch_dependents();
+  // before the dependency wait: only L2 prefetches of the first units' codes
+  // (warp w: unit u + w), which the previous kernels never write
+  if (lane == 0 && u + warp < u_end) {
+    const int uu = u + warp;
+    const LutProblem& L = P.p[lut_problem_of(P, uu)];
+    const int w = (uu - L.unit_begin) / L.tiles;
+    const uint8_t* cp0 = L.codes + l3_offset(L.n, L.m, T, w, uu - L.unit_begin - w * L.tiles, 0);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cp0),
+                 "r"((uint32_t)(NP * l3_slots(L.m, w)) * (uint32_t)kL3SlotBytes)
+                 : "memory");
+  }
+  pdl_wait();
   while (u < u_end) {
     if (tid == 0) {
       int s = 0, uu = u;
@@ -230,7 +309,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
     __syncthreads();
     const int nseg = s_nseg;
     const int ub = s_unit[0], ue = s_unit[nseg];
-    // a unit's codes (2T planes x nb slots, contiguous) as (pointer to lane 0's bytes, slots)
+    // a unit's codes (2T planes x nb slots, contiguous): pointer to lane 0's bytes
     auto unit_codes = [&](int uu, int& seg, int& nb) -> const uint8_t* {
       seg = 0;
 #pragma unroll
@@ -241,53 +320,49 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
       nb = l3_slots(L.m, w);
       return L.codes + l3_offset(L.n, L.m, T, w, uu - L.unit_begin - w * L.tiles, 0);
     };
-    // every unit this warp will take, into L2 now: HBM streams while the tables are built
-    if (lane == 0)
-      for (int uu = ub + warp; uu < ue; uu += kLutWarps) {
-        int sg, nbu;
-        const uint8_t* cp0 = unit_codes(uu, sg, nbu);
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cp0), "r"((uint32_t)(NP * nbu * kL3SlotBytes))
-                     : "memory");
+
+    // load cursor: the warp's units (ub + warp, + 16, ...) slot by slot into
+    // its ring, RING - 1 slots ahead of evaluation; every call commits one group
+    int lu = ub + warp, ljj = 0, lnb = 4, lseg = 0, lk = 0;
+    const uint8_t* lcp = lu < ue ? unit_codes(lu, lseg, lnb) + lane * 16 : nullptr;
+    auto issue = [&]() {
+      if (lcp != nullptr) {
+        const uint32_t dst = ring0 + (uint32_t)lk * SLOT;
+#pragma unroll
+        for (int p = 0; p < NP; ++p)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + (uint32_t)p * 512u),
+                       "l"(lcp + (p * lnb + ljj) * kL3SlotBytes)
+                       : "memory");
+        if (++ljj == lnb) {
+          ljj = 0;
+          lu += kLutWarps;
+          lcp = lu < ue ? unit_codes(lu, lseg, lnb) + lane * 16 : nullptr;
+        }
       }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      lk = lk + 1 == RING ? 0 : lk + 1;
+    };
+#pragma unroll
+    for (int r = 0; r < RING - 1; ++r) issue();  // HBM streams while the tables are built
+
     for (int s = 0; s < nseg; ++s) {
 #pragma unroll
       for (int t = 0; t < M; ++t) {
-        const float pw = lut_build(P.p[s_prob[s]], s_win[s], t, lut_set<M>(s, t));
+        const float pw = lut_build(P.p[s_prob[s]], s_win[s], t, lut_set<M>(s, t), lut_table_base<M>());
         if (tid == 0) s_pow[s][t] = pw;
       }
     }
     __syncthreads();
 
-    // this warp's scale buffer: [2T planes x 2 axes][32 rows] floats
-    float* sscale = reinterpret_cast<float*>(lsm) + warp * (2 * NP * 32);
-    const uint32_t sscale_addr = base + (uint32_t)(warp * 2 * NP * 32 + lane) * 4u;
-    uint4 cw[2][NP];
-    int uu = ub + warp, s = 0, nb = 4;
-    const uint8_t* cp = nullptr;
-    if (uu < ue) {
-      cp = unit_codes(uu, s, nb) + lane * 16;
-#pragma unroll
-      for (int p = 0; p < NP; ++p) cw[0][p] = __ldcg(reinterpret_cast<const uint4*>(cp + p * nb * kL3SlotBytes));
-    }
-    while (uu < ue) {
+    int ck = 0;  // ring slot evaluated next
+    for (int uu = ub + warp; uu < ue; uu += kLutWarps) {
+      int s, nb;
+      unit_codes(uu, s, nb);
       const int pi = s_prob[s], w = s_win[s];
       const LutProblem& L = P.p[pi];
       const int tau = uu - L.unit_begin - w * L.tiles;
       const int64_t j = 32 * (int64_t)tau + lane;
       const bool row_in = j < L.n;
-      // the row's scales into shared memory (zero past n), used by the epilogue
-#pragma unroll
-      for (int k = 0; k < 2 * NP; ++k) {
-        const float* src = row_in ? L.scales + (int64_t)k * L.n + j : L.scales;
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(sscale_addr + (uint32_t)k * 128u), "l"(src),
-                     "r"(row_in ? 4 : 0)
-                     : "memory");
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-      const int un = uu + kLutWarps;
-      int sn = 0, nbn = 4;
-      const uint8_t* cpn = un < ue ? unit_codes(un, sn, nbn) + lane * 16 : nullptr;
-      const uint32_t pstride = (uint32_t)nb * kL3SlotBytes;
       // slot lane ^ (8 jj + i): group (lane & (8 nb - 1)) ^ (8 jj + i), bank = slot
       const uint32_t bbase = 4u * (uint32_t)lane | lut_b_bits<M>(s);
 
@@ -296,63 +371,37 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
       for (int t = 0; t < M; ++t)
 #pragma unroll
         for (int p = 0; p < NP; ++p) acc[t][p][0] = acc[t][p][1] = acc[t][p][2] = acc[t][p][3] = 0.0f;
-
+      float sc[2 * NP];
+#pragma unroll 1
+      for (int jj = 0; jj < nb; ++jj) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(RING - 2) : "memory");
+        uint4 cw[NP];
+        const uint32_t src = ring0 + (uint32_t)ck * SLOT;
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        if (jj < nb) {
-          // next slot of this unit, or after the last slot the next unit's first
-          if (jj + 1 < nb) {
+        for (int p = 0; p < NP; ++p)
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(cw[p].x), "=r"(cw[p].y), "=r"(cw[p].z), "=r"(cw[p].w)
+                       : "r"(src + (uint32_t)p * 512u)
+                       : "memory");
+        ck = ck + 1 == RING ? 0 : ck + 1;
+        if (jj == nb - 1) {  // the row's scales, in flight while the last slot is evaluated
 #pragma unroll
-            for (int p = 0; p < NP; ++p)
-              cw[(jj + 1) & 1][p] = __ldcg(reinterpret_cast<const uint4*>(cp + p * pstride + (jj + 1) * kL3SlotBytes));
-          } else if (cpn != nullptr) {
-#pragma unroll
-            for (int p = 0; p < NP; ++p)
-              cw[(jj + 1) & 1][p] = __ldcg(reinterpret_cast<const uint4*>(cpn + p * nbn * kL3SlotBytes));
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t bi = bbase ^ (uint32_t)(4 * (8 * jj + i));
-            const uint32_t sel = 0x7604u | ((uint32_t)(i & 3) << 4);
-#pragma unroll
-            for (int p = 0; p < NP; ++p) {
-              const uint4 v = cw[jj & 1][p];
-              const uint32_t aP = lut_prmt(i < 4 ? v.x : v.y, bi, sel);
-              const uint32_t aQ = lut_prmt(i < 4 ? v.z : v.w, bi, sel);
-              lut_add(acc[0][p][0], acc[0][p][1], lut_lds<lut_imm<M, 0>()>(aP));
-              lut_add(acc[0][p][2], acc[0][p][3], lut_lds<lut_imm<M, 0>()>(aQ));
-              if constexpr (M > 1) {
-                lut_add(acc[1][p][0], acc[1][p][1], lut_lds<lut_imm<M, 1>()>(aP));
-                lut_add(acc[1][p][2], acc[1][p][3], lut_lds<lut_imm<M, 1>()>(aQ));
-              }
-              if constexpr (M > 2) {
-                lut_add(acc[2][p][0], acc[2][p][1], lut_lds<lut_imm<M, 2>()>(aP));
-                lut_add(acc[2][p][2], acc[2][p][3], lut_lds<lut_imm<M, 2>()>(aQ));
-              }
-              if constexpr (M > 3) {
-                lut_add(acc[3][p][0], acc[3][p][1], lut_lds<lut_imm<M, 3>()>(aP));
-                lut_add(acc[3][p][2], acc[3][p][3], lut_lds<lut_imm<M, 3>()>(aQ));
-              }
-            }
-          }
+          for (int k = 0; k < 2 * NP; ++k) sc[k] = row_in ? __ldg(L.scales + (int64_t)k * L.n + j) : 0.0f;
         }
-      }
-      // the next unit's first slot went to buffer nb & 1; it is read from buffer 0
-      if (nb & 1) {
-#pragma unroll
-        for (int p = 0; p < NP; ++p) cw[0][p] = cw[1][p];
+        lut_slot<T, M>(cw, bbase ^ (uint32_t)(32 * jj), acc);
+        // refill the slot read one evaluation earlier (its registers are consumed)
+        issue();
       }
 
       // epilogue: A_re = (P + Q) / 2, A_im = (P - Q) / 2 per plane, the row's
       // axis scales, then the window's 2^e (the 1/2 folded in)
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
       float yre[M], yim[M];
 #pragma unroll
       for (int t = 0; t < M; ++t) yre[t] = yim[t] = 0.0f;
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
         const int X = p / T;
-        const float s_re = sscale[(2 * p) * 32 + lane], s_im = sscale[(2 * p + 1) * 32 + lane];
+        const float s_re = sc[2 * p], s_im = sc[2 * p + 1];
 #pragma unroll
         for (int t = 0; t < M; ++t) {
           const float ra = acc[t][p][0] + acc[t][p][2], rb = acc[t][p][1] + acc[t][p][3];  // 2 A_re
@@ -380,82 +429,51 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
             L.y[t * n2 + j] = yre[t];
             L.y[t * n2 + L.n + j] = yim[t];
           }
-      } else {  // a partial output; the tile's counter is taken after the warp's last unit
+      } else {  // a partial output, combined over windows by lut_reduce_kernel
         float2* part = P.partials + L.part_begin;
 #pragma unroll
         for (int t = 0; t < M; ++t)
           __stcg(part + (((int64_t)w * L.tiles + tau) * M + t) * 32 + lane, make_float2(yre[t], yim[t]));
       }
-      __syncwarp();  // the scale buffer is refilled for the next unit
-      uu = un;
-      s = sn;
-      nb = nbn;
-      cp = cpn;
     }
-    // Row tiles finished: one fence for all of the warp's partial outputs, then
-    // the counters of up to 32 units at once (lane k takes the warp's k-th
-    // unit); the last window to arrive at a tile sums its partials in window
-    // order and writes y.
-    const int nunits = ue > ub + warp ? (ue - ub - warp + kLutWarps - 1) / kLutWarps : 0;
-    if (nunits > 0) {
-      __threadfence();  // each lane's partial outputs, then all lanes past this point
-      __syncwarp();
-    }
-    for (int k0 = 0; k0 < nunits; k0 += 32) {
-      bool last = false;
-      if (k0 + lane < nunits) {
-        const int uk = ub + warp + (k0 + lane) * kLutWarps;
-        int sk = 0;
-#pragma unroll
-        for (int k = 1; k < S; ++k)
-          if (k < nseg && uk >= s_unit[k]) sk = k;
-        const LutProblem& L = P.p[s_prob[sk]];
-        if (L.windows > 1) {
-          const int tau = uk - L.unit_begin - s_win[sk] * L.tiles;
-          last = atomicAdd(P.counters + L.ctr_begin + tau, 1u) == (unsigned)(L.windows - 1);
-        }
-      }
-      unsigned lastmask = __ballot_sync(0xffffffffu, last);
-      if (lastmask) __threadfence();
-      while (lastmask) {
-        const int k = __ffs(lastmask) - 1;
-        lastmask &= lastmask - 1;
-        const int uk = ub + warp + (k0 + k) * kLutWarps;
-        int sk = 0;
-#pragma unroll
-        for (int kk = 1; kk < S; ++kk)
-          if (kk < nseg && uk >= s_unit[kk]) sk = kk;
-        const LutProblem& L = P.p[s_prob[sk]];
-        const int tau = uk - L.unit_begin - s_win[sk] * L.tiles;
-        const int64_t j = 32 * (int64_t)tau + lane, n2 = 2 * (int64_t)L.n;
-        const float2* part = P.partials + L.part_begin;
-#pragma unroll
-        for (int t = 0; t < M; ++t) {
-          // window order; eight independent loads in flight at a time
-          float sr = 0.0f, si = 0.0f;
-          for (int w0 = 0; w0 < L.windows; w0 += 8) {
-            float2 v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              v[k] = w0 + k < L.windows ? __ldcg(part + (((int64_t)(w0 + k) * L.tiles + tau) * M + t) * 32 + lane)
-                                        : make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              if (w0 + k < L.windows) {
-                sr += v[k].x;
-                si += v[k].y;
-              }
-          }
-          if (j < L.n) {
-            L.y[t * n2 + j] = sr;
-            L.y[t * n2 + L.n + j] = si;
-          }
-        }
-        if (lane == 0) atomicExch(P.counters + L.ctr_begin + tau, 0u);  // ready for the next launch
-      }
-    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy outlives the batch
+
     u = ue;
     if (u < u_end) __syncthreads();  // the tables are rebuilt for the next segments
+  }
+}
+
+// Sums the partial outputs of every row over the layer's windows, in window
+// order, and writes y (eight independent loads in flight per thread).
+__global__ void __launch_bounds__(256) lut_reduce_kernel(const __grid_constant__ LutReduceParams R) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t total = (int64_t)R.total_rows * R.M;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (int64_t)gridDim.x * blockDim.x) {
+    const int row = (int)(idx / R.M), t = (int)(idx - (int64_t)row * R.M);
+    int pi = 0;
+    for (int i = 1; i < R.count; ++i)
+      if (row >= R.p[i].row_begin) pi = i;
+    const LutReduceProblem& L = R.p[pi];
+    const int r = row - L.row_begin, tau = r >> 5, lane = r & 31;
+    float sr = 0.0f, si = 0.0f;
+    for (int w0 = 0; w0 < L.windows; w0 += 8) {
+      float2 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        v[k] = w0 + k < L.windows ? __ldcg(L.part + (((int64_t)(w0 + k) * L.tiles + tau) * R.M + t) * 32 + lane)
+                                  : make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (w0 + k < L.windows) {
+          sr += v[k].x;
+          si += v[k].y;
+        }
+    }
+    if (r < L.n) {
+      L.y[(int64_t)t * 2 * L.n + r] = sr;
+      L.y[(int64_t)t * 2 * L.n + L.n + r] = si;
+    }
   }
 }
 

@@ -194,16 +194,17 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
  * from a table of signed sums).  For layout-3 descriptors (all layers of a
  * group the same layout and T <= 4); layout-2 descriptors are evaluated as by
  * fairy2i_linear_ex / fairy2i_linear_group and the workspace is unused.
- *   workspace : device, caller-owned, at least
+ *   workspace : device, caller-owned scratch of at least
  *               fairy2i_linear_workspace_bytes(qs, count, M) bytes, 256-byte
- *               aligned, ALL ZERO before its first use (e.g. cudaMemset once);
- *               every call leaves it zero again.  It holds one counter per
- *               32-row tile and one partial output per (row, window of 256
- *               columns, token); the last window to finish a tile sums the
- *               partials in window order, so results are deterministic.  Calls
- *               that may run at the same time need separate workspaces.
- *               NULL is allowed when the size query returns 0 (every layer
- *               has m <= 256).
+ *               aligned, any contents (no initialisation needed).  It holds
+ *               one fp32 partial output per (row, window of 256 columns,
+ *               token); a second kernel sums every row's partials in window
+ *               order, so results are deterministic.  Calls that may run at
+ *               the same time need separate workspaces.  NULL is allowed when
+ *               the size query returns 0 (every layer has m <= 256).
+ * Both kernels are launched as programmatic dependents of the preceding work
+ * in the stream (they may start while it finishes and wait for it before
+ * reading activations or writing anything).
  * Tokens go in launches of up to 4 (T <= 2), 2 (T = 3) or 1 (T = 4); each
  * launch streams the codes once.  Precision: each table entry is the fp32 sum
  * of 8 scaled activations rounded once to fp16 (relative error <= 2^-11 per

@@ -192,17 +192,17 @@ def test_layout3_sizes(lib):
 
 
 def test_layout3_workspace_bytes(lib):
-    """One counter per 32-row tile (a 256-byte block) and one float2 partial per
-    (row, window of 256 columns, token of a launch) for layers with several windows."""
+    """One float2 partial output per (row of a 32-row tile, window of 256 columns,
+    token of a launch) for the layers with several windows."""
     def ws(descs, M):
         arr = (f2i.PackedDesc * len(descs))(*descs)
         return lib.fairy2i_linear_workspace_bytes(arr, len(descs), M)
     L3 = f2i.LAYOUT_LUT
     q = _desc(n=2048, m=2048, T=2, version=L3)
-    assert ws([q], 1) == 256 + 64 * 8 * 32 * 8
-    assert ws([q], 4) == 256 + 64 * 8 * 4 * 32 * 8
+    assert ws([q], 1) == 64 * 8 * 32 * 8
+    assert ws([q], 4) == 64 * 8 * 4 * 32 * 8
     assert ws([q], 9) == ws([q], 4)  # launches of at most 4 tokens at T = 2 share it
-    assert ws([_desc(n=2048, m=2048, T=3, version=L3)], 9) == 256 + 64 * 8 * 2 * 32 * 8
+    assert ws([_desc(n=2048, m=2048, T=3, version=L3)], 9) == 64 * 8 * 2 * 32 * 8
     assert ws([_desc(n=100, m=256, T=2, version=L3)], 1) == 0  # one window: written directly
     assert ws([_desc(n=2048, m=2048, T=2)], 1) == 0  # layout 2
     assert ws([q], 0) == 0

@@ -206,15 +206,15 @@ def test_lut_zero_tokens_zero_input_and_nonfinite():
 
 def test_lut_deterministic_and_workspace_reuse():
     """Repeated calls with one workspace: bit-identical outputs (fixed summation
-    order; the row-tile counters are back at zero after every call)."""
+    order), whatever the workspace held before (it needs no initialisation)."""
     R = _R(300, 1500, 4)
     q = _gpu_layer(R, 2)
     x = _x(3, 1500, 4).cuda()
     ws = f2i.workspace([q], 3, "cuda")
     y0 = f2i.linear(q, x, ws=ws)
-    for _ in range(5):
+    for fill in (0x00, 0xFF, 0x7F):
+        ws.fill_(fill)
         assert torch.equal(f2i.linear(q, x, ws=ws), y0)
-    assert not torch.any(ws[:256])  # counters
 
 
 def test_lut_group_equals_single_launches():
