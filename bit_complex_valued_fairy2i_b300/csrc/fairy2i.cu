@@ -666,7 +666,7 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
           part += (int64_t)L.tiles * L.windows * mc * 32;
         }
       }
-      if (units > INT32_MAX / 2 || rrows > INT32_MAX / 8)
+      if (units > INT32_MAX / 2 || rrows > INT32_MAX / 32)
         return fail(FAIRY2I_ERR_UNSUPPORTED, "too many units for one launch");
       P.total_units = (int32_t)units;
       const int ctas = (int)std::min<int64_t>({units, (int64_t)sm_count(), (int64_t)f2i::kLutMaxCtas});
@@ -692,11 +692,17 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
       }
       while (c < ctas) P.cta_begin[c++] = (int32_t)units;
       P.cta_begin[ctas] = (int32_t)units;
+      for (int cc = 0, i = 0; cc < ctas; ++cc) {  // first (layer, window) of every range
+        const int ub = std::min<int>(P.cta_begin[cc], (int)units - 1);
+        while (i + 1 < cnt && ub >= P.p[i + 1].unit_begin) ++i;
+        P.first_prob[cc] = (uint8_t)i;
+        P.first_win[cc] = (uint16_t)((ub - P.p[i].unit_begin) / P.p[i].tiles);
+      }
       fairy2i_status st = launch_lut(P, T, mc, ctas, s);
       if (st != FAIRY2I_OK) return st;
       if (RP.count > 0) {
         RP.total_rows = (int32_t)rrows;
-        const int64_t work = rrows * mc;
+        const int64_t work = rrows * mc * 4;
         const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 8 * (int64_t)sm_count()));
         const cudaError_t e = launch_pdl(f2i::lut_reduce_kernel, dim3(rgrid), dim3(256), 0, s, RP);
         if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "table-lookup reduction launch: %s", cudaGetErrorString(e));

@@ -19,8 +19,9 @@
 // owns row r of a 32-row tile; at each byte position of layout 3 the 32 rows
 // name 32 different groups, so the 32 lanes hit 32 different banks.  The
 // activations of a table are scaled by a power of two (the window maximum
-// lands in [2^11, 2^12)) so that every entry is a normal fp16 number; each
-// entry is the fp32 sum of its 8 terms rounded once to fp16.
+// lands in [2^10, 2^11)) so that every entry is a normal fp16 number; each
+// entry is the fp32 sum of its 8 terms rounded once to fp16, and the entries
+// of two consecutive groups are added in fp16 before the fp32 accumulation.
 //
 // Work: a unit is (layer, window, row tile) = 32 rows x 256 columns x 2T
 // planes.  Units are numbered window-major inside a layer and split evenly
@@ -46,7 +47,7 @@ namespace f2i {
 constexpr int kLutWarps = 16;
 constexpr int kLutThreads = kLutWarps * 32;
 constexpr int kLutMaxGroup = 32;
-constexpr int kLutMaxCtas = 1024;
+constexpr int kLutMaxCtas = 256;
 constexpr uint32_t kLutSmemBytes = 224u * 1024u;  // dynamic shared memory: covers [base, 224 KB) for any base
 
 // Largest token count of one launch for T stages (fp32 accumulators and the
@@ -71,6 +72,10 @@ struct LutParams {
   float2* partials;
   LutProblem p[kLutMaxGroup];
   int32_t cta_begin[kLutMaxCtas + 1];
+  // the first (layer, window) of every CTA's range (the second segment, if
+  // any, is the next window): known before any device work
+  uint8_t first_prob[kLutMaxCtas];
+  uint16_t first_win[kLutMaxCtas];
 };
 
 // The window-combining pass: one thread per (row of a 32-row tile, token) of
@@ -98,6 +103,12 @@ __device__ __forceinline__ uint32_t lut_lds(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF));
   return v;
+}
+// fp16x2 sum of two table entries (one rounding per half)
+__device__ __forceinline__ uint32_t lut_hadd2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 // acc_re += lo(e), acc_im += hi(e): fp16 table entry added in fp32 (one rounding each)
 __device__ __forceinline__ void lut_add(float& re, float& im, uint32_t e) {
@@ -144,30 +155,34 @@ __host__ __device__ constexpr int lut_ring() {
 }
 
 // One slot (8 groups x 2T planes) of a unit: for step i the lane reads group
-// slot bj ^ 4 i of every plane's table (P from the sign byte, Q from the q byte).
+// slot bj ^ 4 i of every plane's table (P from the sign byte, Q from the q
+// byte).  The entries of steps 2 k and 2 k + 1 are added in fp16 (one
+// rounding; the activation scaling keeps the sum below 2^15) and the sum is
+// added to the fp32 accumulators.
 template <int T, int M>
 __device__ __forceinline__ void lut_slot(const uint4 (&c)[2 * T], uint32_t bj, float (&acc)[M][2 * T][4]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t bi = bj ^ (uint32_t)(4 * i);
-    const uint32_t sel = 0x7604u | ((uint32_t)(i & 3) << 4);
+  for (int i = 0; i < 8; i += 2) {
+    const uint32_t b0 = bj ^ (uint32_t)(4 * i), b1 = bj ^ (uint32_t)(4 * (i + 1));
+    const uint32_t sel0 = 0x7604u | ((uint32_t)(i & 3) << 4), sel1 = 0x7604u | ((uint32_t)((i + 1) & 3) << 4);
 #pragma unroll
     for (int p = 0; p < 2 * T; ++p) {
-      const uint32_t aP = lut_prmt(i < 4 ? c[p].x : c[p].y, bi, sel);
-      const uint32_t aQ = lut_prmt(i < 4 ? c[p].z : c[p].w, bi, sel);
-      lut_add(acc[0][p][0], acc[0][p][1], lut_lds<lut_imm<M, 0>()>(aP));
-      lut_add(acc[0][p][2], acc[0][p][3], lut_lds<lut_imm<M, 0>()>(aQ));
+      const uint32_t ws = i < 4 ? c[p].x : c[p].y, wq = i < 4 ? c[p].z : c[p].w;
+      const uint32_t aP0 = lut_prmt(ws, b0, sel0), aP1 = lut_prmt(ws, b1, sel1);
+      const uint32_t aQ0 = lut_prmt(wq, b0, sel0), aQ1 = lut_prmt(wq, b1, sel1);
+      lut_add(acc[0][p][0], acc[0][p][1], lut_hadd2(lut_lds<lut_imm<M, 0>()>(aP0), lut_lds<lut_imm<M, 0>()>(aP1)));
+      lut_add(acc[0][p][2], acc[0][p][3], lut_hadd2(lut_lds<lut_imm<M, 0>()>(aQ0), lut_lds<lut_imm<M, 0>()>(aQ1)));
       if constexpr (M > 1) {
-        lut_add(acc[1][p][0], acc[1][p][1], lut_lds<lut_imm<M, 1>()>(aP));
-        lut_add(acc[1][p][2], acc[1][p][3], lut_lds<lut_imm<M, 1>()>(aQ));
+        lut_add(acc[1][p][0], acc[1][p][1], lut_hadd2(lut_lds<lut_imm<M, 1>()>(aP0), lut_lds<lut_imm<M, 1>()>(aP1)));
+        lut_add(acc[1][p][2], acc[1][p][3], lut_hadd2(lut_lds<lut_imm<M, 1>()>(aQ0), lut_lds<lut_imm<M, 1>()>(aQ1)));
       }
       if constexpr (M > 2) {
-        lut_add(acc[2][p][0], acc[2][p][1], lut_lds<lut_imm<M, 2>()>(aP));
-        lut_add(acc[2][p][2], acc[2][p][3], lut_lds<lut_imm<M, 2>()>(aQ));
+        lut_add(acc[2][p][0], acc[2][p][1], lut_hadd2(lut_lds<lut_imm<M, 2>()>(aP0), lut_lds<lut_imm<M, 2>()>(aP1)));
+        lut_add(acc[2][p][2], acc[2][p][3], lut_hadd2(lut_lds<lut_imm<M, 2>()>(aQ0), lut_lds<lut_imm<M, 2>()>(aQ1)));
       }
       if constexpr (M > 3) {
-        lut_add(acc[3][p][0], acc[3][p][1], lut_lds<lut_imm<M, 3>()>(aP));
-        lut_add(acc[3][p][2], acc[3][p][3], lut_lds<lut_imm<M, 3>()>(aQ));
+        lut_add(acc[3][p][0], acc[3][p][1], lut_hadd2(lut_lds<lut_imm<M, 3>()>(aP0), lut_lds<lut_imm<M, 3>()>(aP1)));
+        lut_add(acc[3][p][2], acc[3][p][3], lut_hadd2(lut_lds<lut_imm<M, 3>()>(aQ0), lut_lds<lut_imm<M, 3>()>(aQ1)));
       }
     }
   }
@@ -214,11 +229,13 @@ __device__ __forceinline__ float lut_build(const LutProblem& L, int w, int t, in
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  // e: mx 2^-e in [2^11, 2^12); clamped so that 2^-e and 2^e are normal floats
+  // e: mx 2^-e in [2^10, 2^11), so an entry (8 terms) stays below 2^14 and
+  // the fp16 sum of two entries below 2^15; clamped so that 2^-e and 2^e are
+  // normal floats
   int e = 0;
   if (mx > 0.0f) {
     const int ex = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // a subnormal maximum gives -127, then the clamp
-    e = max(ex - 11, -126);
+    e = max(ex - 10, -126);
   }
   const float down = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
 #pragma unroll
@@ -262,8 +279,9 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
   constexpr uint32_t SLOT = lut_slot_bytes(T);
   __shared__ int s_nseg;
   __shared__ int s_unit[S + 1];  // unit range of each resident segment
-  __shared__ int s_prob[S], s_win[S];
-  __shared__ float s_pow[S][M];  // 2^e per (segment, token)
+  __shared__ int s_prob[S], s_win[S], s_tau0[S], s_nb[S];
+  __shared__ const uint8_t* s_codes[S];  // codes of the segment's first unit
+  __shared__ float s_pow[S][M];          // 2^e per (segment, token)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // rings at [base, ...), tables at [lut_table_base, 224 KB): all inside this
@@ -278,16 +296,31 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
   const int u_end = P.cta_begin[blockIdx.x + 1];
   int u = P.cta_begin[blockIdx.x];
   pdl_launch_dependents();
-  // before the dependency wait: only L2 prefetches of the first units' codes
-  // (warp w: unit u + w), which the previous kernels never write
-  if (lane == 0 && u + warp < u_end) {
-    const int uu = u + warp;
-    const LutProblem& L = P.p[lut_problem_of(P, uu)];
-    const int w = (uu - L.unit_begin) / L.tiles;
-    const uint8_t* cp0 = L.codes + l3_offset(L.n, L.m, T, w, uu - L.unit_begin - w * L.tiles, 0);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cp0),
-                 "r"((uint32_t)(NP * l3_slots(L.m, w)) * (uint32_t)kL3SlotBytes)
-                 : "memory");
+  // Before the dependency wait only L2 prefetches (the L2 is coherent, so a
+  // prefetch never exposes stale data): warp w the codes of unit u + w, warp
+  // 15 the activations of the first window for every token.
+  if (lane == 0 && u < u_end) {
+    const LutProblem& L0 = P.p[P.first_prob[blockIdx.x]];
+    const int w0 = P.first_win[blockIdx.x];
+    if (warp < kLutWarps - 1 && u + warp < u_end) {
+      const int uu = u + warp;
+      const int pi = uu < L0.unit_begin + (w0 + 1) * L0.tiles ? P.first_prob[blockIdx.x] : lut_problem_of(P, uu);
+      const LutProblem& L = P.p[pi];
+      const int w = (uu - L.unit_begin) / L.tiles;
+      const uint8_t* cp0 = L.codes + l3_offset(L.n, L.m, T, w, uu - L.unit_begin - w * L.tiles, 0);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cp0),
+                   "r"((uint32_t)(NP * l3_slots(L.m, w)) * (uint32_t)kL3SlotBytes)
+                   : "memory");
+    } else if (warp == kLutWarps - 1 && (L0.m & 7) == 0 && (reinterpret_cast<uintptr_t>(L0.x) & 15) == 0) {
+      const int64_t k0 = 256 * (int64_t)w0;
+      const uint32_t bytes = (uint32_t)(min((int64_t)256, (int64_t)L0.m - k0) * 2) & ~15u;
+      for (int t = 0; t < M && bytes > 0; ++t)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(L0.x + (int64_t)t * 2 * L0.m + h * L0.m + k0),
+                       "r"(bytes)
+                       : "memory");
+    }
   }
   pdl_wait();
   while (u < u_end) {
@@ -300,6 +333,9 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
         s_unit[s] = uu;
         s_prob[s] = pi;
         s_win[s] = w;
+        s_tau0[s] = uu - L.unit_begin - w * L.tiles;
+        s_nb[s] = l3_slots(L.m, w);
+        s_codes[s] = L.codes + l3_offset(L.n, L.m, T, w, s_tau0[s], 0);
         uu = min(u_end, L.unit_begin + (w + 1) * L.tiles);
         ++s;
       }
@@ -309,16 +345,15 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
     __syncthreads();
     const int nseg = s_nseg;
     const int ub = s_unit[0], ue = s_unit[nseg];
-    // a unit's codes (2T planes x nb slots, contiguous): pointer to lane 0's bytes
+    // a unit's codes (2T planes x nb slots, contiguous, consecutive tiles of a
+    // segment one after another): pointer to lane 0's bytes
     auto unit_codes = [&](int uu, int& seg, int& nb) -> const uint8_t* {
       seg = 0;
 #pragma unroll
       for (int k = 1; k < S; ++k)
         if (k < nseg && uu >= s_unit[k]) seg = k;
-      const LutProblem& L = P.p[s_prob[seg]];
-      const int w = s_win[seg];
-      nb = l3_slots(L.m, w);
-      return L.codes + l3_offset(L.n, L.m, T, w, uu - L.unit_begin - w * L.tiles, 0);
+      nb = s_nb[seg];
+      return s_codes[seg] + (uint32_t)(uu - s_unit[seg]) * ((uint32_t)(NP * nb) * (uint32_t)kL3SlotBytes);
     };
 
     // load cursor: the warp's units (ub + warp, + 16, ...) slot by slot into
@@ -360,7 +395,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
       unit_codes(uu, s, nb);
       const int pi = s_prob[s], w = s_win[s];
       const LutProblem& L = P.p[pi];
-      const int tau = uu - L.unit_begin - w * L.tiles;
+      const int tau = s_tau0[s] + (uu - s_unit[s]);
       const int64_t j = 32 * (int64_t)tau + lane;
       const bool row_in = j < L.n;
       // slot lane ^ (8 jj + i): group (lane & (8 nb - 1)) ^ (8 jj + i), bank = slot
@@ -443,34 +478,50 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
   }
 }
 
-// Sums the partial outputs of every row over the layer's windows, in window
-// order, and writes y (eight independent loads in flight per thread).
+// Sums the partial outputs of every row over the layer's windows and writes
+// y.  Four threads per (row, token): thread q adds windows q, q + 4, ... in
+// order, then the four sums are added as (s0 + s1) + (s2 + s3); a fixed order.
 __global__ void __launch_bounds__(256) lut_reduce_kernel(const __grid_constant__ LutReduceParams R) {
   pdl_launch_dependents();
   pdl_wait();
-  const int64_t total = (int64_t)R.total_rows * R.M;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (int64_t)gridDim.x * blockDim.x) {
-    const int row = (int)(idx / R.M), t = (int)(idx - (int64_t)row * R.M);
+  const int64_t total = (int64_t)R.total_rows * R.M * 4;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t idx = base + threadIdx.x;  // every thread of a warp takes the loop (shuffles below)
+    const bool live = idx < total;
+    const int64_t item = live ? idx >> 2 : 0;
+    const int q = (int)(idx & 3);
+    const int row = (int)(item / R.M), t = (int)(item - (int64_t)row * R.M);
     int pi = 0;
     for (int i = 1; i < R.count; ++i)
       if (row >= R.p[i].row_begin) pi = i;
     const LutReduceProblem& L = R.p[pi];
     const int r = row - L.row_begin, tau = r >> 5, lane = r & 31;
     float sr = 0.0f, si = 0.0f;
-    for (int w0 = 0; w0 < L.windows; w0 += 8) {
-      float2 v[8];
+    if (live) {
+      float2 v[6];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        v[k] = w0 + k < L.windows ? __ldcg(L.part + (((int64_t)(w0 + k) * L.tiles + tau) * R.M + t) * 32 + lane)
-                                  : make_float2(0.0f, 0.0f);
+      for (int k = 0; k < 6; ++k) {
+        const int w = q + 4 * k;
+        v[k] = w < L.windows ? __ldcg(L.part + (((int64_t)w * L.tiles + tau) * R.M + t) * 32 + lane)
+                             : make_float2(0.0f, 0.0f);
+      }
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (w0 + k < L.windows) {
-          sr += v[k].x;
-          si += v[k].y;
-        }
+      for (int k = 0; k < 6; ++k) {
+        sr += v[k].x;
+        si += v[k].y;
+      }
+      for (int w = q + 24; w < L.windows; w += 4) {  // layers of more than 24 windows
+        const float2 u = __ldcg(L.part + (((int64_t)w * L.tiles + tau) * R.M + t) * 32 + lane);
+        sr += u.x;
+        si += u.y;
+      }
     }
-    if (r < L.n) {
+    // (s0 + s1) + (s2 + s3) over the four threads of the item
+    sr += __shfl_xor_sync(0xffffffffu, sr, 1);
+    si += __shfl_xor_sync(0xffffffffu, si, 1);
+    sr += __shfl_xor_sync(0xffffffffu, sr, 2);
+    si += __shfl_xor_sync(0xffffffffu, si, 2);
+    if (live && q == 0 && r < L.n) {
       L.y[(int64_t)t * 2 * L.n + r] = sr;
       L.y[(int64_t)t * 2 * L.n + L.n + r] = si;
     }
