@@ -88,10 +88,22 @@ class ClockSampler:
         out_dir = os.environ.get("FAIRY2I_CLOCKS_DIR") or tempfile.gettempdir()
         self.path = os.path.join(out_dir, f"fairy2i_clocks_gpu{index}_{os.getpid()}.csv")
 
+    def one_shot(self):
+        """One read of the same fields (the polling loop may take no sample in a short region)."""
+        try:
+            out = subprocess.run(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                  "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+            with open(self.path, "a") as f:
+                f.write(out.stdout)
+        except (OSError, subprocess.SubprocessError):
+            pass
+
     def __enter__(self):
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
+            open(self.path, "w").close()
+            self.one_shot()
+            self.fh = open(self.path, "a")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
@@ -107,6 +119,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.fh.close()
+            self.one_shot()
 
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
@@ -158,14 +171,17 @@ def _max_over_ranks(v: float, world: int) -> float:
 # ---------------------------------------------------------------------------
 # oracle on a sample of rows (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
-def _oracle_sample_setup(max_rows_per_proj: int, seed_config: int = 5):
-    """Oracle-quantized rows of block 0 (rows j = 0, s, 2s, ... of each projection)."""
+def _oracle_sample_setup(max_rows_per_proj: int, seed_config: int = 5, part: int = 0, parts: int = 1):
+    """Oracle-quantized rows of block 0 (rows j = 0, s, 2s, ... of each projection; with
+    `parts` > 1 only share `part` of them)."""
     import oracle
     samples = []
     for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
         n, m = out_f // 2, in_f // 2
         step = max(1, n // max_rows_per_proj)
-        rows = np.arange(0, n, step)[:max_rows_per_proj]
+        rows = np.array_split(np.arange(0, n, step)[:max_rows_per_proj], parts)[part]
+        if len(rows) == 0:
+            continue
         R = inputs.weight_R(seed_config, pi, out_f, in_f)
         Rs = torch.cat([R[rows], R[n + rows]]).numpy()
         Uo, Wo = oracle.convert_f32(Rs)
@@ -187,46 +203,99 @@ def _oracle_run(samples):
     return nbytes, time.perf_counter() - t0
 
 
+def _oracle_worker(rows, part, parts, steps, warmup, ready, go, results):
+    """One host core: its share of the sampled rows, `steps` timed passes after `go`."""
+    samples = _oracle_sample_setup(rows, part=part, parts=parts)
+    for _ in range(warmup):
+        _oracle_run(samples)
+    ready.put(part)
+    go.wait()
+    t0 = time.perf_counter()
+    nb = 0
+    for _ in range(steps):
+        nb += _oracle_run(samples)[0]
+    results.put((nb, time.perf_counter() - t0))
+
+
+def _oracle_all_cores(rows: int, steps: int, warmup: int):
+    """The oracle (unchanged, single-threaded loops) on every host core at once: one
+    spawned process per core, each with its own share of the sampled rows, started
+    together; returns (bytes, seconds of the slowest process, cores)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    cores = os.cpu_count() or 1
+    ready, results, go = ctx.Queue(), ctx.Queue(), ctx.Event()
+    procs = [ctx.Process(target=_oracle_worker, args=(rows, i, cores, steps, warmup, ready, go, results))
+             for i in range(cores)]
+    for p in procs:
+        p.start()
+    for _ in procs:
+        ready.get(timeout=600)
+    go.set()
+    out = [results.get(timeout=600) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+    return sum(o[0] for o in out), max(o[1] for o in out), cores
+
+
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(target_s: float = 10.0):
+    """The oracle on sampled rows of the workload: one thread, then the same rows
+    dealt out to one process per host core (spawned; the oracle itself is unchanged)."""
     rows = 8
     samples = _oracle_sample_setup(rows)
     nb, dt = _oracle_run(samples)
     rows = max(1, min(2048, int(rows * target_s / max(dt, 1e-6))))
     samples = _oracle_sample_setup(rows)
     nb, dt = _oracle_run(samples)
-    return {"value": nb / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"oracle decode (plain C, fp64, 1 thread) of {rows} evenly spaced output rows of each of "
-                      f"the 7 projections of block 0, M=1, T=2; {nb} packed-equivalent bytes in {dt:.2f} s"}
+    single = nb / dt / 1e9
+    cores = os.cpu_count() or 1
+    result = {"value": single, "unit": UNIT, "cores": 1, "kind": "oracle",
+              "sample": f"oracle decode (plain C, fp64) of {rows} evenly spaced output rows of each of "
+                        f"the 7 projections of block 0, M=1, T=2; {nb} packed-equivalent bytes",
+              "cpu_model": _cpu_model(), "nproc": cores, "single_thread_GBps": single}
+    if cores > 1:
+        nbm, dtm, cores = _oracle_all_cores(rows, 1, 1)
+        result.update({"value": nbm / dtm / 1e9, "cores": cores, "all_cores_GBps": nbm / dtm / 1e9,
+                       "sample": result["sample"] + f"; then the same rows dealt out to {cores} processes"})
+    return result
 
 
 def run_reference(args, world, rank):
+    """The oracle (the only executable statement of the method) on the machine's host cores:
+    each step decodes a sample of output rows of the workload, dealt out to one spawned
+    process per core (the oracle's own single-threaded loops, unchanged)."""
     if rank != 0:
         return
     steps_total = args.steps + args.warmup
     budget_s = 120.0
+    cores = os.cpu_count() or 1
     rows = 4
     samples = _oracle_sample_setup(rows)
     nb, dt = _oracle_run(samples)
     per_row = dt / rows
-    rows = max(1, min(512, int(budget_s / steps_total / max(per_row, 1e-9))))
-    samples = _oracle_sample_setup(rows)
-    for _ in range(args.warmup):
-        _oracle_run(samples)
-    t0 = time.perf_counter()
-    nbytes = 0
-    for _ in range(args.steps):
-        b, _ = _oracle_run(samples)
-        nbytes += b
-    dt = time.perf_counter() - t0
+    rows = max(1, min(2048, int(budget_s * cores / steps_total / max(per_row, 1e-9))))
+    nbytes, dt, cores = _oracle_all_cores(rows, args.steps, args.warmup)
     value = nbytes / dt / 1e9
-    sample = (f"each step: oracle decode (plain C, fp64, 1 thread) of {rows} evenly spaced output rows of each "
-              f"of the 7 projections of block 0, M=1, T=2")
+    sample = (f"each step: oracle decode (plain C, fp64) of {rows} evenly spaced output rows of each "
+              f"of the 7 projections of block 0, M=1, T=2, rows dealt out to {cores} processes")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample": sample},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                         "cpu_model": _cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -306,18 +375,20 @@ def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
 
 def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int = 4):
     """Batched decode sweep: per token count M and per algorithm, the 7 projections of
-    `blocks` distinct blocks (205 MB at 4 blocks, above L2), one grouped launch per block;
-    time per block, weight GB/s and tokens/s-equivalent."""
-    stack, xs_full = [], []
+    `blocks` distinct blocks (205 MB at 4 blocks, above L2), one grouped call per block;
+    time per block, weight GB/s and tokens/s-equivalent.  "lut" reads the same weights in
+    layout 3 (one decode launch per 4 tokens at T = 2, plus the window-combining launch)."""
+    stack, stack3, xs_full = [], [], []
     for b in range(blocks):
-        qs, xb = [], []
+        qs, qs3, xb = [], [], []
         for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
             R = inputs.weight_R(3, 7 * b + pi, out_f, in_f, device=dev)
-            U, W = f2i.convert(R)
-            qs.append(f2i.quantize(U, W, T_STAGES, check=False))
-            del R, U, W
+            qs.append(f2i.convert_quantize(R, T_STAGES, check=False))
+            qs3.append(f2i.convert_quantize(R, T_STAGES, check=False, layout=3))
+            del R
             xb.append(inputs.activations(3, 7 * b + pi, max(Ms), in_f, device=dev))
         stack.append(qs)
+        stack3.append(qs3)
         xs_full.append(xb)
     f2i.sync_status()
     nbytes = sum(q.nbytes for q in stack[0])
@@ -327,10 +398,12 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
         xs = [[x[:M].contiguous() for x in xb] for xb in xs_full]
         ys = [[torch.empty((M, 2 * q.n), dtype=torch.float32, device=dev) for q in qs] for qs in stack]
         row = {"M": M}
-        for algo in ("mma", "tcgen05", "auto") + (("tcgen05_sp",) if M <= 8 else ()):
+        for algo in ("lut", "mma", "tcgen05", "auto") + (("tcgen05_sp",) if M <= 8 else ()):
+            st = stack3 if algo == "lut" else stack
+
             def step():
                 for b in range(blocks):
-                    f2i.linear_group(stack[b], xs[b], ys[b], algo=algo)
+                    f2i.linear_group(st[b], xs[b], ys[b], algo=algo)
             for _ in range(3):
                 step()
             torch.cuda.synchronize()
@@ -350,11 +423,11 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
             "bytes_per_block": nbytes, "rows": out}
 
 
-def stack_leg(f2i, dev, T: int, blocks: int, steps: int, warmup: int):
+def stack_leg(f2i, dev, T: int, blocks: int, steps: int, warmup: int, layout: int = 3):
     """The full 32-block LLaMA-2-7B linear stack at T stages: convert + quantize of all
     224 projections (timed per launch), then batch-1 decode of all of them per step
-    (CUDA graph of one grouped launch per block)."""
-    stack, offline = build_stack(f2i, blocks, dev, T)
+    (CUDA graph of one grouped call per block; layout 3 = the table-lookup decode)."""
+    stack, offline = build_stack(f2i, blocks, dev, T, layout)
     nbytes = sum(q.nbytes for layers in stack for q in layers)
     # the same stack through the one-pass convert + quantize (codes written over the first ones)
     fused_ms, e = 0.0, [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -362,7 +435,7 @@ def stack_leg(f2i, dev, T: int, blocks: int, steps: int, warmup: int):
         for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
             R = inputs.weight_R(5, 7 * b + pi, out_f, in_f, device=dev)
             e[0].record()
-            f2i.convert_quantize(R, T, out=stack[b][pi], check=False)
+            f2i.convert_quantize(R, T, out=stack[b][pi], check=False, layout=layout)
             e[1].record()
             e[1].synchronize()
             fused_ms += e[0].elapsed_time(e[1])
@@ -398,8 +471,8 @@ def stack_leg(f2i, dev, T: int, blocks: int, steps: int, warmup: int):
     f2i.sync_status()
     ms = start.elapsed_time(stop) / steps
     del graph, stack
-    return {"T": T, "packed_bytes": nbytes, "decode_ms_per_token": ms, "decode_GBps": nbytes / (ms * 1e-3) / 1e9,
-            "tokens_per_s": 1e3 / ms, **offline}
+    return {"T": T, "layout": layout, "packed_bytes": nbytes, "decode_ms_per_token": ms,
+            "decode_GBps": nbytes / (ms * 1e-3) / 1e9, "tokens_per_s": 1e3 / ms, **offline}
 
 
 def run_stack_only(args, world, rank, local):
@@ -608,7 +681,7 @@ def run_ours(args, world, rank, local):
                    "bytes_per_step": bytes_per_step, "l2": "inputs larger than L2 (1.64 GB working set)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": blocks * args.steps,
+        "gpu_launches": blocks * args.steps * (2 if algo == "lut" else 1),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
                      "traffic": DECODE_TRAFFIC_BYTES if algo in ("auto", "mma") else None,
@@ -618,9 +691,17 @@ def run_ours(args, world, rank, local):
         "clocks": clk.summary(),
         "offline": offline,
     }
+    del graph, e2e_graph
     if not args.no_prefill:
-        del graph
         result["prefill"] = prefill_leg(f2i, dev, peaks, max(3, min(args.steps, 20)), 3, args.prefill_tokens)
+    if not args.no_sweep:
+        result["sweep"] = sweep_leg(f2i, dev)
+    if not args.no_stack:
+        del stack, x_all, y_all, xv, yv, xs, ys
+        torch.cuda.empty_cache()
+        result["stack"] = {"workload": f"llama2-7b linear stack, {blocks} blocks x 7 projections, M=1, layout 3 "
+                                       "(table-lookup decode), T in {1, 2, 3}",
+                           "rows": [stack_leg(f2i, dev, T, blocks, max(3, min(args.steps, 50)), 3) for T in (1, 2, 3)]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
@@ -637,6 +718,8 @@ def main():
     ap.add_argument("--mode", choices=["decode", "prefill", "sweep", "stack", "grad"], default="decode",
                     help="prefill: time only the prefill leg (for profiling)")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the batched-decode sweep (M = 1..64)")
+    ap.add_argument("--no-stack", action="store_true", help="skip the T = 1, 2, 3 stack legs")
     ap.add_argument("--decode-algo", choices=sorted(DECODE_KERNELS), default="lut",
                     help="decode kernel of the default mode (lut = the table-lookup decode on layout 3; "
                          "auto = the library's choice on layout 2)")
