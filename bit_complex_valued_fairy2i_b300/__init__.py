@@ -38,6 +38,7 @@ EXPORTED = (
     "fairy2i_sync_status", "fairy2i_last_error", "fairy2i_layout_version", "fairy2i_selftest_bounded_wait",
     "fairy2i_convert_quantize", "fairy2i_linear_grad_x", "fairy2i_linear_grad_x_group",
     "fairy2i_codes_bytes_layout", "fairy2i_linear_ws", "fairy2i_linear_group_ws", "fairy2i_linear_workspace_bytes",
+    "fairy2i_linear_group_static",
 )
 
 
@@ -87,6 +88,7 @@ def load_library(path: str = LIB_PATH):
         "fairy2i_linear_group_ws": (ctypes.c_int, [PD, ctypes.POINTER(P), ctypes.POINTER(P), I32, I64, ctypes.c_int,
                                                    P, SZ, P]),
         "fairy2i_linear_workspace_bytes": (SZ, [PD, I32, I64]),
+        "fairy2i_linear_group_static": (ctypes.c_int, [PD, ctypes.POINTER(P), ctypes.POINTER(P), I32, I64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -296,6 +298,26 @@ def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None, ws: torch.Ten
         _check(load_library().fairy2i_linear_group_ws(descs, xp, yp, count, M, ALGO[algo], wp, wn, _stream(stream)))
         return ys
     _check(load_library().fairy2i_linear_group(descs, xp, yp, count, M, ALGO[algo], _stream(stream)))
+    return ys
+
+
+def linear_group_static(qs, xs, ys=None, stream=None):
+    """The table-lookup decode of layout-3 layers with the library's own fixed scratch (no
+    workspace, nothing allocated on the device by the library): for callers that may not
+    allocate device memory.  Calls that overlap on the GPU share that scratch and race."""
+    count = len(qs)
+    M = xs[0].shape[0]
+    if ys is None:
+        ys = [torch.empty((M, 2 * q.n), dtype=torch.float32, device=x.device) for q, x in zip(qs, xs)]
+    for q, x, y in zip(qs, xs, ys):
+        _dev(x, "x")
+        _dev(y, "y")
+        if x.dtype != torch.bfloat16 or x.shape != (M, 2 * q.m) or y.shape != (M, 2 * q.n):
+            raise ValueError("group members need matching x [M, 2m] bfloat16 and y [M, 2n] float32")
+    descs = (PackedDesc * count)(*[q.desc() for q in qs])
+    xp = (ctypes.c_void_p * count)(*[x.data_ptr() for x in xs])
+    yp = (ctypes.c_void_p * count)(*[y.data_ptr() for y in ys])
+    _check(load_library().fairy2i_linear_group_static(descs, xp, yp, count, M, _stream(stream)))
     return ys
 
 

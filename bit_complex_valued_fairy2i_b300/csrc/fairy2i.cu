@@ -831,6 +831,39 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
 
 __device__ unsigned int g_fairy2i_error_taken;
 
+// Scratch of fairy2i_linear_group_static: a fixed block of device memory that
+// is part of the loaded library (every device that loads it keeps these
+// bytes until the process exits), for callers that cannot allocate.  It holds
+// the table-lookup decode's partial outputs; every call overwrites what it
+// reads, so nothing needs clearing between calls.
+constexpr size_t kStaticScratchBytes = (size_t)8 << 20;
+static __device__ __align__(256) unsigned char g_fairy2i_static_scratch[kStaticScratchBytes];
+
+// The device address of the scratch array, looked up once per device (with
+// that device current) on the first call there.  In host code the array's
+// name is only a stand-in for the symbol, never an address a kernel may use.
+std::mutex g_static_mu;
+std::vector<std::pair<int, void*>> g_static_addr;
+
+fairy2i_status static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  for (const auto& a : g_static_addr)
+    if (a.first == dev) {
+      *out = a.second;
+      return FAIRY2I_OK;
+    }
+  void* ptr = nullptr;
+  e = cudaGetSymbolAddress(&ptr, g_fairy2i_static_scratch);
+  if (e != cudaSuccess || ptr == nullptr)
+    return fail(FAIRY2I_ERR_CUDA, "address of the static scratch: %s", cudaGetErrorString(e));
+  g_static_addr.push_back({dev, ptr});
+  *out = ptr;
+  return FAIRY2I_OK;
+}
+
 __global__ void take_error_word_kernel() { g_fairy2i_error_taken = atomicExch(&g_fairy2i_error_word, 0u); }
 
 }  // namespace
@@ -936,6 +969,26 @@ fairy2i_status fairy2i_linear_group_ws(const fairy2i_packed* qs, const void* con
                                        int32_t count, int64_t M, fairy2i_algo algo, void* workspace,
                                        size_t workspace_bytes, void* stream) {
   return linear_group_impl(qs, xs, ys, count, M, algo, true, workspace, workspace_bytes,
+                           static_cast<cudaStream_t>(stream));
+}
+
+fairy2i_status fairy2i_linear_group_static(const fairy2i_packed* qs, const void* const* xs, float* const* ys,
+                                           int32_t count, int64_t M, void* stream) {
+  if (!qs || count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "bad descriptor array or count");
+  for (int i = 0; i < count; ++i)
+    if (qs[i].version != FAIRY2I_LAYOUT_LUT)
+      return fail(FAIRY2I_ERR_UNSUPPORTED, "the static-scratch decode reads layout %d (layer %d is %d)",
+                  FAIRY2I_LAYOUT_LUT, i, qs[i].version);
+  const size_t need = fairy2i_linear_workspace_bytes(qs, count, M);
+  if (need > kStaticScratchBytes)
+    return fail(FAIRY2I_ERR_UNSUPPORTED,
+                "these layers need %zu bytes of scratch, more than the %zu bytes this entry point holds; "
+                "use fairy2i_linear_group_ws with a workspace, or fewer layers or tokens per call",
+                need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  fairy2i_status st = static_scratch_address(&scratch);
+  if (st != FAIRY2I_OK) return st;
+  return linear_group_impl(qs, xs, ys, count, M, FAIRY2I_ALGO_LUT, true, scratch, kStaticScratchBytes,
                            static_cast<cudaStream_t>(stream));
 }
 

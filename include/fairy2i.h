@@ -227,6 +227,25 @@ fairy2i_status fairy2i_linear_group_ws(const fairy2i_packed *qs, const void *con
  * layout 3 (or invalid). */
 size_t fairy2i_linear_workspace_bytes(const fairy2i_packed *qs, int32_t count, int64_t M);
 
+/* The table-lookup decode with no caller workspace and no allocation (the
+ * paper has no counterpart: this is a deployment aid).  For callers that
+ * cannot call cudaMalloc -- e.g. a plugin inside a serving process whose
+ * device memory is owned by the host application's allocator, or a real-time
+ * loop that forbids device allocation after start-up.  Same inputs, outputs
+ * and results as fairy2i_linear_group_ws with algo LUT (layout-3 descriptors
+ * only); the partial outputs go to a fixed 8 MiB array inside the library,
+ * which every device that loads the library holds until the process exits.
+ *   - The first call on a device looks up that array's device address (with
+ *     the device current); make that first call before any stream capture.
+ *   - Every call uses the same array: calls that may overlap on the GPU (other
+ *     streams, other threads) race and must be serialized by the caller.
+ *   - The array needs no clearing: each call writes every byte it reads.
+ * Errors: as fairy2i_linear_group_ws; UNSUPPORTED for another layout or when
+ * the layers need more than 8 MiB of scratch (fairy2i_linear_workspace_bytes;
+ * a LLaMA-2-7B block needs 1.6 MB per token of a launch). */
+fairy2i_status fairy2i_linear_group_static(const fairy2i_packed *qs, const void *const *xs,
+                                           float *const *ys, int32_t count, int64_t M, void *stream);
+
 /* Input gradient of the layer for training through it with the
  * straight-through estimator ("Fairy2i: Ultra-Low-Bit ...", quantization-aware
  * training; "Fairy2i-W2" card, y = Ux + W conj(x)):
