@@ -206,12 +206,13 @@ def convert_quantize(R: torch.Tensor, T: int = 2, out: Packed | None = None, str
 _workspaces: dict = {}
 
 
-def workspace(qs, M: int, device, stream=None) -> torch.Tensor | None:
+def workspace(qs, M: int, device, stream=None, descs=None) -> torch.Tensor | None:
     """The device scratch of the table-lookup decode for these layers and token count,
     kept per (device, stream) and grown when a call needs more (None if none is needed).
     Calls on one stream run in order, so they can share it."""
     count = len(qs)
-    descs = (PackedDesc * count)(*[q.desc() for q in qs])
+    if descs is None:
+        descs = (PackedDesc * count)(*[q.desc() for q in qs])
     need = int(load_library().fairy2i_linear_workspace_bytes(descs, count, M))
     if need == 0:
         return None
@@ -293,7 +294,7 @@ def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None, ws: torch.Ten
             raise ValueError("group members need matching x [M, 2m] bfloat16 and y [M, 2n] float32")
     if qs[0].layout == LAYOUT_LUT:
         if ws is None:
-            ws = workspace(qs, M, xs[0].device, stream)
+            ws = workspace(qs, M, xs[0].device, stream, descs)
         wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
         _check(load_library().fairy2i_linear_group_ws(descs, xp, yp, count, M, ALGO[algo], wp, wn, _stream(stream)))
         return ys

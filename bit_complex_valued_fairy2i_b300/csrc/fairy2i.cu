@@ -670,24 +670,28 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
         return fail(FAIRY2I_ERR_UNSUPPORTED, "too many units for one launch");
       P.total_units = (int32_t)units;
       const int ctas = (int)std::min<int64_t>({units, (int64_t)sm_count(), (int64_t)f2i::kLutMaxCtas});
-      // cost-balanced split of the units, in order
+      // cost-balanced split of the units, in order: CTA c starts at the first
+      // unit whose preceding cost reaches c / ctas of the total (costs are
+      // constant inside a (layer, window), so each boundary is one division)
       int64_t total = 0;
       for (int i = 0; i < cnt; ++i) {
         const f2i::LutProblem& L = P.p[i];
         for (int w = 0; w < L.windows; ++w) total += (int64_t)L.tiles * (8 * f2i::l3_slots(L.m, w) + 3);
       }
       int c = 1;
-      int64_t cum = 0;
+      int64_t before = 0;
       P.cta_begin[0] = 0;
       for (int i = 0; i < cnt && c < ctas; ++i) {
         const f2i::LutProblem& L = P.p[i];
         for (int w = 0; w < L.windows && c < ctas; ++w) {
           const int64_t cost = 8 * f2i::l3_slots(L.m, w) + 3;
-          for (int tau = 0; tau < L.tiles && c < ctas; ++tau) {
-            // unit u starts CTA c when the cost before it reaches c / ctas of the total
-            while (c < ctas && cum * ctas >= total * c) P.cta_begin[c++] = L.unit_begin + w * L.tiles + tau;
-            cum += cost;
+          while (c < ctas) {
+            const int64_t need = total * c - before * ctas;  // k * cost * ctas >= need
+            const int64_t k = need <= 0 ? 0 : (need + cost * ctas - 1) / (cost * ctas);
+            if (k >= L.tiles) break;
+            P.cta_begin[c++] = L.unit_begin + w * L.tiles + (int32_t)k;
           }
+          before += (int64_t)L.tiles * cost;
         }
       }
       while (c < ctas) P.cta_begin[c++] = (int32_t)units;
