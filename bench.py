@@ -41,10 +41,11 @@ METRIC = "2-bit WL-complex GEMV weight GB/s vs HBM peak; prefill GEMM TFLOP/s"
 UNIT = "GB/s"
 T_STAGES = 2
 BLOCKS = inputs.LLAMA2_7B_BLOCKS
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch
-# of this workload, from an ncu capture of linear_mma_kernel<4,1,16> (one 16-warp
-# CTA per SM); must be re-measured whenever that kernel changes.
-DECODE_TRAFFIC_BYTES = 51_399_680
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch of
+# this workload per decode kernel, from ncu captures (must be re-measured whenever
+# that kernel changes): linear_lut_kernel<2,1> (the capture in
+# profiles/linear_lut_decode_llama2_7b_block_M1_T2.md) and linear_mma_kernel<4,1,16>.
+DECODE_TRAFFIC_BYTES = {"lut": 51_374_336, "mma": 51_399_680, "auto": 51_399_680}
 # decode kernel and arithmetic per --decode-algo (auto = the 2:4-sparse mma.sync decode at M = 1 on
 # layout 2; lut = the table-lookup decode on layout 3)
 DECODE_KERNELS = {
@@ -684,7 +685,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": blocks * args.steps * (2 if algo == "lut" else 1),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": DECODE_TRAFFIC_BYTES if algo in ("auto", "mma") else None,
+                     "traffic": DECODE_TRAFFIC_BYTES.get(algo),
                      "kernel": DECODE_KERNELS[algo][0], "bytes_per_launch": bytes_per_block,
                      "launch_us": launch_ms * 1e3, "peak_source": peaks["source"],
                      "frac_of_nominal_8TBps": achieved / 8000.0},

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstdarg>
@@ -26,6 +27,13 @@
 #include "linear_lut.cuh"
 
 namespace {
+
+// An NVTX range over one C-ABI call (a no-op unless a profiler is attached),
+// so that timelines show which library call issued which kernels.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 thread_local std::string g_last_error;
 
@@ -896,6 +904,7 @@ size_t fairy2i_scales_count(int64_t n, int32_t T) {
 }
 
 fairy2i_status fairy2i_convert(const float* R, int64_t rows, int64_t cols, void* U, void* W, void* stream) {
+  NvtxRange nvtx_range("fairy2i_convert");
   if (!R || !U || !W) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL pointer argument");
   if (rows < 2 || cols < 2 || (rows & 1) || (cols & 1))
     return fail(FAIRY2I_ERR_SHAPE, "R is %lld x %lld; both dimensions must be even and >= 2", (long long)rows,
@@ -915,6 +924,7 @@ fairy2i_status fairy2i_convert(const float* R, int64_t rows, int64_t cols, void*
 
 fairy2i_status fairy2i_quantize(const void* U, const void* W, int64_t n, int64_t m, int32_t T,
                                 const fairy2i_packed* out, void* stream) {
+  NvtxRange nvtx_range("fairy2i_quantize");
   if (!U || !W) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL weight pointer");
   if (!aligned(U, 8) || !aligned(W, 8)) return fail(FAIRY2I_ERR_INVALID_ARG, "U and W must be 8-byte aligned");
   fairy2i_status st = check_packed(out);
@@ -929,6 +939,7 @@ fairy2i_status fairy2i_quantize(const void* U, const void* W, int64_t n, int64_t
 
 fairy2i_status fairy2i_convert_quantize(const float* R, int64_t rows, int64_t cols, int32_t T,
                                         const fairy2i_packed* out, void* stream) {
+  NvtxRange nvtx_range("fairy2i_convert_quantize");
   if (!R) return fail(FAIRY2I_ERR_INVALID_ARG, "R is NULL");
   if (rows < 2 || cols < 2 || (rows & 1) || (cols & 1))
     return fail(FAIRY2I_ERR_SHAPE, "R is %lld x %lld; both dimensions must be even and >= 2", (long long)rows,
@@ -946,6 +957,7 @@ fairy2i_status fairy2i_convert_quantize(const float* R, int64_t rows, int64_t co
 
 fairy2i_status fairy2i_linear_ex(const fairy2i_packed* q, const void* x, int64_t M, float* y, fairy2i_algo algo,
                                  void* stream) {
+  NvtxRange nvtx_range("fairy2i_linear_ex");
   if (!q) return fail(FAIRY2I_ERR_INVALID_ARG, "packed descriptor is NULL");
   const void* xs[1] = {x};
   float* ys[1] = {y};
@@ -963,6 +975,7 @@ size_t fairy2i_linear_workspace_bytes(const fairy2i_packed* qs, int32_t count, i
 
 fairy2i_status fairy2i_linear_ws(const fairy2i_packed* q, const void* x, int64_t M, float* y, fairy2i_algo algo,
                                  void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("fairy2i_linear_ws");
   if (!q) return fail(FAIRY2I_ERR_INVALID_ARG, "packed descriptor is NULL");
   const void* xs[1] = {x};
   float* ys[1] = {y};
@@ -972,12 +985,14 @@ fairy2i_status fairy2i_linear_ws(const fairy2i_packed* q, const void* x, int64_t
 fairy2i_status fairy2i_linear_group_ws(const fairy2i_packed* qs, const void* const* xs, float* const* ys,
                                        int32_t count, int64_t M, fairy2i_algo algo, void* workspace,
                                        size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("fairy2i_linear_group_ws");
   return linear_group_impl(qs, xs, ys, count, M, algo, true, workspace, workspace_bytes,
                            static_cast<cudaStream_t>(stream));
 }
 
 fairy2i_status fairy2i_linear_group_static(const fairy2i_packed* qs, const void* const* xs, float* const* ys,
                                            int32_t count, int64_t M, void* stream) {
+  NvtxRange nvtx_range("fairy2i_linear_group_static");
   if (!qs || count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "bad descriptor array or count");
   for (int i = 0; i < count; ++i)
     if (qs[i].version != FAIRY2I_LAYOUT_LUT)
@@ -1002,6 +1017,7 @@ fairy2i_status fairy2i_linear(const fairy2i_packed* q, const void* x, int64_t M,
 
 fairy2i_status fairy2i_linear_group(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int32_t count,
                                     int64_t M, fairy2i_algo algo, void* stream) {
+  NvtxRange nvtx_range("fairy2i_linear_group");
   return linear_group_impl(qs, xs, ys, count, M, algo, false, nullptr, 0, static_cast<cudaStream_t>(stream));
 }
 
@@ -1011,6 +1027,7 @@ fairy2i_status fairy2i_linear_grad_x(const fairy2i_packed* q, const float* gy, i
 
 fairy2i_status fairy2i_linear_grad_x_group(const fairy2i_packed* qs, const float* const* gys, float* const* gxs,
                                            int32_t count, int64_t M, void* stream) {
+  NvtxRange nvtx_range("fairy2i_linear_grad_x_group");
   if (count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "count=%d outside [1, 256]", count);
   if (!qs || !gys || !gxs) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL array argument");
   for (int i = 0; i < count; ++i) {
@@ -1060,6 +1077,7 @@ fairy2i_status fairy2i_linear_grad_x_group(const fairy2i_packed* qs, const float
 }
 
 fairy2i_status fairy2i_unpack_codes(const fairy2i_packed* q, uint8_t* codes_out, void* stream) {
+  NvtxRange nvtx_range("fairy2i_unpack_codes");
   fairy2i_status st = check_packed(q);
   if (st != FAIRY2I_OK) return st;
   if (!codes_out) return fail(FAIRY2I_ERR_INVALID_ARG, "codes_out is NULL");
@@ -1073,12 +1091,14 @@ fairy2i_status fairy2i_unpack_codes(const fairy2i_packed* q, uint8_t* codes_out,
 }
 
 fairy2i_status fairy2i_selftest_bounded_wait(int32_t limit_us, void* stream) {
+  NvtxRange nvtx_range("fairy2i_selftest_bounded_wait");
   if (limit_us < 1 || limit_us > 1000000) return fail(FAIRY2I_ERR_INVALID_ARG, "limit_us=%d outside [1, 1000000]", limit_us);
   f2i::bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((uint64_t)limit_us * 1000ull);
   return check_launch("bounded-wait self-test launch");
 }
 
 fairy2i_status fairy2i_sync_status(void* stream) {
+  NvtxRange nvtx_range("fairy2i_sync_status");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
