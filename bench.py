@@ -338,40 +338,59 @@ def build_stack(f2i, blocks: int, dev, T: int = T_STAGES, layout: int = 2):
 
 def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
     """Prefill: the 7 projections of one block at M tokens (1 % outliers x10),
-    one grouped tcgen05 launch per step; executed and dense-equivalent TFLOP/s."""
-    qs, xs, ys = [], [], []
-    flops_exec = flops_dense = 0
+    one grouped launch per step, two kernels: the ternary tcgen05 GEMM over
+    layout 2 (16 n m T flops per token) and the dense GEMM of the dequantized
+    matrix over layout 3 (16 n m flops per token, hi + lo bfloat16 terms).
+    Executed and dense-equivalent TFLOP/s for each; the faster leads."""
+    qs2, qs3, xs, ys = [], [], [], []
+    flops_tern = flops_dq = flops_dense = 0
     for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
         R = inputs.weight_R(4, pi, out_f, in_f, device=dev)
         U, W = f2i.convert(R)
-        q = f2i.quantize(U, W, T_STAGES, check=False)
+        qs2.append(f2i.quantize(U, W, T_STAGES, check=False))
+        qs3.append(f2i.quantize(U, W, T_STAGES, check=False, layout=3))
         del R, U, W
-        qs.append(q)
         xs.append(inputs.activations(4, pi, M, in_f, outliers=True, device=dev))
         ys.append(torch.empty((M, out_f), dtype=torch.float32, device=dev))
         n, m = out_f // 2, in_f // 2
-        flops_exec += 16 * n * m * T_STAGES * M
+        flops_tern += 16 * n * m * T_STAGES * M
+        flops_dq += 16 * n * m * M
         flops_dense += 8 * n * m * M
     f2i.sync_status()
-    for _ in range(warmup):
-        f2i.linear_group(qs, xs, ys, algo="tcgen05")
-    torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(steps):
-        f2i.linear_group(qs, xs, ys, algo="tcgen05")
-    stop.record(stream)
-    torch.cuda.synchronize()
-    f2i.sync_status()
-    ms = start.elapsed_time(stop) / steps
-    tflops = flops_exec / (ms * 1e-3) / 1e12
+
+    def timed(qs, algo):
+        for _ in range(warmup):
+            f2i.linear_group(qs, xs, ys, algo=algo)
+        torch.cuda.synchronize()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            f2i.linear_group(qs, xs, ys, algo=algo)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        f2i.sync_status()
+        return start.elapsed_time(stop) / steps
+
+    legs = {}
+    for key, qs, algo, kernel, fl in (("ternary", qs2, "tcgen05", "linear_tcgen05_kernel<8>", flops_tern),
+                                      ("dequantized", qs3, "tcgen05_dq", f"linear_dq_kernel<{T_STAGES}>", flops_dq)):
+        ms = timed(qs, algo)
+        tf = fl / (ms * 1e-3) / 1e12
+        legs[key] = {"algo": algo, "kernel": kernel, "layout": 2 if key == "ternary" else 3, "ms_per_block": ms,
+                     "executed_flops_per_block": fl, "tflops_executed": tf,
+                     "tflops_dense_equivalent": flops_dense / (ms * 1e-3) / 1e12,
+                     "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "tokens_per_s_per_block": M / (ms * 1e-3)}
+    best = min(legs, key=lambda k: legs[k]["ms_per_block"])
+    b = legs[best]
     return {"workload": f"llama2-7b block prefill, 7 projections, M={M}, T={T_STAGES}, 1% outliers x10, "
-                        "one grouped launch", "kernel": "linear_tcgen05_kernel<8>", "ms_per_block": ms,
-            "executed_flops_per_block": flops_exec, "dense_equivalent_flops_per_block": flops_dense,
-            "tflops_executed": tflops, "tflops_dense_equivalent": flops_dense / (ms * 1e-3) / 1e12,
-            "peak_bf16_tflops": peaks["bf16_tflops"], "frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
-            "peak_source": peaks["source"], "tokens_per_s_per_block": M / (ms * 1e-3), "steps": steps}
+                        "one grouped launch", "kernel": b["kernel"], "algo": b["algo"], "ms_per_block": b["ms_per_block"],
+            "executed_flops_per_block": b["executed_flops_per_block"],
+            "dense_equivalent_flops_per_block": flops_dense, "tflops_executed": b["tflops_executed"],
+            "tflops_dense_equivalent": b["tflops_dense_equivalent"],
+            "peak_bf16_tflops": peaks["bf16_tflops"], "frac_of_bf16_peak": b["frac_of_bf16_peak"],
+            "peak_source": peaks["source"], "tokens_per_s_per_block": b["tokens_per_s_per_block"], "steps": steps,
+            "by_kernel": legs}
 
 
 def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int = 4):

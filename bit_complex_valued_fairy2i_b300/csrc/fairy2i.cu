@@ -25,6 +25,7 @@
 #include "linear_tc_decode.cuh"
 #include "linear_grad.cuh"
 #include "linear_lut.cuh"
+#include "linear_dq.cuh"
 
 namespace {
 
@@ -324,6 +325,75 @@ fairy2i_status make_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t m)
   return FAIRY2I_OK;
 }
 
+// x [M][2m] bfloat16 as a [M][2m] tensor: tiles of 256 tokens x 64 columns,
+// 128-byte swizzle, zero fill outside (the dequantized GEMM's B operand).
+fairy2i_status make_x_map_rows(CUtensorMap* map, const void* x, int64_t M, int64_t m) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  fairy2i_status st = tensor_map_encoder(enc);
+  if (st != FAIRY2I_OK) return st;
+  const cuuint64_t dims[2] = {(cuuint64_t)(2 * m), (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)m * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)f2i::kDqBK, (cuuint32_t)f2i::kDqBN};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FAIRY2I_ERR_CUDA, "cuTensorMapEncodeTiled (x rows) failed (%d)", (int)r);
+  return FAIRY2I_OK;
+}
+
+template <int T>
+fairy2i_status launch_dq_t(const f2i::DqParams& P, cudaStream_t s) {
+  auto k = f2i::linear_dq_kernel<T>;
+  fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(k), f2i::kDqSmemBytes, "dequantized prefill");
+  if (st != FAIRY2I_OK) return st;
+  const int64_t grid = std::min<int64_t>(P.total_tiles, sm_count());
+  k<<<(unsigned)grid, f2i::kDqThreads, f2i::kDqSmemBytes, s>>>(P);
+  return check_launch("dequantized prefill launch");
+}
+
+// The dense GEMM of the dequantized real matrix (layout 3, m a multiple of 8,
+// T <= 4): one launch per kDqMaxGroup layers, tiles of 64 outputs x 256 tokens.
+fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count, int64_t M, int T,
+                      cudaStream_t s) {
+  for (int p0 = 0; p0 < count; p0 += f2i::kDqMaxGroup) {
+    const int cnt = std::min(f2i::kDqMaxGroup, count - p0);
+    f2i::DqParams P;
+    memset(&P, 0, sizeof(P));
+    P.count = cnt;
+    P.T = T;
+    P.M = (int32_t)M;
+    int64_t tiles = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const fairy2i_packed& q = qs[p0 + i];
+      fairy2i_status st = make_x_map_rows(&P.tmap[i], xs[p0 + i], M, q.m);
+      if (st != FAIRY2I_OK) return st;
+      f2i::DqProblem& pr = P.p[i];
+      pr.codes = static_cast<const uint8_t*>(q.codes);
+      pr.scales = q.scales;
+      pr.y = ys[p0 + i];
+      pr.n = (int32_t)q.n;
+      pr.m = (int32_t)q.m;
+      pr.row_tiles = (int32_t)((q.n + 63) / 64);
+      pr.tok_tiles = (int32_t)((M + f2i::kDqBN - 1) / f2i::kDqBN);
+      pr.kpairs = (int32_t)((q.m + f2i::kDqBK - 1) / f2i::kDqBK);
+      pr.tile_begin = tiles;
+      tiles += (int64_t)pr.row_tiles * pr.tok_tiles;
+    }
+    P.total_tiles = tiles;
+    fairy2i_status st;
+    switch (T) {
+      case 1: st = launch_dq_t<1>(P, s); break;
+      case 2: st = launch_dq_t<2>(P, s); break;
+      case 3: st = launch_dq_t<3>(P, s); break;
+      case 4: st = launch_dq_t<4>(P, s); break;
+      default: return fail(FAIRY2I_ERR_UNSUPPORTED, "dequantized prefill supports T <= 4");
+    }
+    if (st != FAIRY2I_OK) return st;
+  }
+  return ok();
+}
+
 template <int RO>
 fairy2i_status launch_tcgen05_t(const f2i::PrefillParams& P, cudaStream_t s) {
   auto k = f2i::linear_tcgen05_kernel<RO>;
@@ -509,6 +579,9 @@ constexpr int64_t kTcDecodeMaxTokens = 8;
 
 // Token count from which FAIRY2I_ALGO_AUTO takes the tcgen05 prefill path.
 constexpr int64_t kPrefillMinTokens = 16;
+// Token count from which AUTO takes the dequantized GEMM over the table-lookup
+// decode on layout 3.
+constexpr int64_t kDqMinTokens = 16;
 
 // The quantizer over U, W (FUSED = false) or straight from R (true); the
 // caller has checked the arguments.  Codes are zeroed first: each row ORs its
@@ -734,7 +807,7 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
   if (count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "count=%d outside [1, 256]", count);
   if (!qs || !xs || !ys) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL array argument");
   if (M < 0) return fail(FAIRY2I_ERR_SHAPE, "M=%lld is negative", (long long)M);
-  if ((int)algo < 0 || (int)algo > 5) return fail(FAIRY2I_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
+  if ((int)algo < 0 || (int)algo > 6) return fail(FAIRY2I_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
   if (!qs) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL descriptor array");
   const int T = qs[0].T;
   for (int i = 0; i < count; ++i) {
@@ -744,11 +817,21 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
     if (qs[i].version != qs[0].version) return fail(FAIRY2I_ERR_SHAPE, "all layers of a group need the same layout");
   }
   if (qs[0].version == FAIRY2I_LAYOUT_LUT) {
-    if (algo != FAIRY2I_ALGO_AUTO && algo != FAIRY2I_ALGO_LUT)
-      return fail(FAIRY2I_ERR_UNSUPPORTED, "layout 3 is read by the table-lookup decode only (algo AUTO or LUT)");
-    if (T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "table-lookup decode supports T <= 4");
-    if (!with_ws)
-      return fail(FAIRY2I_ERR_UNSUPPORTED, "layout 3 needs a workspace: call fairy2i_linear_ws / fairy2i_linear_group_ws");
+    if (algo != FAIRY2I_ALGO_AUTO && algo != FAIRY2I_ALGO_LUT && algo != FAIRY2I_ALGO_TCGEN05_DQ)
+      return fail(FAIRY2I_ERR_UNSUPPORTED, "layout 3 is read by the table-lookup decode and the dequantized GEMM only");
+    if (T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "layout 3 kernels support T <= 4");
+    bool m_mult8_3 = true;
+    for (int i = 0; i < count; ++i) m_mult8_3 = m_mult8_3 && (qs[i].m % 8) == 0;
+    // AUTO: the table lookup below kDqMinTokens tokens when a workspace came with the call,
+    // otherwise (and from kDqMinTokens) the dequantized GEMM, which needs none
+    fairy2i_algo a3 = algo;
+    if (a3 == FAIRY2I_ALGO_AUTO)
+      a3 = (!m_mult8_3 || (with_ws && M < kDqMinTokens)) ? FAIRY2I_ALGO_LUT : FAIRY2I_ALGO_TCGEN05_DQ;
+    if (a3 == FAIRY2I_ALGO_LUT && !with_ws)
+      return fail(FAIRY2I_ERR_UNSUPPORTED,
+                  "the table-lookup decode needs a workspace: call fairy2i_linear_ws / fairy2i_linear_group_ws");
+    if (a3 == FAIRY2I_ALGO_TCGEN05_DQ && !m_mult8_3)
+      return fail(FAIRY2I_ERR_UNSUPPORTED, "the dequantized GEMM needs m to be a multiple of 8");
     if (M == 0) return ok();
     for (int i = 0; i < count; ++i) {
       if (!xs[i] || !ys[i]) return fail(FAIRY2I_ERR_INVALID_ARG, "x or y of layer %d is NULL", i);
@@ -756,9 +839,11 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
         return fail(FAIRY2I_ERR_INVALID_ARG, "x and y must be 16-byte aligned (layer %d)", i);
     }
     if (M > (int64_t)1 << 30) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
+    if (a3 == FAIRY2I_ALGO_TCGEN05_DQ) return run_dq(qs, xs, ys, count, M, T, s);
     return run_lut(qs, xs, ys, count, M, T, ws, ws_bytes, s);
   }
-  if (algo == FAIRY2I_ALGO_LUT) return fail(FAIRY2I_ERR_UNSUPPORTED, "the table-lookup decode reads layout 3 only");
+  if (algo == FAIRY2I_ALGO_LUT || algo == FAIRY2I_ALGO_TCGEN05_DQ)
+    return fail(FAIRY2I_ERR_UNSUPPORTED, "the table-lookup decode and the dequantized GEMM read layout 3 only");
   (void)ws;
   (void)ws_bytes;
   if (M == 0) return ok();  // no tokens: nothing is read or written

@@ -105,10 +105,13 @@ typedef enum {
     FAIRY2I_ALGO_TCGEN05 = 3, /* prefill: codes expanded to bf16 in shared memory, tcgen05.mma */
     FAIRY2I_ALGO_TCGEN05_SP = 4, /* decode, M <= 8, T <= 4: 2:4-sparse tcgen05.mma.sp (e4m3 signs and axis
                                    flags as metadata in tensor memory; x as two exact e4m3 terms) */
-    FAIRY2I_ALGO_LUT = 5      /* layout 3, T <= 4: per window of 256 columns and token, tables of the
+    FAIRY2I_ALGO_LUT = 5,     /* layout 3, T <= 4: per window of 256 columns and token, tables of the
                                  256 signed sums of every 8 activations (fp16 entries, each the fp32 sum
                                  rounded once, activations scaled by a power of two per window); per
                                  code byte one shared-memory lookup and two fp32 adds */
+    FAIRY2I_ALGO_TCGEN05_DQ = 6 /* layout 3, T <= 4, m a multiple of 8: tcgen05 GEMM of the dequantized
+                                 real matrix (Theorem 1 rebuilt from the summed stages) as two bfloat16
+                                 terms hi + lo against x; no workspace */
 } fairy2i_algo;
 
 /* Bytes of the code planes of an n x m layer with T stages in layout
@@ -187,6 +190,12 @@ fairy2i_status fairy2i_linear_ex(const fairy2i_packed *q, const void *x, int64_t
 fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const *xs,
                                     float *const *ys, int32_t count, int64_t M,
                                     fairy2i_algo algo, void *stream);
+
+/* Layout-3 layers through fairy2i_linear / _ex / _group (no workspace) take
+ * the dequantized GEMM (FAIRY2I_ALGO_TCGEN05_DQ; "Fairy2i: Ultra-Low-Bit ...",
+ * Step 3: the stages add up to one matrix, and Step 1: its real form); with a
+ * workspace (the *_ws calls below) AUTO takes the table-lookup decode below 16
+ * tokens and the dequantized GEMM from 16 tokens. */
 
 /* The layer through the table-lookup decode (same y as fairy2i_linear; "Fairy2i:
  * Ultra-Low-Bit ...", "Industry implications: multiplication-free inference":

@@ -103,8 +103,9 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.fairy2i_linear(ctypes.byref(d), p, -1, p, None) == 2
     assert lib.fairy2i_linear(ctypes.byref(d), ctypes.c_void_p(258), 1, p, None) == 1
     assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 7, None) == 1
-    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 6, None) == 1
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, -1, None) == 1
     assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 5, None) == 4  # the table lookup reads layout 3 only
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 6, None) == 4  # so does the dequantized GEMM
     # the sparse tensor-core decode takes at most 8 tokens and 4 stages (checked before any launch)
     assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 9, p, 4, None) == 4
     t5 = _desc(T=5)
@@ -174,7 +175,8 @@ def test_python_wrappers_reject_host_tensors(lib):
     with pytest.raises(ValueError):
         f2i.linear_grad_x(q, torch.zeros((1, 8)))  # host tensor
     # the algorithm names map onto the header's fairy2i_algo values
-    assert f2i.ALGO == {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4, "lut": 5}
+    assert f2i.ALGO == {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4, "lut": 5,
+                        "tcgen05_dq": 6}
 
 
 def test_layout3_sizes(lib):
@@ -212,7 +214,9 @@ def test_layout3_host_errors(lib):
     p = ctypes.c_void_p(256)
     L3 = f2i.LAYOUT_LUT
     d = _desc(n=4, m=600, T=2, version=L3)
-    assert lib.fairy2i_linear(ctypes.byref(d), p, 1, p, None) == 4  # needs the workspace entry point
+    # without a workspace the table lookup is refused; m = 600 is a multiple of 8, so AUTO takes
+    # the dequantized GEMM (which would launch, so it is not called here without a GPU)
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 5, None) == 4
     assert "workspace" in _err(lib)
     assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 1, p, 0, None, 0, None) == 1  # workspace missing
     assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 1, p, 0, p, 16, None) == 1  # workspace too small

@@ -272,8 +272,8 @@ def test_lut_errors():
     import ctypes
     d = q.desc()
     y = torch.empty((1, 80), device="cuda")
-    # plain entry point: layout 3 needs the workspace entry point
-    assert lib.fairy2i_linear(ctypes.byref(d), x.data_ptr(), 1, y.data_ptr(), None) == 4
+    # plain entry point: the table lookup needs the workspace entry point
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), x.data_ptr(), 1, y.data_ptr(), 5, None) == 4
     need = lib.fairy2i_linear_workspace_bytes(ctypes.byref(d), 1, 1)
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     assert lib.fairy2i_linear_ws(ctypes.byref(d), x.data_ptr(), 1, y.data_ptr(), 0, ws.data_ptr(), need - 1,
@@ -344,3 +344,107 @@ def test_full_size_block_group_layout3_sampled(M):
         y = y.cpu().numpy()
         got = np.concatenate([y[:, rows], y[:, q.n + rows]], axis=1)
         assert rel_l2(got, want) <= REL_L2
+
+
+# ---------------------------------------------------------------------------
+# the dequantized GEMM over layout 3 (FAIRY2I_ALGO_TCGEN05_DQ)
+# ---------------------------------------------------------------------------
+# R^ is carried as two bfloat16 terms (<= 2^-18 relative per entry) and summed in fp32 by
+# the tensor cores over 2 (2m) / 16 steps (up to 1376 for m = 5504; each may lose up to
+# 2^-23 of the running sum if the adder truncates): bar 1e-4, ten times inside the
+# layer's 1e-3 (measured 1.06e-5 on the full-size block with outliers)
+DQ_REL_L2 = 1e-4
+DQ_SHAPES = [(8, 64), (37, 136), (33, 200), (256, 256), (300, 704), (64, 1024), (40, 320), (130, 2056)]
+
+
+@pytest.mark.parametrize("n,m", DQ_SHAPES)
+@pytest.mark.parametrize("M", [1, 7, 256, 300])
+def test_dq_parity(n, m, M):
+    R = _R(n, m, 11 * n + m)
+    q = _gpu_layer(R, 2)
+    qU, qW = _oracle_layer(R, 2)
+    x = _x(M, m, n + 3 * m)
+    y = f2i.linear(q, x.cuda(), algo="tcgen05_dq").cpu().numpy()
+    err = rel_l2(y, oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x)))
+    assert err <= DQ_REL_L2, err
+
+
+@pytest.mark.parametrize("T", [1, 3, 4])
+def test_dq_parity_stages(T):
+    n, m, M = 72, 520, 40
+    R = _R(n, m, 60 + T)
+    q = _gpu_layer(R, T)
+    qU, qW = _oracle_layer(R, T)
+    x = _x(M, m, 19 + T, outliers=True)
+    y = f2i.linear(q, x.cuda(), algo="tcgen05_dq").cpu().numpy()
+    assert rel_l2(y, oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x))) <= DQ_REL_L2
+
+
+def test_dq_plain_entry_and_auto():
+    """Layout 3 through the plain entry points (no workspace) takes the dequantized
+    GEMM at any token count; with a workspace AUTO switches to it from 16 tokens."""
+    import ctypes
+    n, m = 100, 600
+    R = _R(n, m, 5)
+    q = _gpu_layer(R, 2)
+    qU, qW = _oracle_layer(R, 2)
+    lib = f2i.load_library()
+    for M in (1, 20):
+        x = _x(M, m, 30 + M)
+        xd = x.cuda()
+        y = torch.empty((M, 2 * n), device="cuda")
+        d = q.desc()
+        assert lib.fairy2i_linear(ctypes.byref(d), xd.data_ptr(), M, y.data_ptr(), None) == 0
+        want = oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x))
+        assert rel_l2(y.cpu().numpy(), want) <= DQ_REL_L2
+        assert rel_l2(f2i.linear(q, xd).cpu().numpy(), want) <= REL_L2  # AUTO with the binding's workspace
+    # m not a multiple of 8: the dequantized GEMM is refused, so the plain entry has
+    # nothing to run; with a workspace the table lookup serves at any token count
+    R7 = _R(16, 100, 6)
+    q7 = _gpu_layer(R7, 2)
+    x7 = _x(40, 100, 7)
+    d7 = q7.desc()
+    y7 = torch.empty((40, 32), device="cuda")
+    xd7 = x7.cuda()
+    assert lib.fairy2i_linear(ctypes.byref(d7), xd7.data_ptr(), 40, y7.data_ptr(), None) == 4
+    assert lib.fairy2i_linear_ex(ctypes.byref(d7), xd7.data_ptr(), 40, y7.data_ptr(), 6, None) == 4
+    qU7, qW7 = _oracle_layer(R7, 2)
+    want7 = oracle.linear_mulfree(qU7, qW7, inputs.bf16_bits(x7))
+    assert rel_l2(f2i.linear(q7, xd7).cpu().numpy(), want7) <= REL_L2
+
+
+def test_dq_group_over_several_launches():
+    shapes = [(40 + 8 * i, 256 + 64 * (i % 5)) for i in range(11)]  # 11 layers: two launches of <= 8
+    qs, xs, wants = [], [], []
+    for i, (n, m) in enumerate(shapes):
+        R = _R(n, m, 900 + i)
+        qs.append(_gpu_layer(R, 2))
+        x = _x(33, m, 950 + i)
+        xs.append(x.cuda())
+        qU, qW = _oracle_layer(R, 2)
+        wants.append(oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x)))
+    ys = f2i.linear_group(qs, xs, algo="tcgen05_dq")
+    for y, want in zip(ys, wants):
+        assert rel_l2(y.cpu().numpy(), want) <= DQ_REL_L2
+
+
+def test_dq_full_size_block_prefill_sampled():
+    """The seven LLaMA-2-7B projections at 2048 tokens with 1 % outliers x10 (the
+    prefill workload), one grouped call, against the oracle on sampled rows."""
+    M = 2048
+    qs, xs, samples = [], [], []
+    for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
+        n = out_f // 2
+        R = inputs.weight_R(4, pi, out_f, in_f)
+        qs.append(f2i.convert_quantize(R.cuda(), 2, layout=L3))
+        x = inputs.activations(4, pi, M, in_f, outliers=True)
+        xs.append(x.cuda())
+        rows = _sample_rows(n, count=6, seed=pi)
+        qU, qW = _oracle_rows(R, rows, 2)
+        toks = np.array([0, 1, 255, 256, 1000, M - 1])
+        samples.append((rows, toks, oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x[toks]))))
+    ys = f2i.linear_group(qs, xs, algo="tcgen05_dq")
+    for q, y, (rows, toks, want) in zip(qs, ys, samples):
+        y = y.cpu().numpy()[toks]
+        got = np.concatenate([y[:, rows], y[:, q.n + rows]], axis=1)
+        assert rel_l2(got, want) <= DQ_REL_L2
