@@ -325,20 +325,24 @@ fairy2i_status make_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t m)
   return FAIRY2I_OK;
 }
 
-// x [M][2m] bfloat16 as a [M][2m] tensor: tiles of 256 tokens x 64 columns,
-// 128-byte swizzle, zero fill outside (the dequantized GEMM's B operand).
-fairy2i_status make_x_map_rows(CUtensorMap* map, const void* x, int64_t M, int64_t m) {
+// One half of x [M][2m] bfloat16 (half 0: Re x, columns 0..m-1; half 1: Im x)
+// as a [M][m] tensor with row pitch 2m: tiles of 256 tokens x 64 columns,
+// 128-byte swizzle, zero fill past m columns and M tokens (the dequantized
+// GEMM's B operand).  The Im half starts 2m bytes in: 16-byte aligned for m a
+// multiple of 8.
+fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64_t m, int half) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   fairy2i_status st = tensor_map_encoder(enc);
   if (st != FAIRY2I_OK) return st;
-  const cuuint64_t dims[2] = {(cuuint64_t)(2 * m), (cuuint64_t)M};
+  const cuuint64_t dims[2] = {(cuuint64_t)m, (cuuint64_t)M};
   const cuuint64_t strides[1] = {(cuuint64_t)m * 4};
   const cuuint32_t box[2] = {(cuuint32_t)f2i::kDqBK, (cuuint32_t)f2i::kDqBN};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+  void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(x) + (half ? 2 * m : 0));
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(FAIRY2I_ERR_CUDA, "cuTensorMapEncodeTiled (x rows) failed (%d)", (int)r);
+  if (r != CUDA_SUCCESS) return fail(FAIRY2I_ERR_CUDA, "cuTensorMapEncodeTiled (x half %d) failed (%d)", half, (int)r);
   return FAIRY2I_OK;
 }
 
@@ -366,8 +370,10 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
     int64_t tiles = 0;
     for (int i = 0; i < cnt; ++i) {
       const fairy2i_packed& q = qs[p0 + i];
-      fairy2i_status st = make_x_map_rows(&P.tmap[i], xs[p0 + i], M, q.m);
-      if (st != FAIRY2I_OK) return st;
+      for (int half = 0; half < 2; ++half) {
+        fairy2i_status st = make_x_map_half(&P.tmap[2 * i + half], xs[p0 + i], M, q.m, half);
+        if (st != FAIRY2I_OK) return st;
+      }
       f2i::DqProblem& pr = P.p[i];
       pr.codes = static_cast<const uint8_t*>(q.codes);
       pr.scales = q.scales;

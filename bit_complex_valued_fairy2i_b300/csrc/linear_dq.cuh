@@ -23,12 +23,13 @@
 //         the two stages of a pair filled by one decode;
 //   A:    hi and lo, 128-byte swizzled K-major, written by 8 producer warps
 //         from the layout-3 codes and the scales;
-//   B:    x [M][2m] bfloat16 by TMA (128-byte swizzle, zero fill past the
-//         edges); columns past m of a Re-x block are cancelled by zero rows of A;
+//   B:    x [M][2m] bfloat16 by TMA through two maps, one per half of x~
+//         (128-byte swizzle, zero fill past m columns and M tokens), so that
+//         the columns of A past m (decoded from zero code bits) meet zeros;
 //   D:    fp32 in TMEM, two accumulators of 256 columns (double buffered).
-// Warp roles (14 warps, one CTA per SM, persistent over tiles): warp 0 TMA
-// for B, warp 1 TMEM allocation and MMA issue, warps 2-9 A producers, warps
-// 10-13 epilogue (tcgen05.ld, stores of y).  All mbarrier waits are bounded.
+// Warp roles (22 warps, one CTA per SM, persistent over tiles): warp 0 TMA
+// for B, warp 1 TMEM allocation and MMA issue, warps 2-17 A producers, warps
+// 18-21 epilogue (tcgen05.ld, stores of y).  All mbarrier waits are bounded.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -45,7 +46,7 @@ constexpr int kDqBK = 64;   // columns per k-block
 constexpr int kDqATerm = kDqBM * kDqBK * 2;   // 16 KB: one term of A
 constexpr int kDqAStage = 2 * kDqATerm;       // hi and lo
 constexpr int kDqBStage = kDqBN * kDqBK * 2;  // 32 KB
-constexpr int kDqProducerWarps = 8;
+constexpr int kDqProducerWarps = 16;
 constexpr int kDqThreads = 32 * (6 + kDqProducerWarps);
 constexpr uint32_t kDqTmemCols = 512;
 constexpr size_t kDqSmemBytes = 1024 + (size_t)kDqStages * (kDqAStage + kDqBStage) + 256;
@@ -63,7 +64,7 @@ struct DqProblem {
 };
 
 struct DqParams {
-  CUtensorMap tmap[kDqMaxGroup];  // x of each problem as a [M][2m] bfloat16 tensor
+  CUtensorMap tmap[2 * kDqMaxGroup];  // per problem: Re x and Im x, each a [M][m] view of x [M][2m]
   DqProblem p[kDqMaxGroup];
   int64_t total_tiles;
   int32_t count, T, M, pad_;
@@ -85,13 +86,34 @@ __device__ __forceinline__ DqTile dq_tile(const DqParams& P, int64_t tile) {
   return c;
 }
 
-// bfloat16 bits of v rounded to nearest even, and of the remainder.
-__device__ __forceinline__ void dq_split(float v, uint32_t& hi, uint32_t& lo) {
-  __nv_bfloat16 h = __float2bfloat16_rn(v);
-  const float hf = __bfloat162float(h);
-  __nv_bfloat16 l = __float2bfloat16_rn(v - hf);  // v - hf is exact in fp32
-  hi = (uint32_t)__bfloat16_as_ushort(h);
-  lo = (uint32_t)__bfloat16_as_ushort(l);
+// bfloat16 pairs of (a, b) rounded to nearest even (a in the low half), and
+// of the remainders a - hi, b - hi (exact in fp32): hi + lo carries each value
+// to 2^-18 relative.
+__device__ __forceinline__ void dq_split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  uint32_t h, l;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(b), "f"(a));
+  const float ra = a - __uint_as_float(h << 16), rb = b - __uint_as_float(h & 0xFFFF0000u);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(l) : "f"(rb), "f"(ra));
+  hi = h;
+  lo = l;
+}
+
+// One code of one stage added to (re, im): column E of a group whose sign bits
+// are s and imaginary-axis flags f; the value is +-s_re on the real axis or
+// +-s_im on the imaginary one.
+template <int E>
+__device__ __forceinline__ void dq_code(float& re, float& im, uint32_t s, uint32_t f, uint32_t sre, uint32_t sim) {
+  asm("{\n\t.reg .pred p;\n\t.reg .b32 t, v;\n\t"
+      "and.b32 t, %2, %6;\n\t"
+      "setp.ne.u32 p, t, 0;\n\t"
+      "selp.b32 v, %5, %4, p;\n\t"
+      "shl.b32 t, %3, %7;\n\t"
+      "and.b32 t, t, 0x80000000;\n\t"
+      "xor.b32 v, v, t;\n\t"
+      "@p add.f32 %1, %1, v;\n\t"
+      "@!p add.f32 %0, %0, v;\n\t}"
+      : "+f"(re), "+f"(im)
+      : "r"(f), "r"(s), "r"(sre), "r"(sim), "n"(1u << E), "n"(31 - E));
 }
 
 template <int T>
@@ -129,7 +151,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0)
-    for (int i = 0; i < P.count; ++i) tma_prefetch_map(&P.tmap[i]);
+    for (int i = 0; i < 2 * P.count; ++i) tma_prefetch_map(&P.tmap[i]);
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kDqTmemCols);
     tmem_relinquish();
@@ -155,8 +177,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
             break;
           }
           mbar_arrive_expect_tx(full_bar(s), (uint32_t)kDqBStage);
-          const int col = (kb & 1) * pr.m + (kb >> 1) * kDqBK;
-          tma_load_2d(sB + (uint32_t)s * kDqBStage, &P.tmap[c.pi], full_bar(s), col, c.tt * kDqBN);
+          tma_load_2d(sB + (uint32_t)s * kDqBStage, &P.tmap[2 * c.pi + (kb & 1)], full_bar(s), (kb >> 1) * kDqBK,
+                      c.tt * kDqBN);
         }
       }
       for (uint32_t k = (it > (uint32_t)kDqStages ? it - kDqStages : 0u); k < it; ++k)
@@ -196,12 +218,16 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
     }
   } else if (warp < 2 + kDqProducerWarps) {
     // ---------------- A producers: codes + scales -> R^ hi / lo ----------------
-    // Thread (jl, qt) owns output jl of the tile (rows 2 jl, 2 jl + 1) and
-    // columns 16 qt .. 16 qt + 15 of every 64-column block, i.e. groups
-    // 2 qt, 2 qt + 1 of the block: one 16-byte layout-3 chunk per plane.
-    const int pt = tid - 64;  // 0..255
-    const int jl = pt >> 2, qt = pt & 3;
+    // Thread (jl, gq) owns output jl of the tile (rows 2 jl, 2 jl + 1) and
+    // group gq (columns 8 gq .. 8 gq + 7) of every 64-column block: one byte
+    // of signs and one of flags per stage plane, out of the row's 16-byte
+    // layout-3 chunk.  The eight lanes of a quarter warp share jl and write
+    // the eight 16-byte chunks of a 128-byte row: no bank conflicts.
+    const int pt = tid - 64;  // 0..511
+    const int jl = pt >> 3, gq = pt & 7;
     const uint32_t row0 = (uint32_t)(2 * jl), row1 = row0 + 1u;
+    const uint32_t o0 = row0 * 128u + (((uint32_t)gq ^ (row0 & 7u)) << 4);
+    const uint32_t o1 = row1 * 128u + (((uint32_t)gq ^ (row1 & 7u)) << 4);
     uint32_t it = 0;
     bool ok = true;
     for (int64_t tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
@@ -211,50 +237,44 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
       const int64_t j = (int64_t)c.rt * 64 + jl;
       const bool live = j < n;
       const int r = (int)(j & 31);
-      // the row's scales (zero past n): [plane][axis]
-      float sre[NP], sim[NP];
+      const uint32_t sel = (uint32_t)l3_byte_of(gq, r);  // byte of the group in both halves of the chunk
+      // the row's scales as bits (zero past n): [plane][axis]
+      uint32_t sre[NP], sim[NP];
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
-        sre[p] = live ? __ldg(pr.scales + (int64_t)(2 * p) * n + j) : 0.0f;
-        sim[p] = live ? __ldg(pr.scales + (int64_t)(2 * p + 1) * n + j) : 0.0f;
+        sre[p] = live ? __float_as_uint(__ldg(pr.scales + (int64_t)(2 * p) * n + j)) : 0u;
+        sim[p] = live ? __float_as_uint(__ldg(pr.scales + (int64_t)(2 * p + 1) * n + j)) : 0u;
       }
       for (int kp = 0; ok && kp < pr.kpairs; ++kp) {
-        // decode 16 columns: (Re, Im) of U^ and W^ in fp32
-        const int64_t c0 = (int64_t)kp * 64 + 16 * qt;  // first column of this thread
-        float ur[16], ui[16], wr[16], wi[16];
+        // (Re, Im) of U^ [0] and W^ [1] for the group's 8 columns, in fp32;
+        // columns past m decode from zero bits and meet zero-filled x
+        float re[2][8], im[2][8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ur[e] = ui[e] = wr[e] = wi[e] = 0.0f;
-        if (live && c0 < m) {
-          const int64_t g0 = c0 >> 3;  // global group of the first 8 columns
-          const int64_t w = g0 >> 5;
-          const int gw = (int)(g0 & 31);
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) re[x][e] = im[x][e] = 0.0f;
+        if (live) {
+          const int64_t w = kp >> 2;
           const int nb = l3_slots(m, w);
-          const uint32_t slot_off = (uint32_t)l3_slot_of(gw, r, nb) * kL3SlotBytes + (uint32_t)r * 16u;
-          const int by0 = l3_byte_of(gw, r), by1 = l3_byte_of(gw + 1, r);
+          const int slot = (kp & 3) ^ ((r >> 3) & (nb - 1));
+          const uint8_t* base = pr.codes + l3_offset(n, m, T, w, j >> 5, 0) + slot * kL3SlotBytes + r * 16;
+          const int pstride = nb * kL3SlotBytes;
 #pragma unroll
           for (int p = 0; p < NP; ++p) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(pr.codes + l3_offset(n, m, T, w, j >> 5, p) + slot_off));
-            const uint32_t sw[2] = {v.x, v.y}, qw[2] = {v.z, v.w};
-            const uint32_t s16 = ((sw[by0 >> 2] >> (8 * (by0 & 3))) & 0xFFu) | (((sw[by1 >> 2] >> (8 * (by1 & 3))) & 0xFFu) << 8);
-            const uint32_t q16 = ((qw[by0 >> 2] >> (8 * (by0 & 3))) & 0xFFu) | (((qw[by1 >> 2] >> (8 * (by1 & 3))) & 0xFFu) << 8);
-            const uint32_t f16 = s16 ^ q16;  // imaginary-axis flags
-            const bool isU = p < T;
-            // columns past m read as zero (their codes are zero bits, i.e. +1)
-            const uint32_t cmask = m - c0 >= 16 ? 0xFFFFu : ((1u << (uint32_t)(m - c0)) - 1u);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              if (!((cmask >> e) & 1u)) continue;
-              const uint32_t sneg = (s16 >> e) & 1u, fim = (f16 >> e) & 1u;
-              const float mag = fim ? sim[p] : sre[p];
-              const float val = __uint_as_float(__float_as_uint(mag) ^ (sneg << 31));
-              if (isU) {
-                ur[e] += fim ? 0.0f : val;
-                ui[e] += fim ? val : 0.0f;
-              } else {
-                wr[e] += fim ? 0.0f : val;
-                wi[e] += fim ? val : 0.0f;
-              }
-            }
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + p * pstride));
+            uint32_t sb, qb;
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sb) : "r"(v.x), "r"(v.y), "r"(sel));
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(qb) : "r"(v.z), "r"(v.w), "r"(sel));
+            const uint32_t fb = sb ^ qb;  // imaginary-axis flags
+            const int x = p < T ? 0 : 1;
+            dq_code<0>(re[x][0], im[x][0], sb, fb, sre[p], sim[p]);
+            dq_code<1>(re[x][1], im[x][1], sb, fb, sre[p], sim[p]);
+            dq_code<2>(re[x][2], im[x][2], sb, fb, sre[p], sim[p]);
+            dq_code<3>(re[x][3], im[x][3], sb, fb, sre[p], sim[p]);
+            dq_code<4>(re[x][4], im[x][4], sb, fb, sre[p], sim[p]);
+            dq_code<5>(re[x][5], im[x][5], sb, fb, sre[p], sim[p]);
+            dq_code<6>(re[x][6], im[x][6], sb, fb, sre[p], sim[p]);
+            dq_code<7>(re[x][7], im[x][7], sb, fb, sre[p], sim[p]);
           }
         }
         // both stages of the pair: k-block 2 kp (Re x columns) and 2 kp + 1 (Im x columns)
@@ -273,49 +293,30 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
           // row 2 jl: Re y, row 2 jl + 1: Im y
           //   Re x block: R^11 = ReU + ReW, R^21 = ImU + ImW
           //   Im x block: R^12 = ImW - ImU, R^22 = ReU - ReW
-          uint32_t h0[8], l0[8], h1[8], l1[8];  // packed pairs of bfloat16 for 16 columns
+          uint32_t h0[4], l0[4], h1[4], l1[4];
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            float a0, a1, b0v, b1v;
+          for (int e = 0; e < 8; e += 2) {
             if (h == 0) {
-              a0 = ur[e] + wr[e];
-              a1 = ur[e + 1] + wr[e + 1];
-              b0v = ui[e] + wi[e];
-              b1v = ui[e + 1] + wi[e + 1];
+              dq_split2(re[0][e] + re[1][e], re[0][e + 1] + re[1][e + 1], h0[e >> 1], l0[e >> 1]);
+              dq_split2(im[0][e] + im[1][e], im[0][e + 1] + im[1][e + 1], h1[e >> 1], l1[e >> 1]);
             } else {
-              a0 = wi[e] - ui[e];
-              a1 = wi[e + 1] - ui[e + 1];
-              b0v = ur[e] - wr[e];
-              b1v = ur[e + 1] - wr[e + 1];
+              dq_split2(im[1][e] - im[0][e], im[1][e + 1] - im[0][e + 1], h0[e >> 1], l0[e >> 1]);
+              dq_split2(re[0][e] - re[1][e], re[0][e + 1] - re[1][e + 1], h1[e >> 1], l1[e >> 1]);
             }
-            uint32_t x0, y0, x1, y1;
-            dq_split(a0, x0, y0);
-            dq_split(a1, x1, y1);
-            h0[e >> 1] = x0 | (x1 << 16);
-            l0[e >> 1] = y0 | (y1 << 16);
-            dq_split(b0v, x0, y0);
-            dq_split(b1v, x1, y1);
-            h1[e >> 1] = x0 | (x1 << 16);
-            l1[e >> 1] = y0 | (y1 << 16);
           }
           const uint32_t st = sA + (uint32_t)s * kDqAStage;
-#pragma unroll
-          for (int hc = 0; hc < 2; ++hc) {
-            const uint32_t cc = (uint32_t)(2 * qt + hc);  // 16-byte chunk of the 128-byte row
-            const uint32_t o0 = row0 * 128u + ((cc ^ (row0 & 7u)) << 4), o1 = row1 * 128u + ((cc ^ (row1 & 7u)) << 4);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + o0), "r"(h0[4 * hc]), "r"(h0[4 * hc + 1]),
-                         "r"(h0[4 * hc + 2]), "r"(h0[4 * hc + 3])
-                         : "memory");
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + o1), "r"(h1[4 * hc]), "r"(h1[4 * hc + 1]),
-                         "r"(h1[4 * hc + 2]), "r"(h1[4 * hc + 3])
-                         : "memory");
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + kDqATerm + o0), "r"(l0[4 * hc]),
-                         "r"(l0[4 * hc + 1]), "r"(l0[4 * hc + 2]), "r"(l0[4 * hc + 3])
-                         : "memory");
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + kDqATerm + o1), "r"(l1[4 * hc]),
-                         "r"(l1[4 * hc + 1]), "r"(l1[4 * hc + 2]), "r"(l1[4 * hc + 3])
-                         : "memory");
-          }
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + o0), "r"(h0[0]), "r"(h0[1]), "r"(h0[2]),
+                       "r"(h0[3])
+                       : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + o1), "r"(h1[0]), "r"(h1[1]), "r"(h1[2]),
+                       "r"(h1[3])
+                       : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + kDqATerm + o0), "r"(l0[0]), "r"(l0[1]),
+                       "r"(l0[2]), "r"(l0[3])
+                       : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + kDqATerm + o1), "r"(l1[0]), "r"(l1[1]),
+                       "r"(l1[2]), "r"(l1[3])
+                       : "memory");
           fence_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(full_bar(s));
