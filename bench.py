@@ -396,8 +396,10 @@ def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
 def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int = 4):
     """Batched decode sweep: per token count M and per algorithm, the 7 projections of
     `blocks` distinct blocks (205 MB at 4 blocks, above L2), one grouped call per block;
-    time per block, weight GB/s and tokens/s-equivalent.  "lut" reads the same weights in
-    layout 3 (one decode launch per 4 tokens at T = 2, plus the window-combining launch)."""
+    time per block, weight GB/s and tokens/s-equivalent.  "lut", "tcgen05_dq" and
+    "auto_layout3" read the same weights in layout 3 (the table lookup: one decode launch
+    per 4 tokens at T = 2, plus the window-combining launch; the dequantized GEMM: one
+    launch with N = M rounded up to 16)."""
     stack, stack3, xs_full = [], [], []
     for b in range(blocks):
         qs, qs3, xb = [], [], []
@@ -418,8 +420,10 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
         xs = [[x[:M].contiguous() for x in xb] for xb in xs_full]
         ys = [[torch.empty((M, 2 * q.n), dtype=torch.float32, device=dev) for q in qs] for qs in stack]
         row = {"M": M}
-        for algo in ("lut", "mma", "tcgen05", "auto") + (("tcgen05_sp",) if M <= 8 else ()):
-            st = stack3 if algo == "lut" else stack
+        for key in ("lut", "tcgen05_dq", "auto_layout3", "mma", "tcgen05", "auto") + \
+                (("tcgen05_sp",) if M <= 8 else ()):
+            st = stack3 if key in ("lut", "tcgen05_dq", "auto_layout3") else stack
+            algo = "auto" if key == "auto_layout3" else key
 
             def step():
                 for b in range(blocks):
@@ -434,7 +438,7 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
             stop.record(stream)
             torch.cuda.synchronize()
             us = start.elapsed_time(stop) / reps / blocks * 1e3
-            row[algo] = {"us_per_block": round(us, 2), "weight_GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+            row[key] = {"us_per_block": round(us, 2), "weight_GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
                          "tokens_per_s_per_block": round(M / (us * 1e-6))}
         out.append(row)
     f2i.sync_status()

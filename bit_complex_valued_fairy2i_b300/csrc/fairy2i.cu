@@ -326,17 +326,17 @@ fairy2i_status make_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t m)
 }
 
 // One half of x [M][2m] bfloat16 (half 0: Re x, columns 0..m-1; half 1: Im x)
-// as a [M][m] tensor with row pitch 2m: tiles of 256 tokens x 64 columns,
+// as a [M][m] tensor with row pitch 2m: tiles of N tokens x 64 columns,
 // 128-byte swizzle, zero fill past m columns and M tokens (the dequantized
 // GEMM's B operand).  The Im half starts 2m bytes in: 16-byte aligned for m a
 // multiple of 8.
-fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64_t m, int half) {
+fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64_t m, int half, int N) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   fairy2i_status st = tensor_map_encoder(enc);
   if (st != FAIRY2I_OK) return st;
   const cuuint64_t dims[2] = {(cuuint64_t)m, (cuuint64_t)M};
   const cuuint64_t strides[1] = {(cuuint64_t)m * 4};
-  const cuuint32_t box[2] = {(cuuint32_t)f2i::kDqBK, (cuuint32_t)f2i::kDqBN};
+  const cuuint32_t box[2] = {(cuuint32_t)f2i::kDqBK, (cuuint32_t)N};
   const cuuint32_t estr[2] = {1, 1};
   void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(x) + (half ? 2 * m : 0));
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
@@ -347,13 +347,49 @@ fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64
 }
 
 template <int T>
-fairy2i_status launch_dq_t(const f2i::DqParams& P, cudaStream_t s) {
+fairy2i_status launch_dq_t(const f2i::DqParams& P, int grid, cudaStream_t s) {
   auto k = f2i::linear_dq_kernel<T>;
   fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(k), f2i::kDqSmemBytes, "dequantized prefill");
   if (st != FAIRY2I_OK) return st;
-  const int64_t grid = std::min<int64_t>(P.total_tiles, sm_count());
   k<<<(unsigned)grid, f2i::kDqThreads, f2i::kDqSmemBytes, s>>>(P);
   return check_launch("dequantized prefill launch");
+}
+
+// Tiles of a launch that fits one or a few waves differ in length (a tile
+// costs one decode + MMA step per 128 columns of x~, plus its epilogue), so a
+// round-robin deal leaves some CTAs with far more steps than the mean. For up
+// to kDqSchedMax tiles the host deals them longest first, each to the CTA
+// with the least work so far; larger launches keep the round-robin deal.
+void dq_schedule(f2i::DqParams& P, int grid) {
+  P.sched_n = 0;
+  if (P.total_tiles > f2i::kDqSchedMax || grid > f2i::kDqMaxCtas || grid < 1) return;
+  std::vector<std::pair<int64_t, int>> order;  // (cost, tile)
+  order.reserve((size_t)P.total_tiles);
+  for (int i = 0; i < P.count; ++i) {
+    const f2i::DqProblem& pr = P.p[i];
+    const int64_t n_tiles = (int64_t)pr.row_tiles * pr.tok_tiles;
+    for (int64_t t = 0; t < n_tiles; ++t) order.emplace_back(pr.kpairs + 1, (int)(pr.tile_begin + t));
+  }
+  std::stable_sort(order.begin(), order.end(),
+                   [](const std::pair<int64_t, int>& a, const std::pair<int64_t, int>& b) { return a.first > b.first; });
+  using Load = std::pair<int64_t, int>;  // (work so far, cta)
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int b = 0; b < grid; ++b) heap.emplace(0, b);
+  std::vector<std::vector<int>> lists((size_t)grid);
+  for (const auto& o : order) {
+    Load l = heap.top();
+    heap.pop();
+    lists[(size_t)l.second].push_back(o.second);
+    l.first += o.first;
+    heap.push(l);
+  }
+  int k = 0;
+  for (int b = 0; b < grid; ++b) {
+    P.cta_begin[b] = (uint16_t)k;
+    for (int t : lists[(size_t)b]) P.sched[k++] = (uint16_t)t;
+  }
+  P.cta_begin[grid] = (uint16_t)k;
+  P.sched_n = k;
 }
 
 // The dense GEMM of the dequantized real matrix (layout 3, m a multiple of 8,
@@ -367,11 +403,12 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
     P.count = cnt;
     P.T = T;
     P.M = (int32_t)M;
+    P.N = M >= f2i::kDqBN ? f2i::kDqBN : (int32_t)((M + 15) / 16 * 16);  // the MMA's N: a multiple of 16
     int64_t tiles = 0;
     for (int i = 0; i < cnt; ++i) {
       const fairy2i_packed& q = qs[p0 + i];
       for (int half = 0; half < 2; ++half) {
-        fairy2i_status st = make_x_map_half(&P.tmap[2 * i + half], xs[p0 + i], M, q.m, half);
+        fairy2i_status st = make_x_map_half(&P.tmap[2 * i + half], xs[p0 + i], M, q.m, half, P.N);
         if (st != FAIRY2I_OK) return st;
       }
       f2i::DqProblem& pr = P.p[i];
@@ -381,18 +418,20 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
       pr.n = (int32_t)q.n;
       pr.m = (int32_t)q.m;
       pr.row_tiles = (int32_t)((q.n + 63) / 64);
-      pr.tok_tiles = (int32_t)((M + f2i::kDqBN - 1) / f2i::kDqBN);
+      pr.tok_tiles = (int32_t)((M + P.N - 1) / P.N);
       pr.kpairs = (int32_t)((q.m + f2i::kDqBK - 1) / f2i::kDqBK);
       pr.tile_begin = tiles;
       tiles += (int64_t)pr.row_tiles * pr.tok_tiles;
     }
     P.total_tiles = tiles;
+    const int grid = (int)std::min<int64_t>(tiles, sm_count());
+    dq_schedule(P, grid);
     fairy2i_status st;
     switch (T) {
-      case 1: st = launch_dq_t<1>(P, s); break;
-      case 2: st = launch_dq_t<2>(P, s); break;
-      case 3: st = launch_dq_t<3>(P, s); break;
-      case 4: st = launch_dq_t<4>(P, s); break;
+      case 1: st = launch_dq_t<1>(P, grid, s); break;
+      case 2: st = launch_dq_t<2>(P, grid, s); break;
+      case 3: st = launch_dq_t<3>(P, grid, s); break;
+      case 4: st = launch_dq_t<4>(P, grid, s); break;
       default: return fail(FAIRY2I_ERR_UNSUPPORTED, "dequantized prefill supports T <= 4");
     }
     if (st != FAIRY2I_OK) return st;

@@ -39,9 +39,11 @@
 namespace f2i {
 
 constexpr int kDqMaxGroup = 8;
+constexpr int kDqSchedMax = 2048;  // tiles a launch may list per CTA (longest first); more run round-robin
+constexpr int kDqMaxCtas = 256;
 constexpr int kDqStages = 3;
 constexpr int kDqBM = 128;  // real rows per tile (64 outputs)
-constexpr int kDqBN = 256;  // tokens per tile
+constexpr int kDqBN = 256;  // tokens per tile (at most; a launch takes N = M rounded up to 16 below 256)
 constexpr int kDqBK = 64;   // columns per k-block
 constexpr int kDqATerm = kDqBM * kDqBK * 2;   // 16 KB: one term of A
 constexpr int kDqAStage = 2 * kDqATerm;       // hi and lo
@@ -67,8 +69,23 @@ struct DqParams {
   CUtensorMap tmap[2 * kDqMaxGroup];  // per problem: Re x and Im x, each a [M][m] view of x [M][2m]
   DqProblem p[kDqMaxGroup];
   int64_t total_tiles;
-  int32_t count, T, M, pad_;
+  int32_t count, T, M;
+  int32_t N;        // tokens per tile: a multiple of 16 in [16, 256]
+  int32_t sched_n;  // 0: tile blockIdx.x + i gridDim.x; else the list below
+  int32_t pad_;
+  uint16_t cta_begin[kDqMaxCtas + 1];  // CTA b runs sched[cta_begin[b] .. cta_begin[b + 1])
+  uint16_t sched[kDqSchedMax];
 };
+
+// The i-th tile of this CTA, or -1 past its last.
+__device__ __forceinline__ int64_t dq_tile_id(const DqParams& P, int64_t i) {
+  if (P.sched_n == 0) {
+    const int64_t t = (int64_t)blockIdx.x + i * gridDim.x;
+    return t < P.total_tiles ? t : -1;
+  }
+  const int64_t k = (int64_t)P.cta_begin[blockIdx.x] + i;
+  return k < (int64_t)P.cta_begin[blockIdx.x + 1] ? (int64_t)P.sched[k] : -1;
+}
 
 struct DqTile {
   int pi;
@@ -120,7 +137,6 @@ template <int T>
 __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_constant__ DqParams P) {
   extern __shared__ uint8_t dq_smem_raw[];
   constexpr int NP = 2 * T;
-  constexpr uint32_t kIdesc = idesc_bf16(kDqBM, kDqBN);
 
   const uint32_t raw = smem_u32(dq_smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -166,7 +182,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+      for (int64_t i = 0; ok; ++i) {
+        const int64_t tile = dq_tile_id(P, i);
+        if (tile < 0) break;
         const DqTile c = dq_tile(P, tile);
         const DqProblem& pr = P.p[c.pi];
         for (int kb = 0; ok && kb < 2 * pr.kpairs; ++kb, ++it) {
@@ -176,9 +194,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(s), (uint32_t)kDqBStage);
+          mbar_arrive_expect_tx(full_bar(s), (uint32_t)P.N * (kDqBK * 2));
           tma_load_2d(sB + (uint32_t)s * kDqBStage, &P.tmap[2 * c.pi + (kb & 1)], full_bar(s), (kb >> 1) * kDqBK,
-                      c.tt * kDqBN);
+                      c.tt * P.N);
         }
       }
       for (uint32_t k = (it > (uint32_t)kDqStages ? it - kDqStages : 0u); k < it; ++k)
@@ -187,9 +205,12 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
   } else if (warp == 1) {
     // ---------------- MMA issuer: hi and lo into one accumulator ----------------
     if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kDqBM, P.N);
       uint32_t it = 0, lt = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x, ++lt) {
+      for (int64_t i = 0; ok; ++i, ++lt) {
+        const int64_t tile = dq_tile_id(P, i);
+        if (tile < 0) break;
         const DqTile c = dq_tile(P, tile);
         const int kbs = 2 * P.p[c.pi].kpairs;
         const int b = (int)(lt & 1u);
@@ -207,9 +228,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
           const uint32_t a0 = sA + (uint32_t)s * kDqAStage, b0 = sB + (uint32_t)s * kDqBStage;
 #pragma unroll
           for (int kk = 0; kk < kDqBK / 16; ++kk) {
-            tc_mma_bf16(d_tmem, sw128_desc(a0 + 32u * kk), sw128_desc(b0 + 32u * kk), kIdesc,
+            tc_mma_bf16(d_tmem, sw128_desc(a0 + 32u * kk), sw128_desc(b0 + 32u * kk), idesc,
                         (kb > 0 || kk > 0) ? 1u : 0u);
-            tc_mma_bf16(d_tmem, sw128_desc(a0 + kDqATerm + 32u * kk), sw128_desc(b0 + 32u * kk), kIdesc, 1u);
+            tc_mma_bf16(d_tmem, sw128_desc(a0 + kDqATerm + 32u * kk), sw128_desc(b0 + 32u * kk), idesc, 1u);
           }
           tc_commit(empty_bar(s));
         }
@@ -230,7 +251,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
     const uint32_t o1 = row1 * 128u + (((uint32_t)gq ^ (row1 & 7u)) << 4);
     uint32_t it = 0;
     bool ok = true;
-    for (int64_t tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+    for (int64_t i = 0; ok; ++i) {
+      const int64_t tile = dq_tile_id(P, i);
+      if (tile < 0) break;
       const DqTile c = dq_tile(P, tile);
       const DqProblem& pr = P.p[c.pi];
       const int64_t n = pr.n, m = pr.m;
@@ -329,7 +352,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
     const int rl = 32 * eq + lane;
     const int jl = rl >> 1, part = rl & 1;
     uint32_t lt = 0;
-    for (int64_t tile = blockIdx.x; tile < P.total_tiles; tile += gridDim.x, ++lt) {
+    for (int64_t i = 0;; ++i, ++lt) {
+      const int64_t tile = dq_tile_id(P, i);
+      if (tile < 0) break;
       const DqTile c = dq_tile(P, tile);
       const DqProblem& pr = P.p[c.pi];
       const int b = (int)(lt & 1u);
@@ -343,14 +368,14 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
       const int64_t ystride = 2 * (int64_t)pr.n;
       float* ycol = pr.y + (int64_t)part * pr.n + j;
 #pragma unroll 1
-      for (int cc = 0; cc < kDqBN / 32; ++cc) {
+      for (int cc = 0; cc < (P.N + 31) / 32; ++cc) {
         uint32_t v[32];
         tmem_ld32(tbase + 32u * cc, v);
         tmem_ld_wait();
         if (j < pr.n) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int64_t tok = (int64_t)c.tt * kDqBN + 32 * cc + e;
+            const int64_t tok = (int64_t)c.tt * P.N + 32 * cc + e;
             if (tok < P.M) ycol[tok * ystride] = __uint_as_float(v[e]);
           }
         }
