@@ -78,33 +78,17 @@ __device__ __forceinline__ int float_exponent(uint32_t bits) {
   return (31 - __clz((int)mant)) - 149;
 }
 
-// trunc(v * 2^(48-e)) for 0 <= v < 2^(e+1), exactly, by integer shifts.
-__device__ __forceinline__ long long scaled_trunc(uint32_t bits, int e) {
-  const uint32_t ef = bits >> 23;
-  uint64_t mant = bits & 0x7FFFFFu;
-  int ev;  // v = mant * 2^ev
-  if (ef == 0) {
-    ev = -149;
-  } else {
-    mant |= 0x800000u;
-    ev = (int)ef - 150;
-  }
-  const int sh = ev + 48 - e;
-  if (sh >= 0) return (long long)(mant << sh);  // < 2^49 by the bound on v
-  if (sh <= -64) return 0;
-  return (long long)(mant >> (-sh));
-}
-
-template <typename Tv>
-__device__ __forceinline__ Tv warp_sum(Tv v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ uint32_t warp_max(uint32_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+// trunc(v 2^(48-e)) for a finite v >= 0 below 2^(e+1), given the bits b of v
+// and c = 102 + e, with 32-bit integer operations and one widening multiply:
+// v = mant 2^(q-150) with q = max(exponent field, 1) and mant carrying the
+// implicit bit when the exponent field is non-zero, so the value is
+// mant 2^(q-c), a left shift of at most 25 or a truncating right shift.
+__device__ __forceinline__ unsigned long long scaled_trunc_int(uint32_t b, int c) {
+  const int q = max((int)(b >> 23), 1);
+  const uint32_t mant = b - ((uint32_t)(q - 1) << 23);
+  const int sh = q - c;
+  const uint32_t hi = __funnelshift_rc(mant, 0u, (uint32_t)max(-sh, 0));  // mant >> (c - q), 0 past 31
+  return (unsigned long long)hi * (unsigned long long)(1u << max(sh, 0));
 }
 
 // Column (inside its 64-column block) of weight c = 4 s + 2 h + e of the
@@ -113,67 +97,16 @@ __device__ __forceinline__ uint32_t warp_max(uint32_t v) {
 __host__ __device__ __forceinline__ int word_col(int c, int q) { return 16 * (c >> 2) + 8 * ((c >> 1) & 1) + 2 * q + (c & 1); }
 
 // One CTA per (output row j, matrix X).  Thread t owns WPT words of the row;
-// word w = 4 kb + q holds the 16 weights at columns 64 kb + word_col(c, q),
-// each code as two bits (sign, real-axis flag) at bits (2c + 1, 2c).
-// The weights stay in registers through all T stages, so HBM sees one read of
-// the row and one write of its codes and scales, and each word is assembled as
-// its codes are decided.  Row-wide maxima, counts and exact sums are block
-// reductions (warp shuffles, then one value per warp in shared memory).
+// a word holds 16 weights (layout 2: columns 64 kb + word_col(c, q) of word
+// w = 4 kb + q; layout 3: 16 consecutive columns) and, per stage, their
+// sign bits and real-axis bits as two 16-bit masks.  The weights stay in
+// registers through all T stages, so HBM sees one read of the row and one
+// write of its codes and scales.  Per stage two block reductions (maxima;
+// exact sums and counts), one barrier each; the scales are formed in every
+// warp and passed on by shuffles.
 constexpr int kQuantThreads = 512;  // words per thread: 1 for m <= 8192, 2 up to 16384
-
-template <typename Tv, typename Op>
-__device__ __forceinline__ void block_reduce2(Tv& a, Tv& b, Tv* sa, Tv* sb, Op op) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = op(a, __shfl_xor_sync(0xffffffffu, a, o));
-    b = op(b, __shfl_xor_sync(0xffffffffu, b, o));
-  }
-  if (lane == 0) {
-    sa[warp] = a;
-    sb[warp] = b;
-  }
-  __syncthreads();
-  a = sa[0];
-  b = sb[0];
-  for (int w = 1; w < nw; ++w) {
-    a = op(a, sa[w]);
-    b = op(b, sb[w]);
-  }
-  __syncthreads();  // sa / sb are reused by the next reduction
-}
-
-// Sums of two 64-bit and two 32-bit values over the block in one round (the
-// counts travel with the exact sums; both are needed only for the scale).
-__device__ __forceinline__ void block_sum_ll2_u2(long long& a, long long& b, uint32_t& c, uint32_t& d,
-                                                 long long* sa, long long* sb, uint32_t* sc, uint32_t* sd) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a += __shfl_xor_sync(0xffffffffu, a, o);
-    b += __shfl_xor_sync(0xffffffffu, b, o);
-    c += __shfl_xor_sync(0xffffffffu, c, o);
-    d += __shfl_xor_sync(0xffffffffu, d, o);
-  }
-  if (lane == 0) {
-    sa[warp] = a;
-    sb[warp] = b;
-    sc[warp] = c;
-    sd[warp] = d;
-  }
-  __syncthreads();
-  a = sa[0];
-  b = sb[0];
-  c = sc[0];
-  d = sd[0];
-  for (int w = 1; w < nw; ++w) {
-    a += sa[w];
-    b += sb[w];
-    c += sc[w];
-    d += sd[w];
-  }
-  __syncthreads();  // the buffers are reused by the next reduction
-}
+// One word per thread: at most 64 registers, so that 8 CTAs of 128 threads
+// (m = 2048) share an SM and hide each other's row loads and barriers.
 
 // Writes the zero 16-byte chunks of a padding row (j >= n) of layout 3: the
 // last row tile's rows past n must read as zero codes.
@@ -201,12 +134,15 @@ __device__ __forceinline__ void l3_zero_row(uint8_t* codes, int64_t n, int64_t m
 // differ).  For layout 3 the grid has a row for every row of the last tile,
 // and rows past n write zero chunks.
 template <int WPT, bool FUSED, int LAYOUT>
-__global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
+__global__ void __launch_bounds__(kQuantThreads, WPT == 1 ? 2 : 1) quantize_words_kernel(
     const float2* __restrict__ U, const float2* __restrict__ W, const float* __restrict__ R, int64_t n, int64_t m,
     int T, uint8_t* __restrict__ codes, float* __restrict__ scales) {
   constexpr int E = 16 * WPT;  // weights per thread
-  __shared__ uint32_t s_u[2][32];
-  __shared__ long long s_l[2][32];
+  // one array per block-wide reduction of a stage: a reduction's array is
+  // rewritten only after two other barriers, so one barrier per reduction
+  __shared__ uint32_t s_mx[2][32];
+  __shared__ unsigned long long s_sum[2][32];
+  __shared__ uint32_t s_cnt[2][32];
   __shared__ float s_scale[2];
 
   const int tid = threadIdx.x;
@@ -264,83 +200,139 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
   const int g = (int)(j & 7), rho = (int)((j >> 3) & 1);
   const int64_t rt = j >> 4;
 
+  const int lane = tid & 31, nwarps = (int)((blockDim.x + 31) >> 5);
   for (int t = 0; t < T; ++t) {
-    // codes: real axis iff |Re| >= |Im|; negative iff the chosen component is < 0
-    // (branch-free; columns outside the matrix keep zero code bits and count nowhere)
-    uint32_t word[WPT], realm[WPT];
-    uint32_t mx0 = 0, mx1 = 0, cnt0 = 0, cnt1 = 0;
+    // codes: real axis iff |Re| >= |Im|; negative iff the chosen component is
+    // < 0 (-0 counts as +).  Columns outside the matrix hold (0, 0): real, not
+    // negative, no weight in any maximum or sum; the masks drop them from the
+    // counts and the imaginary flags.
+    uint32_t sgn[WPT], realm[WPT];
+    uint32_t mx0 = 0, mx1 = 0;
 #pragma unroll
-    for (int u = 0; u < WPT; ++u) word[u] = realm[u] = 0;
+    for (int u = 0; u < WPT; ++u) sgn[u] = realm[u] = 0;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int u = e >> 4, c = e & 15;
-      const bool in = (valid[u] >> c) & 1u;
       const float ar = fabsf(re[e]), ai = fabsf(im[e]);
       const bool real = ar >= ai;
       const bool neg = real ? (re[e] < 0.0f) : (im[e] < 0.0f);
-      const bool isr = in && real, isi = in && !real;
-      word[u] |= (in ? (((neg ? 1u : 0u) << 1) | (real ? 1u : 0u)) : 0u) << (2 * c);
-      realm[u] |= (isr ? 1u : 0u) << c;
-      mx0 = max(mx0, isr ? __float_as_uint(ar) : 0u);
-      mx1 = max(mx1, isi ? __float_as_uint(ai) : 0u);
-      cnt0 += isr ? 1u : 0u;
-      cnt1 += isi ? 1u : 0u;
+      sgn[u] |= neg ? (1u << c) : 0u;
+      realm[u] |= real ? (1u << c) : 0u;
+      mx0 = max(mx0, real ? __float_as_uint(ar) : 0u);
+      mx1 = max(mx1, real ? 0u : __float_as_uint(ai));
     }
-    block_reduce2(mx0, mx1, s_u[0], s_u[1], [](uint32_t x, uint32_t y) { return max(x, y); });
+    uint32_t cnt0 = 0, cnt1 = 0;
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) {
+      realm[u] &= valid[u];
+      cnt0 += __popc(realm[u]);
+      cnt1 += __popc(valid[u] & ~realm[u]);
+    }
+    // block maxima (one barrier)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx0 = max(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = max(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    if (lane == 0) {
+      s_mx[0][tid >> 5] = mx0;
+      s_mx[1][tid >> 5] = mx1;
+    }
+    __syncthreads();
+    mx0 = s_mx[0][0];
+    mx1 = s_mx[1][0];
+    for (int w = 1; w < nwarps; ++w) {
+      mx0 = max(mx0, s_mx[0][w]);
+      mx1 = max(mx1, s_mx[1][w]);
+    }
     const int e0 = mx0 ? float_exponent(mx0) : 0;
     const int e1 = mx1 ? float_exponent(mx1) : 0;
 
-    // exact integer sums of trunc(|v| 2^(48-e)).  With 48 - e <= 127 the
-    // power of two is a float, |v| 2^(48-e) < 2^49 is exact (an exponent
-    // change) and the truncating conversion to u64 is exact; rows whose
-    // maximum is below 2^-79 take the integer-shift path (block-uniform).
-    long long ls0 = 0, ls1 = 0;
+    // exact integer sums of trunc(|v| 2^(48-e)) (each term < 2^49).  Rows
+    // with both maxima at or above 2^-79 take the fp32 path: t = |v| 2^(48-e)
+    // is an exponent change (exact), a round-toward-zero add of 2^23
+    // truncates it below 2^23 (above, t is an integer already), and
+    // round-to-nearest adds of 1.5 2^55 and 1.5 2^39 split it exactly into
+    // integer multiples of 2^32, 2^16 and 1; over at most 32 terms a thread's
+    // sum of each part stays below 2^22 units, so the fp32 sums are exact.
+    // Smaller rows take the integer-shift path (block-uniform branch).
+    unsigned long long ls0 = 0, ls1 = 0;
     if (e0 >= -79 && e1 >= -79) {
-      const float sc0 = __int_as_float((48 - e0 + 127) << 23), sc1 = __int_as_float((48 - e1 + 127) << 23);
+      const float p0 = __int_as_float((48 - e0 + 127) << 23), p1 = __int_as_float((48 - e1 + 127) << 23);
+      const float K1 = 54043195528445952.0f;  // 1.5 2^55
+      const float K2 = 824633720832.0f;       // 1.5 2^39
+      float a0 = 0.0f, b0 = 0.0f, z0 = 0.0f, a1 = 0.0f, b1 = 0.0f, z1 = 0.0f;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int u = e >> 4, c = e & 15;
-        const bool isr = (realm[u] >> c) & 1u, in = (valid[u] >> c) & 1u;
-        const float v = isr ? fabsf(re[e]) : fabsf(im[e]);
-        const long long val = (long long)__float2ull_rz(__fmul_rn(v, isr ? sc0 : sc1));
-        ls0 += isr ? val : 0ll;
-        ls1 += (in && !isr) ? val : 0ll;
+        const bool isr = (realm[u] >> c) & 1u;
+        const float t = __fmul_rn(isr ? fabsf(re[e]) : fabsf(im[e]), isr ? p0 : p1);
+        const float tt = t < 8388608.0f ? __fsub_rn(__fadd_rz(t, 8388608.0f), 8388608.0f) : t;
+        const float A = __fsub_rn(__fadd_rn(tt, K1), K1);
+        const float r1 = __fsub_rn(tt, A);
+        const float B = __fsub_rn(__fadd_rn(r1, K2), K2);
+        const float C = __fsub_rn(r1, B);
+        if (isr) {
+          a0 = __fadd_rn(a0, A);
+          b0 = __fadd_rn(b0, B);
+          z0 = __fadd_rn(z0, C);
+        } else {  // columns outside the matrix add 0
+          a1 = __fadd_rn(a1, A);
+          b1 = __fadd_rn(b1, B);
+          z1 = __fadd_rn(z1, C);
+        }
       }
+      auto whole = [](float a, float b, float z) -> unsigned long long {
+        const long long ia = __float2int_rz(__fmul_rn(a, 2.3283064365386963e-10f));  // a 2^-32
+        const long long ib = __float2int_rz(__fmul_rn(b, 1.52587890625e-05f));       // b 2^-16
+        return (unsigned long long)((ia << 32) + (ib << 16) + (long long)__float2int_rz(z));
+      };
+      ls0 = whole(a0, b0, z0);
+      ls1 = whole(a1, b1, z1);
     } else {
+      const int c0 = 102 + e0, c1 = 102 + e1;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int u = e >> 4, c = e & 15;
-        if (!((valid[u] >> c) & 1u)) continue;
-        if ((realm[u] >> c) & 1u) ls0 += scaled_trunc(__float_as_uint(fabsf(re[e])), e0);
-        else ls1 += scaled_trunc(__float_as_uint(fabsf(im[e])), e1);
+        const bool isr = (realm[u] >> c) & 1u;
+        const unsigned long long val =
+            scaled_trunc_int(__float_as_uint(isr ? fabsf(re[e]) : fabsf(im[e])), isr ? c0 : c1);
+        if (isr) ls0 += val;
+        else ls1 += val;  // columns outside the matrix add trunc(0) = 0
       }
     }
-    block_sum_ll2_u2(ls0, ls1, cnt0, cnt1, s_l[0], s_l[1], s_u[0], s_u[1]);
+    // block sums and counts (one barrier)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
+      cnt0 += __shfl_xor_sync(0xffffffffu, cnt0, o);
+      cnt1 += __shfl_xor_sync(0xffffffffu, cnt1, o);
+    }
+    if (lane == 0) {
+      s_sum[0][tid >> 5] = ls0;
+      s_sum[1][tid >> 5] = ls1;
+      s_cnt[0][tid >> 5] = cnt0;
+      s_cnt[1][tid >> 5] = cnt1;
+    }
+    __syncthreads();
+    // threads 0 and 1 form the two scales (fp64: a handful of instructions on
+    // a slow pipe, so one warp only) while the others store this stage's codes
     if (tid < 2) {
-      const long long sum = tid == 0 ? ls0 : ls1;
-      const uint32_t cnt = tid == 0 ? cnt0 : cnt1;
+      unsigned long long sum = s_sum[tid][0];
+      uint32_t cnt = s_cnt[tid][0];
+      for (int w = 1; w < nwarps; ++w) {
+        sum += s_sum[tid][w];
+        cnt += s_cnt[tid][w];
+      }
       const uint32_t mx = tid == 0 ? mx0 : mx1;
-      const int e = tid == 0 ? e0 : e1;
+      const int ex = tid == 0 ? e0 : e1;
       float sc = 0.0f;
-      if (cnt > 0 && mx != 0) sc = __double2float_rn(ldexp(__ll2double_rn(sum), e - 48) / (double)cnt);
+      if (cnt > 0 && mx != 0) sc = __double2float_rn(ldexp(__ll2double_rn((long long)sum), ex - 48) / (double)cnt);
       s_scale[tid] = sc;
       scales[((int64_t)(X * T + t) * 2 + tid) * n + j] = sc;
     }
-    __syncthreads();
-    const float s_re = s_scale[0], s_im = s_scale[1];
-    __syncthreads();  // s_scale is rewritten by the next stage
 
-    // residual r <- r - (s_re b_re + i s_im b_im), one float32 rounding
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int u = e >> 4, c = e & 15;
-      const bool neg = (word[u] >> (2 * c + 1)) & 1u;
-      const bool isr = (realm[u] >> c) & 1u;
-      const float d = isr ? (neg ? -s_re : s_re) : (neg ? -s_im : s_im);
-      const float upd = __fsub_rn(isr ? re[e] : im[e], d);
-      re[e] = isr ? upd : re[e];
-      im[e] = isr ? im[e] : upd;
-    }
     if (LAYOUT == 3) {
       // layout 3: the (4 / WPT) threads of a 64-column block assemble its
       // sign bytes and q bytes (q = sign XOR imaginary flag) into one 16-byte
@@ -351,9 +343,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
       unsigned long long S = 0, Q = 0;
 #pragma unroll
       for (int u = 0; u < WPT; ++u) {
-        uint32_t s16 = 0;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) s16 |= ((word[u] >> (2 * c + 1)) & 1u) << c;
+        const uint32_t s16 = sgn[u];
         const uint32_t q16 = s16 ^ (valid[u] & ~realm[u] & 0xFFFFu);
         const int g0 = (int)(((w0 + u) & 15) * 2);  // group of the word's first 8 columns in its window
 #pragma unroll
@@ -373,31 +363,51 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_words_kernel(
         *reinterpret_cast<uint4*>(codes + l3_offset(n, m, T, win, j >> 5, X * T + t) + jj * kL3SlotBytes + r * 16) =
             make_uint4((uint32_t)S, (uint32_t)(S >> 32), (uint32_t)Q, (uint32_t)(Q >> 32));
       }
-      continue;
-    }
-    // scatter the codes into the sign and flag words of the row's tile (the
-    // plane was zeroed; the other row of each lane pair ORs its own bits)
-    uint8_t* plane = codes + (int64_t)(X * T + t) * pbytes;
+    } else {
+      // scatter the codes into the sign and flag words of the row's tile (the
+      // plane was zeroed; the other row of each lane pair ORs its own bits)
+      uint8_t* plane = codes + (int64_t)(X * T + t) * pbytes;
 #pragma unroll
-    for (int u = 0; u < WPT; ++u) {
-      const int64_t w = (int64_t)tid * WPT + u;
-      const int64_t kb = w >> 2;
-      if (kb >= KB) continue;
-      const int q = (int)(w & 3);
-      uint32_t sw = 0, fw[4] = {0u, 0u, 0u, 0u};
+      for (int u = 0; u < WPT; ++u) {
+        const int64_t w = (int64_t)tid * WPT + u;
+        const int64_t kb = w >> 2;
+        if (kb >= KB) continue;
+        const int q = (int)(w & 3);
+        uint32_t sw = 0, fw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int sidx = c >> 2, h = (c >> 1) & 1, e = c & 1;
-        const uint32_t v = (word[u] >> (2 * c)) & 3u;  // (sign, real-axis flag)
-        const uint32_t imag = (valid[u] >> c) & 1u & ~v;       // padding columns stay zero
-        sw |= (v >> 1) << sign_bit(sidx, h, rho, e);
-        fw[flag_lane(sidx, h)] |= imag << flag_bit(sidx, q, rho, e);
+        for (int c = 0; c < 16; ++c) {
+          const int sidx = c >> 2, h = (c >> 1) & 1, e = c & 1;
+          const uint32_t neg = (sgn[u] >> c) & 1u;
+          const uint32_t imag = ((valid[u] & ~realm[u]) >> c) & 1u;  // padding columns stay zero
+          sw |= neg << sign_bit(sidx, h, rho, e);
+          fw[flag_lane(sidx, h)] |= imag << flag_bit(sidx, q, rho, e);
+        }
+        if (sw) atomicOr(reinterpret_cast<unsigned int*>(plane + pair_offset(rt, kb, 4 * g + q, KB)), sw);
+#pragma unroll
+        for (int ql = 0; ql < 4; ++ql)
+          if (fw[ql]) atomicOr(reinterpret_cast<unsigned int*>(plane + pair_offset(rt, kb, 4 * g + ql, KB) + 4), fw[ql]);
       }
-      if (sw) atomicOr(reinterpret_cast<unsigned int*>(plane + pair_offset(rt, kb, 4 * g + q, KB)), sw);
-#pragma unroll
-      for (int ql = 0; ql < 4; ++ql)
-        if (fw[ql]) atomicOr(reinterpret_cast<unsigned int*>(plane + pair_offset(rt, kb, 4 * g + ql, KB) + 4), fw[ql]);
     }
+    __syncthreads();
+    const float s_re = s_scale[0], s_im = s_scale[1];
+
+    // residual r <- r - (s_re b_re + i s_im b_im), one float32 rounding
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int u = e >> 4, c = e & 15;
+      const bool neg = (sgn[u] >> c) & 1u;
+      const bool isr = (realm[u] >> c) & 1u;
+      const float d = isr ? (neg ? -s_re : s_re) : (neg ? -s_im : s_im);
+      const float upd = __fsub_rn(isr ? re[e] : im[e], d);
+      re[e] = isr ? upd : re[e];
+      im[e] = isr ? im[e] : upd;
+    }
+#pragma unroll
+    for (int u = 0; u < WPT; ++u)
+      if (valid[u] != 0xFFFFu)  // columns outside the matrix stay (0, 0)
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (!((valid[u] >> c) & 1u)) re[16 * u + c] = im[16 * u + c] = 0.0f;
   }
 }
 
