@@ -512,6 +512,27 @@ def run_stack_only(args, world, rank, local):
                                     "rows": rows}}), flush=True)
 
 
+def run_quantize_only(args, world, rank, local):
+    """Offline weight preparation of `--blocks` blocks at T = 1, 2, 3 on layout 3: convert and
+    quantize of every projection, each launch timed alone (CUDA events); GB/s of R read plus U, W
+    written (convert) and U, W read plus codes and scales written (quantize)."""
+    import bit_complex_valued_fairy2i_b300 as f2i
+    from bit_complex_valued_fairy2i_b300 import build as f2i_build
+
+    f2i_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build_stack(f2i, 1, dev, 1, 3)  # warm-up (first launches, library load), discarded
+    rows = []
+    for T in (1, 2, 3):
+        stack, offline = build_stack(f2i, args.blocks, dev, T, 3)
+        del stack
+        rows.append({"T": T, "layout": 3, **offline})
+    if rank == 0:
+        print(json.dumps({"quantize": {"workload": f"llama2-7b, {args.blocks} blocks x 7 projections, layout 3",
+                                       "rows": rows}}), flush=True)
+
+
 def run_grad_only(args, world, rank, local):
     """Input gradient dL/dx = U^^H g + W^^T conj(g) of every projection of the stack, M = 1, T = 2,
     one CUDA graph of all launches: packed bytes / device time.  Timed with one grouped launch per
@@ -739,7 +760,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["decode", "prefill", "sweep", "stack", "grad"], default="decode",
+    ap.add_argument("--mode", choices=["decode", "prefill", "sweep", "stack", "grad", "quantize"], default="decode",
                     help="prefill: time only the prefill leg (for profiling)")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the batched-decode sweep (M = 1..64)")
@@ -763,6 +784,8 @@ def main():
         run_sweep_only(args, world, rank, local)
     elif args.mode == "stack":
         run_stack_only(args, world, rank, local)
+    elif args.mode == "quantize":
+        run_quantize_only(args, world, rank, local)
     elif args.mode == "grad":
         run_grad_only(args, world, rank, local)
     else:
