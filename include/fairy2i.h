@@ -195,7 +195,13 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
  * the dequantized GEMM (FAIRY2I_ALGO_TCGEN05_DQ; "Fairy2i: Ultra-Low-Bit ...",
  * Step 3: the stages add up to one matrix, and Step 1: its real form); with a
  * workspace (the *_ws calls below) AUTO takes the table-lookup decode below 16
- * tokens and the dequantized GEMM from 16 tokens. */
+ * tokens and the dequantized GEMM from 16 tokens.  The dequantized GEMM needs
+ * m a multiple of 8 (x is read by TMA in two halves, Re x and Im x), so other
+ * layout-3 layers return UNSUPPORTED here and go through the *_ws calls.
+ * Precision: the summed matrix is formed in fp32 and carried as two bfloat16
+ * terms (<= 2^-18 relative per entry), products are exact and sums are fp32:
+ * about 1e-5 relative (L2) against the exact sum.  Tokens run in tiles of
+ * min(256, M rounded up to 16); the codes are decoded once per token tile. */
 
 /* The layer through the table-lookup decode (same y as fairy2i_linear; "Fairy2i:
  * Ultra-Low-Bit ...", "Industry implications: multiplication-free inference":
@@ -221,8 +227,8 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
  * 3e-4 relative (L2) for Gaussian activations.  A token with a non-finite
  * activation gives non-finite outputs.
  * Errors: as fairy2i_linear_ex; INVALID_ARG for a missing, short or
- * misaligned workspace; UNSUPPORTED for layout 3 with another algo than AUTO
- * or LUT, or T > 4. */
+ * misaligned workspace; UNSUPPORTED for layout 3 with another algo than AUTO,
+ * LUT or TCGEN05_DQ, or T > 4. */
 fairy2i_status fairy2i_linear_ws(const fairy2i_packed *q, const void *x, int64_t M, float *y,
                                  fairy2i_algo algo, void *workspace, size_t workspace_bytes,
                                  void *stream);
