@@ -626,7 +626,11 @@ constexpr int64_t kTcDecodeMaxTokens = 8;
 constexpr int64_t kPrefillMinTokens = 16;
 // Token count from which AUTO takes the dequantized GEMM over the table-lookup
 // decode on layout 3.
-constexpr int64_t kDqMinTokens = 16;
+// Layout 3: AUTO's switch from the table lookup (4 tokens per launch at T <= 2,
+// ~57 us per launch on a LLaMA-2-7B block) to the dequantized GEMM (~174 us
+// at any count up to 256): 9-12 tokens cost the same either way, 13 favour
+// the GEMM.
+constexpr int64_t kDqMinTokens = 13;
 
 // The quantizer over U, W (FUSED = false) or straight from R (true); the
 // caller has checked the arguments.  Codes are zeroed first: each row ORs its

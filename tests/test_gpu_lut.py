@@ -382,14 +382,14 @@ def test_dq_parity_stages(T):
 
 def test_dq_plain_entry_and_auto():
     """Layout 3 through the plain entry points (no workspace) takes the dequantized
-    GEMM at any token count; with a workspace AUTO switches to it from 16 tokens."""
+    GEMM at any token count; with a workspace AUTO switches to it from 13 tokens."""
     import ctypes
     n, m = 100, 600
     R = _R(n, m, 5)
     q = _gpu_layer(R, 2)
     qU, qW = _oracle_layer(R, 2)
     lib = f2i.load_library()
-    for M in (1, 20):
+    for M in (1, 12, 13):
         x = _x(M, m, 30 + M)
         xd = x.cuda()
         y = torch.empty((M, 2 * n), device="cuda")
