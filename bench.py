@@ -374,7 +374,7 @@ def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
 
     legs = {}
     for key, qs, algo, kernel, fl in (("ternary", qs2, "tcgen05", "linear_tcgen05_kernel<8>", flops_tern),
-                                      ("dequantized", qs3, "tcgen05_dq", f"linear_dq_kernel<{T_STAGES}>", flops_dq)):
+                                      ("dequantized", qs3, "tcgen05_dq", f"linear_dq_kernel<{T_STAGES},{2 if M > 256 else 1}>", flops_dq)):
         ms = timed(qs, algo)
         tf = fl / (ms * 1e-3) / 1e12
         legs[key] = {"algo": algo, "kernel": kernel, "layout": 2 if key == "ternary" else 3, "ms_per_block": ms,

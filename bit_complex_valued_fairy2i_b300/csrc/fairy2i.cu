@@ -346,12 +346,13 @@ fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64
   return FAIRY2I_OK;
 }
 
-template <int T>
+template <int T, int NT>
 fairy2i_status launch_dq_t(const f2i::DqParams& P, int grid, cudaStream_t s) {
-  auto k = f2i::linear_dq_kernel<T>;
-  fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(k), f2i::kDqSmemBytes, "dequantized prefill");
+  auto k = f2i::linear_dq_kernel<T, NT>;
+  const size_t smem = f2i::dq_smem_bytes<NT>();
+  fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(k), smem, "dequantized prefill");
   if (st != FAIRY2I_OK) return st;
-  k<<<(unsigned)grid, f2i::kDqThreads, f2i::kDqSmemBytes, s>>>(P);
+  k<<<(unsigned)grid, f2i::kDqThreads, smem, s>>>(P);
   return check_launch("dequantized prefill launch");
 }
 
@@ -360,7 +361,7 @@ fairy2i_status launch_dq_t(const f2i::DqParams& P, int grid, cudaStream_t s) {
 // round-robin deal leaves some CTAs with far more steps than the mean. For up
 // to kDqSchedMax tiles the host deals them longest first, each to the CTA
 // with the least work so far; larger launches keep the round-robin deal.
-void dq_schedule(f2i::DqParams& P, int grid) {
+void dq_schedule(f2i::DqParams& P, int grid, int nt) {
   P.sched_n = 0;
   if (P.total_tiles > f2i::kDqSchedMax || grid > f2i::kDqMaxCtas || grid < 1) return;
   std::vector<std::pair<int64_t, int>> order;  // (cost, tile)
@@ -368,7 +369,7 @@ void dq_schedule(f2i::DqParams& P, int grid) {
   for (int i = 0; i < P.count; ++i) {
     const f2i::DqProblem& pr = P.p[i];
     const int64_t n_tiles = (int64_t)pr.row_tiles * pr.tok_tiles;
-    for (int64_t t = 0; t < n_tiles; ++t) order.emplace_back(pr.kpairs + 1, (int)(pr.tile_begin + t));
+    for (int64_t t = 0; t < n_tiles; ++t) order.emplace_back((int64_t)pr.kpairs * nt + 1, (int)(pr.tile_begin + t));
   }
   std::stable_sort(order.begin(), order.end(),
                    [](const std::pair<int64_t, int>& a, const std::pair<int64_t, int>& b) { return a.first > b.first; });
@@ -393,7 +394,8 @@ void dq_schedule(f2i::DqParams& P, int grid) {
 }
 
 // The dense GEMM of the dequantized real matrix (layout 3, m a multiple of 8,
-// T <= 4): one launch per kDqMaxGroup layers, tiles of 64 outputs x 256 tokens.
+// T <= 4): one launch per kDqMaxGroup layers, tiles of 64 outputs x NT N tokens
+// (N = min(256, M rounded up to 16); NT = 2 above 256 tokens).
 fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count, int64_t M, int T,
                       cudaStream_t s) {
   for (int p0 = 0; p0 < count; p0 += f2i::kDqMaxGroup) {
@@ -404,6 +406,7 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
     P.T = T;
     P.M = (int32_t)M;
     P.N = M >= f2i::kDqBN ? f2i::kDqBN : (int32_t)((M + 15) / 16 * 16);  // the MMA's N: a multiple of 16
+    const int nt = M > f2i::kDqBN ? 2 : 1;  // token tiles per decoded k-block pair
     int64_t tiles = 0;
     for (int i = 0; i < cnt; ++i) {
       const fairy2i_packed& q = qs[p0 + i];
@@ -418,20 +421,24 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
       pr.n = (int32_t)q.n;
       pr.m = (int32_t)q.m;
       pr.row_tiles = (int32_t)((q.n + 63) / 64);
-      pr.tok_tiles = (int32_t)((M + P.N - 1) / P.N);
+      pr.tok_tiles = (int32_t)((M + (int64_t)nt * P.N - 1) / ((int64_t)nt * P.N));
       pr.kpairs = (int32_t)((q.m + f2i::kDqBK - 1) / f2i::kDqBK);
       pr.tile_begin = tiles;
       tiles += (int64_t)pr.row_tiles * pr.tok_tiles;
     }
     P.total_tiles = tiles;
     const int grid = (int)std::min<int64_t>(tiles, sm_count());
-    dq_schedule(P, grid);
+    dq_schedule(P, grid, nt);
     fairy2i_status st;
-    switch (T) {
-      case 1: st = launch_dq_t<1>(P, grid, s); break;
-      case 2: st = launch_dq_t<2>(P, grid, s); break;
-      case 3: st = launch_dq_t<3>(P, grid, s); break;
-      case 4: st = launch_dq_t<4>(P, grid, s); break;
+    switch (T * 2 + nt - 1) {
+      case 2: st = launch_dq_t<1, 1>(P, grid, s); break;
+      case 3: st = launch_dq_t<1, 2>(P, grid, s); break;
+      case 4: st = launch_dq_t<2, 1>(P, grid, s); break;
+      case 5: st = launch_dq_t<2, 2>(P, grid, s); break;
+      case 6: st = launch_dq_t<3, 1>(P, grid, s); break;
+      case 7: st = launch_dq_t<3, 2>(P, grid, s); break;
+      case 8: st = launch_dq_t<4, 1>(P, grid, s); break;
+      case 9: st = launch_dq_t<4, 2>(P, grid, s); break;
       default: return fail(FAIRY2I_ERR_UNSUPPORTED, "dequantized prefill supports T <= 4");
     }
     if (st != FAIRY2I_OK) return st;

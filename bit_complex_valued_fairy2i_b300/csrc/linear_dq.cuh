@@ -41,17 +41,26 @@ namespace f2i {
 constexpr int kDqMaxGroup = 8;
 constexpr int kDqSchedMax = 2048;  // tiles a launch may list per CTA (longest first); more run round-robin
 constexpr int kDqMaxCtas = 256;
-constexpr int kDqStages = 3;
 constexpr int kDqBM = 128;  // real rows per tile (64 outputs)
-constexpr int kDqBN = 256;  // tokens per tile (at most; a launch takes N = M rounded up to 16 below 256)
+constexpr int kDqBN = 256;  // tokens per MMA (at most; a launch takes N = M rounded up to 16 below 256)
 constexpr int kDqBK = 64;   // columns per k-block
 constexpr int kDqATerm = kDqBM * kDqBK * 2;   // 16 KB: one term of A
 constexpr int kDqAStage = 2 * kDqATerm;       // hi and lo
-constexpr int kDqBStage = kDqBN * kDqBK * 2;  // 32 KB
+constexpr int kDqBStage = kDqBN * kDqBK * 2;  // 32 KB: x for one MMA
+constexpr int kDqAStages = 3;
 constexpr int kDqProducerWarps = 16;
 constexpr int kDqThreads = 32 * (6 + kDqProducerWarps);
 constexpr uint32_t kDqTmemCols = 512;
-constexpr size_t kDqSmemBytes = 1024 + (size_t)kDqStages * (kDqAStage + kDqBStage) + 256;
+// NT token tiles of N per decoded k-block pair: 1 (M <= 256; the two TMEM
+// accumulators alternate between tiles) or 2 (M > 256; one decode feeds two
+// MMAs, the accumulators hold the tile's two token tiles).  B stages hold NT
+// token tiles: 3 stages of 32 KB or 2 of 64 KB beside the 3 A stages.
+template <int NT>
+__host__ __device__ constexpr int dq_b_stages() { return NT == 2 ? 2 : 3; }
+template <int NT>
+__host__ __device__ constexpr size_t dq_smem_bytes() {
+  return 1024 + (size_t)kDqAStages * kDqAStage + (size_t)dq_b_stages<NT>() * NT * kDqBStage + 256;
+}
 
 struct DqProblem {
   const uint8_t* codes;  // layout 3
@@ -60,7 +69,7 @@ struct DqProblem {
   int32_t n, m;
   int64_t tile_begin;
   int32_t row_tiles;  // tiles of 64 outputs
-  int32_t tok_tiles;  // tiles of 256 tokens
+  int32_t tok_tiles;  // tiles of NT x N tokens
   int32_t kpairs;     // blocks of 64 columns per half of x~
   int32_t pad_;
 };
@@ -70,7 +79,7 @@ struct DqParams {
   DqProblem p[kDqMaxGroup];
   int64_t total_tiles;
   int32_t count, T, M;
-  int32_t N;        // tokens per tile: a multiple of 16 in [16, 256]
+  int32_t N;        // tokens per MMA: a multiple of 16 in [16, 256]
   int32_t sched_n;  // 0: tile blockIdx.x + i gridDim.x; else the list below
   int32_t pad_;
   uint16_t cta_begin[kDqMaxCtas + 1];  // CTA b runs sched[cta_begin[b] .. cta_begin[b + 1])
@@ -133,31 +142,42 @@ __device__ __forceinline__ void dq_code(float& re, float& im, uint32_t s, uint32
       : "r"(f), "r"(s), "r"(sre), "r"(sim), "n"(1u << E), "n"(31 - E));
 }
 
-template <int T>
+template <int T, int NT>
 __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_constant__ DqParams P) {
   extern __shared__ uint8_t dq_smem_raw[];
   constexpr int NP = 2 * T;
+  constexpr int BS = dq_b_stages<NT>();
+  constexpr uint32_t kBStage = (uint32_t)NT * kDqBStage;
 
   const uint32_t raw = smem_u32(dq_smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = dq_smem_raw + (base - raw);
   const uint32_t sA = base;
-  const uint32_t sB = base + kDqStages * kDqAStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kDqStages * (kDqAStage + kDqBStage));
+  const uint32_t sB = base + kDqAStages * kDqAStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kDqAStages * kDqAStage + BS * kBStage);
   const uint32_t bar0 = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(kDqStages + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kDqStages + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kDqStages + 2 + b); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kDqStages + 4);
+  auto fullA = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto emptyA = [&](int s) { return bar0 + 8u * (uint32_t)(kDqAStages + s); };
+  auto fullB = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + s); };
+  auto emptyB = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + BS + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + 2 * BS + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + 2 * BS + 2 + b); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kDqAStages + 2 * BS + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // accumulator of token tile `sub` of the lt-th tile, and how many tiles used it before
+  auto acc_buf = [&](uint32_t lt, int sub) { return NT == 1 ? (int)(lt & 1u) : sub; };
+  auto acc_use = [&](uint32_t lt) { return NT == 1 ? (lt >> 1) : lt; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kDqStages; ++s) {
-      mbar_init(full_bar(s), 1 + kDqProducerWarps);  // TMA arrive.expect_tx + one arrive per producer warp
-      mbar_init(empty_bar(s), 1);                    // tcgen05.commit
+    for (int s = 0; s < kDqAStages; ++s) {
+      mbar_init(fullA(s), kDqProducerWarps);  // one arrive per producer warp
+      mbar_init(emptyA(s), 1);                // tcgen05.commit
+    }
+    for (int s = 0; s < BS; ++s) {
+      mbar_init(fullB(s), 1);   // TMA arrive.expect_tx
+      mbar_init(emptyB(s), 1);  // tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -188,22 +208,24 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         const DqTile c = dq_tile(P, tile);
         const DqProblem& pr = P.p[c.pi];
         for (int kb = 0; ok && kb < 2 * pr.kpairs; ++kb, ++it) {
-          const int s = (int)(it % kDqStages);
-          const uint32_t ph = (it / kDqStages) & 1u;
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) {
+          const int s = (int)(it % BS);
+          const uint32_t ph = (it / BS) & 1u;
+          if (!mbar_wait(emptyB(s), ph ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(s), (uint32_t)P.N * (kDqBK * 2));
-          tma_load_2d(sB + (uint32_t)s * kDqBStage, &P.tmap[2 * c.pi + (kb & 1)], full_bar(s), (kb >> 1) * kDqBK,
-                      c.tt * P.N);
+          mbar_arrive_expect_tx(fullB(s), (uint32_t)NT * (uint32_t)P.N * (kDqBK * 2));
+#pragma unroll
+          for (int sub = 0; sub < NT; ++sub)
+            tma_load_2d(sB + (uint32_t)s * kBStage + (uint32_t)sub * kDqBStage, &P.tmap[2 * c.pi + (kb & 1)], fullB(s),
+                        (kb >> 1) * kDqBK, (c.tt * NT + sub) * P.N);
         }
       }
-      for (uint32_t k = (it > (uint32_t)kDqStages ? it - kDqStages : 0u); k < it; ++k)
-        if (!mbar_wait(full_bar((int)(k % kDqStages)), (k / kDqStages) & 1u, abort_flag)) break;
+      for (uint32_t k = (it > (uint32_t)BS ? it - BS : 0u); k < it; ++k)
+        if (!mbar_wait(fullB((int)(k % BS)), (k / BS) & 1u, abort_flag)) break;
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: hi and lo into one accumulator ----------------
+    // ---------------- MMA issuer: hi and lo into one accumulator per token tile ----------------
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kDqBM, P.N);
       uint32_t it = 0, lt = 0;
@@ -213,28 +235,35 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         if (tile < 0) break;
         const DqTile c = dq_tile(P, tile);
         const int kbs = 2 * P.p[c.pi].kpairs;
-        const int b = (int)(lt & 1u);
-        if (!mbar_wait(acce_bar(b), ((lt >> 1) & 1u) ^ 1u, abort_flag)) break;
+        for (int sub = 0; ok && sub < NT; ++sub)
+          if (!mbar_wait(acce_bar(acc_buf(lt, sub)), (acc_use(lt) & 1u) ^ 1u, abort_flag)) ok = false;
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)b * kDqBN;
         for (int kb = 0; kb < kbs; ++kb, ++it) {
-          const int s = (int)(it % kDqStages);
-          const uint32_t ph = (it / kDqStages) & 1u;
-          if (!mbar_wait(full_bar(s), ph, abort_flag)) {
+          const int sa = (int)(it % kDqAStages), sb = (int)(it % BS);
+          if (!mbar_wait(fullA(sa), (it / kDqAStages) & 1u, abort_flag) ||
+              !mbar_wait(fullB(sb), (it / BS) & 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = sA + (uint32_t)s * kDqAStage, b0 = sB + (uint32_t)s * kDqBStage;
+          const uint32_t a0 = sA + (uint32_t)sa * kDqAStage;
 #pragma unroll
-          for (int kk = 0; kk < kDqBK / 16; ++kk) {
-            tc_mma_bf16(d_tmem, sw128_desc(a0 + 32u * kk), sw128_desc(b0 + 32u * kk), idesc,
-                        (kb > 0 || kk > 0) ? 1u : 0u);
-            tc_mma_bf16(d_tmem, sw128_desc(a0 + kDqATerm + 32u * kk), sw128_desc(b0 + 32u * kk), idesc, 1u);
+          for (int sub = 0; sub < NT; ++sub) {
+            const uint32_t d_tmem = tmem_base + (uint32_t)acc_buf(lt, sub) * kDqBN;
+            const uint32_t b0 = sB + (uint32_t)sb * kBStage + (uint32_t)sub * kDqBStage;
+#pragma unroll
+            for (int kk = 0; kk < kDqBK / 16; ++kk) {
+              tc_mma_bf16(d_tmem, sw128_desc(a0 + 32u * kk), sw128_desc(b0 + 32u * kk), idesc,
+                          (kb > 0 || kk > 0) ? 1u : 0u);
+              tc_mma_bf16(d_tmem, sw128_desc(a0 + kDqATerm + 32u * kk), sw128_desc(b0 + 32u * kk), idesc, 1u);
+            }
           }
-          tc_commit(empty_bar(s));
+          tc_commit(emptyA(sa));
+          tc_commit(emptyB(sb));
         }
-        if (ok) tc_commit(accf_bar(b));
+        if (ok)
+          for (int sub = 0; sub < NT; ++sub) tc_commit(accf_bar(acc_buf(lt, sub)));
       }
     }
   } else if (warp < 2 + kDqProducerWarps) {
@@ -303,11 +332,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         // both stages of the pair: k-block 2 kp (Re x columns) and 2 kp + 1 (Im x columns)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int s = (int)(it % kDqStages);
-          const uint32_t ph = (it / kDqStages) & 1u;
+          const int s = (int)(it % kDqAStages);
+          const uint32_t ph = (it / kDqAStages) & 1u;
           ++it;
           bool got = true;
-          if (lane == 0) got = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag);
+          if (lane == 0) got = mbar_wait(emptyA(s), ph ^ 1u, abort_flag);
           got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
           if (!got) {
             ok = false;
@@ -342,7 +371,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
                        : "memory");
           fence_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(full_bar(s));
+          if (lane == 0) mbar_arrive(fullA(s));
         }
       }
     }
@@ -352,37 +381,44 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
     const int rl = 32 * eq + lane;
     const int jl = rl >> 1, part = rl & 1;
     uint32_t lt = 0;
-    for (int64_t i = 0;; ++i, ++lt) {
+    bool ok = true;
+    for (int64_t i = 0; ok; ++i, ++lt) {
       const int64_t tile = dq_tile_id(P, i);
       if (tile < 0) break;
       const DqTile c = dq_tile(P, tile);
       const DqProblem& pr = P.p[c.pi];
-      const int b = (int)(lt & 1u);
       const int64_t j = (int64_t)c.rt * 64 + jl;
-      bool got = true;
-      if (lane == 0) got = mbar_wait(accf_bar(b), (lt >> 1) & 1u, abort_flag);
-      got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-      if (!got) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(32 * eq) << 16) + (uint32_t)b * kDqBN;
       const int64_t ystride = 2 * (int64_t)pr.n;
       float* ycol = pr.y + (int64_t)part * pr.n + j;
+      for (int sub = 0; sub < NT; ++sub) {
+        const int b = acc_buf(lt, sub);
+        bool got = true;
+        if (lane == 0) got = mbar_wait(accf_bar(b), acc_use(lt) & 1u, abort_flag);
+        got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + ((uint32_t)(32 * eq) << 16) + (uint32_t)b * kDqBN;
+        const int64_t tok0 = ((int64_t)c.tt * NT + sub) * P.N;
 #pragma unroll 1
-      for (int cc = 0; cc < (P.N + 31) / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(tbase + 32u * cc, v);
-        tmem_ld_wait();
-        if (j < pr.n) {
+        for (int cc = 0; cc < (P.N + 31) / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tbase + 32u * cc, v);
+          tmem_ld_wait();
+          if (j < pr.n) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int64_t tok = (int64_t)c.tt * P.N + 32 * cc + e;
-            if (tok < P.M) ycol[tok * ystride] = __uint_as_float(v[e]);
+            for (int e = 0; e < 32; ++e) {
+              const int64_t tok = tok0 + 32 * cc + e;
+              if (tok < P.M) ycol[tok * ystride] = __uint_as_float(v[e]);
+            }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(b));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(b));
     }
   }
 

@@ -358,7 +358,7 @@ DQ_SHAPES = [(8, 64), (37, 136), (33, 200), (256, 256), (300, 704), (64, 1024), 
 
 
 @pytest.mark.parametrize("n,m", DQ_SHAPES)
-@pytest.mark.parametrize("M", [1, 7, 40, 130, 256, 300])  # N = 16, 16, 48, 144, 256, 256
+@pytest.mark.parametrize("M", [1, 7, 40, 130, 256, 300, 513])  # N = 16, 16, 48, 144, 256, 256 (x2), 256 (x2)
 def test_dq_parity(n, m, M):
     R = _R(n, m, 11 * n + m)
     q = _gpu_layer(R, 2)
