@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
       const int64_t j = (int64_t)c.rt * 64 + jl;
       const bool live = j < n;
       const int r = (int)(j & 31);
-      const uint32_t sel = (uint32_t)l3_byte_of(gq, r);  // byte of the group in both halves of the chunk
+      const int sel = l3_byte_of(gq, r);  // byte of the group in both halves of the chunk
       // the row's scales as bits (zero past n): [plane][axis]
       uint32_t sre[NP], sim[NP];
 #pragma unroll
@@ -297,37 +297,60 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         sre[p] = live ? __float_as_uint(__ldg(pr.scales + (int64_t)(2 * p) * n + j)) : 0u;
         sim[p] = live ? __float_as_uint(__ldg(pr.scales + (int64_t)(2 * p + 1) * n + j)) : 0u;
       }
+      // the group's sign and q bytes of every stage plane for pair kp (zero past
+      // n or past the last pair), loaded one pair ahead of their decode for
+      // T <= 2 (more planes would not fit the 80 registers a thread has)
+      auto load_pair = [&](int kp, uint32_t(&sb)[NP], uint32_t(&qb)[NP]) {
+        if (live && kp < pr.kpairs) {
+          const int64_t w = kp >> 2;
+          const int nb = l3_slots(m, w);
+          const int slot = (kp & 3) ^ ((r >> 3) & (nb - 1));
+          const uint8_t* b0 = pr.codes + l3_offset(n, m, T, w, j >> 5, 0) + slot * kL3SlotBytes + r * 16 + sel;
+          const int pstride = nb * kL3SlotBytes;
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            sb[p] = __ldg(b0 + p * pstride);
+            qb[p] = __ldg(b0 + p * pstride + 8);
+          }
+        } else {
+#pragma unroll
+          for (int p = 0; p < NP; ++p) sb[p] = qb[p] = 0u;
+        }
+      };
+      constexpr bool kAhead = T <= 2;
+      uint32_t nsb[NP], nqb[NP];
+      if (kAhead) load_pair(0, nsb, nqb);
       for (int kp = 0; ok && kp < pr.kpairs; ++kp) {
-        // (Re, Im) of U^ [0] and W^ [1] for the group's 8 columns, in fp32;
-        // columns past m decode from zero bits and meet zero-filled x
+        uint32_t csb[NP], cqb[NP];
+        if (kAhead) {
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            csb[p] = nsb[p];
+            cqb[p] = nqb[p];
+          }
+          load_pair(kp + 1, nsb, nqb);
+        } else {
+          load_pair(kp, csb, cqb);
+        }
+        // (Re, Im) of U^ [0] and W^ [1] for the group's 8 columns, in fp32 (zero
+        // scales past n); columns past m decode from zero bits and meet zero-filled x
         float re[2][8], im[2][8];
 #pragma unroll
         for (int x = 0; x < 2; ++x)
 #pragma unroll
           for (int e = 0; e < 8; ++e) re[x][e] = im[x][e] = 0.0f;
-        if (live) {
-          const int64_t w = kp >> 2;
-          const int nb = l3_slots(m, w);
-          const int slot = (kp & 3) ^ ((r >> 3) & (nb - 1));
-          const uint8_t* base = pr.codes + l3_offset(n, m, T, w, j >> 5, 0) + slot * kL3SlotBytes + r * 16;
-          const int pstride = nb * kL3SlotBytes;
 #pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + p * pstride));
-            uint32_t sb, qb;
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sb) : "r"(v.x), "r"(v.y), "r"(sel));
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(qb) : "r"(v.z), "r"(v.w), "r"(sel));
-            const uint32_t fb = sb ^ qb;  // imaginary-axis flags
-            const int x = p < T ? 0 : 1;
-            dq_code<0>(re[x][0], im[x][0], sb, fb, sre[p], sim[p]);
-            dq_code<1>(re[x][1], im[x][1], sb, fb, sre[p], sim[p]);
-            dq_code<2>(re[x][2], im[x][2], sb, fb, sre[p], sim[p]);
-            dq_code<3>(re[x][3], im[x][3], sb, fb, sre[p], sim[p]);
-            dq_code<4>(re[x][4], im[x][4], sb, fb, sre[p], sim[p]);
-            dq_code<5>(re[x][5], im[x][5], sb, fb, sre[p], sim[p]);
-            dq_code<6>(re[x][6], im[x][6], sb, fb, sre[p], sim[p]);
-            dq_code<7>(re[x][7], im[x][7], sb, fb, sre[p], sim[p]);
-          }
+        for (int p = 0; p < NP; ++p) {
+          const uint32_t sb = csb[p], fb = csb[p] ^ cqb[p];  // signs, imaginary-axis flags
+          const int x = p < T ? 0 : 1;
+          dq_code<0>(re[x][0], im[x][0], sb, fb, sre[p], sim[p]);
+          dq_code<1>(re[x][1], im[x][1], sb, fb, sre[p], sim[p]);
+          dq_code<2>(re[x][2], im[x][2], sb, fb, sre[p], sim[p]);
+          dq_code<3>(re[x][3], im[x][3], sb, fb, sre[p], sim[p]);
+          dq_code<4>(re[x][4], im[x][4], sb, fb, sre[p], sim[p]);
+          dq_code<5>(re[x][5], im[x][5], sb, fb, sre[p], sim[p]);
+          dq_code<6>(re[x][6], im[x][6], sb, fb, sre[p], sim[p]);
+          dq_code<7>(re[x][7], im[x][7], sb, fb, sre[p], sim[p]);
         }
         // both stages of the pair: k-block 2 kp (Re x columns) and 2 kp + 1 (Im x columns)
 #pragma unroll
