@@ -370,8 +370,9 @@ def test_dq_parity(n, m, M):
 
 
 @pytest.mark.parametrize("T", [1, 3, 4])
-def test_dq_parity_stages(T):
-    n, m, M = 72, 520, 40
+@pytest.mark.parametrize("M", [40, 300])  # one token tile of 48; two of 256 per decoded pair
+def test_dq_parity_stages(T, M):
+    n, m = 72, 520
     R = _R(n, m, 60 + T)
     q = _gpu_layer(R, T)
     qU, qW = _oracle_layer(R, T)
@@ -413,13 +414,14 @@ def test_dq_plain_entry_and_auto():
     assert rel_l2(f2i.linear(q7, xd7).cpu().numpy(), want7) <= REL_L2
 
 
-def test_dq_group_over_several_launches():
+@pytest.mark.parametrize("M", [33, 300])  # the longest-first deal with one and with two token tiles
+def test_dq_group_over_several_launches(M):
     shapes = [(40 + 8 * i, 256 + 64 * (i % 5)) for i in range(11)]  # 11 layers: two launches of <= 8
     qs, xs, wants = [], [], []
     for i, (n, m) in enumerate(shapes):
         R = _R(n, m, 900 + i)
         qs.append(_gpu_layer(R, 2))
-        x = _x(33, m, 950 + i)
+        x = _x(M, m, 950 + i)
         xs.append(x.cuda())
         qU, qW = _oracle_layer(R, 2)
         wants.append(oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x)))
