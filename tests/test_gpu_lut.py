@@ -450,3 +450,32 @@ def test_dq_full_size_block_prefill_sampled():
         y = y.cpu().numpy()[toks]
         got = np.concatenate([y[:, rows], y[:, q.n + rows]], axis=1)
         assert rel_l2(got, want) <= DQ_REL_L2
+
+
+@pytest.mark.parametrize("layout", [2, L3])
+@pytest.mark.parametrize("T", [1, 2, 3])
+def test_quantize_extreme_row_magnitudes_bit_exact(layout, T):
+    """Rows scaled by powers of two from 2^-130 (subnormal weights) to 2^100, rows at the
+    2^-79 boundary between the quantizer's fp32 and integer-shift sum paths, and rows with one
+    large entry among tiny ones (per-weight truncation of the exact axis sums): codes and
+    scales bit-exact against the oracle in both layouts."""
+    n, m = 48, 200
+    R = _R(n, m, 77 + T)
+    exps = [-130, -110, -100, -81, -80, -79, -78, -77, -60, -20, 0, 20, 60, 100]
+    rows = torch.arange(2 * n) % n
+    scale = torch.tensor([2.0 ** exps[int(j) % len(exps)] for j in rows], dtype=torch.float64)
+    Rs = (R.double() * scale[:, None]).float()
+    # rows 40..47 of both halves: one entry of ordinary size among entries 2^-30 smaller
+    Rs[40:48] *= 2.0 ** -30
+    Rs[n + 40:n + 48] *= 2.0 ** -30
+    Rs[40:48, 3] = 1.5
+    Rs[n + 40:n + 48, m + 7] = -0.75
+    U, W = f2i.convert(Rs.cuda())
+    q = f2i.quantize(U, W, T, layout=layout)
+    qU, qW = _oracle_layer(Rs, T)
+    codes = f2i.unpack_codes(q).cpu().numpy()
+    assert np.array_equal(codes[0], qU.codes) and np.array_equal(codes[1], qW.codes)
+    sc = q.scales.cpu().numpy()
+    assert np.array_equal(sc[0].view(np.uint32), qU.scales.view(np.uint32))
+    assert np.array_equal(sc[1].view(np.uint32), qW.scales.view(np.uint32))
+    f2i.sync_status()
