@@ -406,7 +406,10 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
       for (int t = 0; t < M; ++t)
 #pragma unroll
         for (int p = 0; p < NP; ++p) acc[t][p][0] = acc[t][p][1] = acc[t][p][2] = acc[t][p][3] = 0.0f;
+      // the row's scales, in flight while the unit's slots are evaluated
       float sc[2 * NP];
+#pragma unroll
+      for (int k = 0; k < 2 * NP; ++k) sc[k] = row_in ? __ldg(L.scales + (int64_t)k * L.n + j) : 0.0f;
 #pragma unroll 1
       for (int jj = 0; jj < nb; ++jj) {
         asm volatile("cp.async.wait_group %0;" ::"n"(RING - 2) : "memory");
@@ -419,10 +422,6 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
                        : "r"(src + (uint32_t)p * 512u)
                        : "memory");
         ck = ck + 1 == RING ? 0 : ck + 1;
-        if (jj == nb - 1) {  // the row's scales, in flight while the last slot is evaluated
-#pragma unroll
-          for (int k = 0; k < 2 * NP; ++k) sc[k] = row_in ? __ldg(L.scales + (int64_t)k * L.n + j) : 0.0f;
-        }
         lut_slot<T, M>(cw, bbase ^ (uint32_t)(32 * jj), acc);
         // refill the slot read one evaluation earlier (its registers are consumed)
         issue();
