@@ -162,7 +162,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
   auto emptyB = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + BS + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + 2 * BS + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + 2 * BS + 2 + b); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kDqAStages + 2 * BS + 4);
+  const uint32_t done_bar = bar0 + 8u * (uint32_t)(2 * kDqAStages + 2 * BS + 4);  // every issued MMA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kDqAStages + 2 * BS + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // accumulator of token tile `sub` of the lt-th tile, and how many tiles used it before
   auto acc_buf = [&](uint32_t lt, int sub) { return NT == 1 ? (int)(lt & 1u) : sub; };
@@ -183,6 +184,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
       mbar_init(accf_bar(b), 1);
       mbar_init(acce_bar(b), 4);
     }
+    mbar_init(done_bar, 1);  // tcgen05.commit after the last MMA
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -265,6 +267,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         if (ok)
           for (int sub = 0; sub < NT; ++sub) tc_commit(accf_bar(acc_buf(lt, sub)));
       }
+      // every issued MMA completes before the tensor memory is freed, also when
+      // a wait gave up (then the epilogue may not have waited for them)
+      tc_commit(done_bar);
+      volatile int drain_flag = 0;
+      mbar_wait(done_bar, 0, &drain_flag, 100000000ull);
     }
   } else if (warp < 2 + kDqProducerWarps) {
     // ---------------- A producers: codes + scales -> R^ hi / lo ----------------

@@ -261,7 +261,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
   auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(kPfStages + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kPfStages + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kPfStages + 2 + b); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPfStages + 4);
+  const uint32_t done_bar = bar0 + 8u * (uint32_t)(2 * kPfStages + 4);  // every issued MMA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPfStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
       mbar_init(accf_bar(b), 1);  // tcgen05.commit
       mbar_init(acce_bar(b), 4);  // one arrive per epilogue warp
     }
+    mbar_init(done_bar, 1);  // tcgen05.commit after the last MMA
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -349,6 +351,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
         }
         if (ok) tc_commit(accf_bar(b));
       }
+      // every issued MMA completes before the tensor memory is freed, also when
+      // a wait gave up (then the epilogue may not have waited for them)
+      tc_commit(done_bar);
+      volatile int drain_flag = 0;
+      mbar_wait(done_bar, 0, &drain_flag, 100000000ull);
     }
   } else if (warp < 2 + kPfProducerWarps) {
     // ---------------- A producers: codes -> bfloat16 {+-2, +-0} ----------------
