@@ -225,6 +225,16 @@ def test_layout3_host_errors(lib):
     t5 = _desc(n=4, m=600, T=5, version=L3)
     assert lib.fairy2i_linear_ws(ctypes.byref(t5), p, 1, p, 0, p, 1 << 20, None) == 4
     assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 0, p, 0, None, 0, None) == 0  # no tokens
+    # the dequantized GEMM reads x by TMA in two halves: m must be a multiple of 8; the plain
+    # entry (no workspace) then has nothing to run, explicitly or through AUTO (no launch)
+    d100 = _desc(n=4, m=100, T=2, version=L3)
+    assert lib.fairy2i_linear_ex(ctypes.byref(d100), p, 20, p, 6, None) == 4
+    assert "multiple of 8" in _err(lib)
+    assert lib.fairy2i_linear(ctypes.byref(d100), p, 20, p, None) == 4
+    assert lib.fairy2i_linear_ws(ctypes.byref(d100), p, 20, p, 6, p, 1 << 20, None) == 4
+    # layout-2 descriptors are refused by the layout-3 kernels before any launch
+    d2 = _desc(n=4, m=600, T=2)
+    assert lib.fairy2i_linear_ex(ctypes.byref(d2), p, 20, p, 6, None) == 4
     descs = (f2i.PackedDesc * 2)(d, _desc(n=4, m=600, T=2))
     arr = (ctypes.c_void_p * 2)(256, 512)
     assert lib.fairy2i_linear_group_ws(descs, arr, arr, 2, 1, 0, p, 1 << 20, None) == 2  # mixed layouts
