@@ -833,11 +833,33 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
       }
       while (c < ctas) P.cta_begin[c++] = (int32_t)units;
       P.cta_begin[ctas] = (int32_t)units;
-      for (int cc = 0, i = 0; cc < ctas; ++cc) {  // first (layer, window) of every range
-        const int ub = std::min<int>(P.cta_begin[cc], (int)units - 1);
-        while (i + 1 < cnt && ub >= P.p[i + 1].unit_begin) ++i;
-        P.first_prob[cc] = (uint8_t)i;
-        P.first_win[cc] = (uint16_t)((ub - P.p[i].unit_begin) / P.p[i].tiles);
+      // every CTA's first batch of segments (runs of units inside one (layer,
+      // window)), as the kernel would find them: up to two for one token, one
+      // otherwise (the tables of that many windows fit the shared memory)
+      const int nseg_max = mc == 1 ? 2 : 1;
+      for (int cc = 0; cc < ctas; ++cc) {
+        int uu = P.cta_begin[cc];
+        const int u_end = P.cta_begin[cc + 1];
+        int k = 0;
+        while (k < nseg_max && uu < u_end) {
+          int i = 0;
+          while (i + 1 < cnt && uu >= P.p[i + 1].unit_begin) ++i;
+          const f2i::LutProblem& L = P.p[i];
+          const int w = (uu - L.unit_begin) / L.tiles;
+          f2i::LutSeg& g = P.first[cc][k];
+          g.unit = uu;
+          g.tau0 = uu - L.unit_begin - w * L.tiles;
+          g.win = (uint16_t)w;
+          g.prob = (uint8_t)i;
+          g.nb = (uint8_t)f2i::l3_slots(L.m, w);
+          uu = std::min(u_end, L.unit_begin + (w + 1) * L.tiles);
+          ++k;
+        }
+        if (k == 0) {  // an empty range: the prefetch reads segment 0's layer and window
+          P.first[cc][0] = f2i::LutSeg{u_end, 0, 0, 0, 0};
+        }
+        P.first_nseg[cc] = (uint8_t)k;
+        P.first_end[cc] = uu;
       }
       fairy2i_status st = launch_lut(P, T, mc, ctas, s);
       if (st != FAIRY2I_OK) return st;

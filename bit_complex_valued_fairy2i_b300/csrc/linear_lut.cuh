@@ -67,15 +67,23 @@ struct LutProblem {
   int64_t part_begin;  // first partial output (float2) in the workspace
 };
 
+// A run of a CTA's units inside one (layer, window).
+struct LutSeg {
+  int32_t unit, tau0;  // first unit; its row tile
+  uint16_t win;
+  uint8_t prob, nb;    // layer; slots of the window
+};
+
 struct LutParams {
   int32_t count, M, total_units, pad_;
   float2* partials;
   LutProblem p[kLutMaxGroup];
   int32_t cta_begin[kLutMaxCtas + 1];
-  // the first (layer, window) of every CTA's range (the second segment, if
-  // any, is the next window): known before any device work
-  uint8_t first_prob[kLutMaxCtas];
-  uint16_t first_win[kLutMaxCtas];
+  // every CTA's first batch of segments (up to two), computed on the host so
+  // that no CTA starts with a serial search after the dependency wait
+  LutSeg first[kLutMaxCtas][2];
+  int32_t first_end[kLutMaxCtas];  // unit after the first batch
+  uint8_t first_nseg[kLutMaxCtas];
 };
 
 // The window-combining pass: one thread per (row of a 32-row tile, token) of
@@ -300,11 +308,11 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
   // prefetch never exposes stale data): warp w the codes of unit u + w, warp
   // 15 the activations of the first window for every token.
   if (lane == 0 && u < u_end) {
-    const LutProblem& L0 = P.p[P.first_prob[blockIdx.x]];
-    const int w0 = P.first_win[blockIdx.x];
+    const LutProblem& L0 = P.p[P.first[blockIdx.x][0].prob];
+    const int w0 = P.first[blockIdx.x][0].win;
     if (warp < kLutWarps - 1 && u + warp < u_end) {
       const int uu = u + warp;
-      const int pi = uu < L0.unit_begin + (w0 + 1) * L0.tiles ? P.first_prob[blockIdx.x] : lut_problem_of(P, uu);
+      const int pi = uu < L0.unit_begin + (w0 + 1) * L0.tiles ? P.first[blockIdx.x][0].prob : lut_problem_of(P, uu);
       const LutProblem& L = P.p[pi];
       const int w = (uu - L.unit_begin) / L.tiles;
       const uint8_t* cp0 = L.codes + l3_offset(L.n, L.m, T, w, uu - L.unit_begin - w * L.tiles, 0);
@@ -323,8 +331,26 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
     }
   }
   pdl_wait();
+  bool first_batch = true;
   while (u < u_end) {
-    if (tid == 0) {
+    if (first_batch) {  // the host's segments: one thread per segment
+      const int nseg0 = P.first_nseg[blockIdx.x];
+      if (tid < nseg0) {
+        const LutSeg& g = P.first[blockIdx.x][tid];
+        const LutProblem& L = P.p[g.prob];
+        s_unit[tid] = g.unit;
+        s_prob[tid] = g.prob;
+        s_win[tid] = g.win;
+        s_tau0[tid] = g.tau0;
+        s_nb[tid] = g.nb;
+        s_codes[tid] = L.codes + l3_offset(L.n, L.m, T, g.win, g.tau0, 0);
+      }
+      if (tid == 0) {
+        s_nseg = nseg0;
+        s_unit[nseg0] = P.first_end[blockIdx.x];
+      }
+      first_batch = false;
+    } else if (tid == 0) {
       int s = 0, uu = u;
       while (s < S && uu < u_end) {
         const int pi = lut_problem_of(P, uu);
