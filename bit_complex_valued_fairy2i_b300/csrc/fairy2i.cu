@@ -867,7 +867,11 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
         RP.total_rows = (int32_t)rrows;
         const int64_t work = rrows * mc * 4;
         const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 8 * (int64_t)sm_count()));
-        const cudaError_t e = launch_pdl(f2i::lut_reduce_kernel, dim3(rgrid), dim3(256), 0, s, RP);
+        // an ordinary launch: the decode's CTAs hold a whole SM each, so an early
+        // (programmatic) launch only parks the reduction's CTAs on the SMs the
+        // decode leaves, and measured slower (about 1 us per launch pair)
+        f2i::lut_reduce_kernel<<<rgrid, 256, 0, s>>>(RP);
+        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "table-lookup reduction launch: %s", cudaGetErrorString(e));
         st = check_launch("table-lookup reduction launch");
         if (st != FAIRY2I_OK) return st;

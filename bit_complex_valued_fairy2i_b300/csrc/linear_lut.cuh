@@ -33,10 +33,11 @@
 // kernel adds the windows of every row in window order.  Results are
 // deterministic: every sum has a fixed order.
 //
-// Both kernels are launched as programmatic dependents of the previous
-// kernel in the stream: before griddepcontrol.wait a CTA only issues L2
-// prefetches of its codes (weights, never written by the decode); every read
-// of activations, codes into shared memory, and every write comes after it.
+// The decode is launched as a programmatic dependent of the previous kernel
+// in the stream: before griddepcontrol.wait a CTA only issues L2 prefetches
+// of its codes (weights, never written by the decode) and of its first
+// activations; every read of activations, codes into shared memory, and every
+// write comes after it.  The reduction is an ordinary launch after it.
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -196,21 +197,43 @@ __device__ __forceinline__ void lut_slot(const uint4 (&c)[2 * T], uint32_t bj, f
   }
 }
 
-// Builds the table of (window w of layer L, token t) into set z: warp h
-// writes entries 16 h .. 16 h + 15 of every slot (lane = slot).  Slot S holds
-// group S & (8 nb - 1): a partial window's groups are repeated over all 32
-// slots, so that the lanes that share a group read different banks.  Returns
-// the factor 2^e that undoes the activation scaling.
-__device__ __forceinline__ float lut_build(const LutProblem& L, int w, int t, int z, uint32_t tbase) {
+// The lane's group in window w (its first column), and whether two 16-byte
+// loads fetch its 8 activations (m a multiple of 8, x 16-byte aligned, the
+// group inside the layer).
+__device__ __forceinline__ int64_t lut_group_col(const LutProblem& L, int w) {
+  const int lane = threadIdx.x & 31;
+  return 256 * (int64_t)w + 8 * (lane & (8 * l3_slots(L.m, w) - 1));
+}
+__device__ __forceinline__ bool lut_x_vector(const LutProblem& L, int64_t k0) {
+  return (L.m & 7) == 0 && (reinterpret_cast<uintptr_t>(L.x) & 15) == 0 && k0 < L.m;
+}
+// Issues the two 16-byte loads (Re, Im) of the lane's group for token t, so
+// that they are in flight before the codes; zeros where the build reads the
+// activations one by one instead.
+__device__ __forceinline__ void lut_fetch_x(const LutProblem& L, int w, int t, uint4& va, uint4& vb) {
+  const int64_t k0 = lut_group_col(L, w);
+  va = vb = make_uint4(0u, 0u, 0u, 0u);
+  if (lut_x_vector(L, k0)) {
+    const uint16_t* xa = L.x + (int64_t)t * 2 * L.m;
+    va = *reinterpret_cast<const uint4*>(xa + k0);
+    vb = *reinterpret_cast<const uint4*>(xa + L.m + k0);
+  }
+}
+
+// Builds the table of (window w of layer L, token t) into set z from the
+// lane's activations (va, vb from lut_fetch_x): warp h writes entries
+// 16 h .. 16 h + 15 of every slot (lane = slot).  Slot S holds group
+// S & (8 nb - 1): a partial window's groups are repeated over all 32 slots, so
+// that the lanes that share a group read different banks.  Returns the factor
+// 2^e that undoes the activation scaling.
+__device__ __forceinline__ float lut_build(const LutProblem& L, int w, int t, int z, uint32_t tbase, uint4 va,
+                                           uint4 vb) {
   const int lane = threadIdx.x & 31, h = threadIdx.x >> 5;
   const int64_t m = L.m;
-  const int grp = lane & (8 * l3_slots(m, w) - 1);
-  const int64_t k0 = 256 * (int64_t)w + 8 * grp;
+  const int64_t k0 = lut_group_col(L, w);
   const uint16_t* xa = L.x + (int64_t)t * 2 * m;
   float a[8], b[8];
-  if ((m & 7) == 0 && (reinterpret_cast<uintptr_t>(L.x) & 15) == 0 && k0 < m) {
-    const uint4 va = *reinterpret_cast<const uint4*>(xa + k0);
-    const uint4 vb = *reinterpret_cast<const uint4*>(xa + m + k0);
+  if (lut_x_vector(L, k0)) {
     const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -404,15 +427,26 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
       lk = lk + 1 == RING ? 0 : lk + 1;
     };
 #pragma unroll
-    for (int r = 0; r < RING - 1; ++r) issue();  // HBM streams while the tables are built
-
-    for (int s = 0; s < nseg; ++s) {
+    // the activations of the tables first, then the codes: HBM streams while
+    // the tables are built, and the activations do not queue behind the codes
+    uint4 xva[S][M], xvb[S][M];
 #pragma unroll
-      for (int t = 0; t < M; ++t) {
-        const float pw = lut_build(P.p[s_prob[s]], s_win[s], t, lut_set<M>(s, t), lut_table_base<M>());
-        if (tid == 0) s_pow[s][t] = pw;
-      }
-    }
+    for (int s = 0; s < S; ++s)
+#pragma unroll
+      for (int t = 0; t < M; ++t)
+        if (s < nseg) lut_fetch_x(P.p[s_prob[s]], s_win[s], t, xva[s][t], xvb[s][t]);
+#pragma unroll
+    for (int r = 0; r < RING - 1; ++r) issue();
+
+#pragma unroll
+    for (int s = 0; s < S; ++s)
+#pragma unroll
+      for (int t = 0; t < M; ++t)
+        if (s < nseg) {
+          const float pw =
+              lut_build(P.p[s_prob[s]], s_win[s], t, lut_set<M>(s, t), lut_table_base<M>(), xva[s][t], xvb[s][t]);
+          if (tid == 0) s_pow[s][t] = pw;
+        }
     __syncthreads();
 
     int ck = 0;  // ring slot evaluated next

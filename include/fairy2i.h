@@ -217,9 +217,10 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
  *               order, so results are deterministic.  Calls that may run at
  *               the same time need separate workspaces.  NULL is allowed when
  *               the size query returns 0 (every layer has m <= 256).
- * Both kernels are launched as programmatic dependents of the preceding work
- * in the stream (they may start while it finishes and wait for it before
- * reading activations or writing anything).
+ * The decode kernel is launched as a programmatic dependent of the preceding
+ * work in the stream (it may start while that work finishes and waits for it
+ * before reading activations or writing anything); the summing kernel is an
+ * ordinary launch after it.
  * Tokens go in launches of up to 4 (T <= 2), 2 (T = 3) or 1 (T = 4); each
  * launch streams the codes once.  Precision: each table entry is the fp32 sum
  * of 8 scaled activations rounded once to fp16 (relative error <= 2^-11 per
