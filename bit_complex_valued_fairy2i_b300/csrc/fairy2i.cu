@@ -349,7 +349,7 @@ fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64
 template <int T, int NT>
 fairy2i_status launch_dq_t(const f2i::DqParams& P, int grid, cudaStream_t s) {
   auto k = f2i::linear_dq_kernel<T, NT>;
-  const size_t smem = f2i::dq_smem_bytes<NT>();
+  const size_t smem = f2i::dq_smem_bytes<NT, T>();
   fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(k), smem, "dequantized prefill");
   if (st != FAIRY2I_OK) return st;
   k<<<(unsigned)grid, f2i::kDqThreads, smem, s>>>(P);
@@ -395,7 +395,7 @@ void dq_schedule(f2i::DqParams& P, int grid, int nt) {
 
 // The dense GEMM of the dequantized real matrix (layout 3, m a multiple of 8,
 // T <= 4): one launch per kDqMaxGroup layers, tiles of 64 outputs x NT N tokens
-// (N = min(256, M rounded up to 16); NT = 2 above 256 tokens).
+// (N = min(256, M rounded up to 16); NT = 2 above 256 tokens for T <= 2).
 fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count, int64_t M, int T,
                       cudaStream_t s) {
   for (int p0 = 0; p0 < count; p0 += f2i::kDqMaxGroup) {
@@ -406,7 +406,9 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
     P.T = T;
     P.M = (int32_t)M;
     P.N = M >= f2i::kDqBN ? f2i::kDqBN : (int32_t)((M + 15) / 16 * 16);  // the MMA's N: a multiple of 16
-    const int nt = M > f2i::kDqBN ? 2 : 1;  // token tiles per decoded k-block pair
+    // token tiles per decoded k-block pair (two need the shared memory that the
+    // larger code windows of T > 2 take)
+    const int nt = M > f2i::kDqBN && T <= 2 ? 2 : 1;
     int64_t tiles = 0;
     for (int i = 0; i < cnt; ++i) {
       const fairy2i_packed& q = qs[p0 + i];
@@ -436,9 +438,7 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
       case 4: st = launch_dq_t<2, 1>(P, grid, s); break;
       case 5: st = launch_dq_t<2, 2>(P, grid, s); break;
       case 6: st = launch_dq_t<3, 1>(P, grid, s); break;
-      case 7: st = launch_dq_t<3, 2>(P, grid, s); break;
       case 8: st = launch_dq_t<4, 1>(P, grid, s); break;
-      case 9: st = launch_dq_t<4, 2>(P, grid, s); break;
       default: return fail(FAIRY2I_ERR_UNSUPPORTED, "dequantized prefill supports T <= 4");
     }
     if (st != FAIRY2I_OK) return st;

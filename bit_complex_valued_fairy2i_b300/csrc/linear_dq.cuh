@@ -21,15 +21,20 @@
 //         halves of x~;
 //   K:    blocks of 64 columns in pairs (block c of Re x, block c of Im x),
 //         the two stages of a pair filled by one decode;
-//   A:    hi and lo, 128-byte swizzled K-major, written by 8 producer warps
-//         from the layout-3 codes and the scales;
+//   A:    hi and lo, 128-byte swizzled K-major, written by 16 producer warps
+//         from the codes (in shared memory) and the scales;
+//   codes: per window of 256 columns (4 k-block pairs), the layout-3 bytes of
+//         the tile's two 32-row tiles (contiguous: 2 x 2T planes x the
+//         window's slots x 512 bytes), one bulk copy (cp.async.bulk, the TMA
+//         engine) into a ring of two stages, a window ahead of their decode;
 //   B:    x [M][2m] bfloat16 by TMA through two maps, one per half of x~
 //         (128-byte swizzle, zero fill past m columns and M tokens), so that
 //         the columns of A past m (decoded from zero code bits) meet zeros;
 //   D:    fp32 in TMEM, two accumulators of 256 columns (double buffered).
-// Warp roles (22 warps, one CTA per SM, persistent over tiles): warp 0 TMA
+// Warp roles (23 warps, one CTA per SM, persistent over tiles): warp 0 TMA
 // for B, warp 1 TMEM allocation and MMA issue, warps 2-17 A producers, warps
-// 18-21 epilogue (tcgen05.ld, stores of y).  All mbarrier waits are bounded.
+// 18-21 epilogue (tcgen05.ld, stores of y), warp 22 the code copies.  All
+// mbarrier waits are bounded.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -47,19 +52,25 @@ constexpr int kDqBK = 64;   // columns per k-block
 constexpr int kDqATerm = kDqBM * kDqBK * 2;   // 16 KB: one term of A
 constexpr int kDqAStage = 2 * kDqATerm;       // hi and lo
 constexpr int kDqBStage = kDqBN * kDqBK * 2;  // 32 KB: x for one MMA
-constexpr int kDqAStages = 3;
 constexpr int kDqProducerWarps = 16;
-constexpr int kDqThreads = 32 * (6 + kDqProducerWarps);
+constexpr int kDqThreads = 32 * (7 + kDqProducerWarps);
 constexpr uint32_t kDqTmemCols = 512;
-// NT token tiles of N per decoded k-block pair: 1 (M <= 256; the two TMEM
-// accumulators alternate between tiles) or 2 (M > 256; one decode feeds two
-// MMAs, the accumulators hold the tile's two token tiles).  B stages hold NT
-// token tiles: 3 stages of 32 KB or 2 of 64 KB beside the 3 A stages.
-template <int NT>
-__host__ __device__ constexpr int dq_b_stages() { return NT == 2 ? 2 : 3; }
-template <int NT>
+constexpr int kDqCStages = 2;  // code stages, one window each
+// Code stage: 2 row tiles of 32 x 2T planes x 4 slots x 512 bytes.
+__host__ __device__ constexpr uint32_t dq_c_stage(int T) { return 8192u * (uint32_t)T; }
+// NT token tiles of N per decoded k-block pair: 1 (M <= 256, or T > 2; the
+// two TMEM accumulators alternate between tiles) or 2 (M > 256 and T <= 2;
+// one decode feeds two MMAs, the accumulators hold the tile's two token
+// tiles).  Stages beside the code ring: 3 A and 3 B of 32 KB (NT = 1, T <= 2),
+// else 2 A of 32 KB and 2 B of NT x 32 KB.
+template <int NT, int T>
+__host__ __device__ constexpr int dq_a_stages() { return NT == 1 && T <= 2 ? 3 : 2; }
+template <int NT, int T>
+__host__ __device__ constexpr int dq_b_stages() { return NT == 1 && T <= 2 ? 3 : 2; }
+template <int NT, int T>
 __host__ __device__ constexpr size_t dq_smem_bytes() {
-  return 1024 + (size_t)kDqAStages * kDqAStage + (size_t)dq_b_stages<NT>() * NT * kDqBStage + 256;
+  return 1024 + (size_t)dq_a_stages<NT, T>() * kDqAStage + (size_t)dq_b_stages<NT, T>() * NT * kDqBStage +
+         (size_t)kDqCStages * dq_c_stage(T) + 512;
 }
 
 struct DqProblem {
@@ -124,9 +135,9 @@ __device__ __forceinline__ void dq_split2(float a, float b, uint32_t& hi, uint32
   lo = l;
 }
 
-// One code of one stage added to (re, im): column E of a group whose sign bits
-// are s and imaginary-axis flags f; the value is +-s_re on the real axis or
-// +-s_im on the imaginary one.
+// One code of one stage added to (re, im): bit E of the sign word s and of
+// the imaginary-axis flag word f (a group's column, in the byte of its plane);
+// the value is +-s_re on the real axis or +-s_im on the imaginary one.
 template <int E>
 __device__ __forceinline__ void dq_code(float& re, float& im, uint32_t s, uint32_t f, uint32_t sre, uint32_t sim) {
   asm("{\n\t.reg .pred p;\n\t.reg .b32 t, v;\n\t"
@@ -142,28 +153,64 @@ __device__ __forceinline__ void dq_code(float& re, float& im, uint32_t s, uint32
       : "r"(f), "r"(s), "r"(sre), "r"(sim), "n"(1u << E), "n"(31 - E));
 }
 
+// Bulk copy (no tensor map) of `bytes` from global to this CTA's shared
+// memory, completing on mbarrier `bar` (16-byte aligned ends, multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// The 8 codes of a group in one plane (bits B .. B + 7 of s and f).
+template <int B>
+__device__ __forceinline__ void dq_plane(float (&re)[8], float (&im)[8], uint32_t s, uint32_t f, uint32_t sre,
+                                         uint32_t sim) {
+  dq_code<B + 0>(re[0], im[0], s, f, sre, sim);
+  dq_code<B + 1>(re[1], im[1], s, f, sre, sim);
+  dq_code<B + 2>(re[2], im[2], s, f, sre, sim);
+  dq_code<B + 3>(re[3], im[3], s, f, sre, sim);
+  dq_code<B + 4>(re[4], im[4], s, f, sre, sim);
+  dq_code<B + 5>(re[5], im[5], s, f, sre, sim);
+  dq_code<B + 6>(re[6], im[6], s, f, sre, sim);
+  dq_code<B + 7>(re[7], im[7], s, f, sre, sim);
+}
+
 template <int T, int NT>
 __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_constant__ DqParams P) {
   extern __shared__ uint8_t dq_smem_raw[];
   constexpr int NP = 2 * T;
-  constexpr int BS = dq_b_stages<NT>();
+  constexpr int NW = (NP + 3) / 4;  // words holding one byte per plane
+  static_assert(NT == 1 || T <= 2, "two token tiles per decode only for T <= 2 (shared memory)");
+  static_assert(dq_smem_bytes<NT, T>() <= 232448, "shared memory per CTA");
+  constexpr int AS = dq_a_stages<NT, T>();
+  constexpr int BS = dq_b_stages<NT, T>();
+  constexpr int CS = kDqCStages;
   constexpr uint32_t kBStage = (uint32_t)NT * kDqBStage;
+  constexpr uint32_t kCStage = dq_c_stage(T);
 
   const uint32_t raw = smem_u32(dq_smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = dq_smem_raw + (base - raw);
   const uint32_t sA = base;
-  const uint32_t sB = base + kDqAStages * kDqAStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kDqAStages * kDqAStage + BS * kBStage);
+  const uint32_t sB = base + AS * kDqAStage;
+  const uint32_t sC = sB + BS * kBStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + AS * kDqAStage + BS * kBStage + CS * kCStage);
   const uint32_t bar0 = smem_u32(bars);
   auto fullA = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-  auto emptyA = [&](int s) { return bar0 + 8u * (uint32_t)(kDqAStages + s); };
-  auto fullB = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + s); };
-  auto emptyB = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + BS + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + 2 * BS + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kDqAStages + 2 * BS + 2 + b); };
-  const uint32_t done_bar = bar0 + 8u * (uint32_t)(2 * kDqAStages + 2 * BS + 4);  // every issued MMA complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kDqAStages + 2 * BS + 5);
+  auto emptyA = [&](int s) { return bar0 + 8u * (uint32_t)(AS + s); };
+  auto fullB = [&](int s) { return bar0 + 8u * (uint32_t)(2 * AS + s); };
+  auto emptyB = [&](int s) { return bar0 + 8u * (uint32_t)(2 * AS + BS + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * AS + 2 * BS + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * AS + 2 * BS + 2 + b); };
+  const uint32_t done_bar = bar0 + 8u * (uint32_t)(2 * AS + 2 * BS + 4);  // every issued MMA complete
+  auto fullC = [&](int s) { return bar0 + 8u * (uint32_t)(2 * AS + 2 * BS + 5 + s); };
+  auto emptyC = [&](int s) { return bar0 + 8u * (uint32_t)(2 * AS + 2 * BS + 5 + CS + s); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * AS + 2 * BS + 5 + 2 * CS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // accumulator of token tile `sub` of the lt-th tile, and how many tiles used it before
   auto acc_buf = [&](uint32_t lt, int sub) { return NT == 1 ? (int)(lt & 1u) : sub; };
@@ -172,9 +219,13 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kDqAStages; ++s) {
+    for (int s = 0; s < AS; ++s) {
       mbar_init(fullA(s), kDqProducerWarps);  // one arrive per producer warp
       mbar_init(emptyA(s), 1);                // tcgen05.commit
+    }
+    for (int s = 0; s < CS; ++s) {
+      mbar_init(fullC(s), 1);                 // the code warp's arrive.expect_tx
+      mbar_init(emptyC(s), kDqProducerWarps);  // one arrive per producer warp
     }
     for (int s = 0; s < BS; ++s) {
       mbar_init(fullB(s), 1);   // TMA arrive.expect_tx
@@ -242,8 +293,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         if (!ok) break;
         tc_fence_after();
         for (int kb = 0; kb < kbs; ++kb, ++it) {
-          const int sa = (int)(it % kDqAStages), sb = (int)(it % BS);
-          if (!mbar_wait(fullA(sa), (it / kDqAStages) & 1u, abort_flag) ||
+          const int sa = (int)(it % AS), sb = (int)(it % BS);
+          if (!mbar_wait(fullA(sa), (it / AS) & 1u, abort_flag) ||
               !mbar_wait(fullB(sb), (it / BS) & 1u, abort_flag)) {
             ok = false;
             break;
@@ -278,25 +329,28 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
     // Thread (jl, gq) owns output jl of the tile (rows 2 jl, 2 jl + 1) and
     // group gq (columns 8 gq .. 8 gq + 7) of every 64-column block: one byte
     // of signs and one of flags per stage plane, out of the row's 16-byte
-    // layout-3 chunk.  The eight lanes of a quarter warp share jl and write
-    // the eight 16-byte chunks of a 128-byte row: no bank conflicts.
+    // layout-3 chunk in the code stage.  The eight lanes of a quarter warp
+    // share jl and write the eight 16-byte chunks of a 128-byte row: no bank
+    // conflicts.
     const int pt = tid - 64;  // 0..511
     const int jl = pt >> 3, gq = pt & 7;
     const uint32_t row0 = (uint32_t)(2 * jl), row1 = row0 + 1u;
     const uint32_t o0 = row0 * 128u + (((uint32_t)gq ^ (row0 & 7u)) << 4);
     const uint32_t o1 = row1 * 128u + (((uint32_t)gq ^ (row1 & 7u)) << 4);
-    uint32_t it = 0;
+    // in a code stage (a window of nb slots): row tile th = jl >> 5, row r =
+    // jl & 31; plane p, slot q of the row at ((th 2T + p) nb + q) 512 + 16 r
+    const int cth = jl >> 5, cr = jl & 31;
+    const uint32_t cbyte = (uint32_t)(cr * 16 + l3_byte_of(gq, cr));
+    uint32_t it = 0, itc = 0;  // itc: windows of codes consumed
     bool ok = true;
     for (int64_t i = 0; ok; ++i) {
       const int64_t tile = dq_tile_id(P, i);
       if (tile < 0) break;
       const DqTile c = dq_tile(P, tile);
       const DqProblem& pr = P.p[c.pi];
-      const int64_t n = pr.n, m = pr.m;
+      const int64_t n = pr.n;
       const int64_t j = (int64_t)c.rt * 64 + jl;
       const bool live = j < n;
-      const int r = (int)(j & 31);
-      const int sel = l3_byte_of(gq, r);  // byte of the group in both halves of the chunk
       // the row's scales as bits (zero past n): [plane][axis]
       uint32_t sre[NP], sim[NP];
 #pragma unroll
@@ -304,40 +358,44 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         sre[p] = live ? __float_as_uint(__ldg(pr.scales + (int64_t)(2 * p) * n + j)) : 0u;
         sim[p] = live ? __float_as_uint(__ldg(pr.scales + (int64_t)(2 * p + 1) * n + j)) : 0u;
       }
-      // the group's sign and q bytes of every stage plane for pair kp (zero past
-      // n or past the last pair), loaded one pair ahead of their decode for
-      // T <= 2 (more planes would not fit the 80 registers a thread has)
-      auto load_pair = [&](int kp, uint32_t(&sb)[NP], uint32_t(&qb)[NP]) {
-        if (live && kp < pr.kpairs) {
-          const int64_t w = kp >> 2;
-          const int nb = l3_slots(m, w);
-          const int slot = (kp & 3) ^ ((r >> 3) & (nb - 1));
-          const uint8_t* b0 = pr.codes + l3_offset(n, m, T, w, j >> 5, 0) + slot * kL3SlotBytes + r * 16 + sel;
-          const int pstride = nb * kL3SlotBytes;
+      // the group's sign and q bytes of every stage plane for pair kp (zero
+      // past n), read from the window's code stage one pair ahead of their
+      // decode (plane p's byte at bits 8 (p & 3) of word p >> 2); a stage goes
+      // back to the code warp when its window's last pair has been read
+      auto fetch = [&](int kp, uint32_t(&sw)[NW], uint32_t(&qw)[NW]) -> bool {
+        const uint32_t k = itc + (uint32_t)(kp >> 2);
+        const int cs = (int)(k % CS);
+        if (__any_sync(0xffffffffu, !mbar_wait(fullC(cs), (k / CS) & 1u, abort_flag) ? 1 : 0)) return false;
+        const int nb = l3_slots(pr.m, kp >> 2);
+        const int q = (kp & 3) ^ (cr >> 3 & (nb - 1));
+        const uint32_t cb = sC + (uint32_t)cs * kCStage + (uint32_t)((cth * NP * nb + q) * 512) + cbyte;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) sw[w] = qw[w] = 0u;
+        if (live) {
 #pragma unroll
           for (int p = 0; p < NP; ++p) {
-            sb[p] = __ldg(b0 + p * pstride);
-            qb[p] = __ldg(b0 + p * pstride + 8);
+            sw[p >> 2] |= lds_u8(cb + 512u * (uint32_t)(nb * p)) << (8 * (p & 3));
+            qw[p >> 2] |= lds_u8(cb + 512u * (uint32_t)(nb * p) + 8u) << (8 * (p & 3));
           }
-        } else {
-#pragma unroll
-          for (int p = 0; p < NP; ++p) sb[p] = qb[p] = 0u;
         }
+        return true;
       };
-      constexpr bool kAhead = T <= 2;
-      uint32_t nsb[NP], nqb[NP];
-      if (kAhead) load_pair(0, nsb, nqb);
+      uint32_t nsw[NW], nqw[NW];
+      if (pr.kpairs > 0 && !fetch(0, nsw, nqw)) ok = false;
       for (int kp = 0; ok && kp < pr.kpairs; ++kp) {
-        uint32_t csb[NP], cqb[NP];
-        if (kAhead) {
+        uint32_t sw[NW], fw[NW];  // signs, imaginary-axis flags
 #pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            csb[p] = nsb[p];
-            cqb[p] = nqb[p];
-          }
-          load_pair(kp + 1, nsb, nqb);
-        } else {
-          load_pair(kp, csb, cqb);
+        for (int w = 0; w < NW; ++w) {
+          sw[w] = nsw[w];
+          fw[w] = nsw[w] ^ nqw[w];
+        }
+        if ((kp & 3) == 3 || kp + 1 == pr.kpairs) {  // the window's last pair is in registers
+          __syncwarp();
+          if (lane == 0) mbar_arrive(emptyC((int)((itc + (uint32_t)(kp >> 2)) % CS)));
+        }
+        if (kp + 1 < pr.kpairs && !fetch(kp + 1, nsw, nqw)) {
+          ok = false;
+          break;
         }
         // (Re, Im) of U^ [0] and W^ [1] for the group's 8 columns, in fp32 (zero
         // scales past n); columns past m decode from zero bits and meet zero-filled x
@@ -348,22 +406,20 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
           for (int e = 0; e < 8; ++e) re[x][e] = im[x][e] = 0.0f;
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
-          const uint32_t sb = csb[p], fb = csb[p] ^ cqb[p];  // signs, imaginary-axis flags
+          const uint32_t sb = sw[p >> 2], fb = fw[p >> 2];
           const int x = p < T ? 0 : 1;
-          dq_code<0>(re[x][0], im[x][0], sb, fb, sre[p], sim[p]);
-          dq_code<1>(re[x][1], im[x][1], sb, fb, sre[p], sim[p]);
-          dq_code<2>(re[x][2], im[x][2], sb, fb, sre[p], sim[p]);
-          dq_code<3>(re[x][3], im[x][3], sb, fb, sre[p], sim[p]);
-          dq_code<4>(re[x][4], im[x][4], sb, fb, sre[p], sim[p]);
-          dq_code<5>(re[x][5], im[x][5], sb, fb, sre[p], sim[p]);
-          dq_code<6>(re[x][6], im[x][6], sb, fb, sre[p], sim[p]);
-          dq_code<7>(re[x][7], im[x][7], sb, fb, sre[p], sim[p]);
+          switch (p & 3) {  // resolved at compile time (the loop is unrolled)
+            case 0: dq_plane<0>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
+            case 1: dq_plane<8>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
+            case 2: dq_plane<16>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
+            default: dq_plane<24>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
+          }
         }
         // both stages of the pair: k-block 2 kp (Re x columns) and 2 kp + 1 (Im x columns)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int s = (int)(it % kDqAStages);
-          const uint32_t ph = (it / kDqAStages) & 1u;
+          const int s = (int)(it % AS);
+          const uint32_t ph = (it / AS) & 1u;
           ++it;
           bool got = true;
           if (lane == 0) got = mbar_wait(emptyA(s), ph ^ 1u, abort_flag);
@@ -404,8 +460,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
           if (lane == 0) mbar_arrive(fullA(s));
         }
       }
+      itc += (uint32_t)((pr.kpairs + 3) / 4);
     }
-  } else {
+  } else if (warp < 6 + kDqProducerWarps) {
     // ---------------- epilogue: D row 2 jl + part of token t -> y[t][part n + j] ----------------
     const int eq = warp & 3;  // TMEM lanes 32 eq .. 32 eq + 31
     const int rl = 32 * eq + lane;
@@ -450,6 +507,36 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         if (lane == 0) mbar_arrive(acce_bar(b));
       }
     }
+  } else {
+    // ---------------- code copies: each window's codes into the code ring ----------------
+    // Window w of the tile's two 32-row tiles is one contiguous run of
+    // layout 3 (tile-major inside the window): 2 x 2T planes x nb slots x 512
+    // bytes (one tile's worth at the layer's last tile).
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t i = 0; ok && lane == 0; ++i) {
+      const int64_t tile = dq_tile_id(P, i);
+      if (tile < 0) break;
+      const DqTile c = dq_tile(P, tile);
+      const DqProblem& pr = P.p[c.pi];
+      const int64_t n = pr.n, m = pr.m;
+      const int ntile = (int)min((int64_t)2, l3_tiles(n) - 2 * (int64_t)c.rt);  // row tiles of 32 present
+      const int nw = (pr.kpairs + 3) / 4;
+      for (int w = 0; w < nw; ++w, ++it) {
+        const int s = (int)(it % CS);
+        if (!mbar_wait(emptyC(s), ((it / CS) & 1u) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bytes = (uint32_t)(ntile * NP * l3_slots(m, w)) * (uint32_t)kL3SlotBytes;
+        mbar_arrive_expect_tx(fullC(s), bytes);
+        bulk_load(sC + (uint32_t)s * kCStage, pr.codes + l3_offset(n, m, T, w, 2 * c.rt, 0), bytes, fullC(s));
+      }
+    }
+    // no copy outlives the CTA: wait for the last stages to land
+    if (lane == 0)
+      for (uint32_t k = (it > (uint32_t)CS ? it - CS : 0u); k < it; ++k)
+        if (!mbar_wait(fullC((int)(k % CS)), (k / CS) & 1u, abort_flag)) break;
   }
 
   tc_fence_before();

@@ -426,7 +426,6 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
       asm volatile("cp.async.commit_group;" ::: "memory");
       lk = lk + 1 == RING ? 0 : lk + 1;
     };
-#pragma unroll
     // the activations of the tables first, then the codes: HBM streams while
     // the tables are built, and the activations do not queue behind the codes
     uint4 xva[S][M], xvb[S][M];
