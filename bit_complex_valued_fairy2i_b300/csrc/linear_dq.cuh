@@ -153,13 +153,6 @@ __device__ __forceinline__ void dq_code(float& re, float& im, uint32_t s, uint32
       : "r"(f), "r"(s), "r"(sre), "r"(sim), "n"(1u << E), "n"(31 - E));
 }
 
-// Bulk copy (no tensor map) of `bytes` from global to this CTA's shared
-// memory, completing on mbarrier `bar` (16-byte aligned ends, multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
 __device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -365,7 +358,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
       auto fetch = [&](int kp, uint32_t(&sw)[NW], uint32_t(&qw)[NW]) -> bool {
         const uint32_t k = itc + (uint32_t)(kp >> 2);
         const int cs = (int)(k % CS);
-        if (__any_sync(0xffffffffu, !mbar_wait(fullC(cs), (k / CS) & 1u, abort_flag) ? 1 : 0)) return false;
+        // one wait per window (its copy completes one phase of the barrier)
+        if ((kp & 3) == 0 && __any_sync(0xffffffffu, !mbar_wait(fullC(cs), (k / CS) & 1u, abort_flag) ? 1 : 0))
+          return false;
         const int nb = l3_slots(pr.m, kp >> 2);
         const int q = (kp & 3) ^ (cr >> 3 & (nb - 1));
         const uint32_t cb = sC + (uint32_t)cs * kCStage + (uint32_t)((cth * NP * nb + q) * 512) + cbyte;

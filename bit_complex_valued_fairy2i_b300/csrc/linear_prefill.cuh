@@ -13,21 +13,25 @@
 //
 // GEMM shape per tile:  D[128 code rows][256] += A[128][K] * B[256][K]^T
 //   A: code rows (output jj, plane p, axis a) at row RO*jj + 2p + a, entries
-//      bfloat16 {+2, -2, +0, -0} expanded from the packed codes in shared
-//      memory by two producer warps (128-byte swizzled, K-major).
+//      bfloat16 {+2, -2, +0, -0} expanded from the packed codes by the
+//      producer warps (128-byte swizzled, K-major).  The codes reach shared
+//      memory by the TMA engine: per window of 4 column-block pairs, one bulk
+//      copy (cp.async.bulk) per (16-row tile, plane) of the tile's contiguous
+//      layout-2 run, into a ring of two stages, a window ahead of their use.
 //   B: the activations viewed as [2M][m] (row 2*token + part), which is the
 //      caller's x [M][2m] unchanged; loaded by TMA, 128-byte swizzled.
 //   D: fp32 in TMEM, two accumulators of 256 columns (double buffered).
 // Every product is exact (+-2 times a bfloat16); only the fp32 accumulation
 // rounds.  The factor 2 is removed with the scale (exact).
 //
-// Warp roles (14 warps, one CTA per SM, persistent over tiles):
+// Warp roles (15 warps, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer for B
 //   warp 1      TMEM allocation; one thread issues tcgen05.mma / commit
 //   warps 2-9   A producers: codes -> swizzled bfloat16 tiles (two groups of
 //               four warps, alternate k-blocks)
 //   warps 10-13 epilogue: tcgen05.ld, scales, reduction over the RO code
 //               rows of each output (lane shuffles), stores y
+//   warp 14     bulk copies of the codes
 // All mbarrier waits are bounded (about 2 s); a wait that gives up raises the
 // timeout flag of the device error word and every role winds down.
 #pragma once
@@ -48,10 +52,22 @@ constexpr int kPfBStage = kPfBN * kPfBK * 2;  // 32 KB
 constexpr int kPfProducerWarps = 8;
 constexpr int kPfProducerGroups = 2;  // groups fill alternate k-blocks concurrently
 constexpr int kPfGroupWarps = kPfProducerWarps / kPfProducerGroups;
-constexpr int kPfThreads = 32 * (6 + kPfProducerWarps);
+constexpr int kPfThreads = 32 * (7 + kPfProducerWarps);
 constexpr uint32_t kPfTmemCols = 512;  // two 256-column fp32 accumulators
-constexpr size_t kPfSmemBytes =
-    1024 /* alignment slack */ + (size_t)kPfStages * (kPfAStage + kPfBStage) + 256 /* barriers, TMEM address */;
+// Code ring: two stages of a window of kPfWinPairs column-block pairs for
+// every (16-row tile, plane) of a tile: 2 x 2 planes (T = 1, two row tiles),
+// 4 (T = 2) or at most 8 (T = 3, 4) runs of 4 x 512 bytes.
+constexpr int kPfCStages = 2;
+constexpr int kPfWinPairs = 4;
+constexpr uint32_t kPfCStage = 8u * kPfWinPairs * 512u + 128u;
+// Run idx (= 16-row tile x 2T + plane) of a code stage starts 16 (idx & 7)
+// bytes past its slot, so that the quads' 16-byte words of different planes
+// fall in different bank groups.
+__host__ __device__ __forceinline__ uint32_t pf_run_off(int idx) {
+  return (uint32_t)idx * (kPfWinPairs * 512u) + 16u * (uint32_t)(idx & 7);
+}
+constexpr size_t kPfSmemBytes = 1024 /* alignment slack */ + (size_t)kPfStages * (kPfAStage + kPfBStage) +
+                                (size_t)kPfCStages * kPfCStage + 256 /* barriers, TMEM address */;
 
 struct PrefillProblem {
   const uint8_t* codes;
@@ -136,6 +152,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+// Bulk copy (no tensor map) of `bytes` from global to this CTA's shared
+// memory, completing on mbarrier `bar` (16-byte aligned ends, multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
   asm volatile(
@@ -241,6 +265,13 @@ __device__ __forceinline__ PfTile pf_tile(const PrefillParams& P, int64_t tile) 
   return c;
 }
 
+// First 16-row layout-2 tile of tile rt, J outputs per tile (J = 32: two row
+// tiles; 16: one; 8: half of one).
+template <int J>
+__host__ __device__ __forceinline__ int64_t pf_first_row_tile(int64_t rt) {
+  return J >= 16 ? rt * (J / 16) : rt / (16 / J);
+}
+
 // ---- the kernel -------------------------------------------------------------
 
 // RO = code rows per output: 4T rounded up to a power of two (4, 8, 16).
@@ -255,14 +286,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
   uint8_t* gbase = pf_smem_raw + (base - raw);
   const uint32_t sA = base;
   const uint32_t sB = base + kPfStages * kPfAStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kPfStages * (kPfAStage + kPfBStage));
+  const uint32_t sC = sB + kPfStages * kPfBStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kPfStages * (kPfAStage + kPfBStage) + kPfCStages * kPfCStage);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(kPfStages + s); };
   auto accf_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kPfStages + b); };
   auto acce_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * kPfStages + 2 + b); };
   const uint32_t done_bar = bar0 + 8u * (uint32_t)(2 * kPfStages + 4);  // every issued MMA complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPfStages + 5);
+  auto fullC = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kPfStages + 5 + s); };
+  auto emptyC = [&](int s) { return bar0 + 8u * (uint32_t)(2 * kPfStages + 5 + kPfCStages + s); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPfStages + 5 + 2 * kPfCStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -278,6 +312,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
       mbar_init(acce_bar(b), 4);  // one arrive per epilogue warp
     }
     mbar_init(done_bar, 1);  // tcgen05.commit after the last MMA
+    for (int s = 0; s < kPfCStages; ++s) {
+      mbar_init(fullC(s), 1);                 // the code warp's arrive.expect_tx
+      mbar_init(emptyC(s), kPfProducerWarps);  // one arrive per producer warp
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -367,8 +405,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
     // (q' = 0..3): the signs come from the sign words of the four lanes
     // (g, q') of the output's lane quad, the axis flags from the flag word of
     // lane (g, h + 2 (s >> 1)).  The quad's words of two blocks are 64
-    // contiguous bytes; the next pair of blocks (of this tile or the next) is
-    // loaded while the current one is expanded.
+    // contiguous bytes of the code stage; the next pair of blocks (of this
+    // tile or the next) is read while the current one is expanded.
     const int gt = tid - 64;
     const int grp = gt / (32 * kPfGroupWarps);
     const int lt = gt - grp * 32 * kPfGroupWarps;
@@ -382,14 +420,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
     const uint32_t sw_re = r_re & 7u, sw_im = (r_re + 1u) & 7u;
     const uint32_t smask = 0x80008000u + (uint32_t)(P.M >> 30);  // register-held mask (M < 2^30)
 
-    // loader cursor: tile, its problem's row base and pair count
+    // loader cursor: tile, pair, and the code windows before the tile's first
+    uint32_t ld_wc = 0;
     int64_t ld_tile = blockIdx.x;
     int64_t ld_c2 = 0;
-    const uint8_t* ld_tp = nullptr;  // this thread's row tile of plane p (null: nothing to load)
     int64_t ld_fullc = 0, ld_pairs = 0;
+    bool ld_live = false;  // this thread has a row of the tile (else it expands zeros)
+    uint32_t ld_run = 0;   // its (row tile, plane) run in a code stage
     int ld_g = 0;
     auto set_ld_tile = [&]() {
-      ld_tp = nullptr;
+      ld_live = false;
       if (ld_tile >= P.total_tiles) return;
       const PfTile c = pf_tile(P, ld_tile);
       const PrefillProblem& pr = P.p[c.pi];
@@ -397,42 +437,64 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
       ld_fullc = KB >> 1;
       ld_pairs = (KB + 1) >> 1;
       const int64_t j = c.rt * J + jj;
-      if (!active || j >= pr.n) return;
+      const int rtl = (int)((j >> 4) - pf_first_row_tile<J>(c.rt));
+      ld_run = pf_run_off(rtl * planes + p);
       ld_g = (int)(j & 7);
-      ld_tp = pr.codes + (int64_t)p * plane_bytes(pr.n, pr.m) + (j >> 4) * KB * kTileBytes;
+      ld_live = active && j < pr.n;
     };
+    // the quad's words of the cursor's pair from its window's code stage
+    // (false: a wait gave up)
     uint4 nxt[4];
-    auto load_pair = [&](uint4 (&dst)[4]) {
+    auto load_pair = [&](uint4 (&dst)[4]) -> bool {
 #pragma unroll
       for (int q = 0; q < 4; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-      if (!ld_tp) return;
+      if (ld_tile >= P.total_tiles) return true;
+      const uint32_t k = ld_wc + (uint32_t)(ld_c2 / kPfWinPairs);
+      const int cs = (int)(k % kPfCStages);
+      // one wait per window (its copies complete one phase of the barrier)
+      if (ld_c2 % kPfWinPairs == 0 &&
+          __any_sync(0xffffffffu, !mbar_wait(fullC(cs), (k / kPfCStages) & 1u, abort_flag) ? 1 : 0))
+        return false;
+      if (!ld_live) return true;
+      const uint32_t cb = sC + (uint32_t)cs * kPfCStage + ld_run + (uint32_t)(ld_c2 % kPfWinPairs) * 512u;
       if (ld_c2 < ld_fullc) {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          dst[q] = __ldg(reinterpret_cast<const uint4*>(ld_tp + ld_c2 * 512 + (4 * ld_g + q) * 16));
-      } else {
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(dst[q].x), "=r"(dst[q].y), "=r"(dst[q].z), "=r"(dst[q].w)
+                       : "r"(cb + (uint32_t)(4 * ld_g + q) * 16u)
+                       : "memory");
+      } else {  // an odd last block: 8 bytes a lane
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint2 v = __ldg(reinterpret_cast<const uint2*>(ld_tp + ld_fullc * 512 + (4 * ld_g + q) * 8));
-          dst[q].x = v.x;
-          dst[q].y = v.y;
-        }
+        for (int q = 0; q < 4; ++q)
+          asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                       : "=r"(dst[q].x), "=r"(dst[q].y)
+                       : "r"(cb + (uint32_t)(4 * ld_g + q) * 8u)
+                       : "memory");
       }
+      return true;
     };
+    // past the pair just read: its window's stage goes back to the code warp
+    // after the window's last pair
     auto advance = [&]() {
       if (ld_tile >= P.total_tiles) return;
+      if ((ld_c2 + 1) % kPfWinPairs == 0 || ld_c2 + 1 == ld_pairs) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(emptyC((int)((ld_wc + (uint32_t)(ld_c2 / kPfWinPairs)) % kPfCStages)));
+      }
       if (++ld_c2 == ld_pairs) {
+        ld_wc += (uint32_t)((ld_pairs + kPfWinPairs - 1) / kPfWinPairs);
         ld_c2 = 0;
         ld_tile += gridDim.x;
         set_ld_tile();
       }
     };
     set_ld_tile();
-    load_pair(nxt);
+    bool ld_ok = load_pair(nxt);
     advance();
 
     uint32_t it = 0;
-    bool ok = true;
+    bool ok = ld_ok;
     for (int64_t tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
       const PfTile c = pf_tile(P, tile);
       const PrefillProblem& pr = P.p[c.pi];
@@ -443,7 +505,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
         uint4 cur[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
-        load_pair(nxt);
+        if (!load_pair(nxt)) {
+          ok = false;
+          break;
+        }
         advance();
         const int nb = min(2, pr.kblocks - kb0);
 #pragma unroll
@@ -502,7 +567,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
         }
       }
     }
-  } else {
+  } else if (warp < 6 + kPfProducerWarps) {
     // ---------------- epilogue ----------------
     const int eq = warp & 3;  // TMEM lanes 32 eq .. 32 eq + 31
     const int r = 32 * eq + lane;
@@ -572,6 +637,39 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(b));
     }
+  } else if (lane == 0) {
+    // ---------------- code copies: each window of the tile's codes into the code ring ----------------
+    // Per (16-row tile rtl of the tile, plane p): the run of the window's
+    // block pairs (512 bytes each, an odd last block 256) of layout 2, to
+    // run rtl 2T + p of the stage.
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; ok && tile < P.total_tiles; tile += gridDim.x) {
+      const PfTile c = pf_tile(P, tile);
+      const PrefillProblem& pr = P.p[c.pi];
+      const int64_t KB = col_blocks(pr.m), fullc = KB >> 1, pairs = (KB + 1) >> 1;
+      const int64_t rt0 = pf_first_row_tile<J>(c.rt);
+      const int rtiles = (int)min((int64_t)(J > 16 ? J / 16 : 1), row_tiles(pr.n) - rt0);
+      const int64_t pb = plane_bytes(pr.n, pr.m);
+      for (int64_t c0 = 0; c0 < pairs; c0 += kPfWinPairs, ++it) {
+        const int s = (int)(it % kPfCStages);
+        if (!mbar_wait(emptyC(s), ((it / kPfCStages) & 1u) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int64_t full = max((int64_t)0, min((int64_t)kPfWinPairs, fullc - c0));
+        const int64_t tail = min((int64_t)kPfWinPairs, pairs - c0) > full ? 1 : 0;
+        const uint32_t run = (uint32_t)(full * 512 + tail * 256);
+        mbar_arrive_expect_tx(fullC(s), run * (uint32_t)(rtiles * 2 * T));
+        for (int rtl = 0; rtl < rtiles; ++rtl)
+          for (int p = 0; p < 2 * T; ++p)
+            bulk_load(sC + (uint32_t)s * kPfCStage + pf_run_off(rtl * 2 * T + p),
+                      pr.codes + (int64_t)p * pb + (rt0 + rtl) * KB * kTileBytes + c0 * 512, run, fullC(s));
+      }
+    }
+    // no copy outlives the CTA: wait for the last stages to land
+    for (uint32_t k = (it > (uint32_t)kPfCStages ? it - kPfCStages : 0u); k < it; ++k)
+      if (!mbar_wait(fullC((int)(k % kPfCStages)), (k / kPfCStages) & 1u, abort_flag)) break;
   }
 
   tc_fence_before();
