@@ -104,8 +104,15 @@ def _check(status: int):
         raise Fairy2iError(status, load_library().fairy2i_last_error().decode())
 
 
-def _stream(stream) -> int:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device_index: int | None = None) -> int:
+    """The CUDA stream handle: ``stream`` itself, else the current stream of ``device_index``
+    (or of the current device)."""
     if stream is None:
+        if _raw_stream is not None:
+            return int(_raw_stream(torch.cuda.current_device() if device_index is None else device_index))
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
@@ -137,7 +144,17 @@ class Packed:
     layout: int = LAYOUT_VERSION
 
     def desc(self) -> PackedDesc:
-        return PackedDesc(self.layout, self.T, self.n, self.m, self.codes.data_ptr(), self.scales.data_ptr())
+        """The C descriptor, built once and rebuilt after any field is assigned or when the
+        code or scale storage has moved."""
+        d = self.__dict__.get("_desc")
+        if d is None or d.codes != self.codes.data_ptr() or d.scales != self.scales.data_ptr():
+            d = PackedDesc(self.layout, self.T, self.n, self.m, self.codes.data_ptr(), self.scales.data_ptr())
+            self.__dict__["_desc"] = d
+        return d
+
+    def __setattr__(self, name, value):
+        self.__dict__.pop("_desc", None)
+        object.__setattr__(self, name, value)
 
     @property
     def nbytes(self) -> int:
@@ -204,6 +221,7 @@ def convert_quantize(R: torch.Tensor, T: int = 2, out: Packed | None = None, str
 
 
 _workspaces: dict = {}
+_ws_bytes: dict = {}  # (layer shapes, M) -> workspace bytes
 
 
 def workspace(qs, M: int, device, stream=None, descs=None) -> torch.Tensor | None:
@@ -211,13 +229,18 @@ def workspace(qs, M: int, device, stream=None, descs=None) -> torch.Tensor | Non
     kept per (device, stream) and grown when a call needs more (None if none is needed).
     Calls on one stream run in order, so they can share it."""
     count = len(qs)
-    if descs is None:
-        descs = (PackedDesc * count)(*[q.desc() for q in qs])
-    need = int(load_library().fairy2i_linear_workspace_bytes(descs, count, M))
+    shapes = (tuple((q.layout, q.T, q.n, q.m) for q in qs), M)
+    need = _ws_bytes.get(shapes)
+    if need is None:
+        if descs is None:
+            descs = (PackedDesc * count)(*[q.desc() for q in qs])
+        need = int(load_library().fairy2i_linear_workspace_bytes(descs, count, M))
+        _ws_bytes[shapes] = need
     if need == 0:
         return None
     dev = torch.device(device)
-    key = (dev.index if dev.index is not None else torch.cuda.current_device(), _stream(stream))
+    index = dev.index if dev.index is not None else torch.cuda.current_device()
+    key = (index, _stream(stream, index))
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < need:
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -235,15 +258,15 @@ def linear(q: Packed, x: torch.Tensor, algo: str = "auto", out: torch.Tensor | N
         raise ValueError(f"x must be bfloat16 [M, {2 * q.m}]")
     y = out if out is not None else torch.empty((x.shape[0], 2 * q.n), dtype=torch.float32, device=x.device)
     d = q.desc()
+    s = _stream(stream, x.get_device())
     if q.layout == LAYOUT_LUT:
         if ws is None:
-            ws = workspace([q], x.shape[0], x.device, stream)
+            ws = workspace([q], x.shape[0], x.device, s)
         wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
         _check(load_library().fairy2i_linear_ws(ctypes.byref(d), x.data_ptr(), x.shape[0], y.data_ptr(), ALGO[algo],
-                                                wp, wn, _stream(stream)))
+                                                wp, wn, s))
         return y
-    _check(load_library().fairy2i_linear_ex(ctypes.byref(d), x.data_ptr(), x.shape[0], y.data_ptr(), ALGO[algo],
-                                            _stream(stream)))
+    _check(load_library().fairy2i_linear_ex(ctypes.byref(d), x.data_ptr(), x.shape[0], y.data_ptr(), ALGO[algo], s))
     return y
 
 
@@ -284,21 +307,23 @@ def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None, ws: torch.Ten
     M = xs[0].shape[0]
     if ys is None:
         ys = [torch.empty((M, 2 * q.n), dtype=torch.float32, device=x.device) for q, x in zip(qs, xs)]
-    descs = (PackedDesc * count)(*[q.desc() for q in qs])
-    xp = (ctypes.c_void_p * count)(*[x.data_ptr() for x in xs])
-    yp = (ctypes.c_void_p * count)(*[y.data_ptr() for y in ys])
     for q, x, y in zip(qs, xs, ys):
         _dev(x, "x")
         _dev(y, "y")
         if x.dtype != torch.bfloat16 or x.shape != (M, 2 * q.m) or y.shape != (M, 2 * q.n):
             raise ValueError("group members need matching x [M, 2m] bfloat16 and y [M, 2n] float32")
+    descs = (PackedDesc * count)(*[q.desc() for q in qs])
+    xp = (ctypes.c_void_p * count)(*[x.data_ptr() for x in xs])
+    yp = (ctypes.c_void_p * count)(*[y.data_ptr() for y in ys])
+    index = xs[0].get_device()
+    s = _stream(stream, index)
     if qs[0].layout == LAYOUT_LUT:
         if ws is None:
-            ws = workspace(qs, M, xs[0].device, stream, descs)
+            ws = workspace(qs, M, xs[0].device, s, descs)
         wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
-        _check(load_library().fairy2i_linear_group_ws(descs, xp, yp, count, M, ALGO[algo], wp, wn, _stream(stream)))
+        _check(load_library().fairy2i_linear_group_ws(descs, xp, yp, count, M, ALGO[algo], wp, wn, s))
         return ys
-    _check(load_library().fairy2i_linear_group(descs, xp, yp, count, M, ALGO[algo], _stream(stream)))
+    _check(load_library().fairy2i_linear_group(descs, xp, yp, count, M, ALGO[algo], s))
     return ys
 
 
