@@ -168,28 +168,70 @@ __global__ void __launch_bounds__(kQuantThreads, WPT == 1 ? 2 : 1) quantize_word
   float re[E], im[E];
   bool bad = false;
   uint32_t valid[WPT];
-#pragma unroll
-  for (int u = 0; u < WPT; ++u) valid[u] = 0;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int64_t w = (int64_t)tid * WPT + (e >> 4);
-    const int64_t k = col_of(e);
-    float2 v = make_float2(0.0f, 0.0f);
-    if ((w >> 2) < KB && k < m) {
-      if (FUSED) {
-        // default caching: the row's other matrix (the neighbouring CTA) reads the same R
-        const float r11 = __ldg(top + k), r12 = __ldg(top + m + k);
-        const float r21 = __ldg(bot + k), r22 = __ldg(bot + m + k);
-        v = X == 0 ? make_float2(half_sum(r11, r22), half_diff(r21, r12))   // U
-                   : make_float2(half_diff(r11, r22), half_sum(r12, r21));  // W
-      } else {
-        v = __ldcs(src + k);
-      }
-      valid[e >> 4] |= 1u << (e & 15);
+  // the weight of column k: from U or W, or formed from the four blocks of R
+  // (default caching there: the row's other matrix, the neighbouring CTA,
+  // reads the same R)
+  auto weight = [&](int64_t k) -> float2 {
+    if (FUSED) {
+      const float r11 = __ldg(top + k), r12 = __ldg(top + m + k);
+      const float r21 = __ldg(bot + k), r22 = __ldg(bot + m + k);
+      return X == 0 ? make_float2(half_sum(r11, r22), half_diff(r21, r12))   // U
+                    : make_float2(half_diff(r11, r22), half_sum(r12, r21));  // W
     }
-    bad |= !(isfinite(v.x) && isfinite(v.y));
-    re[e] = v.x;
-    im[e] = v.y;
+    return __ldcs(src + k);
+  };
+  // A word whose 16 columns all lie inside the matrix is read two columns at
+  // a time (its columns come in adjacent pairs k, k + 1 with k even): 16-byte
+  // loads of U or W, 8-byte loads of the R blocks; m even keeps them aligned.
+  // Other words are read one weight at a time.
+  const bool pairs_aligned = (m & 1) == 0;
+#pragma unroll
+  for (int u = 0; u < WPT; ++u) {
+    const int64_t w = (int64_t)tid * WPT + u;
+    const bool whole = (w >> 2) < KB && (LAYOUT == 3 ? w * 16 + 16 <= m : (w >> 2) * 64 + 64 <= m);
+    if (whole && pairs_aligned) {
+      valid[u] = 0xFFFFu;
+#pragma unroll
+      for (int c = 0; c < 16; c += 2) {
+        const int e = 16 * u + c;
+        const int64_t k = col_of(e);
+        float2 v0, v1;
+        if (FUSED) {
+          const float2 r11 = __ldg(reinterpret_cast<const float2*>(top + k));
+          const float2 r12 = __ldg(reinterpret_cast<const float2*>(top + m + k));
+          const float2 r21 = __ldg(reinterpret_cast<const float2*>(bot + k));
+          const float2 r22 = __ldg(reinterpret_cast<const float2*>(bot + m + k));
+          v0 = X == 0 ? make_float2(half_sum(r11.x, r22.x), half_diff(r21.x, r12.x))
+                      : make_float2(half_diff(r11.x, r22.x), half_sum(r12.x, r21.x));
+          v1 = X == 0 ? make_float2(half_sum(r11.y, r22.y), half_diff(r21.y, r12.y))
+                      : make_float2(half_diff(r11.y, r22.y), half_sum(r12.y, r21.y));
+        } else {
+          const float4 v = __ldcs(reinterpret_cast<const float4*>(src + k));
+          v0 = make_float2(v.x, v.y);
+          v1 = make_float2(v.z, v.w);
+        }
+        bad |= !(isfinite(v0.x) && isfinite(v0.y) && isfinite(v1.x) && isfinite(v1.y));
+        re[e] = v0.x;
+        im[e] = v0.y;
+        re[e + 1] = v1.x;
+        im[e + 1] = v1.y;
+      }
+    } else {
+      valid[u] = 0;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int e = 16 * u + c;
+        const int64_t k = col_of(e);
+        float2 v = make_float2(0.0f, 0.0f);
+        if ((w >> 2) < KB && k < m) {
+          v = weight(k);
+          valid[u] |= 1u << c;
+        }
+        bad |= !(isfinite(v.x) && isfinite(v.y));
+        re[e] = v.x;
+        im[e] = v.y;
+      }
+    }
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0) f2i_raise(kErrNonFinite);
