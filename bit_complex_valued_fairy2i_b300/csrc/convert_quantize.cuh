@@ -183,13 +183,34 @@ __global__ void __launch_bounds__(kQuantThreads, WPT == 1 ? 2 : 1) quantize_word
   // A word whose 16 columns all lie inside the matrix is read two columns at
   // a time (its columns come in adjacent pairs k, k + 1 with k even): 16-byte
   // loads of U or W, 8-byte loads of the R blocks; m even keeps them aligned.
-  // Other words are read one weight at a time.
+  // From R on layout 3 (16 consecutive columns, m a multiple of 4) it is
+  // four columns per 16-byte load.  Other words are read one weight at a time.
   const bool pairs_aligned = (m & 1) == 0;
+  const bool quads_aligned = FUSED && LAYOUT == 3 && (m & 3) == 0;
 #pragma unroll
   for (int u = 0; u < WPT; ++u) {
     const int64_t w = (int64_t)tid * WPT + u;
     const bool whole = (w >> 2) < KB && (LAYOUT == 3 ? w * 16 + 16 <= m : (w >> 2) * 64 + 64 <= m);
-    if (whole && pairs_aligned) {
+    if (FUSED && LAYOUT == 3 && whole && quads_aligned) {
+      valid[u] = 0xFFFFu;
+#pragma unroll
+      for (int c = 0; c < 16; c += 4) {
+        const int e = 16 * u + c;
+        const int64_t k = w * 16 + c;
+        const float4 r11 = __ldg(reinterpret_cast<const float4*>(top + k));
+        const float4 r12 = __ldg(reinterpret_cast<const float4*>(top + m + k));
+        const float4 r21 = __ldg(reinterpret_cast<const float4*>(bot + k));
+        const float4 r22 = __ldg(reinterpret_cast<const float4*>(bot + m + k));
+        const float a11[4] = {r11.x, r11.y, r11.z, r11.w}, a12[4] = {r12.x, r12.y, r12.z, r12.w};
+        const float a21[4] = {r21.x, r21.y, r21.z, r21.w}, a22[4] = {r22.x, r22.y, r22.z, r22.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          re[e + i] = X == 0 ? half_sum(a11[i], a22[i]) : half_diff(a11[i], a22[i]);
+          im[e + i] = X == 0 ? half_diff(a21[i], a12[i]) : half_sum(a12[i], a21[i]);
+          bad |= !(isfinite(re[e + i]) && isfinite(im[e + i]));
+        }
+      }
+    } else if (whole && pairs_aligned) {
       valid[u] = 0xFFFFu;
 #pragma unroll
       for (int c = 0; c < 16; c += 2) {
