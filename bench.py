@@ -408,7 +408,10 @@ def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
             "by_kernel": legs}
 
 
-def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int = 4):
+SWEEP_ALGOS = ("lut", "tcgen05_dq", "auto_layout3", "mma", "tcgen05", "auto", "tcgen05_sp")
+
+
+def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int = 4, algos=SWEEP_ALGOS):
     """Batched decode sweep: per token count M and per algorithm, the 7 projections of
     `blocks` distinct blocks (205 MB at 4 blocks, above L2), one grouped call per block;
     time per block, weight GB/s and tokens/s-equivalent.  "lut", "tcgen05_dq" and
@@ -435,8 +438,7 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
         xs = [[x[:M].contiguous() for x in xb] for xb in xs_full]
         ys = [[torch.empty((M, 2 * q.n), dtype=torch.float32, device=dev) for q in qs] for qs in stack]
         row = {"M": M}
-        for key in ("lut", "tcgen05_dq", "auto_layout3", "mma", "tcgen05", "auto") + \
-                (("tcgen05_sp",) if M <= 8 else ()):
+        for key in [a for a in algos if a != "tcgen05_sp" or M <= 8]:
             st = stack3 if key in ("lut", "tcgen05_dq", "auto_layout3") else stack
             algo = "auto" if key == "auto_layout3" else key
 
@@ -613,7 +615,9 @@ def run_sweep_only(args, world, rank, local):
 
     f2i_build.build()
     torch.cuda.set_device(local)
-    res = sweep_leg(f2i, torch.device("cuda", local))
+    Ms = tuple(int(v) for v in args.sweep_ms.split(",")) if args.sweep_ms else (1, 2, 4, 8, 16, 32, 64)
+    algos = tuple(args.sweep_algos.split(",")) if args.sweep_algos else SWEEP_ALGOS
+    res = sweep_leg(f2i, torch.device("cuda", local), Ms=Ms, algos=algos)
     if rank == 0:
         print(json.dumps({"sweep": res}), flush=True)
 
@@ -837,6 +841,9 @@ def main():
                     help="decode kernel of the default mode (lut = the table-lookup decode on layout 3; "
                          "auto = the library's choice on layout 2)")
     ap.add_argument("--prefill-tokens", type=int, default=2048)
+    ap.add_argument("--sweep-ms", default="", help="--mode sweep: token counts, comma-separated (default 1..64)")
+    ap.add_argument("--sweep-algos", default="",
+                    help="--mode sweep: algorithms, comma-separated, from " + ",".join(SWEEP_ALGOS))
     ap.add_argument("--blocks", type=int, default=BLOCKS,
                     help="decoder blocks in the stack (32 = the full model; fewer only for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
