@@ -346,10 +346,10 @@ fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64
   return FAIRY2I_OK;
 }
 
-template <int T, int NT>
+template <int T, int NT, bool SMALL = false>
 fairy2i_status launch_dq_t(const f2i::DqParams& P, int grid, cudaStream_t s) {
-  auto k = f2i::linear_dq_kernel<T, NT>;
-  const size_t smem = f2i::dq_smem_bytes<NT, T>();
+  auto k = f2i::linear_dq_kernel<T, NT, SMALL>;
+  const size_t smem = f2i::dq_smem_bytes<NT, T, SMALL>();
   fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(k), smem, "dequantized prefill");
   if (st != FAIRY2I_OK) return st;
   k<<<(unsigned)grid, f2i::kDqThreads, smem, s>>>(P);
@@ -431,14 +431,15 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
     P.total_tiles = tiles;
     const int grid = (int)std::min<int64_t>(tiles, sm_count());
     dq_schedule(P, grid, nt);
+    const bool small = nt == 1 && P.N <= 64;  // value tables in 8 KB-B-stage room
     fairy2i_status st;
     switch (T * 2 + nt - 1) {
-      case 2: st = launch_dq_t<1, 1>(P, grid, s); break;
+      case 2: st = small ? launch_dq_t<1, 1, true>(P, grid, s) : launch_dq_t<1, 1>(P, grid, s); break;
       case 3: st = launch_dq_t<1, 2>(P, grid, s); break;
-      case 4: st = launch_dq_t<2, 1>(P, grid, s); break;
+      case 4: st = small ? launch_dq_t<2, 1, true>(P, grid, s) : launch_dq_t<2, 1>(P, grid, s); break;
       case 5: st = launch_dq_t<2, 2>(P, grid, s); break;
-      case 6: st = launch_dq_t<3, 1>(P, grid, s); break;
-      case 8: st = launch_dq_t<4, 1>(P, grid, s); break;
+      case 6: st = small ? launch_dq_t<3, 1, true>(P, grid, s) : launch_dq_t<3, 1>(P, grid, s); break;
+      case 8: st = small ? launch_dq_t<4, 1, true>(P, grid, s) : launch_dq_t<4, 1>(P, grid, s); break;
       default: return fail(FAIRY2I_ERR_UNSUPPORTED, "dequantized prefill supports T <= 4");
     }
     if (st != FAIRY2I_OK) return st;

@@ -61,16 +61,32 @@ __host__ __device__ constexpr uint32_t dq_c_stage(int T) { return 8192u * (uint3
 // NT token tiles of N per decoded k-block pair: 1 (M <= 256, or T > 2; the
 // two TMEM accumulators alternate between tiles) or 2 (M > 256 and T <= 2;
 // one decode feeds two MMAs, the accumulators hold the tile's two token
-// tiles).  Stages beside the code ring: 3 A and 3 B of 32 KB (NT = 1, T <= 2),
-// else 2 A of 32 KB and 2 B of NT x 32 KB.
-template <int NT, int T>
-__host__ __device__ constexpr int dq_a_stages() { return NT == 1 && T <= 2 ? 3 : 2; }
-template <int NT, int T>
-__host__ __device__ constexpr int dq_b_stages() { return NT == 1 && T <= 2 ? 3 : 2; }
-template <int NT, int T>
+// tiles).  SMALL (N <= 64, one token tile): the producers set the pace; B
+// stages hold 64 tokens (8 KB) and the room goes to per-row value tables
+// (dq_table_row).  Stages beside the code ring (A 32 KB each):
+//   SMALL:           3 A and 3 B of 8 KB, value tables;
+//   NT = 1, T <= 2:  3 A and 3 B of 32 KB;
+//   otherwise:       2 A and 2 B of NT x 32 KB.
+template <int NT, int T, bool SMALL>
+__host__ __device__ constexpr int dq_a_stages() { return (NT == 1 && T <= 2) || SMALL ? 3 : 2; }
+template <int NT, int T, bool SMALL>
+__host__ __device__ constexpr int dq_b_stages() { return (NT == 1 && T <= 2) || SMALL ? 3 : 2; }
+template <int NT, bool SMALL>
+__host__ __device__ constexpr uint32_t dq_b_stage_bytes() { return SMALL ? 64u * kDqBK * 2u : (uint32_t)NT * kDqBStage; }
+// Value tables: for every row of the tile, matrix X and pair of stages, the 16
+// (Re, Im) sums that the pair's sign and axis bits can select; row stride 16
+// bytes past the tables, so that the rows of a warp start in different banks.
+template <int T>
+__host__ __device__ constexpr int dq_pairs() { return (T + 1) / 2; }
+template <int T>
+__host__ __device__ constexpr uint32_t dq_table_row() { return 2u * dq_pairs<T>() * 16u * 8u + 16u; }
+template <int T, bool SMALL>
+__host__ __device__ constexpr uint32_t dq_table_bytes() { return SMALL ? 64u * dq_table_row<T>() : 0u; }
+template <int NT, int T, bool SMALL>
 __host__ __device__ constexpr size_t dq_smem_bytes() {
-  return 1024 + (size_t)dq_a_stages<NT, T>() * kDqAStage + (size_t)dq_b_stages<NT, T>() * NT * kDqBStage +
-         (size_t)kDqCStages * dq_c_stage(T) + 512;
+  return 1024 + (size_t)dq_a_stages<NT, T, SMALL>() * kDqAStage +
+         (size_t)dq_b_stages<NT, T, SMALL>() * dq_b_stage_bytes<NT, SMALL>() + (size_t)kDqCStages * dq_c_stage(T) +
+         dq_table_bytes<T, SMALL>() + 512;
 }
 
 struct DqProblem {
@@ -159,6 +175,31 @@ __device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
   return v;
 }
 
+// One code of one stage added to (re, im) as dq_code does (same operations):
+// s the sign bit, f the imaginary-axis flag.
+__device__ __forceinline__ void dq_add(float& re, float& im, uint32_t s, uint32_t f, uint32_t sre, uint32_t sim) {
+  const float v = __uint_as_float((f ? sim : sre) ^ (s << 31));
+  if (f) im = __fadd_rn(im, v);
+  else re = __fadd_rn(re, v);
+}
+// Table index of column E from the word (sign, flag of stage 2k; sign, flag of
+// stage 2k + 1) of bytes: bit 3 the first sign, 2 its flag, 1 the second
+// sign, 0 its flag (the multiply gathers bit E of the four bytes, no carries).
+template <int E>
+__device__ __forceinline__ uint32_t dq_index(uint32_t w) {
+  return (((w >> E) & 0x01010101u) * 0x08040201u) >> 24;
+}
+__device__ __forceinline__ uint32_t dq_prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
 // The 8 codes of a group in one plane (bits B .. B + 7 of s and f).
 template <int B>
 __device__ __forceinline__ void dq_plane(float (&re)[8], float (&im)[8], uint32_t s, uint32_t f, uint32_t sre,
@@ -173,17 +214,18 @@ __device__ __forceinline__ void dq_plane(float (&re)[8], float (&im)[8], uint32_
   dq_code<B + 7>(re[7], im[7], s, f, sre, sim);
 }
 
-template <int T, int NT>
+template <int T, int NT, bool SMALL>
 __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_constant__ DqParams P) {
   extern __shared__ uint8_t dq_smem_raw[];
   constexpr int NP = 2 * T;
   constexpr int NW = (NP + 3) / 4;  // words holding one byte per plane
   static_assert(NT == 1 || T <= 2, "two token tiles per decode only for T <= 2 (shared memory)");
-  static_assert(dq_smem_bytes<NT, T>() <= 232448, "shared memory per CTA");
-  constexpr int AS = dq_a_stages<NT, T>();
-  constexpr int BS = dq_b_stages<NT, T>();
+  static_assert(!SMALL || NT == 1, "small token tiles come one per decode");
+  static_assert(dq_smem_bytes<NT, T, SMALL>() <= 232448, "shared memory per CTA");
+  constexpr int AS = dq_a_stages<NT, T, SMALL>();
+  constexpr int BS = dq_b_stages<NT, T, SMALL>();
   constexpr int CS = kDqCStages;
-  constexpr uint32_t kBStage = (uint32_t)NT * kDqBStage;
+  constexpr uint32_t kBStage = dq_b_stage_bytes<NT, SMALL>();
   constexpr uint32_t kCStage = dq_c_stage(T);
 
   const uint32_t raw = smem_u32(dq_smem_raw);
@@ -192,7 +234,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
   const uint32_t sA = base;
   const uint32_t sB = base + AS * kDqAStage;
   const uint32_t sC = sB + BS * kBStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + AS * kDqAStage + BS * kBStage + CS * kCStage);
+  const uint32_t sTab = sC + CS * kCStage;  // value tables (SMALL)
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(gbase + AS * kDqAStage + BS * kBStage + CS * kCStage + dq_table_bytes<T, SMALL>());
   const uint32_t bar0 = smem_u32(bars);
   auto fullA = [&](int s) { return bar0 + 8u * (uint32_t)s; };
   auto emptyA = [&](int s) { return bar0 + 8u * (uint32_t)(AS + s); };
@@ -203,7 +247,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
   const uint32_t done_bar = bar0 + 8u * (uint32_t)(2 * AS + 2 * BS + 4);  // every issued MMA complete
   auto fullC = [&](int s) { return bar0 + 8u * (uint32_t)(2 * AS + 2 * BS + 5 + s); };
   auto emptyC = [&](int s) { return bar0 + 8u * (uint32_t)(2 * AS + 2 * BS + 5 + CS + s); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * AS + 2 * BS + 5 + 2 * CS);
+  const uint32_t prod_bar = bar0 + 8u * (uint32_t)(2 * AS + 2 * BS + 5 + 2 * CS);  // the producer warps meet
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * AS + 2 * BS + 6 + 2 * CS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // accumulator of token tile `sub` of the lt-th tile, and how many tiles used it before
   auto acc_buf = [&](uint32_t lt, int sub) { return NT == 1 ? (int)(lt & 1u) : sub; };
@@ -220,6 +265,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
       mbar_init(fullC(s), 1);                 // the code warp's arrive.expect_tx
       mbar_init(emptyC(s), kDqProducerWarps);  // one arrive per producer warp
     }
+    mbar_init(prod_bar, kDqProducerWarps);
     for (int s = 0; s < BS; ++s) {
       mbar_init(fullB(s), 1);   // TMA arrive.expect_tx
       mbar_init(emptyB(s), 1);  // tcgen05.commit
@@ -336,6 +382,17 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
     const uint32_t cbyte = (uint32_t)(cr * 16 + l3_byte_of(gq, cr));
     uint32_t it = 0, itc = 0;  // itc: windows of codes consumed
     bool ok = true;
+    // SMALL: row jl's value tables
+    constexpr int PAIRS = dq_pairs<T>();
+    const uint32_t trow = sTab + (uint32_t)jl * dq_table_row<T>();
+    uint32_t pbu = 0;  // uses of the producers' barrier
+    auto producers_meet = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(prod_bar);
+      const bool got = mbar_wait(prod_bar, pbu & 1u, abort_flag);
+      ++pbu;
+      return !__any_sync(0xffffffffu, !got);
+    };
     for (int64_t i = 0; ok; ++i) {
       const int64_t tile = dq_tile_id(P, i);
       if (tile < 0) break;
@@ -350,6 +407,39 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
       for (int p = 0; p < NP; ++p) {
         sre[p] = live ? __float_as_uint(__ldg(pr.scales + (int64_t)(2 * p) * n + j)) : 0u;
         sim[p] = live ? __float_as_uint(__ldg(pr.scales + (int64_t)(2 * p + 1) * n + j)) : 0u;
+      }
+      if constexpr (SMALL) {
+        // the tables of row jl: for matrix X and stage pair k, entry idx (bits as
+        // dq_index) holds the pair's (Re, Im) sum, accumulated like dq_code (from
+        // 0, stage 2k first); thread gq writes entries gq and gq + 8 of each.
+        // The producers meet before (the previous tile's tables are read out) and
+        // after (the tables are complete).
+        if (!producers_meet()) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int X = 0; X < 2; ++X)
+#pragma unroll
+          for (int k = 0; k < PAIRS; ++k) {
+            const int p0 = X * T + 2 * k;
+            const bool two = 2 * k + 1 < T;
+            const int p1 = two ? p0 + 1 : p0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t idx = (uint32_t)(gq + 8 * h);
+              float re = 0.0f, im = 0.0f;
+              dq_add(re, im, (idx >> 3) & 1u, (idx >> 2) & 1u, sre[p0], sim[p0]);
+              if (two) dq_add(re, im, (idx >> 1) & 1u, idx & 1u, sre[p1], sim[p1]);
+              asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(trow + (uint32_t)((X * PAIRS + k) * 16 + idx) * 8u),
+                           "f"(re), "f"(im)
+                           : "memory");
+            }
+          }
+        if (!producers_meet()) {
+          ok = false;
+          break;
+        }
       }
       // the group's sign and q bytes of every stage plane for pair kp (zero
       // past n), read from the window's code stage one pair ahead of their
@@ -395,19 +485,49 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         // (Re, Im) of U^ [0] and W^ [1] for the group's 8 columns, in fp32 (zero
         // scales past n); columns past m decode from zero bits and meet zero-filled x
         float re[2][8], im[2][8];
+        if constexpr (SMALL) {
+          // per matrix and stage pair: the word of bytes (sign, flag of stage 2k;
+          // sign, flag of stage 2k + 1), then one table load per column
 #pragma unroll
-        for (int x = 0; x < 2; ++x)
+          for (int X = 0; X < 2; ++X)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) re[x][e] = im[x][e] = 0.0f;
+            for (int k = 0; k < PAIRS; ++k) {
+              const int p0 = X * T + 2 * k;
+              const bool two = 2 * k + 1 < T;
+              const int p1 = two ? p0 + 1 : p0;
+              uint32_t w = dq_prmt(sw[p0 >> 2], fw[p0 >> 2], (uint32_t)((p0 & 3) | ((4 + (p0 & 3)) << 4))) & 0xFFFFu;
+              if (two) w |= dq_prmt(sw[p1 >> 2], fw[p1 >> 2], (uint32_t)((p1 & 3) | ((4 + (p1 & 3)) << 4))) << 16;
+              const uint32_t tb = trow + (uint32_t)((X * PAIRS + k) * 16) * 8u;
+              float2 v[8];
+              v[0] = lds_f2(tb + 8u * dq_index<0>(w));
+              v[1] = lds_f2(tb + 8u * dq_index<1>(w));
+              v[2] = lds_f2(tb + 8u * dq_index<2>(w));
+              v[3] = lds_f2(tb + 8u * dq_index<3>(w));
+              v[4] = lds_f2(tb + 8u * dq_index<4>(w));
+              v[5] = lds_f2(tb + 8u * dq_index<5>(w));
+              v[6] = lds_f2(tb + 8u * dq_index<6>(w));
+              v[7] = lds_f2(tb + 8u * dq_index<7>(w));
 #pragma unroll
-        for (int p = 0; p < NP; ++p) {
-          const uint32_t sb = sw[p >> 2], fb = fw[p >> 2];
-          const int x = p < T ? 0 : 1;
-          switch (p & 3) {  // resolved at compile time (the loop is unrolled)
-            case 0: dq_plane<0>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
-            case 1: dq_plane<8>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
-            case 2: dq_plane<16>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
-            default: dq_plane<24>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
+              for (int e = 0; e < 8; ++e) {
+                re[X][e] = k == 0 ? v[e].x : __fadd_rn(re[X][e], v[e].x);
+                im[X][e] = k == 0 ? v[e].y : __fadd_rn(im[X][e], v[e].y);
+              }
+            }
+        } else {
+#pragma unroll
+          for (int x = 0; x < 2; ++x)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) re[x][e] = im[x][e] = 0.0f;
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            const uint32_t sb = sw[p >> 2], fb = fw[p >> 2];
+            const int x = p < T ? 0 : 1;
+            switch (p & 3) {  // resolved at compile time (the loop is unrolled)
+              case 0: dq_plane<0>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
+              case 1: dq_plane<8>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
+              case 2: dq_plane<16>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
+              default: dq_plane<24>(re[x], im[x], sb, fb, sre[p], sim[p]); break;
+            }
           }
         }
         // both stages of the pair: k-block 2 kp (Re x columns) and 2 kp + 1 (Im x columns)
