@@ -248,3 +248,22 @@ def test_mma_decode_rejects_code_planes_beyond_32bit_offsets(lib):
     big = _desc(n=300000, m=16384, T=2)
     assert lib.fairy2i_linear_ex(ctypes.byref(big), p, 1, p, 2, None) == 4
     assert "32-bit" in _err(lib)
+
+
+def test_packed_descriptor_follows_its_tensors(lib):
+    """The binding builds a layer's C descriptor once; assigning a field, or code and scale
+    storage that moved, gives a fresh one with the current pointers and shape."""
+    codes = torch.zeros(64, dtype=torch.uint8)
+    scales = torch.zeros(2 * 2 * 2 * 8)
+    q = f2i.Packed(8, 16, 2, codes, scales, layout=3)
+    d1 = q.desc()
+    assert q.desc() is d1
+    assert (d1.n, d1.m, d1.T, d1.version) == (8, 16, 2, 3)
+    assert d1.codes == codes.data_ptr() and d1.scales == scales.data_ptr()
+    q.codes = torch.zeros(128, dtype=torch.uint8)  # a new tensor in the field
+    d2 = q.desc()
+    assert d2 is not d1 and d2.codes == q.codes.data_ptr()
+    q.n = 4  # any field assignment
+    assert q.desc().n == 4
+    q.scales.set_(torch.zeros(64).untyped_storage())  # same tensor object, storage moved
+    assert q.desc().scales == q.scales.data_ptr()
