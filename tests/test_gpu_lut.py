@@ -452,6 +452,29 @@ def test_dq_full_size_block_prefill_sampled():
         assert rel_l2(got, want) <= DQ_REL_L2
 
 
+@pytest.mark.parametrize("M", [16, 64, 256])  # value tables up to 64 tokens, the per-plane decode above
+def test_dq_full_size_block_batched_sampled(M):
+    """The seven LLaMA-2-7B projections at batched-decode token counts (the sweep's launch:
+    one grouped call, AUTO on layout 3 takes the dequantized GEMM from 13 tokens), against
+    the oracle on sampled rows and tokens."""
+    qs, xs, samples = [], [], []
+    for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
+        n = out_f // 2
+        R = inputs.weight_R(3, pi, out_f, in_f)
+        qs.append(f2i.convert_quantize(R.cuda(), 2, layout=L3))
+        x = inputs.activations(3, pi, M, in_f)
+        xs.append(x.cuda())
+        rows = _sample_rows(n, count=6, seed=pi + M)
+        qU, qW = _oracle_rows(R, rows, 2)
+        toks = np.unique(np.array([0, 1, M // 2, M - 1]))
+        samples.append((rows, toks, oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x[toks]))))
+    ys = f2i.linear_group(qs, xs)  # AUTO
+    for q, y, (rows, toks, want) in zip(qs, ys, samples):
+        y = y.cpu().numpy()[toks]
+        got = np.concatenate([y[:, rows], y[:, q.n + rows]], axis=1)
+        assert rel_l2(got, want) <= DQ_REL_L2
+
+
 @pytest.mark.parametrize("layout", [2, L3])
 @pytest.mark.parametrize("T", [1, 2, 3])
 def test_quantize_extreme_row_magnitudes_bit_exact(layout, T):
