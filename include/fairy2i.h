@@ -102,7 +102,8 @@ typedef enum {
     FAIRY2I_ALGO_AUTO = 0,    /* pick the fastest kernel for the token count */
     FAIRY2I_ALGO_ADDSUB = 1,  /* CUDA cores: adds/subtracts only, fp32 accumulation */
     FAIRY2I_ALGO_MMA = 2,     /* decode: 2:4-sparse mma.sync, signs as bf16 +-2, axis flags as metadata */
-    FAIRY2I_ALGO_TCGEN05 = 3, /* prefill: codes expanded to bf16 in shared memory, tcgen05.mma */
+    FAIRY2I_ALGO_TCGEN05 = 3, /* prefill: codes staged in shared memory by the TMA engine, expanded
+                                 to bf16 {+-1, 0} rows there, tcgen05.mma, scales in the epilogue */
     FAIRY2I_ALGO_TCGEN05_SP = 4, /* decode, M <= 8, T <= 4: 2:4-sparse tcgen05.mma.sp (e4m3 signs and axis
                                    flags as metadata in tensor memory; x as two exact e4m3 terms) */
     FAIRY2I_ALGO_LUT = 5,     /* layout 3, T <= 4: per window of 256 columns and token, tables of the
@@ -111,7 +112,8 @@ typedef enum {
                                  code byte one shared-memory lookup and two fp32 adds */
     FAIRY2I_ALGO_TCGEN05_DQ = 6 /* layout 3, T <= 4, m a multiple of 8: tcgen05 GEMM of the dequantized
                                  real matrix (Theorem 1 rebuilt from the summed stages) as two bfloat16
-                                 terms hi + lo against x; no workspace */
+                                 terms hi + lo against x; codes staged in shared memory by the TMA
+                                 engine; no workspace */
 } fairy2i_algo;
 
 /* Bytes of the code planes of an n x m layer with T stages in layout
