@@ -103,7 +103,8 @@ typedef enum {
     FAIRY2I_ALGO_ADDSUB = 1,  /* CUDA cores: adds/subtracts only, fp32 accumulation */
     FAIRY2I_ALGO_MMA = 2,     /* decode: 2:4-sparse mma.sync, signs as bf16 +-2, axis flags as metadata */
     FAIRY2I_ALGO_TCGEN05 = 3, /* prefill: codes staged in shared memory by the TMA engine, expanded
-                                 to bf16 {+-1, 0} rows there, tcgen05.mma, scales in the epilogue */
+                                 there to ternary bf16 rows ({+-2, +-0}: the factor 2 leaves with
+                                 the scales), tcgen05.mma, scales in the epilogue */
     FAIRY2I_ALGO_TCGEN05_SP = 4, /* decode, M <= 8, T <= 4: 2:4-sparse tcgen05.mma.sp (e4m3 signs and axis
                                    flags as metadata in tensor memory; x as two exact e4m3 terms) */
     FAIRY2I_ALGO_LUT = 5,     /* layout 3, T <= 4: per window of 256 columns and token, tables of the
