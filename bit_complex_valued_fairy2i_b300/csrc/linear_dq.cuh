@@ -22,7 +22,10 @@
 //   K:    blocks of 64 columns in pairs (block c of Re x, block c of Im x),
 //         the two stages of a pair filled by one decode;
 //   A:    hi and lo, 128-byte swizzled K-major, written by 16 producer warps
-//         from the codes (in shared memory) and the scales;
+//         from the codes (in shared memory) and the scales: per stage plane and
+//         column a signed scale added on its axis, or, with at most 64 tokens,
+//         one load per column and matrix from the row's value tables (the 16
+//         sums a stage pair's sign and axis bits select);
 //   codes: per window of 256 columns (4 k-block pairs), the layout-3 bytes of
 //         the tile's two 32-row tiles (contiguous: 2 x 2T planes x the
 //         window's slots x 512 bytes), one bulk copy (cp.async.bulk, the TMA
