@@ -325,7 +325,7 @@ def test_full_size_projection_layout3_sampled(name, out_f, in_f, T):
     assert rel_l2(got, want) <= REL_L2
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 12])  # 12: three launches of 4 tokens, AUTO's last table-lookup count
 def test_full_size_block_group_layout3_sampled(M):
     """The seven projections of a block in one grouped table-lookup launch (the
     benchmark's launch), against the oracle on sampled rows."""
