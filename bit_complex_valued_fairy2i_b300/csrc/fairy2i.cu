@@ -635,10 +635,10 @@ constexpr int64_t kPrefillMinTokens = 16;
 // Token count from which AUTO takes the dequantized GEMM over the table-lookup
 // decode on layout 3.
 // Layout 3: AUTO's switch from the table lookup (4 tokens per launch at T <= 2,
-// ~57 us per launch on a LLaMA-2-7B block) to the dequantized GEMM (~174 us
-// at any count up to 256): 9-12 tokens cost the same either way, 13 favour
-// the GEMM.
-constexpr int64_t kDqMinTokens = 13;
+// ~58 us per launch on a LLaMA-2-7B block) to the dequantized GEMM (~155 us
+// at any count up to 64): measured per block at 9 / 10 / 11 / 12 tokens,
+// 136.8 / 147.6 / 159.7 / 177.3 us against 155.0 / 154.9 / 155.1 / 155.1 us.
+constexpr int64_t kDqMinTokens = 11;
 
 // The quantizer over U, W (FUSED = false) or straight from R (true); the
 // caller has checked the arguments.  Codes are zeroed first: each row ORs its
