@@ -414,9 +414,11 @@ SWEEP_ALGOS = ("lut", "tcgen05_dq", "auto_layout3", "mma", "tcgen05", "auto", "t
 def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int = 4, algos=SWEEP_ALGOS):
     """Batched decode sweep: per token count M and per algorithm, the 7 projections of
     `blocks` distinct blocks (205 MB at 4 blocks, above L2), one grouped call per block;
-    time per block, weight GB/s and tokens/s-equivalent.  "lut", "tcgen05_dq" and
+    time per block, weight GB/s and tokens/s-equivalent (eager calls; for AUTO on layout 3 also
+    the same calls replayed as a CUDA graph).  "lut", "tcgen05_dq" and
     "auto_layout3" read the same weights in layout 3 (the table lookup: one decode launch
-    per 4 tokens at T = 2, plus the window-combining launch; the dequantized GEMM: one
+    per 2 tokens at T = 2 (the first of 3 for odd M), each with its window-combining launch;
+    the dequantized GEMM: one
     launch with N = M rounded up to 16)."""
     stack, stack3, xs_full = [], [], []
     for b in range(blocks):
@@ -457,6 +459,24 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
             us = start.elapsed_time(stop) / reps / blocks * 1e3
             row[key] = {"us_per_block": round(us, 2), "weight_GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
                          "tokens_per_s_per_block": round(M / (us * 1e-6))}
+            if key == "auto_layout3":
+                # the same calls replayed as one CUDA graph: the device time per block, without
+                # the per-call host work that bounds the eager figure at small M
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    step()
+                graph.replay()
+                torch.cuda.synchronize()
+                start.record(stream)
+                for _ in range(reps):
+                    graph.replay()
+                stop.record(stream)
+                torch.cuda.synchronize()
+                gus = start.elapsed_time(stop) / reps / blocks * 1e3
+                row[key]["graph_us_per_block"] = round(gus, 2)
+                row[key]["graph_weight_GBps"] = round(nbytes / (gus * 1e-6) / 1e9, 1)
+                row[key]["graph_tokens_per_s_per_block"] = round(M / (gus * 1e-6))
+                del graph
         out.append(row)
     f2i.sync_status()
     return {"workload": f"llama2-7b blocks (7 projections each), T=2, {blocks} distinct blocks "

@@ -634,11 +634,12 @@ constexpr int64_t kTcDecodeMaxTokens = 8;
 constexpr int64_t kPrefillMinTokens = 16;
 // Token count from which AUTO takes the dequantized GEMM over the table-lookup
 // decode on layout 3.
-// Layout 3: AUTO's switch from the table lookup (4 tokens per launch at T <= 2,
-// ~58 us per launch on a LLaMA-2-7B block) to the dequantized GEMM (~155 us
-// at any count up to 64): measured per block at 9 / 10 / 11 / 12 tokens,
-// 136.8 / 147.6 / 159.7 / 177.3 us against 155.0 / 154.9 / 155.1 / 155.1 us.
-constexpr int64_t kDqMinTokens = 11;
+// Layout 3: AUTO's switch from the table lookup (launches of 2 or 3 tokens at
+// T <= 2, 27 and 41 us each on a LLaMA-2-7B block) to the dequantized GEMM
+// (~155 us at any count up to 64): measured per block at 10 / 11 / 12 / 13
+// tokens, 141.5 / 154.6 / 169.0 / 182.6 us against 155.3 / 155.1 / 155.4 /
+// 155.4 us.
+constexpr int64_t kDqMinTokens = 12;
 
 // The quantizer over U, W (FUSED = false) or straight from R (true); the
 // caller has checked the arguments.  Codes are zeroed first: each row ORs its
@@ -695,7 +696,7 @@ size_t lut_launch_workspace(const fairy2i_packed* qs, int cnt, int mc) {
 }
 
 size_t lut_workspace(const fairy2i_packed* qs, int count, int64_t M, int T) {
-  const int mc = (int)std::min<int64_t>(M, f2i::lut_max_tokens(T));
+  const int mc = f2i::lut_launch_tokens(M, 0, T);  // the first launch is the largest
   size_t need = 0;
   for (int p0 = 0; p0 < count; p0 += f2i::kLutMaxGroup)
     need = std::max(need, lut_launch_workspace(qs + p0, std::min(f2i::kLutMaxGroup, count - p0), mc));
@@ -735,11 +736,9 @@ fairy2i_status launch_lut(const f2i::LutParams& P, int T, int mc, int ctas, cuda
     case 9: return launch_lut_t<1, 1>(P, ctas, s);
     case 10: return launch_lut_t<1, 2>(P, ctas, s);
     case 11: return launch_lut_t<1, 3>(P, ctas, s);
-    case 12: return launch_lut_t<1, 4>(P, ctas, s);
     case 17: return launch_lut_t<2, 1>(P, ctas, s);
     case 18: return launch_lut_t<2, 2>(P, ctas, s);
     case 19: return launch_lut_t<2, 3>(P, ctas, s);
-    case 20: return launch_lut_t<2, 4>(P, ctas, s);
     case 25: return launch_lut_t<3, 1>(P, ctas, s);
     case 26: return launch_lut_t<3, 2>(P, ctas, s);
     case 33: return launch_lut_t<4, 1>(P, ctas, s);
@@ -747,7 +746,7 @@ fairy2i_status launch_lut(const f2i::LutParams& P, int T, int mc, int ctas, cuda
   }
 }
 
-// One launch per kLutMaxGroup layers and per lut_max_tokens(T) tokens.  Units
+// One launch per kLutMaxGroup layers and per lut_launch_tokens tokens.  Units
 // (layer, window, row tile) are split over one CTA per SM by their cost, in
 // launch order: 8 per slot of codes plus 3 for the unit's epilogue.
 fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count, int64_t M, int T,
@@ -762,14 +761,13 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
   for (int i = 0; i < count; ++i)
     if (f2i::l3_tiles(qs[i].n) * f2i::l3_windows(qs[i].m) > (int64_t)1 << 30)
       return fail(FAIRY2I_ERR_UNSUPPORTED, "layer %d too large for the table-lookup decode", i);
-  const int mcmax = f2i::lut_max_tokens(T);
   std::unique_ptr<f2i::LutParams> holder(new f2i::LutParams);
   f2i::LutParams& P = *holder;
   f2i::LutReduceParams RP;
   for (int p0 = 0; p0 < count; p0 += f2i::kLutMaxGroup) {
     const int cnt = std::min(f2i::kLutMaxGroup, count - p0);
-    for (int64_t t0 = 0; t0 < M; t0 += mcmax) {
-      const int mc = (int)std::min<int64_t>(mcmax, M - t0);
+    for (int64_t t0 = 0, mc = 0; t0 < M; t0 += mc) {
+      mc = f2i::lut_launch_tokens(M, t0, T);
       memset(&P, 0, sizeof(P));
       memset(&RP, 0, sizeof(RP));
       const size_t wsn = lut_launch_workspace(qs + p0, cnt, mc);

@@ -53,7 +53,15 @@ constexpr uint32_t kLutSmemBytes = 224u * 1024u;  // dynamic shared memory: cove
 
 // Largest token count of one launch for T stages (fp32 accumulators and the
 // double-buffered code words stay within 128 registers).
-__host__ __device__ constexpr int lut_max_tokens(int T) { return T <= 2 ? 4 : T == 3 ? 2 : 1; }
+__host__ __device__ constexpr int lut_max_tokens(int T) { return T <= 2 ? 3 : T == 3 ? 2 : 1; }
+// Tokens of the launch that starts at token t0 of M.  For T <= 2, launches of
+// 2 tokens, the first of 3 when M is odd: per LLaMA-2-7B block, launches of 1,
+// 2, 3 and 4 tokens took 17.5, 27.2, 41.0 and 59.0 us, so 2 or 3 tokens a
+// launch cost the least per token.  Otherwise as many as lut_max_tokens.
+__host__ __device__ constexpr int lut_launch_tokens(int64_t M, int64_t t0, int T) {
+  return T > 2 ? (int)(M - t0 < lut_max_tokens(T) ? M - t0 : lut_max_tokens(T))
+               : (t0 == 0 && M >= 3 && (M & 1)) ? 3 : (int)(M - t0 < 2 ? M - t0 : 2);
+}
 
 struct LutProblem {
   const uint8_t* codes;

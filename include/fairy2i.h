@@ -197,8 +197,8 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
 /* Layout-3 layers through fairy2i_linear / _ex / _group (no workspace) take
  * the dequantized GEMM (FAIRY2I_ALGO_TCGEN05_DQ; "Fairy2i: Ultra-Low-Bit ...",
  * Step 3: the stages add up to one matrix, and Step 1: its real form); with a
- * workspace (the *_ws calls below) AUTO takes the table-lookup decode below 11
- * tokens and the dequantized GEMM from 11 tokens.  The dequantized GEMM needs
+ * workspace (the *_ws calls below) AUTO takes the table-lookup decode below 12
+ * tokens and the dequantized GEMM from 12 tokens.  The dequantized GEMM needs
  * m a multiple of 8 (x is read by TMA in two halves, Re x and Im x), so other
  * layout-3 layers return UNSUPPORTED here and go through the *_ws calls.
  * Precision: the summed matrix is formed in fp32 and carried as two bfloat16
@@ -224,8 +224,8 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
  * work in the stream (it may start while that work finishes and waits for it
  * before reading activations or writing anything); the summing kernel is an
  * ordinary launch after it.
- * Tokens go in launches of up to 4 (T <= 2), 2 (T = 3) or 1 (T = 4); each
- * launch streams the codes once.  Precision: each table entry is the fp32 sum
+ * Tokens go in launches of 2 (T <= 2; the first of 3 when M is odd and at
+ * least 3), 2 (T = 3) or 1 (T = 4); each launch streams the codes once.  Precision: each table entry is the fp32 sum
  * of 8 scaled activations rounded once to fp16 (relative error <= 2^-11 per
  * entry), accumulated in fp32; outputs agree with the exact sum to about
  * 3e-4 relative (L2) for Gaussian activations.  A token with a non-finite

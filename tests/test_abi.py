@@ -202,8 +202,9 @@ def test_layout3_workspace_bytes(lib):
     L3 = f2i.LAYOUT_LUT
     q = _desc(n=2048, m=2048, T=2, version=L3)
     assert ws([q], 1) == 64 * 8 * 32 * 8
-    assert ws([q], 4) == 64 * 8 * 4 * 32 * 8
-    assert ws([q], 9) == ws([q], 4)  # launches of at most 4 tokens at T = 2 share it
+    # at T = 2, launches of 2 tokens (the first of 3 when M is odd) share it
+    assert ws([q], 2) == ws([q], 4) == ws([q], 10) == 64 * 8 * 2 * 32 * 8
+    assert ws([q], 3) == ws([q], 9) == 64 * 8 * 3 * 32 * 8
     assert ws([_desc(n=2048, m=2048, T=3, version=L3)], 9) == 64 * 8 * 2 * 32 * 8
     assert ws([_desc(n=100, m=256, T=2, version=L3)], 1) == 0  # one window: written directly
     assert ws([_desc(n=2048, m=2048, T=2)], 1) == 0  # layout 2

@@ -325,7 +325,7 @@ def test_full_size_projection_layout3_sampled(name, out_f, in_f, T):
     assert rel_l2(got, want) <= REL_L2
 
 
-@pytest.mark.parametrize("M", [1, 4, 10])  # 10: three launches (4 + 4 + 2), AUTO's last table-lookup count
+@pytest.mark.parametrize("M", [1, 4, 11])  # 11: five launches (3 + 2 + 2 + 2 + 2), AUTO's last table-lookup count
 def test_full_size_block_group_layout3_sampled(M):
     """The seven projections of a block in one grouped table-lookup launch (the
     benchmark's launch), against the oracle on sampled rows."""
@@ -383,14 +383,14 @@ def test_dq_parity_stages(T, M):
 
 def test_dq_plain_entry_and_auto():
     """Layout 3 through the plain entry points (no workspace) takes the dequantized
-    GEMM at any token count; with a workspace AUTO switches to it from 11 tokens."""
+    GEMM at any token count; with a workspace AUTO switches to it from 12 tokens."""
     import ctypes
     n, m = 100, 600
     R = _R(n, m, 5)
     q = _gpu_layer(R, 2)
     qU, qW = _oracle_layer(R, 2)
     lib = f2i.load_library()
-    for M in (1, 10, 11):
+    for M in (1, 11, 12):
         x = _x(M, m, 30 + M)
         xd = x.cuda()
         y = torch.empty((M, 2 * n), device="cuda")
@@ -455,7 +455,7 @@ def test_dq_full_size_block_prefill_sampled():
 @pytest.mark.parametrize("M", [16, 64, 256])  # value tables up to 64 tokens, the per-plane decode above
 def test_dq_full_size_block_batched_sampled(M):
     """The seven LLaMA-2-7B projections at batched-decode token counts (the sweep's launch:
-    one grouped call, AUTO on layout 3 takes the dequantized GEMM from 11 tokens), against
+    one grouped call, AUTO on layout 3 takes the dequantized GEMM from 12 tokens), against
     the oracle on sampled rows and tokens."""
     qs, xs, samples = [], [], []
     for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
