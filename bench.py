@@ -353,12 +353,14 @@ def build_stack(f2i, blocks: int, dev, T: int = T_STAGES, layout: int = 2):
 
 def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
     """Prefill: the 7 projections of one block at M tokens (1 % outliers x10),
-    one grouped launch per step, two kernels: the ternary tcgen05 GEMM over
-    layout 2 (16 n m T flops per token) and the dense GEMM of the dequantized
-    matrix over layout 3 (16 n m flops per token, hi + lo bfloat16 terms).
+    one grouped call per step, three kernels: the ternary tcgen05 GEMM over
+    layout 2 (16 n m T flops per token), and the dense GEMM of the dequantized
+    matrix over layout 3 in its two forms: hi + lo bfloat16 terms (16 n m flops
+    per token) and one fp16 term against an fp16 copy of x (8 n m flops per
+    token; the copy is made by a conversion launch inside the timed call).
     Executed and dense-equivalent TFLOP/s for each; the faster leads."""
     qs2, qs3, xs, ys = [], [], [], []
-    flops_tern = flops_dq = flops_dense = 0
+    flops_tern = flops_dq = flops_dense = 0  # the fp16 form executes flops_dense
     for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
         R = inputs.weight_R(4, pi, out_f, in_f, device=dev)
         U, W = f2i.convert(R)
@@ -388,10 +390,14 @@ def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
         return start.elapsed_time(stop) / steps
 
     legs = {}
+    nt = 2 if M > 256 else 1
     for key, qs, algo, kernel, fl in (("ternary", qs2, "tcgen05", "linear_tcgen05_kernel<8>", flops_tern),
-                                      ("dequantized", qs3, "tcgen05_dq", f"linear_dq_kernel<{T_STAGES},{2 if M > 256 else 1}>", flops_dq)):
+                                      ("dequantized", qs3, "tcgen05_dq", f"linear_dq_kernel<{T_STAGES},{nt},0,0>", flops_dq),
+                                      ("dequantized_f16", qs3, "tcgen05_dq16",
+                                       f"dq_x16_kernel + linear_dq_kernel<{T_STAGES},{nt},0,1>", flops_dense)):
         ms = timed(qs, algo)
         tf = fl / (ms * 1e-3) / 1e12
+        # the fp16 form runs on the same tensor-core rate as bfloat16 (kind::f16)
         legs[key] = {"algo": algo, "kernel": kernel, "layout": 2 if key == "ternary" else 3, "ms_per_block": ms,
                      "executed_flops_per_block": fl, "tflops_executed": tf,
                      "tflops_dense_equivalent": flops_dense / (ms * 1e-3) / 1e12,
@@ -408,18 +414,18 @@ def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
             "by_kernel": legs}
 
 
-SWEEP_ALGOS = ("lut", "tcgen05_dq", "auto_layout3", "mma", "tcgen05", "auto", "tcgen05_sp")
+SWEEP_ALGOS = ("lut", "tcgen05_dq", "tcgen05_dq16", "auto_layout3", "mma", "tcgen05", "auto", "tcgen05_sp")
 
 
 def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int = 4, algos=SWEEP_ALGOS):
     """Batched decode sweep: per token count M and per algorithm, the 7 projections of
     `blocks` distinct blocks (205 MB at 4 blocks, above L2), one grouped call per block;
     time per block, weight GB/s and tokens/s-equivalent (eager calls; for AUTO on layout 3 also
-    the same calls replayed as a CUDA graph).  "lut", "tcgen05_dq" and
+    the same calls replayed as a CUDA graph).  "lut", "tcgen05_dq", "tcgen05_dq16" and
     "auto_layout3" read the same weights in layout 3 (the table lookup: one decode launch
     per 2 tokens at T = 2 (the first of 3 for odd M), each with its window-combining launch;
-    the dequantized GEMM: one
-    launch with N = M rounded up to 16)."""
+    the dequantized GEMM: one launch with N = M rounded up to 16, in the fp16 form after a
+    conversion launch of the activations)."""
     stack, stack3, xs_full = [], [], []
     for b in range(blocks):
         qs, qs3, xb = [], [], []
@@ -441,7 +447,7 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
         ys = [[torch.empty((M, 2 * q.n), dtype=torch.float32, device=dev) for q in qs] for qs in stack]
         row = {"M": M}
         for key in [a for a in algos if a != "tcgen05_sp" or M <= 8]:
-            st = stack3 if key in ("lut", "tcgen05_dq", "auto_layout3") else stack
+            st = stack3 if key in ("lut", "tcgen05_dq", "tcgen05_dq16", "auto_layout3") else stack
             algo = "auto" if key == "auto_layout3" else key
 
             def step():

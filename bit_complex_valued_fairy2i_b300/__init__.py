@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(_HERE, "libfairy2i.so")
 OK = 0
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "SHAPE", 3: "NONFINITE", 4: "UNSUPPORTED", 5: "CUDA",
                 6: "TIMEOUT"}
-ALGO = {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4, "lut": 5, "tcgen05_dq": 6}
+ALGO = {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4, "lut": 5, "tcgen05_dq": 6, "tcgen05_dq16": 7}
 LAYOUT_VERSION = 2
 LAYOUT_LUT = 3
 

@@ -325,12 +325,12 @@ fairy2i_status make_x_map(CUtensorMap* map, const void* x, int64_t M, int64_t m)
   return FAIRY2I_OK;
 }
 
-// One half of x [M][2m] bfloat16 (half 0: Re x, columns 0..m-1; half 1: Im x)
-// as a [M][m] tensor with row pitch 2m: tiles of N tokens x 64 columns,
-// 128-byte swizzle, zero fill past m columns and M tokens (the dequantized
-// GEMM's B operand).  The Im half starts 2m bytes in: 16-byte aligned for m a
-// multiple of 8.
-fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64_t m, int half, int N) {
+// One half of x [M][2m] bfloat16, or of its fp16 copy (half 0: Re x, columns
+// 0..m-1; half 1: Im x) as a [M][m] tensor with row pitch 2m: tiles of N
+// tokens x 64 columns, 128-byte swizzle, zero fill past m columns and M tokens
+// (the dequantized GEMM's B operand).  The Im half starts 2m bytes in:
+// 16-byte aligned for m a multiple of 8.
+fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64_t m, int half, int N, bool f16) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   fairy2i_status st = tensor_map_encoder(enc);
   if (st != FAIRY2I_OK) return st;
@@ -339,17 +339,18 @@ fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64
   const cuuint32_t box[2] = {(cuuint32_t)f2i::kDqBK, (cuuint32_t)N};
   const cuuint32_t estr[2] = {1, 1};
   void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(x) + (half ? 2 * m : 0));
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+  const CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                         strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FAIRY2I_ERR_CUDA, "cuTensorMapEncodeTiled (x half %d) failed (%d)", half, (int)r);
   return FAIRY2I_OK;
 }
 
-template <int T, int NT, bool SMALL = false>
+template <int T, int NT, bool SMALL, bool F16>
 fairy2i_status launch_dq_t(const f2i::DqParams& P, int grid, cudaStream_t s) {
-  auto k = f2i::linear_dq_kernel<T, NT, SMALL>;
-  const size_t smem = f2i::dq_smem_bytes<NT, T, SMALL>();
+  auto k = f2i::linear_dq_kernel<T, NT, SMALL, F16>;
+  const size_t smem = f2i::dq_smem_bytes<NT, T, SMALL, F16>();
   fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(k), smem, "dequantized prefill");
   if (st != FAIRY2I_OK) return st;
   k<<<(unsigned)grid, f2i::kDqThreads, smem, s>>>(P);
@@ -393,13 +394,66 @@ void dq_schedule(f2i::DqParams& P, int grid, int nt) {
   P.sched_n = k;
 }
 
+constexpr size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Workspace of the fp16 form for one launch's layers: per layer the fp16 copy
+// of x (M x 2m values) and the per-token factors (M floats), each 256-byte
+// aligned; launches run in stream order and reuse it.
+size_t dq16_launch_workspace(const fairy2i_packed* qs, int cnt, int64_t M) {
+  size_t need = 0;
+  for (int i = 0; i < cnt; ++i) need += round256((size_t)M * 4 * (size_t)qs[i].m) + round256((size_t)M * 4);
+  return need;
+}
+size_t dq16_workspace(const fairy2i_packed* qs, int count, int64_t M) {
+  size_t need = 0;
+  for (int p0 = 0; p0 < count; p0 += f2i::kDqMaxGroup)
+    need = std::max(need, dq16_launch_workspace(qs + p0, std::min(f2i::kDqMaxGroup, count - p0), M));
+  return need;
+}
+
+template <int T, int NT, bool SMALL>
+fairy2i_status launch_dq_form(const f2i::DqParams& P, int grid, bool f16, cudaStream_t s) {
+  return f16 ? launch_dq_t<T, NT, SMALL, true>(P, grid, s) : launch_dq_t<T, NT, SMALL, false>(P, grid, s);
+}
+
 // The dense GEMM of the dequantized real matrix (layout 3, m a multiple of 8,
 // T <= 4): one launch per kDqMaxGroup layers, tiles of 64 outputs x NT N tokens
 // (N = min(256, M rounded up to 16); NT = 2 above 256 tokens for T <= 2).
+// f16: the fp16 form, each launch preceded by the activations' conversion
+// into the workspace (dq16_workspace bytes, 256-byte aligned; checked here).
 fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count, int64_t M, int T,
-                      cudaStream_t s) {
+                      cudaStream_t s, bool f16 = false, void* ws = nullptr, size_t ws_bytes = 0) {
+  if (f16) {
+    const size_t need = dq16_workspace(qs, count, M);
+    if (!ws) return fail(FAIRY2I_ERR_INVALID_ARG, "the fp16 dequantized GEMM needs a workspace of %zu bytes", need);
+    if (ws_bytes < need)
+      return fail(FAIRY2I_ERR_INVALID_ARG, "workspace of %zu bytes, the fp16 dequantized GEMM needs %zu", ws_bytes, need);
+    if (!aligned(ws, 256)) return fail(FAIRY2I_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  }
   for (int p0 = 0; p0 < count; p0 += f2i::kDqMaxGroup) {
     const int cnt = std::min(f2i::kDqMaxGroup, count - p0);
+    const void* xb[f2i::kDqMaxGroup];  // the B operand of each layer: x or its fp16 copy
+    const float* xf[f2i::kDqMaxGroup] = {};
+    for (int i = 0; i < cnt; ++i) xb[i] = xs[p0 + i];
+    if (f16) {
+      f2i::DqXParams XP;
+      memset(&XP, 0, sizeof(XP));
+      XP.count = cnt;
+      uint8_t* w = static_cast<uint8_t*>(ws);
+      for (int i = 0; i < cnt; ++i) {
+        XP.x[i] = static_cast<const uint16_t*>(xs[p0 + i]);
+        XP.xh[i] = reinterpret_cast<uint16_t*>(w);
+        w += round256((size_t)M * 4 * (size_t)qs[p0 + i].m);
+        XP.xfac[i] = reinterpret_cast<float*>(w);
+        w += round256((size_t)M * 4);
+        XP.m[i] = (int32_t)qs[p0 + i].m;
+        xb[i] = XP.xh[i];
+        xf[i] = XP.xfac[i];
+      }
+      f2i::dq_x16_kernel<<<dim3((unsigned)M, (unsigned)cnt), f2i::kDqXThreads, 0, s>>>(XP);
+      fairy2i_status st = check_launch("activation conversion launch");
+      if (st != FAIRY2I_OK) return st;
+    }
     f2i::DqParams P;
     memset(&P, 0, sizeof(P));
     P.count = cnt;
@@ -413,13 +467,14 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
     for (int i = 0; i < cnt; ++i) {
       const fairy2i_packed& q = qs[p0 + i];
       for (int half = 0; half < 2; ++half) {
-        fairy2i_status st = make_x_map_half(&P.tmap[2 * i + half], xs[p0 + i], M, q.m, half, P.N);
+        fairy2i_status st = make_x_map_half(&P.tmap[2 * i + half], xb[i], M, q.m, half, P.N, f16);
         if (st != FAIRY2I_OK) return st;
       }
       f2i::DqProblem& pr = P.p[i];
       pr.codes = static_cast<const uint8_t*>(q.codes);
       pr.scales = q.scales;
       pr.y = ys[p0 + i];
+      pr.xfac = xf[i];
       pr.n = (int32_t)q.n;
       pr.m = (int32_t)q.m;
       pr.row_tiles = (int32_t)((q.n + 63) / 64);
@@ -434,12 +489,12 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
     const bool small = nt == 1 && P.N <= 64;  // value tables in 8 KB-B-stage room
     fairy2i_status st;
     switch (T * 2 + nt - 1) {
-      case 2: st = small ? launch_dq_t<1, 1, true>(P, grid, s) : launch_dq_t<1, 1>(P, grid, s); break;
-      case 3: st = launch_dq_t<1, 2>(P, grid, s); break;
-      case 4: st = small ? launch_dq_t<2, 1, true>(P, grid, s) : launch_dq_t<2, 1>(P, grid, s); break;
-      case 5: st = launch_dq_t<2, 2>(P, grid, s); break;
-      case 6: st = small ? launch_dq_t<3, 1, true>(P, grid, s) : launch_dq_t<3, 1>(P, grid, s); break;
-      case 8: st = small ? launch_dq_t<4, 1, true>(P, grid, s) : launch_dq_t<4, 1>(P, grid, s); break;
+      case 2: st = small ? launch_dq_form<1, 1, true>(P, grid, f16, s) : launch_dq_form<1, 1, false>(P, grid, f16, s); break;
+      case 3: st = launch_dq_form<1, 2, false>(P, grid, f16, s); break;
+      case 4: st = small ? launch_dq_form<2, 1, true>(P, grid, f16, s) : launch_dq_form<2, 1, false>(P, grid, f16, s); break;
+      case 5: st = launch_dq_form<2, 2, false>(P, grid, f16, s); break;
+      case 6: st = small ? launch_dq_form<3, 1, true>(P, grid, f16, s) : launch_dq_form<3, 1, false>(P, grid, f16, s); break;
+      case 8: st = small ? launch_dq_form<4, 1, true>(P, grid, f16, s) : launch_dq_form<4, 1, false>(P, grid, f16, s); break;
       default: return fail(FAIRY2I_ERR_UNSUPPORTED, "dequantized prefill supports T <= 4");
     }
     if (st != FAIRY2I_OK) return st;
@@ -632,14 +687,13 @@ constexpr int64_t kTcDecodeMaxTokens = 8;
 
 // Token count from which FAIRY2I_ALGO_AUTO takes the tcgen05 prefill path.
 constexpr int64_t kPrefillMinTokens = 16;
-// Token count from which AUTO takes the dequantized GEMM over the table-lookup
-// decode on layout 3.
-// Layout 3: AUTO's switch from the table lookup (launches of 2 or 3 tokens at
-// T <= 2, 27 and 41 us each on a LLaMA-2-7B block) to the dequantized GEMM
-// (~155 us at any count up to 64): measured per block at 10 / 11 / 12 / 13
-// tokens, 141.5 / 154.6 / 169.0 / 182.6 us against 155.3 / 155.1 / 155.4 /
-// 155.4 us.
-constexpr int64_t kDqMinTokens = 12;
+// Token count from which AUTO, given a workspace, takes the fp16 dequantized
+// GEMM over the table-lookup decode on layout 3.  The table lookup runs in
+// launches of 2 or 3 tokens at T <= 2 (27 and 41 us each on a LLaMA-2-7B
+// block), the fp16 GEMM takes ~141 us at any count up to 64: measured per
+// block (eager / CUDA graph) at 10 tokens 139.6 / 128.5 us against 140.6 /
+// 136, at 11 tokens 154.6 us against 140.5.
+constexpr int64_t kDqMinTokens = 11;
 
 // The quantizer over U, W (FUSED = false) or straight from R (true); the
 // caller has checked the arguments.  Codes are zeroed first: each row ORs its
@@ -888,7 +942,7 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
   if (count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "count=%d outside [1, 256]", count);
   if (!qs || !xs || !ys) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL array argument");
   if (M < 0) return fail(FAIRY2I_ERR_SHAPE, "M=%lld is negative", (long long)M);
-  if ((int)algo < 0 || (int)algo > 6) return fail(FAIRY2I_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
+  if ((int)algo < 0 || (int)algo > 7) return fail(FAIRY2I_ERR_INVALID_ARG, "unknown algo %d", (int)algo);
   if (!qs) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL descriptor array");
   const int T = qs[0].T;
   for (int i = 0; i < count; ++i) {
@@ -898,20 +952,23 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
     if (qs[i].version != qs[0].version) return fail(FAIRY2I_ERR_SHAPE, "all layers of a group need the same layout");
   }
   if (qs[0].version == FAIRY2I_LAYOUT_LUT) {
-    if (algo != FAIRY2I_ALGO_AUTO && algo != FAIRY2I_ALGO_LUT && algo != FAIRY2I_ALGO_TCGEN05_DQ)
+    if (algo != FAIRY2I_ALGO_AUTO && algo != FAIRY2I_ALGO_LUT && algo != FAIRY2I_ALGO_TCGEN05_DQ &&
+        algo != FAIRY2I_ALGO_TCGEN05_DQ16)
       return fail(FAIRY2I_ERR_UNSUPPORTED, "layout 3 is read by the table-lookup decode and the dequantized GEMM only");
     if (T > 4) return fail(FAIRY2I_ERR_UNSUPPORTED, "layout 3 kernels support T <= 4");
     bool m_mult8_3 = true;
     for (int i = 0; i < count; ++i) m_mult8_3 = m_mult8_3 && (qs[i].m % 8) == 0;
-    // AUTO: the table lookup below kDqMinTokens tokens when a workspace came with the call,
-    // otherwise (and from kDqMinTokens) the dequantized GEMM, which needs none
+    // AUTO: with a workspace, the table lookup below kDqMinTokens tokens and the
+    // fp16 dequantized GEMM from there; without one, the bfloat16 dequantized GEMM
     fairy2i_algo a3 = algo;
-    if (a3 == FAIRY2I_ALGO_AUTO)
-      a3 = (!m_mult8_3 || (with_ws && M < kDqMinTokens)) ? FAIRY2I_ALGO_LUT : FAIRY2I_ALGO_TCGEN05_DQ;
-    if (a3 == FAIRY2I_ALGO_LUT && !with_ws)
-      return fail(FAIRY2I_ERR_UNSUPPORTED,
-                  "the table-lookup decode needs a workspace: call fairy2i_linear_ws / fairy2i_linear_group_ws");
-    if (a3 == FAIRY2I_ALGO_TCGEN05_DQ && !m_mult8_3)
+    if (a3 == FAIRY2I_ALGO_AUTO) {
+      if (!m_mult8_3 || (with_ws && M < kDqMinTokens)) a3 = FAIRY2I_ALGO_LUT;
+      else a3 = with_ws ? FAIRY2I_ALGO_TCGEN05_DQ16 : FAIRY2I_ALGO_TCGEN05_DQ;
+    }
+    if ((a3 == FAIRY2I_ALGO_LUT || a3 == FAIRY2I_ALGO_TCGEN05_DQ16) && !with_ws)
+      return fail(FAIRY2I_ERR_UNSUPPORTED, "the table-lookup decode and the fp16 dequantized GEMM need a workspace: "
+                                           "call fairy2i_linear_ws / fairy2i_linear_group_ws");
+    if ((a3 == FAIRY2I_ALGO_TCGEN05_DQ || a3 == FAIRY2I_ALGO_TCGEN05_DQ16) && !m_mult8_3)
       return fail(FAIRY2I_ERR_UNSUPPORTED, "the dequantized GEMM needs m to be a multiple of 8");
     if (M == 0) return ok();
     for (int i = 0; i < count; ++i) {
@@ -921,9 +978,10 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
     }
     if (M > (int64_t)1 << 30) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
     if (a3 == FAIRY2I_ALGO_TCGEN05_DQ) return run_dq(qs, xs, ys, count, M, T, s);
+    if (a3 == FAIRY2I_ALGO_TCGEN05_DQ16) return run_dq(qs, xs, ys, count, M, T, s, true, ws, ws_bytes);
     return run_lut(qs, xs, ys, count, M, T, ws, ws_bytes, s);
   }
-  if (algo == FAIRY2I_ALGO_LUT || algo == FAIRY2I_ALGO_TCGEN05_DQ)
+  if (algo == FAIRY2I_ALGO_LUT || algo == FAIRY2I_ALGO_TCGEN05_DQ || algo == FAIRY2I_ALGO_TCGEN05_DQ16)
     return fail(FAIRY2I_ERR_UNSUPPORTED, "the table-lookup decode and the dequantized GEMM read layout 3 only");
   (void)ws;
   (void)ws_bytes;
@@ -1130,13 +1188,22 @@ fairy2i_status fairy2i_linear_ex(const fairy2i_packed* q, const void* x, int64_t
   return linear_group_impl(q, xs, ys, 1, M, algo, false, nullptr, 0, static_cast<cudaStream_t>(stream));
 }
 
-size_t fairy2i_linear_workspace_bytes(const fairy2i_packed* qs, int32_t count, int64_t M) {
-  if (!qs || count < 1 || count > 256 || M < 1) return 0;
+// Layout-3 descriptors the workspace kernels accept (same T <= 4, n, m >= 1).
+bool ws_layers_ok(const fairy2i_packed* qs, int32_t count, int64_t M) {
+  if (!qs || count < 1 || count > 256 || M < 1) return false;
   for (int i = 0; i < count; ++i)
     if (qs[i].version != FAIRY2I_LAYOUT_LUT || qs[i].T < 1 || qs[i].T > 4 || qs[i].T != qs[0].T || qs[i].n < 1 ||
         qs[i].m < 1)
-      return 0;
-  return lut_workspace(qs, count, M, qs[0].T);
+      return false;
+  return true;
+}
+
+size_t fairy2i_linear_workspace_bytes(const fairy2i_packed* qs, int32_t count, int64_t M) {
+  if (!ws_layers_ok(qs, count, M)) return 0;
+  bool m_mult8 = true;
+  for (int i = 0; i < count; ++i) m_mult8 = m_mult8 && (qs[i].m % 8) == 0;
+  const size_t lut = lut_workspace(qs, count, M, qs[0].T);
+  return m_mult8 ? std::max(lut, dq16_workspace(qs, count, M)) : lut;
 }
 
 fairy2i_status fairy2i_linear_ws(const fairy2i_packed* q, const void* x, int64_t M, float* y, fairy2i_algo algo,
@@ -1164,7 +1231,7 @@ fairy2i_status fairy2i_linear_group_static(const fairy2i_packed* qs, const void*
     if (qs[i].version != FAIRY2I_LAYOUT_LUT)
       return fail(FAIRY2I_ERR_UNSUPPORTED, "the static-scratch decode reads layout %d (layer %d is %d)",
                   FAIRY2I_LAYOUT_LUT, i, qs[i].version);
-  const size_t need = fairy2i_linear_workspace_bytes(qs, count, M);
+  const size_t need = ws_layers_ok(qs, count, M) ? lut_workspace(qs, count, M, qs[0].T) : 0;
   if (need > kStaticScratchBytes)
     return fail(FAIRY2I_ERR_UNSUPPORTED,
                 "these layers need %zu bytes of scratch, more than the %zu bytes this entry point holds; "

@@ -9,11 +9,18 @@
 //   R^11 = Re U^ + Re W^   R^12 = Im W^ - Im U^
 //   R^21 = Im U^ + Im W^   R^22 = Re U^ - Re W^
 // Every token is then one row of a dense real GEMM, y~ = R^ x~, which the
-// 5th-generation tensor cores run with bfloat16 operands: R^ = hi + lo, hi the
-// bfloat16 rounding of R^ (formed in fp32) and lo the bfloat16 rounding of the
-// remainder, so R^ is carried to ~2^-18 relative and every product is exact
-// in the fp32 accumulators.  Executed flops: 2 terms x 2 (2n)(2m) per token =
-// 16 n m, against 16 n m T for the ternary form of linear_prefill.cuh.
+// 5th-generation tensor cores run in one of two forms:
+//   bfloat16 (F16 = false): R^ = hi + lo, hi the bfloat16 rounding of R^
+//     (formed in fp32) and lo the bfloat16 rounding of the remainder, so R^ is
+//     carried to ~2^-18 relative; x as given.  Executed flops: 2 terms x
+//     2 (2n)(2m) per token = 16 n m, against 16 n m T for the ternary form of
+//     linear_prefill.cuh;
+//   fp16 (F16 = true): one term, every row of R^ scaled by a power of two so
+//     that its largest possible entry is below 2^15 and rounded once to fp16
+//     (2^-11 relative); x scaled per token by a power of two into fp16 by
+//     dq_x16_kernel (exact: a bfloat16 value has 8 significant bits), both
+//     powers of two undone in the epilogue.  8 n m flops per token.
+// Every product is exact in the fp32 accumulators.
 //
 // GEMM shape per tile: D[128 rows][256 tokens] += A[128][K] * B[256][K]^T
 //   rows: 64 outputs j, row 2 jl = Re y_j, row 2 jl + 1 = Im y_j, so that one
@@ -21,7 +28,7 @@
 //         halves of x~;
 //   K:    blocks of 64 columns in pairs (block c of Re x, block c of Im x),
 //         the two stages of a pair filled by one decode;
-//   A:    hi and lo, 128-byte swizzled K-major, written by 16 producer warps
+//   A:    hi and lo (or the fp16 term), 128-byte swizzled K-major, written by 16 producer warps
 //         from the codes (in shared memory) and the scales: per stage plane and
 //         column a signed scale added on its axis, or, with at most 64 tokens,
 //         one load per column and matrix from the row's value tables (the 16
@@ -30,7 +37,7 @@
 //         the tile's two 32-row tiles (contiguous: 2 x 2T planes x the
 //         window's slots x 512 bytes), one bulk copy (cp.async.bulk, the TMA
 //         engine) into a ring of two stages, a window ahead of their decode;
-//   B:    x [M][2m] bfloat16 by TMA through two maps, one per half of x~
+//   B:    x [M][2m] bfloat16 (or its fp16 copy) by TMA through two maps, one per half of x~
 //         (128-byte swizzle, zero fill past m columns and M tokens), so that
 //         the columns of A past m (decoded from zero code bits) meet zeros;
 //   D:    fp32 in TMEM, two accumulators of 256 columns (double buffered).
@@ -40,6 +47,7 @@
 // mbarrier waits are bounded.
 #pragma once
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 #include "layout.cuh"
 #include "linear_prefill.cuh"
@@ -53,7 +61,6 @@ constexpr int kDqBM = 128;  // real rows per tile (64 outputs)
 constexpr int kDqBN = 256;  // tokens per MMA (at most; a launch takes N = M rounded up to 16 below 256)
 constexpr int kDqBK = 64;   // columns per k-block
 constexpr int kDqATerm = kDqBM * kDqBK * 2;   // 16 KB: one term of A
-constexpr int kDqAStage = 2 * kDqATerm;       // hi and lo
 constexpr int kDqBStage = kDqBN * kDqBK * 2;  // 32 KB: x for one MMA
 constexpr int kDqProducerWarps = 16;
 constexpr int kDqThreads = 32 * (7 + kDqProducerWarps);
@@ -70,8 +77,16 @@ __host__ __device__ constexpr uint32_t dq_c_stage(int T) { return 8192u * (uint3
 //   SMALL:           3 A and 3 B of 8 KB, value tables;
 //   NT = 1, T <= 2:  3 A and 3 B of 32 KB;
 //   otherwise:       2 A and 2 B of NT x 32 KB.
-template <int NT, int T, bool SMALL>
-__host__ __device__ constexpr int dq_a_stages() { return (NT == 1 && T <= 2) || SMALL ? 3 : 2; }
+// An A stage holds hi and lo (32 KB), or with F16 the one term (16 KB) and
+// then twice as many A stages.  (Value tables beyond SMALL, in the room the
+// F16 stages leave, measured slower: 175.8 against 161.0 us per LLaMA-2-7B
+// block at 256 tokens, 861 against 851 at 2048.)
+template <bool F16>
+__host__ __device__ constexpr uint32_t dq_a_stage_bytes() { return F16 ? kDqATerm : 2u * kDqATerm; }
+template <int NT, int T, bool SMALL, bool F16>
+__host__ __device__ constexpr int dq_a_stages() { return ((NT == 1 && T <= 2) || SMALL ? 3 : 2) * (F16 ? 2 : 1); }
+template <bool SMALL, bool F16>
+__host__ __device__ constexpr bool dq_tables() { return SMALL; }
 template <int NT, int T, bool SMALL>
 __host__ __device__ constexpr int dq_b_stages() { return (NT == 1 && T <= 2) || SMALL ? 3 : 2; }
 template <int NT, bool SMALL>
@@ -83,19 +98,20 @@ template <int T>
 __host__ __device__ constexpr int dq_pairs() { return (T + 1) / 2; }
 template <int T>
 __host__ __device__ constexpr uint32_t dq_table_row() { return 2u * dq_pairs<T>() * 16u * 8u + 16u; }
-template <int T, bool SMALL>
-__host__ __device__ constexpr uint32_t dq_table_bytes() { return SMALL ? 64u * dq_table_row<T>() : 0u; }
-template <int NT, int T, bool SMALL>
+template <int T, bool TAB>
+__host__ __device__ constexpr uint32_t dq_table_bytes() { return TAB ? 64u * dq_table_row<T>() : 0u; }
+template <int NT, int T, bool SMALL, bool F16>
 __host__ __device__ constexpr size_t dq_smem_bytes() {
-  return 1024 + (size_t)dq_a_stages<NT, T, SMALL>() * kDqAStage +
+  return 1024 + (size_t)dq_a_stages<NT, T, SMALL, F16>() * dq_a_stage_bytes<F16>() +
          (size_t)dq_b_stages<NT, T, SMALL>() * dq_b_stage_bytes<NT, SMALL>() + (size_t)kDqCStages * dq_c_stage(T) +
-         dq_table_bytes<T, SMALL>() + 512;
+         dq_table_bytes<T, dq_tables<SMALL, F16>()>() + 512;
 }
 
 struct DqProblem {
   const uint8_t* codes;  // layout 3
   const float* scales;
   float* y;
+  const float* xfac;  // F16: per token, 2^-f of its fp16 copy (x scaled by 2^f)
   int32_t n, m;
   int64_t tile_begin;
   int32_t row_tiles;  // tiles of 64 outputs
@@ -153,6 +169,22 @@ __device__ __forceinline__ void dq_split2(float a, float b, uint32_t& hi, uint32
   hi = h;
   lo = l;
 }
+
+// fp16 pair of (a, b) rounded to nearest even, a in the low half.
+__device__ __forceinline__ uint32_t dq_f16x2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// F16 form: the power of two e by which a row of R^ is scaled, from the bits
+// of the row's 4T scales (non-negative): the largest scale times 2^e lies in
+// [2^11, 2^12), so every entry of the scaled row (a signed sum of at most 2T
+// <= 8 scales) is below 2^15 and stays in the fp16 range.  e is clamped to
+// [-64, 64] (a row of zero scales gets 64), so 2^e and 2^-e are normal floats.
+__device__ __forceinline__ int dq_row_exp(uint32_t max_bits) {
+  return min(64, max(-64, 138 - (int)((max_bits >> 23) & 0xFFu)));
+}
+__device__ __forceinline__ float dq_pow2(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
 // One code of one stage added to (re, im): bit E of the sign word s and of
 // the imaginary-axis flag word f (a group's column, in the byte of its plane);
@@ -217,29 +249,31 @@ __device__ __forceinline__ void dq_plane(float (&re)[8], float (&im)[8], uint32_
   dq_code<B + 7>(re[7], im[7], s, f, sre, sim);
 }
 
-template <int T, int NT, bool SMALL>
+template <int T, int NT, bool SMALL, bool F16>
 __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_constant__ DqParams P) {
   extern __shared__ uint8_t dq_smem_raw[];
   constexpr int NP = 2 * T;
   constexpr int NW = (NP + 3) / 4;  // words holding one byte per plane
   static_assert(NT == 1 || T <= 2, "two token tiles per decode only for T <= 2 (shared memory)");
   static_assert(!SMALL || NT == 1, "small token tiles come one per decode");
-  static_assert(dq_smem_bytes<NT, T, SMALL>() <= 232448, "shared memory per CTA");
-  constexpr int AS = dq_a_stages<NT, T, SMALL>();
+  static_assert(dq_smem_bytes<NT, T, SMALL, F16>() <= 232448, "shared memory per CTA");
+  constexpr int AS = dq_a_stages<NT, T, SMALL, F16>();
+  constexpr uint32_t kAStage = dq_a_stage_bytes<F16>();
   constexpr int BS = dq_b_stages<NT, T, SMALL>();
   constexpr int CS = kDqCStages;
   constexpr uint32_t kBStage = dq_b_stage_bytes<NT, SMALL>();
+  constexpr bool TAB = dq_tables<SMALL, F16>();
   constexpr uint32_t kCStage = dq_c_stage(T);
 
   const uint32_t raw = smem_u32(dq_smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = dq_smem_raw + (base - raw);
   const uint32_t sA = base;
-  const uint32_t sB = base + AS * kDqAStage;
+  const uint32_t sB = base + AS * kAStage;
   const uint32_t sC = sB + BS * kBStage;
-  const uint32_t sTab = sC + CS * kCStage;  // value tables (SMALL)
+  const uint32_t sTab = sC + CS * kCStage;  // value tables (TAB)
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(gbase + AS * kDqAStage + BS * kBStage + CS * kCStage + dq_table_bytes<T, SMALL>());
+      reinterpret_cast<uint64_t*>(gbase + AS * kAStage + BS * kBStage + CS * kCStage + dq_table_bytes<T, TAB>());
   const uint32_t bar0 = smem_u32(bars);
   auto fullA = [&](int s) { return bar0 + 8u * (uint32_t)s; };
   auto emptyA = [&](int s) { return bar0 + 8u * (uint32_t)(AS + s); };
@@ -320,9 +354,9 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         if (!mbar_wait(fullB((int)(k % BS)), (k / BS) & 1u, abort_flag)) break;
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: hi and lo into one accumulator per token tile ----------------
+    // ---------------- MMA issuer: hi and lo (or the fp16 term) into one accumulator per token tile ----------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kDqBM, P.N);
+      const uint32_t idesc = F16 ? idesc_f16(kDqBM, P.N) : idesc_bf16(kDqBM, P.N);
       uint32_t it = 0, lt = 0;
       bool ok = true;
       for (int64_t i = 0; ok; ++i, ++lt) {
@@ -342,7 +376,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = sA + (uint32_t)sa * kDqAStage;
+          const uint32_t a0 = sA + (uint32_t)sa * kAStage;
 #pragma unroll
           for (int sub = 0; sub < NT; ++sub) {
             const uint32_t d_tmem = tmem_base + (uint32_t)acc_buf(lt, sub) * kDqBN;
@@ -351,7 +385,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
             for (int kk = 0; kk < kDqBK / 16; ++kk) {
               tc_mma_bf16(d_tmem, sw128_desc(a0 + 32u * kk), sw128_desc(b0 + 32u * kk), idesc,
                           (kb > 0 || kk > 0) ? 1u : 0u);
-              tc_mma_bf16(d_tmem, sw128_desc(a0 + kDqATerm + 32u * kk), sw128_desc(b0 + 32u * kk), idesc, 1u);
+              if constexpr (!F16)
+                tc_mma_bf16(d_tmem, sw128_desc(a0 + kDqATerm + 32u * kk), sw128_desc(b0 + 32u * kk), idesc, 1u);
             }
           }
           tc_commit(emptyA(sa));
@@ -385,7 +420,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
     const uint32_t cbyte = (uint32_t)(cr * 16 + l3_byte_of(gq, cr));
     uint32_t it = 0, itc = 0;  // itc: windows of codes consumed
     bool ok = true;
-    // SMALL: row jl's value tables
+    // TAB: row jl's value tables
     constexpr int PAIRS = dq_pairs<T>();
     const uint32_t trow = sTab + (uint32_t)jl * dq_table_row<T>();
     uint32_t pbu = 0;  // uses of the producers' barrier
@@ -411,7 +446,18 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         sre[p] = live ? __float_as_uint(__ldg(pr.scales + (int64_t)(2 * p) * n + j)) : 0u;
         sim[p] = live ? __float_as_uint(__ldg(pr.scales + (int64_t)(2 * p + 1) * n + j)) : 0u;
       }
-      if constexpr (SMALL) {
+      if constexpr (F16) {  // the row's scales times 2^e (exact), so R^ is formed scaled
+        uint32_t mb = 0;
+#pragma unroll
+        for (int p = 0; p < NP; ++p) mb = max(mb, max(sre[p], sim[p]));
+        const float f = dq_pow2(dq_row_exp(mb));
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          sre[p] = __float_as_uint(__uint_as_float(sre[p]) * f);
+          sim[p] = __float_as_uint(__uint_as_float(sim[p]) * f);
+        }
+      }
+      if constexpr (TAB) {
         // the tables of row jl: for matrix X and stage pair k, entry idx (bits as
         // dq_index) holds the pair's (Re, Im) sum, accumulated like dq_code (from
         // 0, stage 2k first); thread gq writes entries gq and gq + 8 of each.
@@ -488,7 +534,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
         // (Re, Im) of U^ [0] and W^ [1] for the group's 8 columns, in fp32 (zero
         // scales past n); columns past m decode from zero bits and meet zero-filled x
         float re[2][8], im[2][8];
-        if constexpr (SMALL) {
+        if constexpr (TAB) {
           // per matrix and stage pair: the word of bytes (sign, flag of stage 2k;
           // sign, flag of stage 2k + 1), then one table load per column
 #pragma unroll
@@ -549,30 +595,51 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
           // row 2 jl: Re y, row 2 jl + 1: Im y
           //   Re x block: R^11 = ReU + ReW, R^21 = ImU + ImW
           //   Im x block: R^12 = ImW - ImU, R^22 = ReU - ReW
-          uint32_t h0[4], l0[4], h1[4], l1[4];
+          if constexpr (F16) {
+            uint32_t a0[4], a1[4];
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            if (h == 0) {
-              dq_split2(re[0][e] + re[1][e], re[0][e + 1] + re[1][e + 1], h0[e >> 1], l0[e >> 1]);
-              dq_split2(im[0][e] + im[1][e], im[0][e + 1] + im[1][e + 1], h1[e >> 1], l1[e >> 1]);
-            } else {
-              dq_split2(im[1][e] - im[0][e], im[1][e + 1] - im[0][e + 1], h0[e >> 1], l0[e >> 1]);
-              dq_split2(re[0][e] - re[1][e], re[0][e + 1] - re[1][e + 1], h1[e >> 1], l1[e >> 1]);
+            for (int e = 0; e < 8; e += 2) {
+              if (h == 0) {
+                a0[e >> 1] = dq_f16x2(re[0][e] + re[1][e], re[0][e + 1] + re[1][e + 1]);
+                a1[e >> 1] = dq_f16x2(im[0][e] + im[1][e], im[0][e + 1] + im[1][e + 1]);
+              } else {
+                a0[e >> 1] = dq_f16x2(im[1][e] - im[0][e], im[1][e + 1] - im[0][e + 1]);
+                a1[e >> 1] = dq_f16x2(re[0][e] - re[1][e], re[0][e + 1] - re[1][e + 1]);
+              }
             }
+            const uint32_t st = sA + (uint32_t)s * kAStage;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + o0), "r"(a0[0]), "r"(a0[1]), "r"(a0[2]),
+                         "r"(a0[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + o1), "r"(a1[0]), "r"(a1[1]), "r"(a1[2]),
+                         "r"(a1[3])
+                         : "memory");
+          } else {
+            uint32_t h0[4], l0[4], h1[4], l1[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              if (h == 0) {
+                dq_split2(re[0][e] + re[1][e], re[0][e + 1] + re[1][e + 1], h0[e >> 1], l0[e >> 1]);
+                dq_split2(im[0][e] + im[1][e], im[0][e + 1] + im[1][e + 1], h1[e >> 1], l1[e >> 1]);
+              } else {
+                dq_split2(im[1][e] - im[0][e], im[1][e + 1] - im[0][e + 1], h0[e >> 1], l0[e >> 1]);
+                dq_split2(re[0][e] - re[1][e], re[0][e + 1] - re[1][e + 1], h1[e >> 1], l1[e >> 1]);
+              }
+            }
+            const uint32_t st = sA + (uint32_t)s * kAStage;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + o0), "r"(h0[0]), "r"(h0[1]), "r"(h0[2]),
+                         "r"(h0[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + o1), "r"(h1[0]), "r"(h1[1]), "r"(h1[2]),
+                         "r"(h1[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + kDqATerm + o0), "r"(l0[0]), "r"(l0[1]),
+                         "r"(l0[2]), "r"(l0[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + kDqATerm + o1), "r"(l1[0]), "r"(l1[1]),
+                         "r"(l1[2]), "r"(l1[3])
+                         : "memory");
           }
-          const uint32_t st = sA + (uint32_t)s * kDqAStage;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + o0), "r"(h0[0]), "r"(h0[1]), "r"(h0[2]),
-                       "r"(h0[3])
-                       : "memory");
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + o1), "r"(h1[0]), "r"(h1[1]), "r"(h1[2]),
-                       "r"(h1[3])
-                       : "memory");
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + kDqATerm + o0), "r"(l0[0]), "r"(l0[1]),
-                       "r"(l0[2]), "r"(l0[3])
-                       : "memory");
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(st + kDqATerm + o1), "r"(l1[0]), "r"(l1[1]),
-                       "r"(l1[2]), "r"(l1[3])
-                       : "memory");
           fence_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(fullA(s));
@@ -595,6 +662,15 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
       const int64_t j = (int64_t)c.rt * 64 + jl;
       const int64_t ystride = 2 * (int64_t)pr.n;
       float* ycol = pr.y + (int64_t)part * pr.n + j;
+      float rfac = 1.0f;  // F16: 2^-e of the row's scaling (the producers' e, from the same scales)
+      if constexpr (F16) {
+        if (j < pr.n) {
+          uint32_t mb = 0;
+#pragma unroll
+          for (int p = 0; p < 2 * NP; ++p) mb = max(mb, __float_as_uint(__ldg(pr.scales + (int64_t)p * pr.n + j)));
+          rfac = dq_pow2(-dq_row_exp(mb));
+        }
+      }
       for (int sub = 0; sub < NT; ++sub) {
         const int b = acc_buf(lt, sub);
         bool got = true;
@@ -616,7 +692,10 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const int64_t tok = tok0 + 32 * cc + e;
-              if (tok < P.M) ycol[tok * ystride] = __uint_as_float(v[e]);
+              if (tok < P.M) {
+                if constexpr (F16) ycol[tok * ystride] = __uint_as_float(v[e]) * rfac * __ldg(pr.xfac + tok);
+                else ycol[tok * ystride] = __uint_as_float(v[e]);
+              }
             }
           }
         }
@@ -662,6 +741,63 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kDqTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The activations of the F16 form: per layer and token, x~ (2m bfloat16, m a
+// multiple of 8) times 2^f as fp16 into xh, and 2^-f into xfac.  f puts the
+// token's largest magnitude in [2^14, 2^15) (f = 0 for a token of zeros or
+// with Inf/NaN, whose values then convert as they are; at most 64, so a token
+// below 2^-50 keeps fewer significant bits).  Every finite bfloat16 value the
+// scaling leaves at or above 2^-17 is exact in fp16 (8 significant bits).
+// One CTA per (token, layer); two passes over the row (the second from cache).
+constexpr int kDqXThreads = 256;
+struct DqXParams {
+  const uint16_t* x[kDqMaxGroup];
+  uint16_t* xh[kDqMaxGroup];
+  float* xfac[kDqMaxGroup];
+  int32_t m[kDqMaxGroup];
+  int32_t count, pad_;
+};
+
+__device__ __forceinline__ uint32_t dq_bf16x2_to_f16x2(uint32_t w, float f) {
+  return dq_f16x2(__uint_as_float(w << 16) * f, __uint_as_float(w & 0xFFFF0000u) * f);
+}
+
+__global__ void __launch_bounds__(kDqXThreads) dq_x16_kernel(const __grid_constant__ DqXParams P) {
+  const int l = blockIdx.y;
+  const int64_t t = blockIdx.x, m = P.m[l];
+  const uint4* src = reinterpret_cast<const uint4*>(P.x[l] + t * 2 * m);
+  uint4* dst = reinterpret_cast<uint4*>(P.xh[l] + t * 2 * m);
+  const int chunks = (int)(m / 4);  // 16-byte chunks of the 2m values
+  uint32_t mx = 0;                  // largest magnitude (bits), two lanes of 16
+  for (int c = threadIdx.x; c < chunks; c += kDqXThreads) {
+    const uint4 v = __ldg(src + c);
+    mx = __vmaxu2(mx, v.x & 0x7FFF7FFFu);
+    mx = __vmaxu2(mx, v.y & 0x7FFF7FFFu);
+    mx = __vmaxu2(mx, v.z & 0x7FFF7FFFu);
+    mx = __vmaxu2(mx, v.w & 0x7FFF7FFFu);
+  }
+  mx = __reduce_max_sync(0xFFFFFFFFu, max(mx & 0xFFFFu, mx >> 16));
+  __shared__ uint32_t wmax[kDqXThreads / 32];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  uint32_t b = 0;
+#pragma unroll
+  for (int w = 0; w < kDqXThreads / 32; ++w) b = max(b, wmax[w]);
+  // a bfloat16 magnitude with biased exponent E lies in [2^(E-127), 2^(E-126))
+  const int f = (b == 0 || b >= 0x7F80u) ? 0 : min(64, 141 - (int)(b >> 7));
+  const float up = dq_pow2(f);
+  if (threadIdx.x == 0) P.xfac[l][t] = dq_pow2(-f);
+  for (int c = threadIdx.x; c < chunks; c += kDqXThreads) {
+    const uint4 v = __ldg(src + c);
+    uint4 o;
+    o.x = dq_bf16x2_to_f16x2(v.x, up);
+    o.y = dq_bf16x2_to_f16x2(v.y, up);
+    o.z = dq_bf16x2_to_f16x2(v.z, up);
+    o.w = dq_bf16x2_to_f16x2(v.w, up);
+    dst[c] = o;
   }
 }
 

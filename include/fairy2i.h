@@ -111,10 +111,14 @@ typedef enum {
                                  256 signed sums of every 8 activations (fp16 entries, each the fp32 sum
                                  rounded once, activations scaled by a power of two per window); per
                                  code byte one shared-memory lookup and two fp32 adds */
-    FAIRY2I_ALGO_TCGEN05_DQ = 6 /* layout 3, T <= 4, m a multiple of 8: tcgen05 GEMM of the dequantized
+    FAIRY2I_ALGO_TCGEN05_DQ = 6, /* layout 3, T <= 4, m a multiple of 8: tcgen05 GEMM of the dequantized
                                  real matrix (Theorem 1 rebuilt from the summed stages) as two bfloat16
                                  terms hi + lo against x; codes staged in shared memory by the TMA
                                  engine; no workspace */
+    FAIRY2I_ALGO_TCGEN05_DQ16 = 7 /* as TCGEN05_DQ with one fp16 term (rows scaled by powers of two)
+                                 against an fp16 copy of x scaled per token by a power of two (made
+                                 in the workspace by a conversion kernel): half the MMAs and A
+                                 bytes; fairy2i_linear_ws / fairy2i_linear_group_ws only */
 } fairy2i_algo;
 
 /* Bytes of the code planes of an n x m layer with T stages in layout
@@ -197,14 +201,24 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
 /* Layout-3 layers through fairy2i_linear / _ex / _group (no workspace) take
  * the dequantized GEMM (FAIRY2I_ALGO_TCGEN05_DQ; "Fairy2i: Ultra-Low-Bit ...",
  * Step 3: the stages add up to one matrix, and Step 1: its real form); with a
- * workspace (the *_ws calls below) AUTO takes the table-lookup decode below 12
- * tokens and the dequantized GEMM from 12 tokens.  The dequantized GEMM needs
- * m a multiple of 8 (x is read by TMA in two halves, Re x and Im x), so other
- * layout-3 layers return UNSUPPORTED here and go through the *_ws calls.
- * Precision: the summed matrix is formed in fp32 and carried as two bfloat16
- * terms (<= 2^-18 relative per entry), products are exact and sums are fp32:
- * about 1e-5 relative (L2) against the exact sum.  Tokens run in tiles of
- * min(256, M rounded up to 16); the codes are decoded once per token tile. */
+ * workspace (the *_ws calls below) AUTO takes the table-lookup decode below 11
+ * tokens and the fp16 dequantized GEMM (FAIRY2I_ALGO_TCGEN05_DQ16) from 11
+ * tokens.  The dequantized GEMM needs m a multiple of 8 (x is read by TMA in
+ * two halves, Re x and Im x), so other layout-3 layers return UNSUPPORTED here
+ * and go through the *_ws calls.
+ * Precision (TCGEN05_DQ): the summed matrix is formed in fp32 and carried as
+ * two bfloat16 terms (<= 2^-18 relative per entry), products are exact and
+ * sums are fp32: about 1e-5 relative (L2) against the exact sum.
+ * Precision (TCGEN05_DQ16): each row of the summed matrix is scaled by a power
+ * of two and rounded once to fp16 (<= 2^-11 relative per entry); each token of
+ * x is scaled by a power of two into fp16, exactly for every value at or above
+ * 2^-31 of the token's largest; products are exact, sums fp32, and both
+ * powers of two are undone on the fp32 result: about 3e-4 relative (L2) for
+ * Gaussian weights.  Precision drops for weight scales below 2^-53 or above
+ * 2^75 and for tokens whose largest magnitude is below 2^-50 (the powers of
+ * two are clamped to 2^+-64); a token with Inf or NaN gives non-finite outputs.
+ * Tokens run in tiles of min(256, M rounded up to 16); the codes are decoded
+ * once per token tile. */
 
 /* The layer through the table-lookup decode (same y as fairy2i_linear; "Fairy2i:
  * Ultra-Low-Bit ...", "Industry implications: multiplication-free inference":
@@ -214,12 +228,14 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
  * fairy2i_linear_ex / fairy2i_linear_group and the workspace is unused.
  *   workspace : device, caller-owned scratch of at least
  *               fairy2i_linear_workspace_bytes(qs, count, M) bytes, 256-byte
- *               aligned, any contents (no initialisation needed).  It holds
- *               one fp32 partial output per (row, window of 256 columns,
- *               token); a second kernel sums every row's partials in window
- *               order, so results are deterministic.  Calls that may run at
- *               the same time need separate workspaces.  NULL is allowed when
- *               the size query returns 0 (every layer has m <= 256).
+ *               aligned, any contents (no initialisation needed).  The table
+ *               lookup keeps one fp32 partial output per (row, window of 256
+ *               columns, token) there; a second kernel sums every row's
+ *               partials in window order, so results are deterministic.  The
+ *               fp16 dequantized GEMM keeps the fp16 copy of x (4 m bytes per
+ *               token and layer) and the tokens' powers of two there.  Calls
+ *               that may run at the same time need separate workspaces.  NULL
+ *               is allowed when the size query returns 0.
  * The decode kernel is launched as a programmatic dependent of the preceding
  * work in the stream (it may start while that work finishes and waits for it
  * before reading activations or writing anything); the summing kernel is an
@@ -232,7 +248,8 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
  * activation gives non-finite outputs.
  * Errors: as fairy2i_linear_ex; INVALID_ARG for a missing, short or
  * misaligned workspace; UNSUPPORTED for layout 3 with another algo than AUTO,
- * LUT or TCGEN05_DQ, or T > 4. */
+ * LUT, TCGEN05_DQ or TCGEN05_DQ16, for T > 4, or for a dequantized GEMM with m
+ * not a multiple of 8. */
 fairy2i_status fairy2i_linear_ws(const fairy2i_packed *q, const void *x, int64_t M, float *y,
                                  fairy2i_algo algo, void *workspace, size_t workspace_bytes,
                                  void *stream);
@@ -242,8 +259,9 @@ fairy2i_status fairy2i_linear_group_ws(const fairy2i_packed *qs, const void *con
                                        size_t workspace_bytes, void *stream);
 
 /* Workspace bytes of fairy2i_linear_ws / fairy2i_linear_group_ws for these
- * layers and token count: 0 if none is needed or the descriptors are not
- * layout 3 (or invalid). */
+ * layers and token count, enough for every algorithm those calls accept (the
+ * table lookup, and for m a multiple of 8 the fp16 dequantized GEMM): 0 if
+ * the descriptors are not layout 3 (or invalid). */
 size_t fairy2i_linear_workspace_bytes(const fairy2i_packed *qs, int32_t count, int64_t M);
 
 /* The table-lookup decode with no caller workspace and no allocation (the
@@ -260,8 +278,8 @@ size_t fairy2i_linear_workspace_bytes(const fairy2i_packed *qs, int32_t count, i
  *     streams, other threads) race and must be serialized by the caller.
  *   - The array needs no clearing: each call writes every byte it reads.
  * Errors: as fairy2i_linear_group_ws; UNSUPPORTED for another layout or when
- * the layers need more than 8 MiB of scratch (fairy2i_linear_workspace_bytes;
- * a LLaMA-2-7B block needs 1.6 MB per token of a launch). */
+ * the table lookup needs more than 8 MiB of scratch for these layers (a
+ * LLaMA-2-7B block needs 1.6 MB per token of a launch). */
 fairy2i_status fairy2i_linear_group_static(const fairy2i_packed *qs, const void *const *xs,
                                            float *const *ys, int32_t count, int64_t M, void *stream);
 

@@ -102,7 +102,8 @@ def test_linear_rejects_bad_arguments(lib):
     assert lib.fairy2i_linear(ctypes.byref(d), None, 0, None, None) == 0  # M = 0: pointers unused
     assert lib.fairy2i_linear(ctypes.byref(d), p, -1, p, None) == 2
     assert lib.fairy2i_linear(ctypes.byref(d), ctypes.c_void_p(258), 1, p, None) == 1
-    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 7, None) == 1
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 8, None) == 1  # no such algo
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 7, None) == 4  # the fp16 dequantized GEMM: layout 3
     assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, -1, None) == 1
     assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 5, None) == 4  # the table lookup reads layout 3 only
     assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 1, p, 6, None) == 4  # so does the dequantized GEMM
@@ -176,7 +177,7 @@ def test_python_wrappers_reject_host_tensors(lib):
         f2i.linear_grad_x(q, torch.zeros((1, 8)))  # host tensor
     # the algorithm names map onto the header's fairy2i_algo values
     assert f2i.ALGO == {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4, "lut": 5,
-                        "tcgen05_dq": 6}
+                        "tcgen05_dq": 6, "tcgen05_dq16": 7}
 
 
 def test_layout3_sizes(lib):
@@ -194,8 +195,10 @@ def test_layout3_sizes(lib):
 
 
 def test_layout3_workspace_bytes(lib):
-    """One float2 partial output per (row of a 32-row tile, window of 256 columns,
-    token of a launch) for the layers with several windows."""
+    """The larger of the table lookup's need (one float2 partial output per (row of a
+    32-row tile, window of 256 columns, token of a launch) for the layers with several
+    windows) and, for m a multiple of 8, the fp16 dequantized GEMM's (per layer of a
+    launch, the fp16 copy of x and a float per token, each rounded up to 256 bytes)."""
     def ws(descs, M):
         arr = (f2i.PackedDesc * len(descs))(*descs)
         return lib.fairy2i_linear_workspace_bytes(arr, len(descs), M)
@@ -206,9 +209,33 @@ def test_layout3_workspace_bytes(lib):
     assert ws([q], 2) == ws([q], 4) == ws([q], 10) == 64 * 8 * 2 * 32 * 8
     assert ws([q], 3) == ws([q], 9) == 64 * 8 * 3 * 32 * 8
     assert ws([_desc(n=2048, m=2048, T=3, version=L3)], 9) == 64 * 8 * 2 * 32 * 8
-    assert ws([_desc(n=100, m=256, T=2, version=L3)], 1) == 0  # one window: written directly
+    # one window: the table lookup writes y directly; the fp16 copy of one token remains
+    assert ws([_desc(n=100, m=256, T=2, version=L3)], 1) == 1024 + 256
+    assert ws([_desc(n=100, m=250, T=2, version=L3)], 1) == 0  # and none for m not a multiple of 8
+    r256 = lambda v: (v + 255) // 256 * 256
+    assert ws([q], 2048) == r256(2048 * 4 * 2048) + r256(2048 * 4)
+    # nine layers: launches of 8 and 1 reuse the workspace, so the larger launch sets it
+    nine = [_desc(n=64, m=8 * (i + 1), T=2, version=L3) for i in range(9)]
+    assert ws(nine, 100) == sum(r256(100 * 4 * 8 * (i + 1)) + r256(400) for i in range(8))
     assert ws([_desc(n=2048, m=2048, T=2)], 1) == 0  # layout 2
     assert ws([q], 0) == 0
+
+
+def test_dq16_host_errors(lib):
+    """The fp16 dequantized GEMM's argument checks (all before any launch)."""
+    p = ctypes.c_void_p(256)
+    L3 = f2i.LAYOUT_LUT
+    d = _desc(n=4, m=600, T=2, version=L3)
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 16, p, 7, None) == 4  # needs a workspace
+    assert "workspace" in _err(lib)
+    assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 16, p, 7, None, 0, None) == 1  # workspace missing
+    assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 16, p, 7, p, 16, None) == 1  # too small
+    assert lib.fairy2i_linear_ws(ctypes.byref(d), p, 16, p, 7, ctypes.c_void_p(272), 1 << 20, None) == 1
+    d7 = _desc(n=4, m=100, T=2, version=L3)
+    assert lib.fairy2i_linear_ws(ctypes.byref(d7), p, 16, p, 7, p, 1 << 20, None) == 4  # m not a multiple of 8
+    d2 = _desc(n=4, m=600, T=2)
+    assert lib.fairy2i_linear_ws(ctypes.byref(d2), p, 16, p, 7, p, 1 << 20, None) == 4  # layout 2
+    assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 16, p, 8, None) == 1  # no such algo
 
 
 def test_layout3_host_errors(lib):

@@ -276,8 +276,8 @@ def test_lut_errors():
     assert lib.fairy2i_linear_ex(ctypes.byref(d), x.data_ptr(), 1, y.data_ptr(), 5, None) == 4
     need = lib.fairy2i_linear_workspace_bytes(ctypes.byref(d), 1, 1)
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
-    assert lib.fairy2i_linear_ws(ctypes.byref(d), x.data_ptr(), 1, y.data_ptr(), 0, ws.data_ptr(), need - 1,
-                                 None) == 1
+    assert lib.fairy2i_linear_ws(ctypes.byref(d), x.data_ptr(), 1, y.data_ptr(), 0, ws.data_ptr(), 16,
+                                 None) == 1  # the table lookup needs 1536 bytes here
     assert lib.fairy2i_linear_ws(ctypes.byref(d), x.data_ptr(), 1, y.data_ptr(), 2, ws.data_ptr(), need,
                                  None) == 4  # mma does not read layout 3
     with pytest.raises(f2i.Fairy2iError):
@@ -325,7 +325,7 @@ def test_full_size_projection_layout3_sampled(name, out_f, in_f, T):
     assert rel_l2(got, want) <= REL_L2
 
 
-@pytest.mark.parametrize("M", [1, 4, 11])  # 11: five launches (3 + 2 + 2 + 2 + 2), AUTO's last table-lookup count
+@pytest.mark.parametrize("M", [1, 4, 10, 11])  # 10: AUTO's last table-lookup count; 11: 3 + 2 + 2 + 2 + 2
 def test_full_size_block_group_layout3_sampled(M):
     """The seven projections of a block in one grouped table-lookup launch (the
     benchmark's launch), against the oracle on sampled rows."""
@@ -339,7 +339,7 @@ def test_full_size_block_group_layout3_sampled(M):
         rows = _sample_rows(n, count=8, seed=pi)
         qU, qW = _oracle_rows(R, rows, 2)
         samples.append((rows, oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x))))
-    ys = f2i.linear_group(qs, xs)
+    ys = f2i.linear_group(qs, xs, algo="lut")
     for q, y, (rows, want) in zip(qs, ys, samples):
         y = y.cpu().numpy()
         got = np.concatenate([y[:, rows], y[:, q.n + rows]], axis=1)
@@ -383,14 +383,14 @@ def test_dq_parity_stages(T, M):
 
 def test_dq_plain_entry_and_auto():
     """Layout 3 through the plain entry points (no workspace) takes the dequantized
-    GEMM at any token count; with a workspace AUTO switches to it from 12 tokens."""
+    GEMM at any token count; with a workspace AUTO switches to the fp16 form from 11 tokens."""
     import ctypes
     n, m = 100, 600
     R = _R(n, m, 5)
     q = _gpu_layer(R, 2)
     qU, qW = _oracle_layer(R, 2)
     lib = f2i.load_library()
-    for M in (1, 11, 12):
+    for M in (1, 10, 11):
         x = _x(M, m, 30 + M)
         xd = x.cuda()
         y = torch.empty((M, 2 * n), device="cuda")
@@ -454,9 +454,9 @@ def test_dq_full_size_block_prefill_sampled():
 
 @pytest.mark.parametrize("M", [16, 64, 256])  # value tables up to 64 tokens, the per-plane decode above
 def test_dq_full_size_block_batched_sampled(M):
-    """The seven LLaMA-2-7B projections at batched-decode token counts (the sweep's launch:
-    one grouped call, AUTO on layout 3 takes the dequantized GEMM from 12 tokens), against
-    the oracle on sampled rows and tokens."""
+    """The seven LLaMA-2-7B projections at batched-decode token counts through the bfloat16
+    form (one grouped call; AUTO takes the fp16 form, tested beside it), against the oracle
+    on sampled rows and tokens."""
     qs, xs, samples = [], [], []
     for pi, (name, out_f, in_f) in enumerate(inputs.LLAMA2_7B_BLOCK):
         n = out_f // 2
@@ -468,7 +468,7 @@ def test_dq_full_size_block_batched_sampled(M):
         qU, qW = _oracle_rows(R, rows, 2)
         toks = np.unique(np.array([0, 1, M // 2, M - 1]))
         samples.append((rows, toks, oracle.linear_mulfree(qU, qW, inputs.bf16_bits(x[toks]))))
-    ys = f2i.linear_group(qs, xs)  # AUTO
+    ys = f2i.linear_group(qs, xs, algo="tcgen05_dq")
     for q, y, (rows, toks, want) in zip(qs, ys, samples):
         y = y.cpu().numpy()[toks]
         got = np.concatenate([y[:, rows], y[:, q.n + rows]], axis=1)
