@@ -38,8 +38,9 @@ EXPORTED = (
     "fairy2i_sync_status", "fairy2i_last_error", "fairy2i_layout_version", "fairy2i_selftest_bounded_wait",
     "fairy2i_convert_quantize", "fairy2i_linear_grad_x", "fairy2i_linear_grad_x_group",
     "fairy2i_codes_bytes_layout", "fairy2i_linear_ws", "fairy2i_linear_group_ws", "fairy2i_linear_workspace_bytes",
-    "fairy2i_linear_group_static",
+    "fairy2i_linear_group_static", "fairy2i_linear_group_ws_out",
 )
+OUT = {torch.float32: 0, torch.bfloat16: 1}  # fairy2i_out
 
 
 class Fairy2iError(RuntimeError):
@@ -89,6 +90,8 @@ def load_library(path: str = LIB_PATH):
                                                    P, SZ, P]),
         "fairy2i_linear_workspace_bytes": (SZ, [PD, I32, I64]),
         "fairy2i_linear_group_static": (ctypes.c_int, [PD, ctypes.POINTER(P), ctypes.POINTER(P), I32, I64, P]),
+        "fairy2i_linear_group_ws_out": (ctypes.c_int, [PD, ctypes.POINTER(P), ctypes.POINTER(P), I32, I64,
+                                                       ctypes.c_int, ctypes.c_int, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -300,18 +303,22 @@ def linear_grad_x_group(qs, gys, outs=None, stream=None):
     return outs
 
 
-def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None, ws: torch.Tensor | None = None):
+def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None, ws: torch.Tensor | None = None,
+                 out_dtype=torch.float32):
     """Evaluate several layers (same T, layout and token count) in one launch; layout-3 layers
-    use workspace ``ws`` (by default the one kept for this device and stream)."""
+    use workspace ``ws`` (by default the one kept for this device and stream) and may write
+    bfloat16 outputs (``out_dtype``: the float32 result rounded once)."""
     count = len(qs)
     M = xs[0].shape[0]
+    if out_dtype not in OUT:
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
     if ys is None:
-        ys = [torch.empty((M, 2 * q.n), dtype=torch.float32, device=x.device) for q, x in zip(qs, xs)]
+        ys = [torch.empty((M, 2 * q.n), dtype=out_dtype, device=x.device) for q, x in zip(qs, xs)]
     for q, x, y in zip(qs, xs, ys):
         _dev(x, "x")
         _dev(y, "y")
-        if x.dtype != torch.bfloat16 or x.shape != (M, 2 * q.m) or y.shape != (M, 2 * q.n):
-            raise ValueError("group members need matching x [M, 2m] bfloat16 and y [M, 2n] float32")
+        if x.dtype != torch.bfloat16 or x.shape != (M, 2 * q.m) or y.shape != (M, 2 * q.n) or y.dtype != out_dtype:
+            raise ValueError("group members need matching x [M, 2m] bfloat16 and y [M, 2n] of out_dtype")
     descs = (PackedDesc * count)(*[q.desc() for q in qs])
     xp = (ctypes.c_void_p * count)(*[x.data_ptr() for x in xs])
     yp = (ctypes.c_void_p * count)(*[y.data_ptr() for y in ys])
@@ -321,8 +328,14 @@ def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None, ws: torch.Ten
         if ws is None:
             ws = workspace(qs, M, xs[0].device, s, descs)
         wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
-        _check(load_library().fairy2i_linear_group_ws(descs, xp, yp, count, M, ALGO[algo], wp, wn, s))
+        if out_dtype == torch.float32:
+            _check(load_library().fairy2i_linear_group_ws(descs, xp, yp, count, M, ALGO[algo], wp, wn, s))
+        else:
+            _check(load_library().fairy2i_linear_group_ws_out(descs, xp, yp, count, M, ALGO[algo], OUT[out_dtype],
+                                                              wp, wn, s))
         return ys
+    if out_dtype != torch.float32:
+        raise ValueError("bfloat16 outputs are written for layout-3 layers only")
     _check(load_library().fairy2i_linear_group(descs, xp, yp, count, M, ALGO[algo], s))
     return ys
 

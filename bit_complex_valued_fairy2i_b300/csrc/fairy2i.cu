@@ -422,7 +422,8 @@ fairy2i_status launch_dq_form(const f2i::DqParams& P, int grid, bool f16, cudaSt
 // f16: the fp16 form, each launch preceded by the activations' conversion
 // into the workspace (dq16_workspace bytes, 256-byte aligned; checked here).
 fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count, int64_t M, int T,
-                      cudaStream_t s, bool f16 = false, void* ws = nullptr, size_t ws_bytes = 0) {
+                      cudaStream_t s, bool f16 = false, void* ws = nullptr, size_t ws_bytes = 0,
+                      bool out_bf16 = false) {
   if (f16) {
     const size_t need = dq16_workspace(qs, count, M);
     if (!ws) return fail(FAIRY2I_ERR_INVALID_ARG, "the fp16 dequantized GEMM needs a workspace of %zu bytes", need);
@@ -475,6 +476,7 @@ fairy2i_status run_dq(const fairy2i_packed* qs, const void* const* xs, float* co
       pr.scales = q.scales;
       pr.y = ys[p0 + i];
       pr.xfac = xf[i];
+      pr.out_bf16 = out_bf16 ? 1 : 0;
       pr.n = (int32_t)q.n;
       pr.m = (int32_t)q.m;
       pr.row_tiles = (int32_t)((q.n + 63) / 64);
@@ -804,7 +806,7 @@ fairy2i_status launch_lut(const f2i::LutParams& P, int T, int mc, int ctas, cuda
 // (layer, window, row tile) are split over one CTA per SM by their cost, in
 // launch order: 8 per slot of codes plus 3 for the unit's epilogue.
 fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int count, int64_t M, int T,
-                       void* ws, size_t ws_bytes, cudaStream_t s) {
+                       void* ws, size_t ws_bytes, cudaStream_t s, bool out_bf16 = false) {
   const size_t need = lut_workspace(qs, count, M, T);
   if (need > 0) {
     if (!ws) return fail(FAIRY2I_ERR_INVALID_ARG, "table-lookup decode needs a workspace of %zu bytes", need);
@@ -836,7 +838,9 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
         L.codes = static_cast<const uint8_t*>(q.codes);
         L.scales = q.scales;
         L.x = static_cast<const uint16_t*>(xs[p0 + i]) + t0 * 2 * q.m;
-        L.y = ys[p0 + i] + t0 * 2 * q.n;
+        L.y = reinterpret_cast<float*>(reinterpret_cast<char*>(ys[p0 + i]) +
+                                       t0 * 2 * q.n * (out_bf16 ? 2 : (int64_t)sizeof(float)));
+        L.out_bf16 = out_bf16 ? 1 : 0;
         L.n = (int32_t)q.n;
         L.m = (int32_t)q.m;
         L.tiles = (int32_t)f2i::l3_tiles(q.n);
@@ -847,6 +851,7 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
         if (L.windows > 1) {
           f2i::LutReduceProblem& Rp = RP.p[RP.count++];
           Rp.y = L.y;
+          Rp.out_bf16 = L.out_bf16;
           Rp.part = P.partials + part;
           Rp.n = L.n;
           Rp.tiles = L.tiles;
@@ -936,9 +941,10 @@ fairy2i_status run_lut(const fairy2i_packed* qs, const void* const* xs, float* c
 
 // with_ws: the call came through a *_ws entry point (workspace may still be
 // NULL when none is needed).
+// out_bf16: y holds bfloat16 elements (layout 3 only).
 fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs, float* const* ys, int32_t count,
                                  int64_t M, fairy2i_algo algo, bool with_ws, void* ws, size_t ws_bytes,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, bool out_bf16 = false) {
   if (count < 1 || count > 256) return fail(FAIRY2I_ERR_INVALID_ARG, "count=%d outside [1, 256]", count);
   if (!qs || !xs || !ys) return fail(FAIRY2I_ERR_INVALID_ARG, "NULL array argument");
   if (M < 0) return fail(FAIRY2I_ERR_SHAPE, "M=%lld is negative", (long long)M);
@@ -977,10 +983,11 @@ fairy2i_status linear_group_impl(const fairy2i_packed* qs, const void* const* xs
         return fail(FAIRY2I_ERR_INVALID_ARG, "x and y must be 16-byte aligned (layer %d)", i);
     }
     if (M > (int64_t)1 << 30) return fail(FAIRY2I_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
-    if (a3 == FAIRY2I_ALGO_TCGEN05_DQ) return run_dq(qs, xs, ys, count, M, T, s);
-    if (a3 == FAIRY2I_ALGO_TCGEN05_DQ16) return run_dq(qs, xs, ys, count, M, T, s, true, ws, ws_bytes);
-    return run_lut(qs, xs, ys, count, M, T, ws, ws_bytes, s);
+    if (a3 == FAIRY2I_ALGO_TCGEN05_DQ) return run_dq(qs, xs, ys, count, M, T, s, false, nullptr, 0, out_bf16);
+    if (a3 == FAIRY2I_ALGO_TCGEN05_DQ16) return run_dq(qs, xs, ys, count, M, T, s, true, ws, ws_bytes, out_bf16);
+    return run_lut(qs, xs, ys, count, M, T, ws, ws_bytes, s, out_bf16);
   }
+  if (out_bf16) return fail(FAIRY2I_ERR_UNSUPPORTED, "bfloat16 outputs are written by the layout-3 kernels only");
   if (algo == FAIRY2I_ALGO_LUT || algo == FAIRY2I_ALGO_TCGEN05_DQ || algo == FAIRY2I_ALGO_TCGEN05_DQ16)
     return fail(FAIRY2I_ERR_UNSUPPORTED, "the table-lookup decode and the dequantized GEMM read layout 3 only");
   (void)ws;
@@ -1221,6 +1228,16 @@ fairy2i_status fairy2i_linear_group_ws(const fairy2i_packed* qs, const void* con
   NvtxRange nvtx_range("fairy2i_linear_group_ws");
   return linear_group_impl(qs, xs, ys, count, M, algo, true, workspace, workspace_bytes,
                            static_cast<cudaStream_t>(stream));
+}
+
+fairy2i_status fairy2i_linear_group_ws_out(const fairy2i_packed* qs, const void* const* xs, void* const* ys,
+                                           int32_t count, int64_t M, fairy2i_algo algo, fairy2i_out out,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx_range("fairy2i_linear_group_ws_out");
+  if (out != FAIRY2I_OUT_F32 && out != FAIRY2I_OUT_BF16)
+    return fail(FAIRY2I_ERR_INVALID_ARG, "unknown output type %d", (int)out);
+  return linear_group_impl(qs, xs, reinterpret_cast<float* const*>(ys), count, M, algo, true, workspace,
+                           workspace_bytes, static_cast<cudaStream_t>(stream), out == FAIRY2I_OUT_BF16);
 }
 
 fairy2i_status fairy2i_linear_group_static(const fairy2i_packed* qs, const void* const* xs, float* const* ys,

@@ -29,8 +29,17 @@
 // stores 8 bytes per lane.  Padding rows and columns hold zero bits.
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
 
 namespace f2i {
+
+// One output value to y[i]: fp32, or (bf16 != 0) rounded to nearest even to
+// bfloat16 in a buffer of bfloat16 elements (the same value the fp32 output
+// holds, rounded once).
+__device__ __forceinline__ void store_y(float* y, int64_t i, float v, int32_t bf16) {
+  if (bf16) reinterpret_cast<__nv_bfloat16*>(y)[i] = __float2bfloat16_rn(v);
+  else y[i] = v;
+}
 
 constexpr int kRowsPerTile = 16;
 constexpr int kColsPerBlock = 64;

@@ -117,7 +117,7 @@ struct DqProblem {
   int32_t row_tiles;  // tiles of 64 outputs
   int32_t tok_tiles;  // tiles of NT x N tokens
   int32_t kpairs;     // blocks of 64 columns per half of x~
-  int32_t pad_;
+  int32_t out_bf16;   // y holds bfloat16 elements
 };
 
 struct DqParams {
@@ -661,7 +661,6 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
       const DqProblem& pr = P.p[c.pi];
       const int64_t j = (int64_t)c.rt * 64 + jl;
       const int64_t ystride = 2 * (int64_t)pr.n;
-      float* ycol = pr.y + (int64_t)part * pr.n + j;
       float rfac = 1.0f;  // F16: 2^-e of the row's scaling (the producers' e, from the same scales)
       if constexpr (F16) {
         if (j < pr.n) {
@@ -693,8 +692,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
             for (int e = 0; e < 32; ++e) {
               const int64_t tok = tok0 + 32 * cc + e;
               if (tok < P.M) {
-                if constexpr (F16) ycol[tok * ystride] = __uint_as_float(v[e]) * rfac * __ldg(pr.xfac + tok);
-                else ycol[tok * ystride] = __uint_as_float(v[e]);
+                const float o = F16 ? __uint_as_float(v[e]) * rfac * __ldg(pr.xfac + tok) : __uint_as_float(v[e]);
+                store_y(pr.y, tok * ystride + (int64_t)part * pr.n + j, o, pr.out_bf16);
               }
             }
           }

@@ -67,12 +67,12 @@ struct LutProblem {
   const uint8_t* codes;
   const float* scales;
   const uint16_t* x;  // bfloat16 [M][2m] (this launch's tokens)
-  float* y;           // [M][2n]
+  float* y;           // [M][2n], fp32 or (out_bf16) bfloat16 elements
   int32_t n, m;
   int32_t tiles;       // row tiles of 32 rows
   int32_t windows;     // column windows of 256
   int32_t unit_begin;  // first unit of the layer in the launch
-  int32_t pad_;
+  int32_t out_bf16;
   int64_t part_begin;  // first partial output (float2) in the workspace
 };
 
@@ -98,9 +98,10 @@ struct LutParams {
 // The window-combining pass: one thread per (row of a 32-row tile, token) of
 // every layer with more than one window.
 struct LutReduceProblem {
-  float* y;
+  float* y;            // fp32 or (out_bf16) bfloat16 elements
   const float2* part;  // [window][tile][token][32]
   int32_t n, tiles, windows, row_begin;  // row_begin: first padded row of the layer in the pass
+  int32_t out_bf16, pad_;
 };
 struct LutReduceParams {
   int32_t count, M, total_rows, pad_;
@@ -527,8 +528,8 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
         if (row_in)
 #pragma unroll
           for (int t = 0; t < M; ++t) {
-            L.y[t * n2 + j] = yre[t];
-            L.y[t * n2 + L.n + j] = yim[t];
+            store_y(L.y, t * n2 + j, yre[t], L.out_bf16);
+            store_y(L.y, t * n2 + L.n + j, yim[t], L.out_bf16);
           }
       } else {  // a partial output, combined over windows by lut_reduce_kernel
         float2* part = P.partials + L.part_begin;
@@ -588,8 +589,8 @@ __global__ void __launch_bounds__(256) lut_reduce_kernel(const __grid_constant__
     sr += __shfl_xor_sync(0xffffffffu, sr, 2);
     si += __shfl_xor_sync(0xffffffffu, si, 2);
     if (live && q == 0 && r < L.n) {
-      L.y[(int64_t)t * 2 * L.n + r] = sr;
-      L.y[(int64_t)t * 2 * L.n + L.n + r] = si;
+      store_y(L.y, (int64_t)t * 2 * L.n + r, sr, L.out_bf16);
+      store_y(L.y, (int64_t)t * 2 * L.n + L.n + r, si, L.out_bf16);
     }
   }
 }

@@ -258,6 +258,26 @@ fairy2i_status fairy2i_linear_group_ws(const fairy2i_packed *qs, const void *con
                                        fairy2i_algo algo, void *workspace,
                                        size_t workspace_bytes, void *stream);
 
+/* Output element type of fairy2i_linear_group_ws_out. */
+typedef enum {
+    FAIRY2I_OUT_F32 = 0,  /* float32, as every other linear call writes */
+    FAIRY2I_OUT_BF16 = 1  /* bfloat16: the float32 result rounded once to nearest even */
+} fairy2i_out;
+
+/* fairy2i_linear_group_ws with a choice of output type, for a caller whose next
+ * layer reads bfloat16 activations (the paper has no counterpart; the decoder
+ * stack's activations are bfloat16 on the model card).  ys[i] is a device
+ * array [M][2n] of `out` elements, 16-byte aligned.  With FAIRY2I_OUT_BF16 each
+ * output is the value FAIRY2I_OUT_F32 would hold, rounded once to bfloat16
+ * (relative error <= 2^-9 against it), written by the kernel that forms it:
+ * no extra launch.  Layout-3 layers only.
+ * Errors: as fairy2i_linear_group_ws; INVALID_ARG for an unknown `out`;
+ * UNSUPPORTED for FAIRY2I_OUT_BF16 with layout-2 layers. */
+fairy2i_status fairy2i_linear_group_ws_out(const fairy2i_packed *qs, const void *const *xs,
+                                           void *const *ys, int32_t count, int64_t M,
+                                           fairy2i_algo algo, fairy2i_out out, void *workspace,
+                                           size_t workspace_bytes, void *stream);
+
 /* Workspace bytes of fairy2i_linear_ws / fairy2i_linear_group_ws for these
  * layers and token count, enough for every algorithm those calls accept (the
  * table lookup, and for m a multiple of 8 the fp16 dequantized GEMM): 0 if

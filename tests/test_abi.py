@@ -238,6 +238,19 @@ def test_dq16_host_errors(lib):
     assert lib.fairy2i_linear_ex(ctypes.byref(d), p, 16, p, 8, None) == 1  # no such algo
 
 
+def test_bf16_output_host_errors(lib):
+    """fairy2i_linear_group_ws_out: an unknown output type, and bfloat16 outputs for
+    layout-2 layers, are refused before any launch."""
+    p = ctypes.c_void_p(256)
+    xp = (ctypes.c_void_p * 1)(p)
+    yp = (ctypes.c_void_p * 1)(p)
+    d3 = (f2i.PackedDesc * 1)(_desc(n=4, m=600, T=2, version=f2i.LAYOUT_LUT))
+    assert lib.fairy2i_linear_group_ws_out(d3, xp, yp, 1, 16, 0, 2, p, 1 << 20, None) == 1
+    d2 = (f2i.PackedDesc * 1)(_desc(n=4, m=600, T=2))
+    assert lib.fairy2i_linear_group_ws_out(d2, xp, yp, 1, 16, 0, 1, p, 1 << 20, None) == 4
+    assert "layout-3" in _err(lib)
+
+
 def test_layout3_host_errors(lib):
     p = ctypes.c_void_p(256)
     L3 = f2i.LAYOUT_LUT

@@ -179,3 +179,21 @@ def test_dq16_full_size_block_sampled(M):
         y = y.cpu().numpy()[toks]
         got = np.concatenate([y[:, rows], y[:, q.n + rows]], axis=1)
         assert rel_l2(got, want) <= DQ16_REL_L2
+
+
+@pytest.mark.parametrize("algo,M", [("lut", 1), ("lut", 3), ("lut", 5), ("tcgen05_dq", 40), ("tcgen05_dq16", 40),
+                                    ("tcgen05_dq16", 300), ("auto", 16)])
+def test_bf16_outputs_are_the_rounded_fp32_outputs(algo, M):
+    """fairy2i_linear_group_ws_out with bfloat16 outputs: every element equals the float32
+    call's element rounded to nearest even, for one-window layers (written by the table
+    lookup's decode launch) and several-window ones (written by its summing launch), and for
+    both forms of the dequantized GEMM."""
+    shapes = [(40, 256), (37, 600), (64, 1024)]
+    qs, xs = [], []
+    for i, (n, m) in enumerate(shapes):
+        qs.append(_layer(_R(n, m, 70 + i), 2)[0])
+        xs.append(_x(M, m, 80 + i).cuda())
+    y32 = f2i.linear_group(qs, xs, algo=algo)
+    y16 = f2i.linear_group(qs, xs, algo=algo, out_dtype=torch.bfloat16)
+    for a, b in zip(y32, y16):
+        assert b.dtype == torch.bfloat16 and torch.equal(a.to(torch.bfloat16), b)
