@@ -585,10 +585,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
           const int s = (int)(it % AS);
           const uint32_t ph = (it / AS) & 1u;
           ++it;
-          bool got = true;
-          if (lane == 0) got = mbar_wait(emptyA(s), ph ^ 1u, abort_flag);
-          got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-          if (!got) {
+          // every lane polls the stage's barrier (no divergent branch)
+          if (__any_sync(0xffffffffu, !mbar_wait(emptyA(s), ph ^ 1u, abort_flag))) {
             ok = false;
             break;
           }

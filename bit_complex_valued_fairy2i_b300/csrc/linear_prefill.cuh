@@ -523,10 +523,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) linear_tcgen05_kernel(const __g
           const bool mine = (int)(it % kPfProducerGroups) == grp;
           ++it;
           if (!mine) continue;
-          bool got = true;
-          if (lane == 0) got = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag);
-          got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-          if (!got) {
+          // every lane polls the stage's barrier (no divergent branch)
+          if (__any_sync(0xffffffffu, !mbar_wait(empty_bar(s), ph ^ 1u, abort_flag))) {
             ok = false;
             break;
           }
