@@ -122,6 +122,12 @@ __device__ __forceinline__ uint32_t lut_lds(uint32_t addr) {
   asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF));
   return v;
 }
+template <uint32_t OFF>
+__device__ __forceinline__ uint2 lut_lds2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(addr), "n"(OFF));
+  return v;
+}
 // fp16x2 sum of two table entries (one rounding per half)
 __device__ __forceinline__ uint32_t lut_hadd2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -145,9 +151,18 @@ __device__ __forceinline__ int lut_problem_of(const LutParams& P, int u) {
 
 // Shared-memory map: the warps' code rings from the bottom, the tables in the
 // top one (M <= 2) or two (M = 3, 4) 64 KB regions below 224 KB.  Table set z
-// of a resident segment s and token t: region z >> 1, half z & 1 (+128 bytes);
-// M = 1 keeps two windows (one region), M = 2 one window (both tokens in one
-// region), M = 3, 4 one window (four sets, two regions).
+// of a resident segment s and token t, in region z >> 1 (256 bytes per entry
+// index):
+//   M = 1: two windows, slot S of set z at 4 S + 128 (z & 1);
+//   M = 3 (and M = 2 at T > 2): one window, slot S of token t at
+//   4 S + 128 (t & 1) of region t >> 1;
+//   M = 2 at T <= 2: one window, the two tokens' entries of slot S side by
+//   side at 8 S + 4 t, so one 8-byte load reads both.
+//   (Pairs at M = 3 measured slower, 46.3 against 41.2 us per LLaMA-2-7B
+//   block: the third token's loads then need more registers than the kernel
+//   has; at T = 3 the pair kernel spills too.)
+template <int T, int M>
+__host__ __device__ constexpr bool lut_pairs() { return T <= 2 && M == 2; }
 template <int M>
 __host__ __device__ constexpr uint32_t lut_table_base() { return M <= 2 ? 160u * 1024u : 96u * 1024u; }
 template <int M>
@@ -158,8 +173,13 @@ __device__ __forceinline__ int lut_set(int s, int t) { return M == 1 ? s : t; }
 // half) and the part given as an immediate offset of the loads.
 template <int M>
 __device__ __forceinline__ uint32_t lut_b_bits(int s) { return M == 1 ? ((uint32_t)s & 1u) << 7 : 0u; }
-template <int M, int t>
-__host__ __device__ constexpr uint32_t lut_imm() { return lut_table_base<M>() + 65536u * (t >> 1) + 128u * (t & 1); }
+template <int T, int M, int t>
+__host__ __device__ constexpr uint32_t lut_imm() {
+  return lut_table_base<M>() + 65536u * (t >> 1) + (lut_pairs<T, M>() ? 0u : 128u * (t & 1));
+}
+// Bytes per slot of an entry row: 4, or 8 for token pairs.
+template <int T, int M>
+__host__ __device__ constexpr uint32_t lut_slot_stride() { return lut_pairs<T, M>() ? 8u : 4u; }
 // Code ring of a warp: RING slots of 2T planes x 512 bytes (32 lanes x 16
 // bytes) filled by cp.async; a slot is refilled after the evaluation that
 // read it, so RING - 1 slots are in flight (at most 4 slots; the rings of the
@@ -173,34 +193,48 @@ __host__ __device__ constexpr int lut_ring() {
 }
 
 // One slot (8 groups x 2T planes) of a unit: for step i the lane reads group
-// slot bj ^ 4 i of every plane's table (P from the sign byte, Q from the q
-// byte).  The entries of steps 2 k and 2 k + 1 are added in fp16 (one
-// rounding; the activation scaling keeps the sum below 2^15) and the sum is
-// added to the fp32 accumulators.
+// slot bj ^ i of every plane's table (P from the sign byte, Q from the q
+// byte; bj and the XOR in units of the slot stride).  The entries of steps
+// 2 k and 2 k + 1 are added in fp16 (one rounding; the activation scaling
+// keeps the sum below 2^15) and the sum is added to the fp32 accumulators.
+// With token pairs one 8-byte load serves both tokens.
 template <int T, int M>
 __device__ __forceinline__ void lut_slot(const uint4 (&c)[2 * T], uint32_t bj, float (&acc)[M][2 * T][4]) {
+  static_assert(M <= 3, "at most three tokens per launch");
+  constexpr uint32_t SW = lut_slot_stride<T, M>();
 #pragma unroll
   for (int i = 0; i < 8; i += 2) {
-    const uint32_t b0 = bj ^ (uint32_t)(4 * i), b1 = bj ^ (uint32_t)(4 * (i + 1));
+    const uint32_t b0 = bj ^ (SW * (uint32_t)i), b1 = bj ^ (SW * (uint32_t)(i + 1));
     const uint32_t sel0 = 0x7604u | ((uint32_t)(i & 3) << 4), sel1 = 0x7604u | ((uint32_t)((i + 1) & 3) << 4);
 #pragma unroll
     for (int p = 0; p < 2 * T; ++p) {
       const uint32_t ws = i < 4 ? c[p].x : c[p].y, wq = i < 4 ? c[p].z : c[p].w;
       const uint32_t aP0 = lut_prmt(ws, b0, sel0), aP1 = lut_prmt(ws, b1, sel1);
       const uint32_t aQ0 = lut_prmt(wq, b0, sel0), aQ1 = lut_prmt(wq, b1, sel1);
-      lut_add(acc[0][p][0], acc[0][p][1], lut_hadd2(lut_lds<lut_imm<M, 0>()>(aP0), lut_lds<lut_imm<M, 0>()>(aP1)));
-      lut_add(acc[0][p][2], acc[0][p][3], lut_hadd2(lut_lds<lut_imm<M, 0>()>(aQ0), lut_lds<lut_imm<M, 0>()>(aQ1)));
-      if constexpr (M > 1) {
-        lut_add(acc[1][p][0], acc[1][p][1], lut_hadd2(lut_lds<lut_imm<M, 1>()>(aP0), lut_lds<lut_imm<M, 1>()>(aP1)));
-        lut_add(acc[1][p][2], acc[1][p][3], lut_hadd2(lut_lds<lut_imm<M, 1>()>(aQ0), lut_lds<lut_imm<M, 1>()>(aQ1)));
-      }
-      if constexpr (M > 2) {
-        lut_add(acc[2][p][0], acc[2][p][1], lut_hadd2(lut_lds<lut_imm<M, 2>()>(aP0), lut_lds<lut_imm<M, 2>()>(aP1)));
-        lut_add(acc[2][p][2], acc[2][p][3], lut_hadd2(lut_lds<lut_imm<M, 2>()>(aQ0), lut_lds<lut_imm<M, 2>()>(aQ1)));
-      }
-      if constexpr (M > 3) {
-        lut_add(acc[3][p][0], acc[3][p][1], lut_hadd2(lut_lds<lut_imm<M, 3>()>(aP0), lut_lds<lut_imm<M, 3>()>(aP1)));
-        lut_add(acc[3][p][2], acc[3][p][3], lut_hadd2(lut_lds<lut_imm<M, 3>()>(aQ0), lut_lds<lut_imm<M, 3>()>(aQ1)));
+      if constexpr (!lut_pairs<T, M>()) {
+        lut_add(acc[0][p][0], acc[0][p][1], lut_hadd2(lut_lds<lut_imm<T, M, 0>()>(aP0), lut_lds<lut_imm<T, M, 0>()>(aP1)));
+        lut_add(acc[0][p][2], acc[0][p][3], lut_hadd2(lut_lds<lut_imm<T, M, 0>()>(aQ0), lut_lds<lut_imm<T, M, 0>()>(aQ1)));
+        if constexpr (M > 1) {
+          lut_add(acc[1][p][0], acc[1][p][1],
+                  lut_hadd2(lut_lds<lut_imm<T, M, 1>()>(aP0), lut_lds<lut_imm<T, M, 1>()>(aP1)));
+          lut_add(acc[1][p][2], acc[1][p][3],
+                  lut_hadd2(lut_lds<lut_imm<T, M, 1>()>(aQ0), lut_lds<lut_imm<T, M, 1>()>(aQ1)));
+        }
+        if constexpr (M > 2) {
+          lut_add(acc[2][p][0], acc[2][p][1],
+                  lut_hadd2(lut_lds<lut_imm<T, M, 2>()>(aP0), lut_lds<lut_imm<T, M, 2>()>(aP1)));
+          lut_add(acc[2][p][2], acc[2][p][3],
+                  lut_hadd2(lut_lds<lut_imm<T, M, 2>()>(aQ0), lut_lds<lut_imm<T, M, 2>()>(aQ1)));
+        }
+      } else {
+        {
+          const uint2 p0 = lut_lds2<lut_imm<T, M, 0>()>(aP0), p1 = lut_lds2<lut_imm<T, M, 0>()>(aP1);
+          const uint2 q0 = lut_lds2<lut_imm<T, M, 0>()>(aQ0), q1 = lut_lds2<lut_imm<T, M, 0>()>(aQ1);
+          lut_add(acc[0][p][0], acc[0][p][1], lut_hadd2(p0.x, p1.x));
+          lut_add(acc[0][p][2], acc[0][p][3], lut_hadd2(q0.x, q1.x));
+          lut_add(acc[1][p][0], acc[1][p][1], lut_hadd2(p0.y, p1.y));
+          lut_add(acc[1][p][2], acc[1][p][3], lut_hadd2(q0.y, q1.y));
+        }
       }
     }
   }
@@ -235,6 +269,7 @@ __device__ __forceinline__ void lut_fetch_x(const LutProblem& L, int w, int t, u
 // S & (8 nb - 1): a partial window's groups are repeated over all 32 slots, so
 // that the lanes that share a group read different banks.  Returns the factor
 // 2^e that undoes the activation scaling.
+template <bool PAIRS>
 __device__ __forceinline__ float lut_build(const LutProblem& L, int w, int t, int z, uint32_t tbase, uint4 va,
                                            uint4 vb) {
   const int lane = threadIdx.x & 31, h = threadIdx.x >> 5;
@@ -299,12 +334,16 @@ __device__ __forceinline__ float lut_build(const LutProblem& L, int w, int t, in
     qr[v] = ((v & 1) ? -a[2] : a[2]) + ((v & 2) ? -a[3] : a[3]) + hr;
     qi[v] = ((v & 1) ? -b[2] : b[2]) + ((v & 2) ? -b[3] : b[3]) + hi;
   }
-  const uint32_t set_addr = tbase + ((uint32_t)z >> 1) * 65536u + ((uint32_t)z & 1u) * 128u;
+  // slot = lane: 4 bytes apart in the set's own half-row, or (PAIRS) 8 apart
+  // beside the pair's other token
+  const uint32_t set_addr =
+      tbase + ((uint32_t)z >> 1) * 65536u + (PAIRS ? ((uint32_t)z & 1u) * 4u : ((uint32_t)z & 1u) * 128u);
+  const uint32_t sw = PAIRS ? 8u : 4u;
 #pragma unroll
   for (int l = 0; l < 16; ++l) {
     const float er = pr[l & 3] + qr[l >> 2], ei = pi[l & 3] + qi[l >> 2];
     const __half2 hv = __floats2half2_rn(er, ei);
-    const uint32_t addr = set_addr + (uint32_t)(16 * h + l) * 256u + 4u * (uint32_t)lane;
+    const uint32_t addr = set_addr + (uint32_t)(16 * h + l) * 256u + sw * (uint32_t)lane;
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(*reinterpret_cast<const uint32_t*>(&hv)) : "memory");
   }
   return __uint_as_float((uint32_t)(127 + e) << 23);  // 2^e
@@ -452,7 +491,8 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
       for (int t = 0; t < M; ++t)
         if (s < nseg) {
           const float pw =
-              lut_build(P.p[s_prob[s]], s_win[s], t, lut_set<M>(s, t), lut_table_base<M>(), xva[s][t], xvb[s][t]);
+              lut_build<lut_pairs<T, M>()>(P.p[s_prob[s]], s_win[s], t, lut_set<M>(s, t), lut_table_base<M>(),
+                                        xva[s][t], xvb[s][t]);
           if (tid == 0) s_pow[s][t] = pw;
         }
     __syncthreads();
@@ -467,7 +507,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
       const int64_t j = 32 * (int64_t)tau + lane;
       const bool row_in = j < L.n;
       // slot lane ^ (8 jj + i): group (lane & (8 nb - 1)) ^ (8 jj + i), bank = slot
-      const uint32_t bbase = 4u * (uint32_t)lane | lut_b_bits<M>(s);
+      const uint32_t bbase = lut_slot_stride<T, M>() * (uint32_t)lane | lut_b_bits<M>(s);
 
       float acc[M][NP][4];
 #pragma unroll
@@ -490,7 +530,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) linear_lut_kernel(const __grid
                        : "r"(src + (uint32_t)p * 512u)
                        : "memory");
         ck = ck + 1 == RING ? 0 : ck + 1;
-        lut_slot<T, M>(cw, bbase ^ (uint32_t)(32 * jj), acc);
+        lut_slot<T, M>(cw, bbase ^ (lut_slot_stride<T, M>() * 8u * (uint32_t)jj), acc);
         // refill the slot read one evaluation earlier (its registers are consumed)
         issue();
       }
