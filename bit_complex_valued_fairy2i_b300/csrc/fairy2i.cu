@@ -347,13 +347,39 @@ fairy2i_status make_x_map_half(CUtensorMap* map, const void* x, int64_t M, int64
   return FAIRY2I_OK;
 }
 
+// Launches a kernel as a programmatic dependent of the previous work in the
+// stream (it may start while that work finishes; its griddepcontrol.wait
+// orders everything that depends on it).
+template <typename Kernel, typename Params>
+cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Params& P) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, P);
+}
+
+// The fp16 form is a programmatic dependent of its conversion launch: it sets
+// up and decodes codes while the conversion finishes; only the threads that
+// read the fp16 copy or the tokens' factors wait for it.
 template <int T, int NT, bool SMALL, bool F16>
 fairy2i_status launch_dq_t(const f2i::DqParams& P, int grid, cudaStream_t s) {
   auto k = f2i::linear_dq_kernel<T, NT, SMALL, F16>;
   const size_t smem = f2i::dq_smem_bytes<NT, T, SMALL, F16>();
   fairy2i_status st = ensure_smem(reinterpret_cast<const void*>(k), smem, "dequantized prefill");
   if (st != FAIRY2I_OK) return st;
-  k<<<(unsigned)grid, f2i::kDqThreads, smem, s>>>(P);
+  if (F16) {
+    const cudaError_t e = launch_pdl(k, dim3((unsigned)grid), dim3(f2i::kDqThreads), smem, s, P);
+    if (e != cudaSuccess) return fail(FAIRY2I_ERR_CUDA, "dequantized prefill launch: %s", cudaGetErrorString(e));
+  } else {
+    k<<<(unsigned)grid, f2i::kDqThreads, smem, s>>>(P);
+  }
   return check_launch("dequantized prefill launch");
 }
 
@@ -759,23 +785,6 @@ size_t lut_workspace(const fairy2i_packed* qs, int count, int64_t M, int T) {
   return need;
 }
 
-// Launches a kernel as a programmatic dependent of the previous work in the
-// stream (it may start while that work finishes; its griddepcontrol.wait
-// orders everything that depends on it).
-template <typename Kernel, typename Params>
-cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Params& P) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, P);
-}
 
 template <int T, int M>
 fairy2i_status launch_lut_t(const f2i::LutParams& P, int ctas, cudaStream_t s) {

@@ -33,6 +33,11 @@
 
 namespace f2i {
 
+// Programmatic dependent launch: let the next kernel in the stream launch, and
+// wait until the previous one has completed with its writes visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // One output value to y[i]: fp32, or (bf16 != 0) rounded to nearest even to
 // bfloat16 in a buffer of bfloat16 elements (the same value the fp32 output
 // holds, rounded once).

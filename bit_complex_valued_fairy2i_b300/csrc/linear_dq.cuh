@@ -329,6 +329,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
   if (warp == 0) {
     // ---------------- TMA producer: activations, k-blocks in pairs (Re x, Im x) ----------------
     if (lane == 0) {
+      if constexpr (F16) pdl_wait();  // the fp16 copy of x comes from the conversion launch before
       uint32_t it = 0;
       bool ok = true;
       for (int64_t i = 0; ok; ++i) {
@@ -649,6 +650,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) linear_dq_kernel(const __grid_c
     // ---------------- epilogue: D row 2 jl + part of token t -> y[t][part n + j] ----------------
     const int eq = warp & 3;  // TMEM lanes 32 eq .. 32 eq + 31
     const int rl = 32 * eq + lane;
+    if constexpr (F16) pdl_wait();  // the tokens' factors come from the conversion launch
     const int jl = rl >> 1, part = rl & 1;
     uint32_t lt = 0;
     bool ok = true;
@@ -763,6 +765,7 @@ __device__ __forceinline__ uint32_t dq_bf16x2_to_f16x2(uint32_t w, float f) {
 }
 
 __global__ void __launch_bounds__(kDqXThreads) dq_x16_kernel(const __grid_constant__ DqXParams P) {
+  pdl_launch_dependents();  // the GEMM may set up and decode codes meanwhile
   const int l = blockIdx.y;
   const int64_t t = blockIdx.x, m = P.m[l];
   const uint4* src = reinterpret_cast<const uint4*>(P.x[l] + t * 2 * m);

@@ -239,7 +239,9 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
  * The decode kernel is launched as a programmatic dependent of the preceding
  * work in the stream (it may start while that work finishes and waits for it
  * before reading activations or writing anything); the summing kernel is an
- * ordinary launch after it.
+ * ordinary launch after it.  The fp16 dequantized GEMM is an ordinary
+ * conversion launch and then the GEMM as its programmatic dependent (only the
+ * GEMM's reads of the converted activations wait for the conversion).
  * Tokens go in launches of 2 (T <= 2; the first of 3 when M is odd and at
  * least 3), 2 (T = 3) or 1 (T = 4); each launch streams the codes once.  Precision: each table entry is the fp32 sum
  * of 8 scaled activations rounded once to fp16 (relative error <= 2^-11 per
