@@ -717,11 +717,11 @@ constexpr int64_t kTcDecodeMaxTokens = 8;
 constexpr int64_t kPrefillMinTokens = 16;
 // Token count from which AUTO, given a workspace, takes the fp16 dequantized
 // GEMM over the table-lookup decode on layout 3.  The table lookup runs in
-// launches of 2 or 3 tokens at T <= 2 (27 and 41 us each on a LLaMA-2-7B
-// block), the fp16 GEMM takes ~141 us at any count up to 64: measured per
-// block (eager / CUDA graph) at 10 tokens 139.6 / 128.5 us against 140.6 /
-// 136, at 11 tokens 154.6 us against 140.5.
-constexpr int64_t kDqMinTokens = 11;
+// launches of 2 or 3 tokens at T <= 2 (26.6 and 41 us each on a LLaMA-2-7B
+// block), the fp16 GEMM takes ~128 us at any count up to 16: measured per
+// block (eager / CUDA graph) at 9 tokens 123.9 / 115.3 us against 127.6 /
+// 125.0, at 10 tokens 134.4 / 125.2 against 128.0 / 125.3.
+constexpr int64_t kDqMinTokens = 10;
 
 // The quantizer over U, W (FUSED = false) or straight from R (true); the
 // caller has checked the arguments.  Codes are zeroed first: each row ORs its

@@ -201,8 +201,8 @@ fairy2i_status fairy2i_linear_group(const fairy2i_packed *qs, const void *const 
 /* Layout-3 layers through fairy2i_linear / _ex / _group (no workspace) take
  * the dequantized GEMM (FAIRY2I_ALGO_TCGEN05_DQ; "Fairy2i: Ultra-Low-Bit ...",
  * Step 3: the stages add up to one matrix, and Step 1: its real form); with a
- * workspace (the *_ws calls below) AUTO takes the table-lookup decode below 11
- * tokens and the fp16 dequantized GEMM (FAIRY2I_ALGO_TCGEN05_DQ16) from 11
+ * workspace (the *_ws calls below) AUTO takes the table-lookup decode below 10
+ * tokens and the fp16 dequantized GEMM (FAIRY2I_ALGO_TCGEN05_DQ16) from 10
  * tokens.  The dequantized GEMM needs m a multiple of 8 (x is read by TMA in
  * two halves, Re x and Im x), so other layout-3 layers return UNSUPPORTED here
  * and go through the *_ws calls.

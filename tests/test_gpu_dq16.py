@@ -134,7 +134,7 @@ def test_dq16_group_over_several_launches(M):
 
 
 def test_dq16_is_auto_with_workspace():
-    """With a workspace AUTO takes the fp16 form from 11 tokens: the same bits as the
+    """With a workspace AUTO takes the fp16 form from 10 tokens: the same bits as the
     explicit call; without one (the plain entry point) the bfloat16 form."""
     n, m = 100, 600
     q, qU, qW = _layer(_R(n, m, 14), 2)

@@ -325,7 +325,7 @@ def test_full_size_projection_layout3_sampled(name, out_f, in_f, T):
     assert rel_l2(got, want) <= REL_L2
 
 
-@pytest.mark.parametrize("M", [1, 4, 10, 11])  # 10: AUTO's last table-lookup count; 11: 3 + 2 + 2 + 2 + 2
+@pytest.mark.parametrize("M", [1, 4, 9, 11])  # 9: AUTO's last table-lookup count; 11: 3 + 2 + 2 + 2 + 2
 def test_full_size_block_group_layout3_sampled(M):
     """The seven projections of a block in one grouped table-lookup launch (the
     benchmark's launch), against the oracle on sampled rows."""
@@ -383,14 +383,14 @@ def test_dq_parity_stages(T, M):
 
 def test_dq_plain_entry_and_auto():
     """Layout 3 through the plain entry points (no workspace) takes the dequantized
-    GEMM at any token count; with a workspace AUTO switches to the fp16 form from 11 tokens."""
+    GEMM at any token count; with a workspace AUTO switches to the fp16 form from 10 tokens."""
     import ctypes
     n, m = 100, 600
     R = _R(n, m, 5)
     q = _gpu_layer(R, 2)
     qU, qW = _oracle_layer(R, 2)
     lib = f2i.load_library()
-    for M in (1, 10, 11):
+    for M in (1, 9, 10):
         x = _x(M, m, 30 + M)
         xd = x.cuda()
         y = torch.empty((M, 2 * n), device="cuda")
