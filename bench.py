@@ -377,17 +377,23 @@ def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
     stream = torch.cuda.current_stream()
 
     def timed(qs, algo):
-        for _ in range(warmup):
-            f2i.linear_group(qs, xs, ys, algo=algo)
-        torch.cuda.synchronize()
+        """ms per call over at least `steps` calls and 0.2 s (so that the clock sampler sees the
+        sustained, power-capped state of a long prefill), with the clocks seen meanwhile."""
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        for _ in range(steps):
+        for _ in range(warmup):
             f2i.linear_group(qs, xs, ys, algo=algo)
         stop.record(stream)
         torch.cuda.synchronize()
+        reps = max(steps, int(200.0 / max(start.elapsed_time(stop) / max(warmup, 1), 1e-3)) + 1)
+        with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+            start.record(stream)
+            for _ in range(reps):
+                f2i.linear_group(qs, xs, ys, algo=algo)
+            stop.record(stream)
+            torch.cuda.synchronize()
         f2i.sync_status()
-        return start.elapsed_time(stop) / steps
+        return start.elapsed_time(stop) / reps, reps, clk.summary()
 
     legs = {}
     nt = 2 if M > 256 else 1
@@ -395,13 +401,15 @@ def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
                                       ("dequantized", qs3, "tcgen05_dq", f"linear_dq_kernel<{T_STAGES},{nt},0,0>", flops_dq),
                                       ("dequantized_f16", qs3, "tcgen05_dq16",
                                        f"dq_x16_kernel + linear_dq_kernel<{T_STAGES},{nt},0,1>", flops_dense)):
-        ms = timed(qs, algo)
+        ms, reps, clocks = timed(qs, algo)
         tf = fl / (ms * 1e-3) / 1e12
         # the fp16 form runs on the same tensor-core rate as bfloat16 (kind::f16)
         legs[key] = {"algo": algo, "kernel": kernel, "layout": 2 if key == "ternary" else 3, "ms_per_block": ms,
                      "executed_flops_per_block": fl, "tflops_executed": tf,
                      "tflops_dense_equivalent": flops_dense / (ms * 1e-3) / 1e12,
-                     "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "tokens_per_s_per_block": M / (ms * 1e-3)}
+                     "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+                     "frac_of_bf16_sustained": tf / peaks["bf16_tflops_sustained"],
+                     "tokens_per_s_per_block": M / (ms * 1e-3), "calls_timed": reps, "clocks": clocks}
     best = min(legs, key=lambda k: legs[k]["ms_per_block"])
     b = legs[best]
     return {"workload": f"llama2-7b block prefill, 7 projections, M={M}, T={T_STAGES}, 1% outliers x10, "
@@ -410,6 +418,9 @@ def prefill_leg(f2i, dev, peaks, steps: int, warmup: int, M: int = 2048):
             "dense_equivalent_flops_per_block": flops_dense, "tflops_executed": b["tflops_executed"],
             "tflops_dense_equivalent": b["tflops_dense_equivalent"],
             "peak_bf16_tflops": peaks["bf16_tflops"], "frac_of_bf16_peak": b["frac_of_bf16_peak"],
+            "peak_bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
+            "frac_of_bf16_sustained": b["frac_of_bf16_sustained"], "clocks": b["clocks"],
+            "calls_timed": b["calls_timed"],
             "peak_source": peaks["source"], "tokens_per_s_per_block": b["tokens_per_s_per_block"], "steps": steps,
             "by_kernel": legs}
 
