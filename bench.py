@@ -461,9 +461,11 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
             st = stack3 if key in ("lut", "tcgen05_dq", "tcgen05_dq16", "auto_layout3") else stack
             algo = "auto" if key == "auto_layout3" else key
 
+            calls = [f2i.GroupCall(st[b], xs[b], ys[b], algo=algo) for b in range(blocks)]
+
             def step():
-                for b in range(blocks):
-                    f2i.linear_group(st[b], xs[b], ys[b], algo=algo)
+                for c in calls:
+                    c()
             for _ in range(3):
                 step()
             torch.cuda.synchronize()
@@ -479,9 +481,12 @@ def sweep_leg(f2i, dev, Ms=(1, 2, 4, 8, 16, 32, 64), reps: int = 10, blocks: int
             if key == "auto_layout3":
                 # the same calls replayed as one CUDA graph: the device time per block, without
                 # the per-call host work that bounds the eager figure at small M
+                # (calls prepared inside the capture: a prepared call keeps the stream it was
+                # built on, and the capture runs on a stream of its own)
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph):
-                    step()
+                    for b in range(blocks):
+                        f2i.GroupCall(st[b], xs[b], ys[b], algo=algo)()
                 graph.replay()
                 torch.cuda.synchronize()
                 start.record(stream)
@@ -820,6 +825,24 @@ def run_ours(args, world, rank, local):
         eager_step()
     e2e_eager_s = _max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
 
+    # the same with each block's call prepared once (f2i.GroupCall): per step only the C call's
+    # own host work (checks, launch parameters, the launches) remains
+    calls = [f2i.GroupCall(stack[b], xs[b], ys[b], algo=algo) for b in range(blocks)]
+
+    def prepared_step():
+        x_all.copy_(x_host, non_blocking=True)
+        for c in calls:
+            c()
+        y_host.copy_(y_all, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        prepared_step()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        prepared_step()
+    e2e_prepared_s = _max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+
     achieved = bytes_per_block / (launch_ms * 1e-3) / 1e9
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -834,7 +857,10 @@ def run_ours(args, world, rank, local):
                 "ms_per_step": e2e_s * 1e3, "ms_per_step_per_block_waits": e2e_per_block_s * 1e3,
                 "ms_per_step_two_waits": e2e_one_wait_s * 1e3,
                 "eager": {"value": bytes_per_step * world / e2e_eager_s / 1e9, "ms_per_step": e2e_eager_s * 1e3,
-                          "note": "no CUDA graph: per-call host work included"}},
+                          "note": "no CUDA graph: per-call host work included"},
+                "eager_prepared": {"value": bytes_per_step * world / e2e_prepared_s / 1e9,
+                                   "ms_per_step": e2e_prepared_s * 1e3,
+                                   "note": "no CUDA graph, each block's call prepared once (GroupCall)"}},
         "gpu_launches": blocks * args.steps * (2 if algo == "lut" else 1),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],

@@ -303,41 +303,62 @@ def linear_grad_x_group(qs, gys, outs=None, stream=None):
     return outs
 
 
+class GroupCall:
+    """A grouped linear call prepared once: layers, inputs, outputs, algorithm, stream and
+    workspace fixed, the C arguments (descriptor array, pointer arrays) built here.  Calling it
+    issues the launches again with no per-call marshalling -- for loops that reuse the same
+    buffers (a serving step, a benchmark): the tensors' contents may change between calls, the
+    tensors themselves may not.  The stream is fixed too (the current one when prepared, unless
+    given): prepare a call inside a CUDA-graph capture to have it captured.  ``ys`` (allocated
+    if not given) are the outputs."""
+
+    def __init__(self, qs, xs, ys=None, algo: str = "auto", stream=None, ws: torch.Tensor | None = None,
+                 out_dtype=torch.float32):
+        count = len(qs)
+        M = xs[0].shape[0]
+        if out_dtype not in OUT:
+            raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+        if ys is None:
+            ys = [torch.empty((M, 2 * q.n), dtype=out_dtype, device=x.device) for q, x in zip(qs, xs)]
+        for q, x, y in zip(qs, xs, ys):
+            _dev(x, "x")
+            _dev(y, "y")
+            if x.dtype != torch.bfloat16 or x.shape != (M, 2 * q.m) or y.shape != (M, 2 * q.n) or y.dtype != out_dtype:
+                raise ValueError("group members need matching x [M, 2m] bfloat16 and y [M, 2n] of out_dtype")
+        lib = load_library()
+        descs = (PackedDesc * count)(*[q.desc() for q in qs])
+        xp = (ctypes.c_void_p * count)(*[x.data_ptr() for x in xs])
+        yp = (ctypes.c_void_p * count)(*[y.data_ptr() for y in ys])
+        s = _stream(stream, xs[0].get_device())
+        if qs[0].layout == LAYOUT_LUT:
+            if ws is None:
+                ws = workspace(qs, M, xs[0].device, s, descs)
+            wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
+            if out_dtype == torch.float32:
+                self._fn, self._args = lib.fairy2i_linear_group_ws, (descs, xp, yp, count, M, ALGO[algo], wp, wn, s)
+            else:
+                self._fn = lib.fairy2i_linear_group_ws_out
+                self._args = (descs, xp, yp, count, M, ALGO[algo], OUT[out_dtype], wp, wn, s)
+        else:
+            if out_dtype != torch.float32:
+                raise ValueError("bfloat16 outputs are written for layout-3 layers only")
+            self._fn, self._args = lib.fairy2i_linear_group, (descs, xp, yp, count, M, ALGO[algo], s)
+        # the tensors whose addresses the arguments hold stay alive with the call
+        self._keep = (list(qs), list(xs), ws)
+        self.ys = ys
+
+    def __call__(self):
+        _check(self._fn(*self._args))
+        return self.ys
+
+
 def linear_group(qs, xs, ys=None, algo: str = "auto", stream=None, ws: torch.Tensor | None = None,
                  out_dtype=torch.float32):
     """Evaluate several layers (same T, layout and token count) in one launch; layout-3 layers
     use workspace ``ws`` (by default the one kept for this device and stream) and may write
-    bfloat16 outputs (``out_dtype``: the float32 result rounded once)."""
-    count = len(qs)
-    M = xs[0].shape[0]
-    if out_dtype not in OUT:
-        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
-    if ys is None:
-        ys = [torch.empty((M, 2 * q.n), dtype=out_dtype, device=x.device) for q, x in zip(qs, xs)]
-    for q, x, y in zip(qs, xs, ys):
-        _dev(x, "x")
-        _dev(y, "y")
-        if x.dtype != torch.bfloat16 or x.shape != (M, 2 * q.m) or y.shape != (M, 2 * q.n) or y.dtype != out_dtype:
-            raise ValueError("group members need matching x [M, 2m] bfloat16 and y [M, 2n] of out_dtype")
-    descs = (PackedDesc * count)(*[q.desc() for q in qs])
-    xp = (ctypes.c_void_p * count)(*[x.data_ptr() for x in xs])
-    yp = (ctypes.c_void_p * count)(*[y.data_ptr() for y in ys])
-    index = xs[0].get_device()
-    s = _stream(stream, index)
-    if qs[0].layout == LAYOUT_LUT:
-        if ws is None:
-            ws = workspace(qs, M, xs[0].device, s, descs)
-        wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
-        if out_dtype == torch.float32:
-            _check(load_library().fairy2i_linear_group_ws(descs, xp, yp, count, M, ALGO[algo], wp, wn, s))
-        else:
-            _check(load_library().fairy2i_linear_group_ws_out(descs, xp, yp, count, M, ALGO[algo], OUT[out_dtype],
-                                                              wp, wn, s))
-        return ys
-    if out_dtype != torch.float32:
-        raise ValueError("bfloat16 outputs are written for layout-3 layers only")
-    _check(load_library().fairy2i_linear_group(descs, xp, yp, count, M, ALGO[algo], s))
-    return ys
+    bfloat16 outputs (``out_dtype``: the float32 result rounded once).  For a loop over the same
+    buffers, ``GroupCall`` prepares the arguments once."""
+    return GroupCall(qs, xs, ys, algo, stream, ws, out_dtype)()
 
 
 def linear_group_static(qs, xs, ys=None, stream=None):

@@ -175,6 +175,8 @@ def test_python_wrappers_reject_host_tensors(lib):
         f2i.linear(q, torch.zeros((1, 16), dtype=torch.bfloat16))  # host tensor
     with pytest.raises(ValueError):
         f2i.linear_grad_x(q, torch.zeros((1, 8)))  # host tensor
+    with pytest.raises(ValueError):
+        f2i.GroupCall([q], [torch.zeros((1, 16), dtype=torch.bfloat16)])  # host tensor
     # the algorithm names map onto the header's fairy2i_algo values
     assert f2i.ALGO == {"auto": 0, "addsub": 1, "mma": 2, "tcgen05": 3, "tcgen05_sp": 4, "lut": 5,
                         "tcgen05_dq": 6, "tcgen05_dq16": 7}

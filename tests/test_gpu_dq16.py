@@ -197,3 +197,24 @@ def test_bf16_outputs_are_the_rounded_fp32_outputs(algo, M):
     y16 = f2i.linear_group(qs, xs, algo=algo, out_dtype=torch.bfloat16)
     for a, b in zip(y32, y16):
         assert b.dtype == torch.bfloat16 and torch.equal(a.to(torch.bfloat16), b)
+
+
+@pytest.mark.parametrize("layout,algo,M", [(L3, "lut", 1), (L3, "tcgen05_dq16", 40), (L3, "auto", 3), (2, "mma", 2),
+                                           (2, "tcgen05", 33)])
+def test_group_call_prepared_once(layout, algo, M):
+    """GroupCall: arguments built once, then called again after the inputs changed in place;
+    every call equals a fresh linear_group call on the same inputs, bit for bit."""
+    shapes = [(40, 256), (37, 600)]
+    qs, xs = [], []
+    for i, (n, m) in enumerate(shapes):
+        U, W = f2i.convert(_R(n, m, 40 + i).cuda())
+        qs.append(f2i.quantize(U, W, 2, layout=layout))
+        xs.append(_x(M, m, 50 + i).cuda())
+    call = f2i.GroupCall(qs, xs, algo=algo)
+    for step in range(3):
+        got = [y.clone() for y in call()]
+        want = f2i.linear_group(qs, xs, algo=algo)
+        for a, b in zip(got, want):
+            assert torch.equal(a, b), step
+        for x in xs:
+            x.mul_(-2)  # exact in bfloat16
