@@ -872,19 +872,20 @@ def run_ours(args, world, rank, local):
         "offline": offline,
     }
     del graph, e2e_graph, e2e_graph1
-    # the sweep before the prefill: right after the prefill's long tensor-core load the first
-    # sweep rows measured up to 3x slower for some kernels (55 against 19 us per block for the
-    # table lookup at M = 1), an after-effect of the previous leg, not of the kernels timed
+    # the prefill leg last among the GPU legs: for a second or two after its long tensor-core
+    # load the next measurements ran up to 3x slower (55 against 19 us per block for the
+    # table lookup at M = 1 in the sweep, 0.95 against 2.2 TB/s for the stack's T = 1
+    # quantize), an after-effect of that leg, not of the kernels timed
     if not args.no_sweep:
         result["sweep"] = sweep_leg(f2i, dev)
-    if not args.no_prefill:
-        result["prefill"] = prefill_leg(f2i, dev, peaks, max(3, min(args.steps, 20)), 3, args.prefill_tokens)
     if not args.no_stack:
         del stack, x_all, y_all, xv, yv, xs, ys
         torch.cuda.empty_cache()
         result["stack"] = {"workload": f"llama2-7b linear stack, {blocks} blocks x 7 projections, M=1, layout 3 "
                                        "(table-lookup decode), T in {1, 2, 3}",
                            "rows": [stack_leg(f2i, dev, T, blocks, max(3, min(args.steps, 50)), 3) for T in (1, 2, 3)]}
+    if not args.no_prefill:
+        result["prefill"] = prefill_leg(f2i, dev, peaks, max(3, min(args.steps, 20)), 3, args.prefill_tokens)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
