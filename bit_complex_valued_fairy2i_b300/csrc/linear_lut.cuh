@@ -48,7 +48,7 @@ namespace f2i {
 constexpr int kLutWarps = 16;
 constexpr int kLutThreads = kLutWarps * 32;
 constexpr int kLutMaxGroup = 32;
-constexpr int kLutMaxCtas = 256;
+constexpr int kLutMaxCtas = 160;  // one CTA per SM (148 on B300); bounds the launch parameters
 constexpr uint32_t kLutSmemBytes = 224u * 1024u;  // dynamic shared memory: covers [base, 224 KB) for any base
 
 // Largest token count of one launch for T stages (fp32 accumulators and the
